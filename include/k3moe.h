@@ -1,0 +1,168 @@
+/*
+ * k3moe.h -- C ABI of the GB300 (sm_103a) MXFP4 mixture-of-experts layer library (libk3moe.so).
+ *
+ * The layer (Kimi-K3 style, as described by the kimi-k3-in-c review,
+ * blog.123qwe.co.kr/?p=4411, tables "한눈에 보는 kimi-k3-in-c" and "KDA·MLA·MoE", and the
+ * kimi-k3-in-c README, rosettalens.com/s/ko/kimi-k3-in-c, section "shard census"):
+ *   for each token x (d_model values)
+ *     logits  l_e = x . W_e (+ b_e)                      e = 0..n_routed-1      (router)
+ *     top-k   the k largest logits, equal logits -> lower index first
+ *     gates   w_i = exp(l_i - l_max) / sum_{j in top-k} exp(l_j - l_max)       (renormalised softmax)
+ *     expert  o = W_down (SiLU(W_gate x) * (W_up x))     on MXFP4 weights        (SiLU-gated GLU)
+ *     output  y = sum_i w_i o_{e_i} + sum_s o_s          (n_shared always-on experts, weight 1)
+ *
+ * MXFP4 (OCP MX v1.0): 4-bit E2M1 codes plus one E8M0 scale byte (2^(b-127), 0xFF = NaN) per
+ * 32 consecutive weights along the reduction axis, 0.53125 B per weight. Expert record, one per
+ * expert, contiguous, `record_stride` bytes apart (d = d_model, f = d_ff):
+ *   [gate codes f x d/2][gate scales f x d/32][up codes f x d/2][up scales f x d/32]
+ *   [down codes d x f/2][down scales d x f/32]
+ * Codes are row-major, two per byte, the even column in the low nibble. A record of the
+ * d_model 7168 / d_ff 1536 shape is 17,547,264 bytes (the census figure).
+ *
+ * Conventions shared by every call below:
+ *  - Pointers are DEVICE pointers unless marked "host". The caller owns all memory; nothing is
+ *    allocated by a compute call and nothing is kept after it returns.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *  - Invalid arguments return K3MOE_ERR_INVALID_ARGUMENT synchronously and launch nothing:
+ *    a NULL required pointer, T < 0, T > the workspace's token capacity, top_k < 1 or
+ *    top_k > min(n_routed, 32), n_routed > 4096, n_shared < 0 or > 8, d_model or d_ff not a
+ *    positive multiple of 128, record_stride < the record size or not a multiple of 256,
+ *    a pointer not 16-byte aligned, or an unknown enum value.
+ *    Legal configurations this library does not implement return K3MOE_ERR_UNSUPPORTED.
+ *  - T = 0 is a no-op that returns K3MOE_OK.
+ *  - Bad data found on the device (an expert index outside [0, n_routed) given to
+ *    k3moe_expert_ffn, or an E8M0 scale byte 0xFF) sets a status word in the workspace; the
+ *    affected output is not trusted. k3moe_check_device_status reports it as
+ *    K3MOE_ERR_DEVICE_CHECK. Kernels never trap and never wait without a bound.
+ *  - CUDA launch errors return K3MOE_ERR_CUDA.
+ *  - The workspace (`ws`, `ws_bytes`) is scratch owned by the caller: size it with
+ *    k3moe_workspace_bytes, zero-fill it once after allocation, and do not run two calls
+ *    that share a workspace concurrently. Calls on different workspaces are independent;
+ *    the library has no other mutable global state.
+ */
+#ifndef K3MOE_H
+#define K3MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define K3MOE_API __attribute__((visibility("default")))
+#else
+#define K3MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  K3MOE_OK = 0,
+  K3MOE_ERR_INVALID_ARGUMENT = 1,
+  K3MOE_ERR_UNSUPPORTED = 2,
+  K3MOE_ERR_WORKSPACE = 3,
+  K3MOE_ERR_CUDA = 4,
+  K3MOE_ERR_DEVICE_CHECK = 5,
+  K3MOE_ERR_TIMEOUT = 6
+} k3moe_status;
+
+/* Router score function. Only the softmax score is implemented. */
+enum { K3MOE_SCORE_SOFTMAX = 0, K3MOE_SCORE_SIGMOID_BIAS = 1 };
+/* Activation handling in the expert FFN. Only the exact mode is implemented: activations keep
+   their input precision (bf16 exactly, fp32 to ~2^-22) and h keeps ~2^-22 relative precision. */
+enum { K3MOE_ACT_EXACT = 0, K3MOE_ACT_MXFP4 = 1 };
+/* Element type of the token activations x. */
+enum { K3MOE_X_BF16 = 0, K3MOE_X_F32 = 1 };
+
+typedef struct {
+  int32_t d_model;       /* hidden size d (7168 for the K3 shape) */
+  int32_t d_ff;          /* expert intermediate size f (1536) */
+  int32_t n_routed;      /* routed experts E (896) */
+  int32_t top_k;         /* experts selected per token k (16) */
+  int32_t n_shared;      /* always-on shared experts S (2) */
+  int32_t score_func;    /* K3MOE_SCORE_* */
+  int32_t act_mode;      /* K3MOE_ACT_* */
+  int32_t x_dtype;       /* K3MOE_X_* */
+  int64_t record_stride; /* bytes between expert records (>= record size, multiple of 256) */
+} k3moe_config;
+
+/* Bytes of one expert record for this config: 3 * d_model * d_ff * 17 / 32 (host only; 0 if invalid). */
+K3MOE_API size_t k3moe_record_bytes(const k3moe_config* cfg /* host */);
+
+/* Workspace bytes needed for calls of up to `max_tokens` tokens (host only; 0 if invalid). */
+K3MOE_API size_t k3moe_workspace_bytes(const k3moe_config* cfg /* host */, int64_t max_tokens);
+
+/*
+ * Router: softmax over the n_routed logits of each token, top-k, renormalised gates.
+ * (The review's list of header invariants describes a sigmoid score whose bias changes only
+ * the selection; that score is K3MOE_SCORE_SIGMOID_BIAS and returns K3MOE_ERR_UNSUPPORTED.)
+ *   x        [T, d_model] bf16 or fp32 (cfg->x_dtype), row-major
+ *   w_router [n_routed, d_model] fp32, row-major
+ *   bias     [n_routed] fp32 added to every logit before selection and softmax, or NULL
+ *   topk_idx [T, top_k] int32 out: expert ids, descending logit, ties to the lower id
+ *   topk_w   [T, top_k] fp32 out: gates, summing to 1 per token
+ */
+K3MOE_API k3moe_status k3moe_route(const k3moe_config* cfg /* host */, const void* x, int64_t T,
+                         const float* w_router, const float* bias, int32_t* topk_idx, float* topk_w,
+                         void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Expert FFN and combine for given routing (review, table "KDA·MLA·MoE": the experts multiply
+ * MXFP4 nibbles directly; the layer's 2 shared experts run for every token).
+ *   x              [T, d_model] bf16 or fp32
+ *   topk_idx       [T, top_k] int32 expert ids in [0, n_routed) (checked on the device)
+ *   topk_w         [T, top_k] fp32 gate weights
+ *   routed_records n_routed records, record_stride bytes apart (16-byte aligned base)
+ *   shared_records n_shared records, record_stride bytes apart (may be NULL if n_shared == 0)
+ *   y              [T, d_model] fp32 out, overwritten
+ */
+K3MOE_API k3moe_status k3moe_expert_ffn(const k3moe_config* cfg /* host */, const void* x, int64_t T,
+                              const int32_t* topk_idx, const float* topk_w,
+                              const uint8_t* routed_records, const uint8_t* shared_records, float* y,
+                              void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * The whole layer: k3moe_route followed by k3moe_expert_ffn, sharing one workspace.
+ *   topk_idx_out / topk_w_out: optional [T, top_k] outputs of the routing (NULL to skip).
+ */
+K3MOE_API k3moe_status k3moe_layer(const k3moe_config* cfg /* host */, const void* x, int64_t T,
+                         const float* w_router, const float* bias, const uint8_t* routed_records,
+                         const uint8_t* shared_records, float* y, int32_t* topk_idx_out,
+                         float* topk_w_out, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * k3moe_layer with phase timing, for profiling: `events` points to 4 cudaEvent_t handles created by
+ * the caller; they are recorded on `stream` before the router kernel, before the gate/up kernel,
+ * before the down-projection kernel and after it. Same kernels and results as k3moe_layer.
+ */
+K3MOE_API k3moe_status k3moe_layer_timed(const k3moe_config* cfg /* host */, const void* x, int64_t T,
+                                         const float* w_router, const float* bias,
+                                         const uint8_t* routed_records, const uint8_t* shared_records,
+                                         float* y, int32_t* topk_idx_out, float* topk_w_out, void* ws,
+                                         size_t ws_bytes, void* stream, void* const* events /* host */);
+
+/*
+ * Pre-norm residual step of a stack of layers: xn = RMSNorm(x) with unit weight,
+ * xn_j = x_j / sqrt(mean_j(x^2) + eps) (RMSNorm is one of the engine's ops in the review's
+ * "k3_ops.c" row). x, xn: [T, d] fp32.
+ */
+K3MOE_API k3moe_status k3moe_rmsnorm(const float* x, int64_t T, int32_t d, float eps, float* xn, void* stream);
+
+/* Residual add x += y over n fp32 values. */
+K3MOE_API k3moe_status k3moe_residual_add(float* x, const float* y, int64_t n, void* stream);
+
+/*
+ * Synchronise `stream`, read the workspace's device status word, clear it, and return
+ * K3MOE_ERR_DEVICE_CHECK if bad data was seen since the last check, else K3MOE_OK
+ * (K3MOE_ERR_CUDA if the stream reports an error).
+ */
+K3MOE_API k3moe_status k3moe_check_device_status(void* ws, void* stream);
+
+/* Static description of a status code (host only). */
+K3MOE_API const char* k3moe_status_string(k3moe_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* K3MOE_H */

@@ -1,0 +1,284 @@
+// C ABI of libk3moe.so (declared in include/k3moe.h): argument validation, the workspace
+// layout, and the launch sequence of each call. No call allocates memory.
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/k3moe.h"
+#include "k3moe_kernels.h"
+
+namespace {
+
+using k3::Cfg;
+using k3::Ws;
+
+constexpr long long kMaxE = 4096;
+constexpr long long kMaxK = 32;
+constexpr long long kMaxS = 8;
+
+size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+long long record_bytes_of(const k3moe_config* c) {
+  return 3LL * ((long long)c->d_model * c->d_ff / 2 + (long long)c->d_model * c->d_ff / 32);
+}
+
+k3moe_status validate(const k3moe_config* c) {
+  if (!c) return K3MOE_ERR_INVALID_ARGUMENT;
+  if (c->d_model <= 0 || c->d_model % 128 || c->d_ff <= 0 || c->d_ff % 128) return K3MOE_ERR_INVALID_ARGUMENT;
+  if (c->n_routed < 1 || c->n_routed > kMaxE) return K3MOE_ERR_INVALID_ARGUMENT;
+  if (c->top_k < 1 || c->top_k > kMaxK || c->top_k > c->n_routed) return K3MOE_ERR_INVALID_ARGUMENT;
+  if (c->n_shared < 0 || c->n_shared > kMaxS) return K3MOE_ERR_INVALID_ARGUMENT;
+  if (c->score_func != K3MOE_SCORE_SOFTMAX && c->score_func != K3MOE_SCORE_SIGMOID_BIAS)
+    return K3MOE_ERR_INVALID_ARGUMENT;
+  if (c->act_mode != K3MOE_ACT_EXACT && c->act_mode != K3MOE_ACT_MXFP4) return K3MOE_ERR_INVALID_ARGUMENT;
+  if (c->x_dtype != K3MOE_X_BF16 && c->x_dtype != K3MOE_X_F32) return K3MOE_ERR_INVALID_ARGUMENT;
+  if (c->record_stride < record_bytes_of(c) || c->record_stride % 256) return K3MOE_ERR_INVALID_ARGUMENT;
+  if ((long long)c->d_model * c->d_ff > (1LL << 40)) return K3MOE_ERR_INVALID_ARGUMENT;
+  if (c->score_func != K3MOE_SCORE_SOFTMAX || c->act_mode != K3MOE_ACT_EXACT) return K3MOE_ERR_UNSUPPORTED;
+  return K3MOE_OK;
+}
+
+bool tokens_ok(const k3moe_config* c, int64_t T) {
+  return T >= 0 && T * (long long)(c->top_k + c->n_shared) < (1LL << 30) && T <= (1LL << 26);
+}
+
+// Upper bound on work groups for T tokens (work groups of one token: the largest count).
+long long wg_bound(const k3moe_config* c, long long T) {
+  long long slots = T * c->top_k;
+  long long distinct = slots < c->n_routed ? slots : c->n_routed;
+  return distinct + slots + (long long)c->n_shared * T + 1;
+}
+
+struct Layout {
+  size_t ctrl, logits, topk_idx, topk_w, counts, cursor, offsets, wgoff, perm_tok, perm_w, inv, wgs, xact, xexp, hact,
+      hexp, part, tilecnt, total;
+};
+
+Layout make_layout(const k3moe_config* c, long long T) {
+  const long long E = c->n_routed, k = c->top_k, S = c->n_shared, d = c->d_model, f = c->d_ff;
+  const long long P = T * (k + S);
+  Layout L{};
+  size_t o = 0;
+  auto take = [&](size_t& field, size_t bytes) {
+    field = o;
+    o = align_up(o + (bytes ? bytes : 1));
+  };
+  take(L.ctrl, sizeof(int) * k3::CTRL_WORDS);
+  take(L.logits, sizeof(float) * T * E);
+  take(L.topk_idx, sizeof(int) * T * k);
+  take(L.topk_w, sizeof(float) * T * k);
+  take(L.counts, sizeof(int) * E);
+  take(L.cursor, sizeof(int) * E);
+  take(L.offsets, sizeof(int) * (E + 1));
+  take(L.wgoff, sizeof(int) * (E + 1));
+  take(L.perm_tok, sizeof(int) * P);
+  take(L.perm_w, sizeof(float) * P);
+  take(L.inv, sizeof(int) * T * k);
+  take(L.wgs, sizeof(k3::WorkGroup) * wg_bound(c, T));
+  take(L.xact, sizeof(__half) * T * 2 * d);
+  take(L.xexp, (size_t)(T * (d / 32)));
+  take(L.hact, sizeof(__half) * P * 2 * f);
+  take(L.hexp, (size_t)(P * (f / 32)));
+  take(L.part, sizeof(float) * P * d);
+  take(L.tilecnt, sizeof(int) * (d / 32));
+  L.total = o;
+  return L;
+}
+
+Ws bind(const Layout& L, void* base) {
+  char* b = static_cast<char*>(base);
+  Ws w;
+  w.ctrl = reinterpret_cast<int*>(b + L.ctrl);
+  w.logits = reinterpret_cast<float*>(b + L.logits);
+  w.topk_idx = reinterpret_cast<int*>(b + L.topk_idx);
+  w.topk_w = reinterpret_cast<float*>(b + L.topk_w);
+  w.counts = reinterpret_cast<int*>(b + L.counts);
+  w.cursor = reinterpret_cast<int*>(b + L.cursor);
+  w.offsets = reinterpret_cast<int*>(b + L.offsets);
+  w.wgoff = reinterpret_cast<int*>(b + L.wgoff);
+  w.perm_tok = reinterpret_cast<int*>(b + L.perm_tok);
+  w.perm_w = reinterpret_cast<float*>(b + L.perm_w);
+  w.inv = reinterpret_cast<int*>(b + L.inv);
+  w.wgs = reinterpret_cast<k3::WorkGroup*>(b + L.wgs);
+  w.xact = reinterpret_cast<__half*>(b + L.xact);
+  w.xexp = reinterpret_cast<int8_t*>(b + L.xexp);
+  w.hact = reinterpret_cast<__half*>(b + L.hact);
+  w.hexp = reinterpret_cast<int8_t*>(b + L.hexp);
+  w.part = reinterpret_cast<float*>(b + L.part);
+  w.tilecnt = reinterpret_cast<int*>(b + L.tilecnt);
+  return w;
+}
+
+Cfg make_cfg(const k3moe_config* c, long long T) {
+  Cfg k;
+  k.d = c->d_model;
+  k.f = c->d_ff;
+  k.E = c->n_routed;
+  k.k = c->top_k;
+  k.S = c->n_shared;
+  k.x_f32 = c->x_dtype == K3MOE_X_F32 ? 1 : 0;
+  k.xplanes = k.x_f32 ? 2 : 1;
+  k.wgt = T == 1 ? 1 : 4;
+  k.stride = c->record_stride;
+  return k;
+}
+
+k3moe_status check_ws(const k3moe_config* c, long long T, void* ws, size_t ws_bytes, Layout* L) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return K3MOE_ERR_INVALID_ARGUMENT;
+  *L = make_layout(c, T);
+  if (ws_bytes < L->total) return K3MOE_ERR_WORKSPACE;
+  return K3MOE_OK;
+}
+
+k3moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+size_t k3moe_record_bytes(const k3moe_config* cfg) {
+  if (!cfg || cfg->d_model <= 0 || cfg->d_ff <= 0 || cfg->d_model % 32 || cfg->d_ff % 32) return 0;
+  return (size_t)record_bytes_of(cfg);
+}
+
+size_t k3moe_workspace_bytes(const k3moe_config* cfg, int64_t max_tokens) {
+  if (validate(cfg) != K3MOE_OK || !tokens_ok(cfg, max_tokens)) return 0;
+  return make_layout(cfg, max_tokens < 1 ? 1 : max_tokens).total;
+}
+
+k3moe_status k3moe_route(const k3moe_config* cfg, const void* x, int64_t T, const float* w_router, const float* bias,
+                         int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes, void* stream) {
+  k3moe_status s = validate(cfg);
+  if (s != K3MOE_OK) return s;
+  if (!tokens_ok(cfg, T)) return K3MOE_ERR_INVALID_ARGUMENT;
+  if (!x || !w_router || !topk_idx || !topk_w) return K3MOE_ERR_INVALID_ARGUMENT;
+  if (!aligned16(x) || !aligned16(w_router) || (bias && !aligned16(bias)) || !aligned16(topk_idx) ||
+      !aligned16(topk_w))
+    return K3MOE_ERR_INVALID_ARGUMENT;
+  if (T == 0) return K3MOE_OK;
+  Layout L;
+  if ((s = check_ws(cfg, T, ws, ws_bytes, &L)) != K3MOE_OK) return s;
+  const Cfg c = make_cfg(cfg, T);
+  return cuda_status(k3::launch_route(c, bind(L, ws), x, T, w_router, bias, topk_idx, topk_w, k3::RM_USER_OUT,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+k3moe_status k3moe_expert_ffn(const k3moe_config* cfg, const void* x, int64_t T, const int32_t* topk_idx,
+                              const float* topk_w, const uint8_t* routed_records, const uint8_t* shared_records,
+                              float* y, void* ws, size_t ws_bytes, void* stream) {
+  k3moe_status s = validate(cfg);
+  if (s != K3MOE_OK) return s;
+  if (!tokens_ok(cfg, T)) return K3MOE_ERR_INVALID_ARGUMENT;
+  if (!x || !topk_idx || !topk_w || !routed_records || !y || (cfg->n_shared > 0 && !shared_records))
+    return K3MOE_ERR_INVALID_ARGUMENT;
+  if (!aligned16(x) || !aligned16(topk_idx) || !aligned16(topk_w) || !aligned16(routed_records) || !aligned16(y) ||
+      (shared_records && !aligned16(shared_records)))
+    return K3MOE_ERR_INVALID_ARGUMENT;
+  if (T == 0) return K3MOE_OK;
+  Layout L;
+  if ((s = check_ws(cfg, T, ws, ws_bytes, &L)) != K3MOE_OK) return s;
+  const Cfg c = make_cfg(cfg, T);
+  const Ws w = bind(L, ws);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = k3::launch_prep(c, w, x, T, topk_idx, topk_w, st);
+  if (e == cudaSuccess) e = k3::launch_gateup(c, w, routed_records, shared_records, y, T, wg_bound(cfg, T), st);
+  if (e == cudaSuccess) e = k3::launch_down(c, w, routed_records, shared_records, y, T, wg_bound(cfg, T), st);
+  return cuda_status(e);
+}
+
+}  // extern "C"
+
+namespace {
+
+k3moe_status layer_impl(const k3moe_config* cfg, const void* x, int64_t T, const float* w_router, const float* bias,
+                        const uint8_t* routed_records, const uint8_t* shared_records, float* y, int32_t* topk_idx_out,
+                        float* topk_w_out, void* ws, size_t ws_bytes, void* stream, void* const* events) {
+  k3moe_status s = validate(cfg);
+  if (s != K3MOE_OK) return s;
+  if (!tokens_ok(cfg, T)) return K3MOE_ERR_INVALID_ARGUMENT;
+  if (!x || !w_router || !routed_records || !y || (cfg->n_shared > 0 && !shared_records))
+    return K3MOE_ERR_INVALID_ARGUMENT;
+  if (!aligned16(x) || !aligned16(w_router) || (bias && !aligned16(bias)) || !aligned16(routed_records) ||
+      !aligned16(y) || (shared_records && !aligned16(shared_records)) || (topk_idx_out && !aligned16(topk_idx_out)) ||
+      (topk_w_out && !aligned16(topk_w_out)))
+    return K3MOE_ERR_INVALID_ARGUMENT;
+  if (events && (!events[0] || !events[1] || !events[2] || !events[3])) return K3MOE_ERR_INVALID_ARGUMENT;
+  if (T == 0) return K3MOE_OK;
+  Layout L;
+  if ((s = check_ws(cfg, T, ws, ws_bytes, &L)) != K3MOE_OK) return s;
+  const Cfg c = make_cfg(cfg, T);
+  const Ws w = bind(L, ws);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const long long wgb = wg_bound(cfg, T);
+  cudaError_t e = cudaSuccess;
+  if (events) e = cudaEventRecord(static_cast<cudaEvent_t>(events[0]), st);
+  if (e == cudaSuccess)
+    e = k3::launch_route(c, w, x, T, w_router, bias, topk_idx_out, topk_w_out,
+                         k3::RM_USER_OUT | k3::RM_XPREP | k3::RM_PERMUTE, st);
+  if (e == cudaSuccess && events) e = cudaEventRecord(static_cast<cudaEvent_t>(events[1]), st);
+  if (e == cudaSuccess) e = k3::launch_gateup(c, w, routed_records, shared_records, y, T, wgb, st);
+  if (e == cudaSuccess && events) e = cudaEventRecord(static_cast<cudaEvent_t>(events[2]), st);
+  if (e == cudaSuccess) e = k3::launch_down(c, w, routed_records, shared_records, y, T, wgb, st);
+  if (e == cudaSuccess && events) e = cudaEventRecord(static_cast<cudaEvent_t>(events[3]), st);
+  return cuda_status(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+k3moe_status k3moe_layer(const k3moe_config* cfg, const void* x, int64_t T, const float* w_router, const float* bias,
+                         const uint8_t* routed_records, const uint8_t* shared_records, float* y, int32_t* topk_idx_out,
+                         float* topk_w_out, void* ws, size_t ws_bytes, void* stream) {
+  return layer_impl(cfg, x, T, w_router, bias, routed_records, shared_records, y, topk_idx_out, topk_w_out, ws,
+                    ws_bytes, stream, nullptr);
+}
+
+k3moe_status k3moe_layer_timed(const k3moe_config* cfg, const void* x, int64_t T, const float* w_router,
+                               const float* bias, const uint8_t* routed_records, const uint8_t* shared_records,
+                               float* y, int32_t* topk_idx_out, float* topk_w_out, void* ws, size_t ws_bytes,
+                               void* stream, void* const* events) {
+  if (!events) return K3MOE_ERR_INVALID_ARGUMENT;
+  return layer_impl(cfg, x, T, w_router, bias, routed_records, shared_records, y, topk_idx_out, topk_w_out, ws,
+                    ws_bytes, stream, events);
+}
+
+k3moe_status k3moe_rmsnorm(const float* x, int64_t T, int32_t d, float eps, float* xn, void* stream) {
+  if (!x || !xn || T < 0 || d <= 0 || !(eps >= 0.0f)) return K3MOE_ERR_INVALID_ARGUMENT;
+  if (T == 0) return K3MOE_OK;
+  return cuda_status(k3::launch_rmsnorm(x, T, d, eps, xn, static_cast<cudaStream_t>(stream)));
+}
+
+k3moe_status k3moe_residual_add(float* x, const float* y, int64_t n, void* stream) {
+  if (!x || !y || n < 0) return K3MOE_ERR_INVALID_ARGUMENT;
+  if (n == 0) return K3MOE_OK;
+  return cuda_status(k3::launch_residual_add(x, y, n, static_cast<cudaStream_t>(stream)));
+}
+
+k3moe_status k3moe_check_device_status(void* ws, void* stream) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return K3MOE_ERR_INVALID_ARGUMENT;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int flags = 0;
+  if (cudaMemcpyAsync(&flags, ws, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess) return K3MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return K3MOE_ERR_CUDA;
+  if (flags == 0) return K3MOE_OK;
+  if (cudaMemsetAsync(ws, 0, sizeof(int), st) != cudaSuccess) return K3MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return K3MOE_ERR_CUDA;
+  return K3MOE_ERR_DEVICE_CHECK;
+}
+
+const char* k3moe_status_string(k3moe_status s) {
+  switch (s) {
+    case K3MOE_OK: return "ok";
+    case K3MOE_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case K3MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+    case K3MOE_ERR_WORKSPACE: return "workspace too small";
+    case K3MOE_ERR_CUDA: return "CUDA error";
+    case K3MOE_ERR_DEVICE_CHECK: return "bad data detected on the device";
+    case K3MOE_ERR_TIMEOUT: return "bounded wait timed out on the device";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,25 @@
+// Host-side launch interface between the C-ABI layer (k3moe_api.cu) and the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "k3moe_common.cuh"
+
+namespace k3 {
+
+// k3moe_route.cu
+enum RouteMode { RM_USER_OUT = 1, RM_XPREP = 2, RM_PERMUTE = 4 };
+cudaError_t launch_route(const Cfg& c, const Ws& ws, const void* x, long long T, const float* W, const float* bias,
+                         int* out_idx, float* out_w, int mode, cudaStream_t st);
+cudaError_t launch_prep(const Cfg& c, const Ws& ws, const void* x, long long T, const int* idx, const float* w,
+                        cudaStream_t st);
+cudaError_t launch_rmsnorm(const float* x, long long T, int d, float eps, float* out, cudaStream_t st);
+cudaError_t launch_residual_add(float* x, const float* y, long long n, cudaStream_t st);
+
+// k3moe_ffn.cu
+cudaError_t launch_gateup(const Cfg& c, const Ws& ws, const uint8_t* routed, const uint8_t* shared, float* y,
+                          long long T, long long wg_max, cudaStream_t st);
+cudaError_t launch_down(const Cfg& c, const Ws& ws, const uint8_t* routed, const uint8_t* shared, float* y,
+                        long long T, long long wg_max, cudaStream_t st);
+
+}  // namespace k3

@@ -45,7 +45,9 @@ static void fill_codes(uint8_t* dst, int64_t n, uint64_t key) {
     int64_t i = 0;
     for (; i + 8 <= n; i += 8) {
         uint64_t w = k3s_value(key, (uint64_t)(i / 8));
-        for (int b = 0; b < 8; ++b) dst[i + b] = (uint8_t)(w >> (8 * b));
+        uint8_t le[8];
+        for (int b = 0; b < 8; ++b) le[b] = (uint8_t)(w >> (8 * b)); /* byte b = bits 8b..8b+7 */
+        memcpy(dst + i, le, 8);
     }
     if (i < n) {
         uint64_t w = k3s_value(key, (uint64_t)(i / 8));

@@ -1,0 +1,91 @@
+"""The C ABI: libk3moe.so loads, exports every function include/k3moe.h declares, and rejects invalid
+arguments on the host before any CUDA call (CPU only, no compute)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mxfp4_routed_expert_k3moe_gb300 as k3
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "k3moe.h")).read()
+    return sorted(set(re.findall(r"K3MOE_API\s+[\w\s\*]*?\b(k3moe_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_calls():
+    names = declared_functions()
+    for n in ["k3moe_route", "k3moe_expert_ffn", "k3moe_layer", "k3moe_workspace_bytes", "k3moe_check_device_status"]:
+        assert n in names
+    assert sorted(names) == sorted(k3.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = k3.load()
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+
+
+K3CFG = dict(d_model=7168, d_ff=1536, n_routed=896, top_k=16, n_shared=2)
+
+
+def test_record_and_workspace_sizes():
+    cfg = k3.Config.make(**K3CFG)
+    assert k3.record_bytes(cfg) == 17547264
+    assert cfg.record_stride == 17547264  # already a multiple of 4096
+    w1, w64 = k3.workspace_bytes(cfg, 1), k3.workspace_bytes(cfg, 64)
+    assert 0 < w1 < w64
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("d_model", 100, k3.ERR_INVALID_ARGUMENT),
+    ("d_ff", 0, k3.ERR_INVALID_ARGUMENT),
+    ("top_k", 0, k3.ERR_INVALID_ARGUMENT),
+    ("top_k", 33, k3.ERR_INVALID_ARGUMENT),
+    ("n_routed", 5000, k3.ERR_INVALID_ARGUMENT),
+    ("n_shared", -1, k3.ERR_INVALID_ARGUMENT),
+    ("record_stride", 17547264 - 256, k3.ERR_INVALID_ARGUMENT),
+    ("record_stride", 17547264 + 8, k3.ERR_INVALID_ARGUMENT),
+    ("x_dtype", 7, k3.ERR_INVALID_ARGUMENT),
+    ("score_func", k3.SCORE_SIGMOID_BIAS, k3.ERR_UNSUPPORTED),
+    ("act_mode", k3.ACT_MXFP4, k3.ERR_UNSUPPORTED),
+])
+def test_invalid_config_rejected_on_host(field, value, code):
+    cfg = k3.Config.make(**K3CFG)
+    setattr(cfg, field, value)
+    lib = k3.load()
+    fake = ctypes.c_void_p(1 << 20)  # never dereferenced: validation fails first
+    rc = lib.k3moe_layer(ctypes.byref(cfg), fake, 1, fake, None, fake, fake, fake, None, None, fake, 1 << 30, None)
+    assert rc == code
+
+
+def test_invalid_pointers_rejected_on_host():
+    cfg = k3.Config.make(**K3CFG)
+    lib = k3.load()
+    a = ctypes.c_void_p(1 << 20)
+    mis = ctypes.c_void_p((1 << 20) + 8)
+    big = 1 << 34
+    assert lib.k3moe_layer(ctypes.byref(cfg), None, 1, a, None, a, a, a, None, None, a, big, None) == 1
+    assert lib.k3moe_layer(ctypes.byref(cfg), mis, 1, a, None, a, a, a, None, None, a, big, None) == 1
+    assert lib.k3moe_layer(ctypes.byref(cfg), a, -1, a, None, a, a, a, None, None, a, big, None) == 1
+    assert lib.k3moe_route(ctypes.byref(cfg), a, 1, a, None, None, a, a, big, None) == 1
+    assert lib.k3moe_expert_ffn(ctypes.byref(cfg), a, 1, a, a, a, None, a, a, big, None) == 1  # shared missing
+    ws_mis = ctypes.c_void_p((1 << 20) + 16)
+    assert lib.k3moe_layer(ctypes.byref(cfg), a, 1, a, None, a, a, a, None, None, ws_mis, big, None) == 1
+    assert lib.k3moe_layer(ctypes.byref(cfg), a, 4, a, None, a, a, a, None, None, a, 1024, None) == k3.ERR_WORKSPACE
+
+
+def test_zero_tokens_launches_nothing():
+    cfg = k3.Config.make(**K3CFG)
+    lib = k3.load()
+    a = ctypes.c_void_p(1 << 20)
+    assert lib.k3moe_layer(ctypes.byref(cfg), a, 0, a, None, a, a, a, None, None, a, 0, None) == k3.OK
+
+
+def test_status_strings():
+    for code in range(7):
+        assert k3.status_string(code)
+    assert k3.status_string(99) == "unknown status"

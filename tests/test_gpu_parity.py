@@ -1,0 +1,246 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle on the same seeded inputs.
+
+Bars: expert indices exact except where the oracle's k-th and (k+1)-th logits differ by < 1e-5;
+outputs within max|y_gpu - y_ref| / max|y_ref| <= 2e-3 (fp32 accumulation against fp64).
+"""
+import numpy as np
+import pytest
+
+import synth
+from harness import REL_TOL, DeviceLayer, gate_err, index_parity, rel_err
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():  # pragma: no cover - CPU machine
+    pytest.skip("needs a GPU", allow_module_level=True)
+
+import mxfp4_routed_expert_k3moe_gb300 as k3  # noqa: E402
+
+MID = synth.LayerShape(d_model=512, d_ff=256, n_routed=64, top_k=6, n_shared=2)
+
+
+def run_layer(L: DeviceLayer, xd, T, ws=None):
+    sh = L.shape
+    y = torch.empty((T, sh.d_model), dtype=torch.float32, device="cuda")
+    idx = torch.empty((T, sh.top_k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, sh.top_k), dtype=torch.float32, device="cuda")
+    if ws is None:
+        ws = torch.zeros(k3.workspace_bytes(L.cfg, max(T, 1)), dtype=torch.uint8, device="cuda")
+    k3.layer(L.cfg, xd, T, L.W, L.bias, L.routed, L.shared, y, ws, idx, w)
+    assert k3.check_device_status(ws) == k3.OK
+    torch.cuda.synchronize()
+    return y.cpu().numpy(), idx.cpu().numpy(), w.cpu().numpy()
+
+
+def check_layer(L: DeviceLayer, T: int, sample=None, batch=0):
+    xh, xd = L.tokens(T, batch)
+    y, idx, w = run_layer(L, xd, T)
+    rows = np.arange(T) if sample is None else np.asarray(sample)
+    y_ref, idx_ref, w_ref, logits_ref = L.oracle(xh, rows)
+    ok, near = index_parity(idx[rows], idx_ref, logits_ref, L.shape.top_k)
+    assert ok, "top-k indices differ from the oracle beyond the near-tie rule"
+    keep = [i for i in range(len(rows)) if i not in near]
+    assert gate_err(idx[rows], w[rows], idx_ref, w_ref) < 1e-5
+    err = rel_err(y[rows][keep], y_ref[keep])
+    assert err <= REL_TOL, err
+    return err
+
+
+# ------------------------------------------------------------------ generator
+
+
+def test_device_generator_matches_host():
+    sh = synth.TINY
+    L = DeviceLayer(sh, seed=0)
+    dev = L.routed.cpu().numpy().reshape(sh.n_routed, L.stride)
+    host = synth.records_host(sh, 0, 0, range(sh.n_routed), L.stride)
+    assert np.array_equal(dev, host)
+    shd = L.shared.cpu().numpy().reshape(-1, L.stride)[: sh.n_shared]
+    assert np.array_equal(shd, synth.records_host(sh, 0, 0, [sh.n_routed], L.stride))
+
+
+@pytest.fixture(scope="module")
+def k3_decode_b1():
+    return DeviceLayer(synth.K3, seed=1)
+
+
+@pytest.fixture(scope="module")
+def k3_decode_b64():
+    return DeviceLayer(synth.K3, seed=2, zipf_s=1.1)
+
+
+def test_device_generator_matches_host_k3(k3_decode_b1):
+    L = k3_decode_b1
+    for e in (0, 517, 895):
+        dev = L.routed[e * L.stride:(e + 1) * L.stride].cpu().numpy()
+        assert np.array_equal(dev, synth.records_host(L.shape, 1, 0, [e], L.stride)[0])
+
+
+# ------------------------------------------------------------------ layer parity
+
+
+def test_layer_tiny_f32():
+    L = DeviceLayer(synth.TINY, seed=0, x_dtype="f32")
+    check_layer(L, 8)
+
+
+@pytest.mark.parametrize("x_dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("T", [1, 2, 5, 37])
+def test_layer_mid_ragged(x_dtype, T):
+    L = DeviceLayer(MID, seed=7, x_dtype=x_dtype)
+    check_layer(L, T)
+
+
+def test_layer_mid_zipf_skew():
+    """Skewed routing: popular experts get many tokens (work groups split, several passes)."""
+    L = DeviceLayer(MID, seed=8, zipf_s=3.0)
+    check_layer(L, 45)
+
+
+def test_layer_all_experts_selected_no_shared():
+    sh = synth.LayerShape(d_model=256, d_ff=128, n_routed=8, top_k=8, n_shared=0)
+    L = DeviceLayer(sh, seed=9)
+    check_layer(L, 11)
+
+
+def test_layer_decode_b1_full_size(k3_decode_b1):
+    err = check_layer(k3_decode_b1, 1)
+    assert err < 1e-4
+
+
+def test_layer_decode_b64_zipf_full_size(k3_decode_b64):
+    check_layer(k3_decode_b64, 64, sample=list(range(0, 64, 4)))
+
+
+def test_layer_prefill_4096_sampled():
+    L = DeviceLayer(synth.K3, seed=3)
+    check_layer(L, 4096, sample=[0, 1, 777, 2048, 4095])
+
+
+# ------------------------------------------------------------------ separate entry points
+
+
+def test_route_only():
+    L = DeviceLayer(MID, seed=10, zipf_s=1.1)
+    T = 29
+    xh, xd = L.tokens(T)
+    idx = torch.empty((T, MID.top_k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, MID.top_k), dtype=torch.float32, device="cuda")
+    ws = torch.zeros(k3.workspace_bytes(L.cfg, T), dtype=torch.uint8, device="cuda")
+    k3.route(L.cfg, xd, T, L.W, L.bias, idx, w, ws)
+    torch.cuda.synchronize()
+    _, idx_ref, w_ref, logits_ref = L.oracle(xh)
+    ok, near = index_parity(idx.cpu().numpy(), idx_ref, logits_ref, MID.top_k)
+    assert ok
+    wn = w.cpu().numpy()
+    assert np.allclose(wn.sum(axis=1), 1.0, atol=1e-6)
+    assert gate_err(idx.cpu().numpy(), wn, idx_ref, w_ref) < 1e-6
+
+
+def test_expert_ffn_given_routing():
+    L = DeviceLayer(MID, seed=11, x_dtype="f32")
+    T = 13
+    xh, xd = L.tokens(T)
+    rng = np.random.default_rng(0)
+    idx = np.stack([rng.choice(MID.n_routed, MID.top_k, replace=False) for _ in range(T)]).astype(np.int32)
+    idx[3, :] = np.arange(MID.top_k)  # overlapping expert sets
+    w = rng.random((T, MID.top_k)).astype(np.float32)
+    y = torch.empty((T, MID.d_model), dtype=torch.float32, device="cuda")
+    ws = torch.zeros(k3.workspace_bytes(L.cfg, T), dtype=torch.uint8, device="cuda")
+    k3.expert_ffn(L.cfg, xd, T, torch.from_numpy(idx).cuda(), torch.from_numpy(w).cuda(), L.routed, L.shared, y, ws)
+    assert k3.check_device_status(ws) == k3.OK
+    y_ref = L.oracle_ffn(xh, idx, w)
+    assert rel_err(y.cpu().numpy(), y_ref) <= REL_TOL
+
+
+def test_zero_tokens_is_noop():
+    L = DeviceLayer(MID, seed=12)
+    y = torch.full((1, MID.d_model), 7.0, device="cuda")
+    ws = torch.zeros(k3.workspace_bytes(L.cfg, 1), dtype=torch.uint8, device="cuda")
+    _, xd = L.tokens(1)
+    k3.layer(L.cfg, xd, 0, L.W, L.bias, L.routed, L.shared, y, ws)
+    torch.cuda.synchronize()
+    assert torch.all(y == 7.0)
+
+
+def test_repeatable_and_batch_invariant():
+    L = DeviceLayer(MID, seed=13)
+    xh, xd = L.tokens(9)
+    y1, i1, _ = run_layer(L, xd, 9)
+    y2, i2, _ = run_layer(L, xd, 9)
+    assert np.array_equal(i1, i2) and np.array_equal(y1, y2)
+    y3, i3, _ = run_layer(L, xd[4:5].contiguous(), 1)
+    assert np.array_equal(i3[0], i1[4])
+    assert rel_err(y3[0], y1[4]) < 1e-6
+
+
+# ------------------------------------------------------------------ device-side data checks
+
+
+def test_bad_expert_id_sets_device_status():
+    L = DeviceLayer(MID, seed=14)
+    T = 3
+    _, xd = L.tokens(T)
+    idx = torch.tensor([[0, 1, 2, 3, 4, 5], [6, 7, 8, 9, 10, 999], [1, 2, 3, 4, 5, 6]], dtype=torch.int32,
+                       device="cuda")
+    w = torch.full((T, MID.top_k), 1.0 / MID.top_k, device="cuda")
+    y = torch.empty((T, MID.d_model), device="cuda")
+    ws = torch.zeros(k3.workspace_bytes(L.cfg, T), dtype=torch.uint8, device="cuda")
+    k3.expert_ffn(L.cfg, xd, T, idx, w, L.routed, L.shared, y, ws)
+    assert k3.check_device_status(ws) == k3.ERR_DEVICE_CHECK
+    assert k3.check_device_status(ws) == k3.OK  # the check clears the word
+
+
+def test_nan_scale_byte_sets_device_status():
+    L = DeviceLayer(MID, seed=15)
+    T = 2
+    xh, xd = L.tokens(T)
+    _, idx_ref, _, _ = L.oracle(xh)
+    e = int(idx_ref[0, 0])
+    nc = MID.d_model * MID.d_ff // 2
+    L.routed[e * L.stride + nc + 3] = 255  # one gate scale byte of a selected expert
+    y = torch.empty((T, MID.d_model), device="cuda")
+    ws = torch.zeros(k3.workspace_bytes(L.cfg, T), dtype=torch.uint8, device="cuda")
+    k3.layer(L.cfg, xd, T, L.W, L.bias, L.routed, L.shared, y, ws)
+    assert k3.check_device_status(ws) == k3.ERR_DEVICE_CHECK
+
+
+def test_workspace_too_small_is_rejected():
+    L = DeviceLayer(MID, seed=16)
+    _, xd = L.tokens(4)
+    y = torch.empty((4, MID.d_model), device="cuda")
+    ws = torch.zeros(k3.workspace_bytes(L.cfg, 2), dtype=torch.uint8, device="cuda")
+    with pytest.raises(k3.K3moeError) as ei:
+        k3.layer(L.cfg, xd, 4, L.W, L.bias, L.routed, L.shared, y, ws)
+    assert ei.value.code == k3.ERR_WORKSPACE
+
+
+# ------------------------------------------------------------------ stack harness (pre-norm residual)
+
+
+def test_stack_prenorm_residual_teacher_forced():
+    """x_{l+1} = x_l + Layer_l(RMSNorm(x_l)), each layer checked on the GPU's own layer input."""
+    import oracle
+    sh = MID
+    T = 7
+    layers = [DeviceLayer(sh, seed=40 + l, layer=l, zipf_s=1.1, x_dtype="f32") for l in range(4)]
+    x0 = synth.tokens(sh, 40, T, "f32")
+    x = torch.from_numpy(x0).cuda()
+    xn = torch.empty_like(x)
+    y = torch.empty_like(x)
+    ws = torch.zeros(k3.workspace_bytes(layers[0].cfg, T), dtype=torch.uint8, device="cuda")
+    for L in layers:
+        k3.rmsnorm(x, T, sh.d_model, 1e-6, xn)
+        torch.cuda.synchronize()
+        xin = x.cpu().numpy().astype(np.float64)
+        xn_h = xn.cpu().numpy()
+        assert np.allclose(xn_h, oracle.rmsnorm(xin, 1e-6), rtol=2e-6, atol=1e-6)
+        k3.layer(L.cfg, xn, T, L.W, L.bias, L.routed, L.shared, y, ws)
+        torch.cuda.synchronize()
+        y_ref, idx_ref, _, logits_ref = L.oracle(xn_h)
+        err = rel_err(y.cpu().numpy(), y_ref)
+        assert err <= REL_TOL, err
+        k3.residual_add(x, y, T * sh.d_model)
+    torch.cuda.synchronize()
+    assert torch.isfinite(x).all()
