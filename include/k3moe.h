@@ -68,6 +68,7 @@ typedef enum {
 
 /* Router score function. Only the softmax score is implemented. */
 enum { K3MOE_SCORE_SOFTMAX = 0, K3MOE_SCORE_SIGMOID_BIAS = 1 };
+/* Legal but not implemented: d_model > 25600 (the router stages whole rows in shared memory). */
 /* Activation handling in the expert FFN. Only the exact mode is implemented: activations keep
    their input precision (bf16 exactly, fp32 to ~2^-22) and h keeps ~2^-22 relative precision. */
 enum { K3MOE_ACT_EXACT = 0, K3MOE_ACT_MXFP4 = 1 };

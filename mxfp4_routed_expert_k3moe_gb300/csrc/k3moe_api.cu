@@ -14,6 +14,8 @@ using k3::Ws;
 constexpr long long kMaxE = 4096;
 constexpr long long kMaxK = 32;
 constexpr long long kMaxS = 8;
+constexpr int kMaxDModel = 25600;
+constexpr long long kGateUpParts = 4;  // gate/up reduction axis split across warps
 
 size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -36,6 +38,7 @@ k3moe_status validate(const k3moe_config* c) {
   if (c->record_stride < record_bytes_of(c) || c->record_stride % 256) return K3MOE_ERR_INVALID_ARGUMENT;
   if ((long long)c->d_model * c->d_ff > (1LL << 40)) return K3MOE_ERR_INVALID_ARGUMENT;
   if (c->score_func != K3MOE_SCORE_SOFTMAX || c->act_mode != K3MOE_ACT_EXACT) return K3MOE_ERR_UNSUPPORTED;
+  if (c->d_model > kMaxDModel) return K3MOE_ERR_UNSUPPORTED;  // router rows are staged in shared memory
   return K3MOE_OK;
 }
 
@@ -52,7 +55,7 @@ long long wg_bound(const k3moe_config* c, long long T) {
 
 struct Layout {
   size_t ctrl, logits, topk_idx, topk_w, counts, cursor, offsets, wgoff, perm_tok, perm_w, inv, wgs, xact, xexp, hact,
-      hexp, part, tilecnt, total;
+      hexp, part, tilecnt, gupart, gucnt, rtcnt, total;
 };
 
 Layout make_layout(const k3moe_config* c, long long T) {
@@ -77,11 +80,14 @@ Layout make_layout(const k3moe_config* c, long long T) {
   take(L.inv, sizeof(int) * T * k);
   take(L.wgs, sizeof(k3::WorkGroup) * wg_bound(c, T));
   take(L.xact, sizeof(__half) * T * 2 * d);
-  take(L.xexp, (size_t)(T * (d / 32)));
+  take(L.xexp, (size_t)T);
   take(L.hact, sizeof(__half) * P * 2 * f);
   take(L.hexp, (size_t)(P * (f / 32)));
   take(L.part, sizeof(float) * P * d);
   take(L.tilecnt, sizeof(int) * (d / 32));
+  take(L.gupart, sizeof(float) * P * kGateUpParts * 2 * f);
+  take(L.gucnt, sizeof(int) * wg_bound(c, T) * (f / 32));
+  take(L.rtcnt, sizeof(int) * ((T + 7) / 8));
   L.total = o;
   return L;
 }
@@ -107,6 +113,9 @@ Ws bind(const Layout& L, void* base) {
   w.hexp = reinterpret_cast<int8_t*>(b + L.hexp);
   w.part = reinterpret_cast<float*>(b + L.part);
   w.tilecnt = reinterpret_cast<int*>(b + L.tilecnt);
+  w.gupart = reinterpret_cast<float*>(b + L.gupart);
+  w.gucnt = reinterpret_cast<int*>(b + L.gucnt);
+  w.rtcnt = reinterpret_cast<int*>(b + L.rtcnt);
   return w;
 }
 
@@ -120,6 +129,7 @@ Cfg make_cfg(const k3moe_config* c, long long T) {
   k.x_f32 = c->x_dtype == K3MOE_X_F32 ? 1 : 0;
   k.xplanes = k.x_f32 ? 2 : 1;
   k.wgt = T == 1 ? 1 : 4;
+  k.ks = (int)kGateUpParts;
   k.stride = c->record_stride;
   return k;
 }

@@ -13,13 +13,14 @@ struct Cfg {
   int xplanes;        // fp16 planes per activation row: 1 (bf16 x is exact in one plane) or 2 (fp32 x: hi + lo)
   int x_f32;          // 1 if x is fp32, 0 if bf16
   int wgt;            // max tokens per work group
+  int ks;             // parts of the gate/up reduction axis (d) processed by separate warps
   long long stride;   // bytes between expert records
 };
 
 // Control block at the start of the workspace (int32 slots).
 enum CtrlSlot {
   CTRL_STATUS = 0,       // status bits, read and cleared by k3moe_check_device_status
-  CTRL_ROUTER_DONE = 1,  // CTAs of the router kernel that finished (last one does top-k)
+  CTRL_ROUTER_DONE = 1,  // router token tiles whose top-k is done (the last builds the permutation)
   CTRL_NWG = 2,          // number of work groups built by the permutation
   CTRL_WORDS = 64
 };
@@ -45,11 +46,14 @@ struct Ws {
   int* inv;           // [T*k] position of routed slot (t, i), -1 if the slot was rejected
   WorkGroup* wgs;     // [WGmax]
   __half* xact;       // [T, xplanes, d] scaled fp16 planes of x
-  int8_t* xexp;       // [T, d/32] per-block power-of-two exponent c: plane values = x * 2^c
+  int8_t* xexp;       // [T] per-token power-of-two exponent c: plane values = x * 2^c
   __half* hact;       // [P, 2, f] scaled fp16 hi/lo planes of h
   int8_t* hexp;       // [P, f/32]
   float* part;        // [P, d] gate-weighted down-projection outputs per position
   int* tilecnt;       // [d/32] work groups finished per 32-row block of the down projection
+  float* gupart;      // [P, ks, 2, f] partial gate/up sums of the ks reduction-axis parts
+  int* gucnt;         // [WGmax * f/32] parts finished per (work group, 32-row block)
+  int* rtcnt;         // [ceil(T/8)] router CTAs finished per token tile
 };
 
 // ----------------------------------------------------------------------------- small helpers
@@ -106,7 +110,7 @@ __device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t& o0, uint32
 // D = A(16x16, row) * B(16x8, col) + C, fp16 inputs, fp32 accumulate (warp-wide).
 __device__ __forceinline__ void mma_f16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                               uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};\n"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])

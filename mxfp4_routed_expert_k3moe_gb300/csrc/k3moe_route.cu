@@ -17,78 +17,188 @@ namespace k3 {
 
 namespace {
 
-constexpr int kRouteWarps = 4;  // expert rows per router CTA (one warp each)
-constexpr int kRouteTT = 8;     // tokens per router warp
 constexpr int kMaxE = 4096;
+constexpr int kRouteMaxSmem = 200 * 1024;  // router CTA: x tile + permutation scratch + candidates
 
-__device__ __forceinline__ float load_x(const void* x, int x_f32, long long idx) {
-  if (x_f32) return reinterpret_cast<const float*>(x)[idx];
-  uint32_t b = reinterpret_cast<const uint16_t*>(x)[idx];
-  return __uint_as_float(b << 16);
-}
-
-// One warp per 32-element block of x: the block's fp16 plane(s) and its exponent.
-__device__ void xprep_blocks(const Cfg& c, const Ws& ws, const void* x, long long T, long long first, long long step) {
-  const int lane = threadIdx.x & 31;
-  const int kb_per_row = c.d / 32;
-  const long long nblk = T * kb_per_row;
-  for (long long b = first; b < nblk; b += step) {
-    const long long t = b / kb_per_row;
-    const int kb = (int)(b - t * kb_per_row);
-    const float v = load_x(x, c.x_f32, t * c.d + kb * 32 + lane);
-    float a = fabsf(v);
+// Eight consecutive activations (bf16 or fp32) starting at element idx (a multiple of 8).
+__device__ __forceinline__ void load8(const void* x, int x_f32, long long idx, float (&v)[8]) {
+  if (x_f32) {
+    const float4 p = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(x) + idx);
+    const float4 q = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(x) + idx + 4);
+    v[0] = p.x; v[1] = p.y; v[2] = p.z; v[3] = p.w; v[4] = q.x; v[5] = q.y; v[6] = q.z; v[7] = q.w;
+  } else {
+    const uint4 p = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(x) + idx);
+    const uint32_t w[4] = {p.x, p.y, p.z, p.w};
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-    const int e = plane_exponent(a);
-    const float s = v * pow2i(e);
-    const __half hi = __float2half_rn(s);
-    ws.xact[(t * c.xplanes) * c.d + kb * 32 + lane] = hi;
-    if (c.xplanes == 2) ws.xact[(t * 2 + 1) * c.d + kb * 32 + lane] = __float2half_rn(s - __half2float(hi));
-    if (lane == 0) ws.xexp[t * kb_per_row + kb] = (int8_t)e;
+    for (int q = 0; q < 4; ++q) {
+      v[2 * q] = __uint_as_float(w[q] << 16);
+      v[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
+    }
   }
 }
 
-// Orderable 64-bit key: larger logit first, then lower expert id. Key 0 marks a taken entry.
+// fp16 plane(s) of eight consecutive elements j..j+7 of token t, scaled by sc (a power of two).
+__device__ __forceinline__ void convert8(const Cfg& c, const Ws& ws, const void* x, long long t, int j, float sc) {
+  float v[8];
+  load8(x, c.x_f32, t * c.d + j, v);
+  __align__(16) __half hi[8], lo[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const float s = v[q] * sc;
+    hi[q] = __float2half_rn(s);
+    lo[q] = __float2half_rn(s - __half2float(hi[q]));
+  }
+  *reinterpret_cast<uint4*>(ws.xact + (t * c.xplanes) * c.d + j) = *reinterpret_cast<const uint4*>(hi);
+  if (c.xplanes == 2) *reinterpret_cast<uint4*>(ws.xact + (t * 2 + 1) * c.d + j) = *reinterpret_cast<const uint4*>(lo);
+}
+
+// Same, reading the eight elements from a token row staged in shared memory.
+__device__ __forceinline__ void convert8_shared(const Cfg& c, const Ws& ws, const uint8_t* xrow, long long t, int j,
+                                                float sc) {
+  float v[8];
+  if (c.x_f32) {
+    const float4 p = *reinterpret_cast<const float4*>(xrow + 4 * j);
+    const float4 q = *reinterpret_cast<const float4*>(xrow + 4 * j + 16);
+    v[0] = p.x; v[1] = p.y; v[2] = p.z; v[3] = p.w; v[4] = q.x; v[5] = q.y; v[6] = q.z; v[7] = q.w;
+  } else {
+    const uint4 p = *reinterpret_cast<const uint4*>(xrow + 2 * j);
+    const uint32_t w[4] = {p.x, p.y, p.z, p.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      v[2 * q] = __uint_as_float(w[q] << 16);
+      v[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
+    }
+  }
+  __align__(16) __half hi[8], lo[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const float s = v[q] * sc;
+    hi[q] = __float2half_rn(s);
+    lo[q] = __float2half_rn(s - __half2float(hi[q]));
+  }
+  *reinterpret_cast<uint4*>(ws.xact + (t * c.xplanes) * c.d + j) = *reinterpret_cast<const uint4*>(hi);
+  if (c.xplanes == 2) *reinterpret_cast<uint4*>(ws.xact + (t * 2 + 1) * c.d + j) = *reinterpret_cast<const uint4*>(lo);
+}
+
+// One warp per token: the fp16 plane(s) of x scaled by one power of two per token, chosen so that
+// max|x_t| * 2^c lies in [2^14, 2^15). A bf16 token is exact in one plane; an fp32 token keeps
+// ~22 significant bits in the hi + lo planes.
+__device__ void xprep_rows(const Cfg& c, const Ws& ws, const void* x, long long T, long long first, long long step) {
+  const int lane = threadIdx.x & 31;
+  for (long long t = first; t < T; t += step) {
+    float a = 0.0f;
+    for (int j = lane * 8; j < c.d; j += 256) {
+      float v[8];
+      load8(x, c.x_f32, t * c.d + j, v);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) a = fmaxf(a, fabsf(v[q]));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    const int e = plane_exponent(a);
+    const float sc = pow2i(e);
+    for (int j = lane * 8; j < c.d; j += 256) convert8(c, ws, x, t, j, sc);
+    if (lane == 0) ws.xexp[t] = (int8_t)e;
+  }
+}
+
+// Orderable 64-bit key: larger logit first, then lower expert id. Key 0 marks an empty entry.
 __device__ __forceinline__ unsigned long long topk_key(float l, int e) {
   uint32_t u = __float_as_uint(l);
   uint32_t o = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
   return ((unsigned long long)o << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)e);
 }
+__device__ __forceinline__ int key_expert(unsigned long long key) {
+  return (int)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
+}
 
-// One warp: top-k of one token's logits and the renormalised softmax gates.
-__device__ void topk_token(int E, int k, const float* logits_t, unsigned long long* keys, int* idx_out,
-                           float* w_out, int* idx_user, float* w_user) {
+template <int R>
+__device__ __forceinline__ unsigned long long local_max(const unsigned long long (&key)[R]) {
+  unsigned long long t[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) t[r] = key[r];
+#pragma unroll
+  for (int h = R / 2; h >= 1; h /= 2)
+#pragma unroll
+    for (int r = 0; r < h; ++r) t[r] = t[r + h] > t[r] ? t[r + h] : t[r];
+  return t[0];
+}
+
+// One warp: the k largest keys held in registers (R per lane), in descending order; lane r < k
+// returns the r-th (0 if fewer than r+1 keys exist). Each round takes the warp-wide maximum of the
+// lanes' cached local maxima; only the lane that owned it clears the key and recomputes its maximum.
+template <int R>
+__device__ unsigned long long warp_topk(unsigned long long (&key)[R], int k) {
   const int lane = threadIdx.x & 31;
-  for (int e = lane; e < E; e += 32) keys[e] = topk_key(__ldcg(&logits_t[e]), e);
-  __syncwarp();
-  int my_e = 0;
+  unsigned long long lm = local_max<R>(key);
+  unsigned long long mine = 0;
   for (int r = 0; r < k; ++r) {
-    unsigned long long best = 0;
-    for (int e = lane; e < E; e += 32) best = keys[e] > best ? keys[e] : best;
+    unsigned long long best = lm;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-      unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
+      const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
       best = other > best ? other : best;
     }
-    const int e_best = (int)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFull));
-    __syncwarp();
-    if (lane == (e_best & 31)) keys[e_best] = 0ull;
-    if (lane == r) my_e = e_best;
-    __syncwarp();
-  }
-  const float my_l = (lane < k) ? __ldcg(&logits_t[my_e]) : 0.0f;
-  const float lmax = __shfl_sync(0xffffffffu, my_l, 0);
-  const float ex = (lane < k) ? expf(my_l - lmax) : 0.0f;
-  float sum = ex;
+    if (lane == r) mine = best;
+    if (best != 0ull && lm == best) {  // keys are unique: exactly one owner
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-  if (lane < k) {
-    const float w = ex / sum;
-    idx_out[lane] = my_e;
-    w_out[lane] = w;
-    if (idx_user) idx_user[lane] = my_e;
-    if (w_user) w_user[lane] = w;
+      for (int q = 0; q < R; ++q) key[q] = (key[q] == best) ? 0ull : key[q];
+      lm = local_max<R>(key);
+    }
   }
+  return mine;
+}
+
+// Stage 1 of the block top-k: warp w takes experts lane + 32 (w + nw q), q < R.
+template <int R>
+__device__ __forceinline__ unsigned long long topk_stage1(int E, int k, const float* logits_t) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  unsigned long long key[R];
+#pragma unroll
+  for (int q = 0; q < R; ++q) {
+    const int e = lane + 32 * (warp + nw * q);
+    key[q] = (e < E) ? topk_key(__ldcg(&logits_t[e]), e) : 0ull;
+  }
+  return warp_topk<R>(key, k);
+}
+
+// Top-k and renormalised softmax gates of one token, by the whole CTA (2 to 8 warps): every warp
+// selects the k best of its share of the experts, then warp 0 selects the k best of those
+// candidates. `cand` is shared memory for 32 keys per warp. Ends with __syncthreads.
+__device__ void topk_block(int E, int k, const float* logits_t, unsigned long long* cand, int* idx_out, float* w_out,
+                           int* idx_user, float* w_user) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int per_lane = (E + 32 * nw - 1) / (32 * nw);
+  unsigned long long m;
+  if (per_lane <= 1) m = topk_stage1<1>(E, k, logits_t);
+  else if (per_lane <= 2) m = topk_stage1<2>(E, k, logits_t);
+  else if (per_lane <= 4) m = topk_stage1<4>(E, k, logits_t);
+  else if (per_lane <= 8) m = topk_stage1<8>(E, k, logits_t);
+  else if (per_lane <= 16) m = topk_stage1<16>(E, k, logits_t);
+  else m = topk_stage1<32>(E, k, logits_t);
+  cand[warp * 32 + lane] = (lane < k) ? m : 0ull;
+  __syncthreads();
+  if (warp == 0) {
+    unsigned long long key[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) key[q] = (q < nw) ? cand[q * 32 + lane] : 0ull;
+    const unsigned long long best = warp_topk<8>(key, k);
+    const int my_e = key_expert(best);
+    const float my_l = (lane < k) ? __ldcg(&logits_t[my_e]) : 0.0f;
+    const float lmax = __shfl_sync(0xffffffffu, my_l, 0);
+    const float ex = (lane < k) ? expf(my_l - lmax) : 0.0f;
+    float sum = ex;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (lane < k) {
+      const float w = ex / sum;
+      idx_out[lane] = my_e;
+      w_out[lane] = w;
+      if (idx_user) idx_user[lane] = my_e;
+      if (w_user) w_user[lane] = w;
+    }
+  }
+  __syncthreads();
 }
 
 // Exclusive block-wide scan of two int arrays of length n (in place into out0/out1, total at [n]).
@@ -128,39 +238,43 @@ __device__ void block_scan2(const int* in0, const int* in1, int* out0, int* out1
 }
 
 // One CTA: positions, inverse map and work groups for T tokens' routed slots plus the shared experts.
-__device__ void build_permutation(const Cfg& c, const Ws& ws, long long T, const int* idx, const float* w) {
+// `sm` is shared-memory scratch of 4E + 2 ints (counts, cursors, offsets, work-group offsets).
+__device__ void build_permutation(const Cfg& c, const Ws& ws, long long T, const int* idx, const float* w, int* sm) {
   __shared__ int s_tmp[64];
   const int tid = threadIdx.x, nt = blockDim.x;
   const int E = c.E, k = c.k, W = c.wgt;
+  int* counts = sm;
+  int* cursor = sm + E;
+  int* offsets = sm + 2 * E;      // E + 1
+  int* wgoff = sm + 3 * E + 1;    // E + 1
   const long long nslot = T * k;
-  for (int e = tid; e < E; e += nt) { ws.counts[e] = 0; ws.cursor[e] = 0; }
+  for (int e = tid; e < E; e += nt) { counts[e] = 0; cursor[e] = 0; }
   __syncthreads();
   for (long long s = tid; s < nslot; s += nt) {
     const int e = idx[s];
     if (e < 0 || e >= E) set_status(ws.ctrl, ST_BAD_EXPERT);
-    else atomicAdd(&ws.counts[e], 1);
+    else atomicAdd(&counts[e], 1);
   }
   __syncthreads();
-  // wg counts per expert go into `cursor` temporarily, then the scans
-  for (int e = tid; e < E; e += nt) ws.cursor[e] = (ws.counts[e] + W - 1) / W;
+  for (int e = tid; e < E; e += nt) cursor[e] = (counts[e] + W - 1) / W;  // work groups per expert
   __syncthreads();
-  block_scan2(ws.counts, ws.cursor, ws.offsets, ws.wgoff, E, s_tmp);
-  for (int e = tid; e < E; e += nt) ws.cursor[e] = 0;
+  block_scan2(counts, cursor, offsets, wgoff, E, s_tmp);
+  for (int e = tid; e < E; e += nt) cursor[e] = 0;
   __syncthreads();
   for (long long s = tid; s < nslot; s += nt) {
     const int e = idx[s];
     if (e < 0 || e >= E) { ws.inv[s] = -1; continue; }
-    const int pos = ws.offsets[e] + atomicAdd(&ws.cursor[e], 1);
+    const int pos = offsets[e] + atomicAdd(&cursor[e], 1);
     ws.perm_tok[pos] = (int)(s / k);
     ws.perm_w[pos] = w[s];
     ws.inv[s] = pos;
   }
   for (int e = tid; e < E; e += nt) {
-    const int n = ws.counts[e];
-    int g = ws.wgoff[e];
-    for (int p = 0; p < n; p += W, ++g) ws.wgs[g] = WorkGroup{e, ws.offsets[e] + p, min(W, n - p), 0};
+    const int n = counts[e];
+    int g = wgoff[e];
+    for (int p = 0; p < n; p += W, ++g) ws.wgs[g] = WorkGroup{e, offsets[e] + p, min(W, n - p), 0};
   }
-  const int n_routed_wg = ws.wgoff[E];
+  const int n_routed_wg = wgoff[E];
   const long long pr = nslot;  // shared positions start after all routed slots
   const int nwt = (int)((T + W - 1) / W);
   for (int q = tid; q < c.S * nwt; q += nt) {
@@ -174,6 +288,7 @@ __device__ void build_permutation(const Cfg& c, const Ws& ws, long long T, const
   }
   for (int rb = tid; rb < c.d / 32; rb += nt) ws.tilecnt[rb] = 0;
   if (tid == 0) ws.ctrl[CTRL_NWG] = n_routed_wg + c.S * nwt;
+  __syncthreads();
 }
 
 struct RouteArgs {
@@ -188,78 +303,141 @@ struct RouteArgs {
   int mode;
 };
 
-__global__ void __launch_bounds__(kRouteWarps * 32) k_route(RouteArgs a) {
-  extern __shared__ unsigned long long s_keys[];  // [kRouteWarps][E], used by the last CTA only
+// Shared-memory layout of the router CTA: [x tile | permutation scratch (aliased)][top-k candidates].
+__host__ __device__ __forceinline__ size_t route_tile_bytes(const Cfg& c, int tt) {
+  const size_t xt = (size_t)tt * c.d * (c.x_f32 ? 4 : 2);
+  const size_t perm = sizeof(int) * (4 * (size_t)c.E + 2);
+  const size_t m = xt > perm ? xt : perm;
+  return (m + 15) & ~(size_t)15;
+}
+
+template <int TT>
+__global__ void __launch_bounds__(256) k_route(RouteArgs a) {
+  extern __shared__ __align__(16) uint8_t smem[];
   __shared__ int s_last;
   const Cfg& c = a.c;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long nblocks = (long long)gridDim.x * gridDim.y;
-  const long long bid = (long long)blockIdx.y * gridDim.x + blockIdx.x;
+  const int nw = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * nw + warp;
+  const long long t0 = (long long)blockIdx.y * TT;
+  const int ntt = (int)min((long long)TT, a.T - t0);
+  const int esz = c.x_f32 ? 4 : 2;
+  const int row_bytes = c.d * esz;
+  unsigned long long* cand = reinterpret_cast<unsigned long long*>(smem + route_tile_bytes(c, TT));
 
-  if (a.mode & RM_XPREP) xprep_blocks(c, a.ws, a.x, a.T, bid * kRouteWarps + warp, nblocks * kRouteWarps);
+  // the token tile of x goes to shared memory once per CTA
+  {
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(a.x) + t0 * row_bytes;
+    const uint32_t dst = (uint32_t)__cvta_generic_to_shared(smem);
+    const int bytes = ntt * row_bytes;
+    for (int off = threadIdx.x * 16; off < bytes; off += blockDim.x * 16)
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + off), "l"(src + off) : "memory");
+    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
+  }
 
-  // logits of expert row e for up to kRouteTT tokens
-  const int e = blockIdx.x * kRouteWarps + warp;
-  const long long t0 = (long long)blockIdx.y * kRouteTT;
+  // logits of expert row e for the tile's tokens; the same pass finds max|x_t| of each token.
+  // Each segment issues all of its router-weight loads before any arithmetic.
+  constexpr int U = (TT == 1) ? 14 : 8;
   if (e < c.E) {
-    float acc[kRouteTT];
+    float acc[TT], am[TT];
 #pragma unroll
-    for (int tt = 0; tt < kRouteTT; ++tt) acc[tt] = 0.0f;
+    for (int tt = 0; tt < TT; ++tt) acc[tt] = am[tt] = 0.0f;
     const float* wrow = a.W + (long long)e * c.d;
-    const int ntt = (int)min((long long)kRouteTT, a.T - t0);
-#pragma unroll 2
-    for (int j = lane * 4; j < c.d; j += 128) {
-      const uint4 wv = ld_stream_v4(wrow + j);
-      const float w0 = __uint_as_float(wv.x), w1 = __uint_as_float(wv.y), w2 = __uint_as_float(wv.z),
-                  w3 = __uint_as_float(wv.w);
+    for (int j0 = 0; j0 < c.d; j0 += 128 * U) {
+      uint4 wv[U];
 #pragma unroll
-      for (int tt = 0; tt < kRouteTT; ++tt) {
-        if (tt < ntt) {
-          const long long xi = (t0 + tt) * c.d + j;
-          float x0, x1, x2, x3;
-          if (c.x_f32) {
-            const float4 xv = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.x) + xi);
-            x0 = xv.x; x1 = xv.y; x2 = xv.z; x3 = xv.w;
-          } else {
-            const uint2 xv = *reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(a.x) + xi);
-            x0 = __uint_as_float(xv.x << 16); x1 = __uint_as_float(xv.x & 0xFFFF0000u);
-            x2 = __uint_as_float(xv.y << 16); x3 = __uint_as_float(xv.y & 0xFFFF0000u);
+      for (int u = 0; u < U; ++u) {
+        const int j = j0 + u * 128 + lane * 4;
+        wv[u] = (j < c.d) ? ld_stream_v4(wrow + j) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int j = j0 + u * 128 + lane * 4;
+        if (j < c.d) {
+          const float w4[4] = {__uint_as_float(wv[u].x), __uint_as_float(wv[u].y), __uint_as_float(wv[u].z),
+                               __uint_as_float(wv[u].w)};
+#pragma unroll
+          for (int tt = 0; tt < TT; ++tt) {
+            if (tt < ntt) {
+              float xv[4];
+              const uint8_t* xr = smem + tt * row_bytes;
+              if (c.x_f32) {
+                const float4 q = *reinterpret_cast<const float4*>(xr + 4 * j);
+                xv[0] = q.x; xv[1] = q.y; xv[2] = q.z; xv[3] = q.w;
+              } else {
+                const uint2 q = *reinterpret_cast<const uint2*>(xr + 2 * j);
+                xv[0] = __uint_as_float(q.x << 16); xv[1] = __uint_as_float(q.x & 0xFFFF0000u);
+                xv[2] = __uint_as_float(q.y << 16); xv[3] = __uint_as_float(q.y & 0xFFFF0000u);
+              }
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                acc[tt] = fmaf(w4[q], xv[q], acc[tt]);
+                am[tt] = fmaxf(am[tt], fabsf(xv[q]));
+              }
+            }
           }
-          acc[tt] = fmaf(w0, x0, acc[tt]);
-          acc[tt] = fmaf(w1, x1, acc[tt]);
-          acc[tt] = fmaf(w2, x2, acc[tt]);
-          acc[tt] = fmaf(w3, x3, acc[tt]);
         }
       }
     }
     const float b = a.bias ? a.bias[e] : 0.0f;
 #pragma unroll
-    for (int tt = 0; tt < kRouteTT; ++tt) {
-      float v = acc[tt];
+    for (int tt = 0; tt < TT; ++tt) {
+      float v = acc[tt], m = am[tt];
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      for (int o = 16; o > 0; o >>= 1) {
+        v += __shfl_xor_sync(0xffffffffu, v, o);
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      }
+      am[tt] = m;
       if (lane == 0 && tt < ntt) a.ws.logits[(t0 + tt) * c.E + e] = v + b;
     }
+    // activation planes: warp e converts elements [256e, 256e + 256) of each token of the tile
+    if ((a.mode & RM_XPREP) && e * 256 < c.d) {
+      const int j = e * 256 + lane * 8;
+#pragma unroll
+      for (int tt = 0; tt < TT; ++tt) {
+        if (tt < ntt && j < c.d) {
+          const long long t = t0 + tt;
+          const int ex = plane_exponent(am[tt]);
+          convert8_shared(c, a.ws, smem + tt * row_bytes, t, j, pow2i(ex));
+          if (e == 0 && lane == 0) a.ws.xexp[t] = (int8_t)ex;
+        }
+      }
+    }
+    if (lane == 0) __threadfence();
   }
 
-  // the last CTA to finish selects the top-k of every token and builds the permutation
+  // the last CTA of each token tile selects the top-k of its tokens ...
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
-    const int prev = atomicAdd(&a.ws.ctrl[CTRL_ROUTER_DONE], 1);
-    s_last = (prev == (int)nblocks - 1);
+    const int prev = atomicAdd(&a.ws.rtcnt[blockIdx.y], 1);
+    s_last = (prev == (int)gridDim.x - 1);
   }
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  for (long long t = warp; t < a.T; t += kRouteWarps) {
-    topk_token(c.E, c.k, a.ws.logits + t * c.E, s_keys + (long long)warp * c.E, a.ws.topk_idx + t * c.k,
-               a.ws.topk_w + t * c.k, (a.mode & RM_USER_OUT) && a.out_idx ? a.out_idx + t * c.k : nullptr,
+  for (int tt = 0; tt < ntt; ++tt) {
+    const long long t = t0 + tt;
+    topk_block(c.E, c.k, a.ws.logits + t * c.E, cand, a.ws.topk_idx + t * c.k, a.ws.topk_w + t * c.k,
+               (a.mode & RM_USER_OUT) && a.out_idx ? a.out_idx + t * c.k : nullptr,
                (a.mode & RM_USER_OUT) && a.out_w ? a.out_w + t * c.k : nullptr);
   }
-  __syncthreads();
-  if (a.mode & RM_PERMUTE) build_permutation(c, a.ws, a.T, a.ws.topk_idx, a.ws.topk_w);
-  if (threadIdx.x == 0) a.ws.ctrl[CTRL_ROUTER_DONE] = 0;
+  if (threadIdx.x == 0) a.ws.rtcnt[blockIdx.y] = 0;
+  // ... and the last token tile to finish builds the permutation (directly when there is one tile)
+  if (gridDim.y > 1) {
+    if (threadIdx.x < 32) __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const int prev = atomicAdd(&a.ws.ctrl[CTRL_ROUTER_DONE], 1);
+      s_last = (prev == (int)gridDim.y - 1);
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    if (threadIdx.x == 0) a.ws.ctrl[CTRL_ROUTER_DONE] = 0;
+  }
+  if (a.mode & RM_PERMUTE)
+    build_permutation(c, a.ws, a.T, a.ws.topk_idx, a.ws.topk_w, reinterpret_cast<int*>(smem));
 }
 
 struct PrepArgs {
@@ -273,12 +451,13 @@ struct PrepArgs {
 
 // Activation planes for k3moe_expert_ffn (CTAs 1..), permutation of the given routing (CTA 0).
 __global__ void __launch_bounds__(256) k_prep(PrepArgs a) {
+  extern __shared__ int s_perm[];  // 4E + 2 ints
   if (blockIdx.x == 0) {
-    build_permutation(a.c, a.ws, a.T, a.idx, a.w);
+    build_permutation(a.c, a.ws, a.T, a.idx, a.w, s_perm);
     return;
   }
   const int warp = threadIdx.x >> 5;
-  xprep_blocks(a.c, a.ws, a.x, a.T, (long long)(blockIdx.x - 1) * 8 + warp, (long long)(gridDim.x - 1) * 8);
+  xprep_rows(a.c, a.ws, a.x, a.T, (long long)(blockIdx.x - 1) * 8 + warp, (long long)(gridDim.x - 1) * 8);
 }
 
 __global__ void __launch_bounds__(256) k_rmsnorm(const float* x, long long T, int d, float eps, float* out) {
@@ -308,28 +487,46 @@ bool g_route_attr_set = false;
 
 }  // namespace
 
+template <int TT>
+cudaError_t launch_route_tt(const RouteArgs& a, int warps, cudaStream_t st) {
+  const size_t smem = route_tile_bytes(a.c, TT) + sizeof(unsigned long long) * 32 * warps;
+  if (smem > (size_t)kRouteMaxSmem) return cudaErrorInvalidValue;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(k_route<TT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRouteMaxSmem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  dim3 grid((a.c.E + warps - 1) / warps, (unsigned)((a.T + TT - 1) / TT));
+  k_route<TT><<<grid, warps * 32, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_route(const Cfg& c, const Ws& ws, const void* x, long long T, const float* W, const float* bias,
                          int* out_idx, float* out_w, int mode, cudaStream_t st) {
-  const size_t smem = sizeof(unsigned long long) * kRouteWarps * (size_t)c.E;
-  if (!g_route_attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_route, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(sizeof(unsigned long long) * kRouteWarps * kMaxE));
-    if (e != cudaSuccess) return e;
-    g_route_attr_set = true;
-  }
   RouteArgs a{c, ws, x, T, W, bias, out_idx, out_w, mode};
-  dim3 grid((c.E + kRouteWarps - 1) / kRouteWarps, (unsigned)((T + kRouteTT - 1) / kRouteTT));
-  k_route<<<grid, kRouteWarps * 32, smem, st>>>(a);
-  return cudaGetLastError();
+  // largest token tile (<= T) whose staged activations fit in shared memory
+  auto fits = [&](int tt, int warps) {
+    return route_tile_bytes(c, tt) + sizeof(unsigned long long) * 32 * warps <= (size_t)kRouteMaxSmem;
+  };
+  if (T >= 8 && fits(8, 8)) return launch_route_tt<8>(a, 8, st);
+  if (T >= 4 && fits(4, 8)) return launch_route_tt<4>(a, 8, st);
+  if (T >= 2 && fits(2, 4)) return launch_route_tt<2>(a, 4, st);
+  return launch_route_tt<1>(a, 4, st);
 }
 
 cudaError_t launch_prep(const Cfg& c, const Ws& ws, const void* x, long long T, const int* idx, const float* w,
                         cudaStream_t st) {
   PrepArgs a{c, ws, x, T, idx, w};
-  long long nblk = T * (c.d / 32);
-  long long ctas = 1 + (nblk + 7) / 8;
+  long long ctas = 1 + (T + 7) / 8;
   if (ctas > 1 + 152 * 8) ctas = 1 + 152 * 8;
-  k_prep<<<(unsigned)ctas, 256, 0, st>>>(a);
+  if (!g_route_attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(k_prep, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)(sizeof(int) * (4 * kMaxE + 2)));
+    if (e != cudaSuccess) return e;
+    g_route_attr_set = true;
+  }
+  k_prep<<<(unsigned)ctas, 256, sizeof(int) * (4 * (size_t)c.E + 2), st>>>(a);
   return cudaGetLastError();
 }
 
