@@ -143,6 +143,25 @@ K3MOE_API k3moe_status k3moe_layer_timed(const k3moe_config* cfg /* host */, con
                                          size_t ws_bytes, void* stream, void* const* events /* host */);
 
 /*
+ * The whole layer for callers that cannot allocate device memory (no counterpart in the pages:
+ * an interface addition of this library). Some programs own every device allocation through
+ * their own pool and forbid other cudaMalloc calls, and latency-critical callers cannot afford
+ * cudaMalloc's device synchronisation; this call needs no workspace from them. Its scratch is a
+ * fixed K3MOE_STATIC_SCRATCH_BYTES array in device memory declared by the library (resident on
+ * every GPU that loads it until exit); calls needing more (k3moe_workspace_bytes(cfg, T) larger,
+ * i.e. T > 2 at the 7168/1536/896 shape) return K3MOE_ERR_WORKSPACE. It allocates nothing,
+ * clears the scratch it uses at the start of each call, and otherwise behaves like k3moe_layer
+ * without the optional top-k outputs. All calls on a device share the array: calls that overlap
+ * on the GPU race and give wrong results. The first call on a device looks up the array's
+ * address; make it before any stream capture. Device-side data checks are not reported.
+ */
+#define K3MOE_STATIC_SCRATCH_BYTES (4u << 20)
+K3MOE_API k3moe_status k3moe_layer_static(const k3moe_config* cfg /* host */, const void* x, int64_t T,
+                                          const float* w_router, const float* bias,
+                                          const uint8_t* routed_records, const uint8_t* shared_records,
+                                          float* y, void* stream);
+
+/*
  * Pre-norm residual step of a stack of layers: xn = RMSNorm(x) with unit weight,
  * xn_j = x_j / sqrt(mean_j(x^2) + eps) (RMSNorm is one of the engine's ops in the review's
  * "k3_ops.c" row). x, xn: [T, d] fp32.

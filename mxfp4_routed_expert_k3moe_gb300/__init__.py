@@ -13,7 +13,7 @@ import os
 from ._build import LIB, build
 
 __all__ = ["Config", "K3moeError", "load", "record_bytes", "workspace_bytes", "route", "expert_ffn", "layer",
-           "layer_timed",
+           "layer_timed", "layer_static",
            "rmsnorm", "residual_add", "check_device_status", "status_string", "X_BF16", "X_F32"]
 
 OK, ERR_INVALID_ARGUMENT, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE_CHECK, ERR_TIMEOUT = range(7)
@@ -22,7 +22,8 @@ ACT_EXACT, ACT_MXFP4 = 0, 1
 X_BF16, X_F32 = 0, 1
 
 EXPORTS = ["k3moe_record_bytes", "k3moe_workspace_bytes", "k3moe_route", "k3moe_expert_ffn", "k3moe_layer",
-           "k3moe_layer_timed", "k3moe_rmsnorm", "k3moe_residual_add", "k3moe_check_device_status", "k3moe_status_string"]
+           "k3moe_layer_timed", "k3moe_layer_static", "k3moe_rmsnorm", "k3moe_residual_add",
+           "k3moe_check_device_status", "k3moe_status_string"]
 
 
 class Config(ctypes.Structure):
@@ -67,6 +68,8 @@ def load(path: str | None = None):
         L.k3moe_expert_ffn.argtypes = [cfgp, _P, _I64, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
         L.k3moe_layer.argtypes = [cfgp, _P, _I64, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
         L.k3moe_layer_timed.argtypes = [cfgp, _P, _I64, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]
+        L.k3moe_layer_static.argtypes = [cfgp, _P, _I64, _P, _P, _P, _P, _P, _P]
+        L.k3moe_layer_static.restype = ctypes.c_int
         L.k3moe_rmsnorm.argtypes = [_P, _I64, ctypes.c_int32, ctypes.c_float, _P, _P]
         L.k3moe_residual_add.argtypes = [_P, _P, _I64, _P]
         L.k3moe_check_device_status.argtypes = [_P, _P]
@@ -134,6 +137,13 @@ def layer_timed(cfg, x, T, w_router, bias, routed, shared, y, ws, events, topk_i
     _check(load().k3moe_layer_timed(ctypes.byref(cfg), _ptr(x), T, _ptr(w_router), _ptr(bias), _ptr(routed),
                                     _ptr(shared), _ptr(y), _ptr(topk_idx), _ptr(topk_w), _ptr(ws),
                                     ws.numel() * ws.element_size(), _stream(stream), ev), "k3moe_layer_timed")
+
+
+def layer_static(cfg, x, T, w_router, bias, routed, shared, y, stream=None):
+    """k3moe_layer_static: the layer without a workspace argument, for callers that cannot allocate
+    device memory; its scratch is a fixed 4 MiB array inside the library (see include/k3moe.h)."""
+    _check(load().k3moe_layer_static(ctypes.byref(cfg), _ptr(x), T, _ptr(w_router), _ptr(bias), _ptr(routed),
+                                     _ptr(shared), _ptr(y), _stream(stream)), "k3moe_layer_static")
 
 
 def rmsnorm(x, T, d, eps, xn, stream=None):
