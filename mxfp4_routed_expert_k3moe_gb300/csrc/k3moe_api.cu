@@ -15,7 +15,13 @@ constexpr long long kMaxE = 4096;
 constexpr long long kMaxK = 32;
 constexpr long long kMaxS = 8;
 constexpr int kMaxDModel = 25600;
-constexpr long long kGateUpParts = 4;  // gate/up reduction axis split across warps
+// Reduction parts of the gate/up projection: at a few tokens the (work group, row tile) items are
+// too few to spread over the SMs, so each is split along d into 4 parts summed by the last one.
+long long gateup_parts(long long T, long long d) {
+  const long long p = T <= 4 ? 4 : 1;
+  return p < d / 128 ? p : d / 128;
+}
+constexpr long long kMaxTerms = 3;     // E4M3 terms per activation block (x: 2 bf16 / 3 fp32; h: 3)
 
 size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -54,8 +60,8 @@ long long wg_bound(const k3moe_config* c, long long T) {
 }
 
 struct Layout {
-  size_t ctrl, logits, topk_idx, topk_w, counts, cursor, offsets, wgoff, perm_tok, perm_w, inv, wgs, xact, xexp, hact,
-      hexp, part, tilecnt, gupart, gucnt, rtcnt, total;
+  size_t ctrl, logits, topk_idx, topk_w, counts, cursor, offsets, wgoff, perm_tok, perm_w, inv, wgs, xq, xs, hq, hs,
+      part, gupart, rtcnt, total;
 };
 
 Layout make_layout(const k3moe_config* c, long long T) {
@@ -79,14 +85,12 @@ Layout make_layout(const k3moe_config* c, long long T) {
   take(L.perm_w, sizeof(float) * P);
   take(L.inv, sizeof(int) * T * k);
   take(L.wgs, sizeof(k3::WorkGroup) * wg_bound(c, T));
-  take(L.xact, sizeof(__half) * T * 2 * d);
-  take(L.xexp, (size_t)T);
-  take(L.hact, sizeof(__half) * P * 2 * f);
-  take(L.hexp, (size_t)(P * (f / 32)));
+  take(L.xq, (size_t)(T * kMaxTerms * d));
+  take(L.xs, (size_t)(T * kMaxTerms * (d / 32)));
+  take(L.hq, (size_t)(P * kMaxTerms * f));
+  take(L.hs, (size_t)(P * kMaxTerms * (f / 32)));
   take(L.part, sizeof(float) * P * d);
-  take(L.tilecnt, sizeof(int) * (d / 32));
-  take(L.gupart, sizeof(float) * P * kGateUpParts * 2 * f);
-  take(L.gucnt, sizeof(int) * wg_bound(c, T) * (f / 32));
+  take(L.gupart, sizeof(float) * P * gateup_parts(T, d) * 2 * f);
   take(L.rtcnt, sizeof(int) * ((T + 7) / 8));
   L.total = o;
   return L;
@@ -107,14 +111,12 @@ Ws bind(const Layout& L, void* base) {
   w.perm_w = reinterpret_cast<float*>(b + L.perm_w);
   w.inv = reinterpret_cast<int*>(b + L.inv);
   w.wgs = reinterpret_cast<k3::WorkGroup*>(b + L.wgs);
-  w.xact = reinterpret_cast<__half*>(b + L.xact);
-  w.xexp = reinterpret_cast<int8_t*>(b + L.xexp);
-  w.hact = reinterpret_cast<__half*>(b + L.hact);
-  w.hexp = reinterpret_cast<int8_t*>(b + L.hexp);
+  w.xq = reinterpret_cast<uint8_t*>(b + L.xq);
+  w.xs = reinterpret_cast<uint8_t*>(b + L.xs);
+  w.hq = reinterpret_cast<uint8_t*>(b + L.hq);
+  w.hs = reinterpret_cast<uint8_t*>(b + L.hs);
   w.part = reinterpret_cast<float*>(b + L.part);
-  w.tilecnt = reinterpret_cast<int*>(b + L.tilecnt);
   w.gupart = reinterpret_cast<float*>(b + L.gupart);
-  w.gucnt = reinterpret_cast<int*>(b + L.gucnt);
   w.rtcnt = reinterpret_cast<int*>(b + L.rtcnt);
   return w;
 }
@@ -127,9 +129,10 @@ Cfg make_cfg(const k3moe_config* c, long long T) {
   k.k = c->top_k;
   k.S = c->n_shared;
   k.x_f32 = c->x_dtype == K3MOE_X_F32 ? 1 : 0;
-  k.xplanes = k.x_f32 ? 2 : 1;
-  k.wgt = T == 1 ? 1 : 4;
-  k.ks = (int)kGateUpParts;
+  k.wgt = (int)(T < 32 ? T : 32);
+  k.ks = (int)gateup_parts(T, c->d_model);
+  k.xterms = k.x_f32 ? 3 : 2;
+  k.hterms = 3;
   k.stride = c->record_stride;
   return k;
 }
@@ -154,7 +157,10 @@ size_t k3moe_record_bytes(const k3moe_config* cfg) {
 
 size_t k3moe_workspace_bytes(const k3moe_config* cfg, int64_t max_tokens) {
   if (validate(cfg) != K3MOE_OK || !tokens_ok(cfg, max_tokens)) return 0;
-  return make_layout(cfg, max_tokens < 1 ? 1 : max_tokens).total;
+  // the layout grows with T except where the gate/up split drops from 4 parts to 1 (above 4 tokens)
+  const long long T = max_tokens < 1 ? 1 : max_tokens;
+  const size_t a = make_layout(cfg, T).total, b = make_layout(cfg, T < 4 ? T : 4).total;
+  return a > b ? a : b;
 }
 
 k3moe_status k3moe_route(const k3moe_config* cfg, const void* x, int64_t T, const float* w_router, const float* bias,
@@ -275,7 +281,7 @@ k3moe_status k3moe_check_device_status(void* ws, void* stream) {
   if (flags == 0) return K3MOE_OK;
   if (cudaMemsetAsync(ws, 0, sizeof(int), st) != cudaSuccess) return K3MOE_ERR_CUDA;
   if (cudaStreamSynchronize(st) != cudaSuccess) return K3MOE_ERR_CUDA;
-  return K3MOE_ERR_DEVICE_CHECK;
+  return (flags & k3::ST_TIMEOUT) ? K3MOE_ERR_TIMEOUT : K3MOE_ERR_DEVICE_CHECK;
 }
 
 const char* k3moe_status_string(k3moe_status s) {

@@ -10,10 +10,11 @@ namespace k3 {
 // ----------------------------------------------------------------------------- configuration
 struct Cfg {
   int d, f, E, k, S;  // d_model, d_ff, routed experts, top-k, shared experts
-  int xplanes;        // fp16 planes per activation row: 1 (bf16 x is exact in one plane) or 2 (fp32 x: hi + lo)
   int x_f32;          // 1 if x is fp32, 0 if bf16
   int wgt;            // max tokens per work group
-  int ks;             // parts of the gate/up reduction axis (d) processed by separate warps
+  int ks;             // reduction parts of gate/up (allocated in the workspace)
+  int xterms;         // E4M3 terms per activation block of x (2 for bf16 x, 3 for fp32 x)
+  int hterms;         // E4M3 terms per block of h
   long long stride;   // bytes between expert records
 };
 
@@ -22,6 +23,7 @@ enum CtrlSlot {
   CTRL_STATUS = 0,       // status bits, read and cleared by k3moe_check_device_status
   CTRL_ROUTER_DONE = 1,  // router token tiles whose top-k is done (the last builds the permutation)
   CTRL_NWG = 2,          // number of work groups built by the permutation
+  CTRL_NPOS = 3,         // number of routed positions (slots with a valid expert id)
   CTRL_WORDS = 64
 };
 enum StatusBits { ST_BAD_EXPERT = 1, ST_NAN_SCALE = 2, ST_TIMEOUT = 4 };
@@ -45,14 +47,12 @@ struct Ws {
   float* perm_w;      // [P] gate weight of each position (1 for shared)
   int* inv;           // [T*k] position of routed slot (t, i), -1 if the slot was rejected
   WorkGroup* wgs;     // [WGmax]
-  __half* xact;       // [T, xplanes, d] scaled fp16 planes of x
-  int8_t* xexp;       // [T] per-token power-of-two exponent c: plane values = x * 2^c
-  __half* hact;       // [P, 2, f] scaled fp16 hi/lo planes of h
-  int8_t* hexp;       // [P, f/32]
+  uint8_t* xq;        // [T * xterms, d] E4M3 terms of x (row t*xterms + j)
+  uint8_t* xs;        // [T * xterms, d/32] their E8M0 block scales
+  uint8_t* hq;        // [P * hterms, f] E4M3 terms of h (row p*hterms + j)
+  uint8_t* hs;        // [P * hterms, f/32] their E8M0 block scales
   float* part;        // [P, d] gate-weighted down-projection outputs per position
-  int* tilecnt;       // [d/32] work groups finished per 32-row block of the down projection
-  float* gupart;      // [P, ks, 2, f] partial gate/up sums of the ks reduction-axis parts
-  int* gucnt;         // [WGmax * f/32] parts finished per (work group, 32-row block)
+  float* gupart;      // [P, ks, 2, f] partial gate/up sums of the reduction parts
   int* rtcnt;         // [ceil(T/8)] router CTAs finished per token tile
 };
 
@@ -61,20 +61,6 @@ __device__ __forceinline__ float pow2i(int e) {
   // exact 2^e; fast path for normal results
   if (e >= -126 && e <= 127) return __int_as_float((e + 127) << 23);
   return ldexpf(1.0f, e);
-}
-
-// Exponent c such that max|v| * 2^c lies in [2^14, 2^15): the block's fp16 plane is then exact
-// for bf16 inputs and keeps 11 significant bits (22 with the lo plane) for fp32 values.
-__device__ __forceinline__ int plane_exponent(float amax) {
-  if (!(amax > 0.0f) || !(amax <= 3.402823466e38f)) return 0;
-  int c = 14 - ilogbf(amax);
-  return c > 120 ? 120 : c;
-}
-
-__device__ __forceinline__ uint32_t ld_nc_u32(const void* p) {
-  uint32_t v;
-  asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
-  return v;
 }
 
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
@@ -91,33 +77,32 @@ __device__ __forceinline__ uint4 ld_v4(const void* p) {
   return v;
 }
 
-// Four packed E2M1 pairs (one 32-bit word = 8 codes, even element in each low nibble) to four
-// f16x2 registers holding the exact element values: out[b] = (elem 2b, elem 2b+1).
-__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t& o0, uint32_t& o1, uint32_t& o2,
-                                                uint32_t& o3) {
-  asm("{\n"
-      " .reg .b8 b0, b1, b2, b3;\n"
-      " mov.b32 {b0, b1, b2, b3}, %4;\n"
-      " cvt.rn.f16x2.e2m1x2 %0, b0;\n"
-      " cvt.rn.f16x2.e2m1x2 %1, b1;\n"
-      " cvt.rn.f16x2.e2m1x2 %2, b2;\n"
-      " cvt.rn.f16x2.e2m1x2 %3, b3;\n"
-      "}\n"
-      : "=r"(o0), "=r"(o1), "=r"(o2), "=r"(o3)
-      : "r"(w));
-}
-
-// D = A(16x16, row) * B(16x8, col) + C, fp16 inputs, fp32 accumulate (warp-wide).
-__device__ __forceinline__ void mma_f16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                              uint32_t b0, uint32_t b1) {
-  asm(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};\n"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+// Split one 32-element block (one value per lane of the warp) into `terms` E4M3 terms with E8M0
+// block scales: term j = RN_e4m3(r_j / 2^{e_j}) with e_j = floor(log2 max|r_j|) - 7 (so the block
+// maximum maps into [128, 256), inside E4M3's range), r_0 = v, r_{j+1} = r_j - term_j 2^{e_j}.
+// Lane l writes codes[j * code_stride] of its element; lane 0 writes scales[j * scale_stride].
+__device__ __forceinline__ void split_terms(float v, int terms, uint8_t* codes, long long code_stride, uint8_t* scales,
+                                            long long scale_stride, int lane) {
+  float r = v;
+  for (int j = 0; j < terms; ++j) {
+    float amax = fabsf(r);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    int e = 0;
+    if (amax > 0.0f && amax <= 3.402823466e38f) e = ilogbf(amax) - 7;
+    e = e < -127 ? -127 : (e > 127 ? 127 : e);
+    const float s = r * pow2i(-e);
+    uint16_t q2;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(q2) : "f"(0.0f), "f"(s));
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(q2));
+    r -= __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu))) * pow2i(e);
+    codes[j * code_stride] = (uint8_t)(q2 & 0xFFu);
+    if (lane == 0) scales[j * scale_stride] = (uint8_t)(e + 127);
+  }
+}
 
 __device__ __forceinline__ void set_status(int* ctrl, int bits) { atomicOr(&ctrl[CTRL_STATUS], bits); }
 

@@ -16,7 +16,7 @@ cudaError_t launch_prep(const Cfg& c, const Ws& ws, const void* x, long long T, 
 cudaError_t launch_rmsnorm(const float* x, long long T, int d, float eps, float* out, cudaStream_t st);
 cudaError_t launch_residual_add(float* x, const float* y, long long n, cudaStream_t st);
 
-// k3moe_ffn.cu
+// k3moe_tc.cu (tcgen05 expert FFN)
 cudaError_t launch_gateup(const Cfg& c, const Ws& ws, const uint8_t* routed, const uint8_t* shared, float* y,
                           long long T, long long wg_max, cudaStream_t st);
 cudaError_t launch_down(const Cfg& c, const Ws& ws, const uint8_t* routed, const uint8_t* shared, float* y,

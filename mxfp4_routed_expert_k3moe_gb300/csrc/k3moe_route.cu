@@ -20,86 +20,22 @@ namespace {
 constexpr int kMaxE = 4096;
 constexpr int kRouteMaxSmem = 200 * 1024;  // router CTA: x tile + permutation scratch + candidates
 
-// Eight consecutive activations (bf16 or fp32) starting at element idx (a multiple of 8).
-__device__ __forceinline__ void load8(const void* x, int x_f32, long long idx, float (&v)[8]) {
-  if (x_f32) {
-    const float4 p = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(x) + idx);
-    const float4 q = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(x) + idx + 4);
-    v[0] = p.x; v[1] = p.y; v[2] = p.z; v[3] = p.w; v[4] = q.x; v[5] = q.y; v[6] = q.z; v[7] = q.w;
-  } else {
-    const uint4 p = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(x) + idx);
-    const uint32_t w[4] = {p.x, p.y, p.z, p.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      v[2 * q] = __uint_as_float(w[q] << 16);
-      v[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
-    }
-  }
+__device__ __forceinline__ float load_x(const void* x, int x_f32, long long idx) {
+  if (x_f32) return reinterpret_cast<const float*>(x)[idx];
+  return __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(x)[idx] << 16);
 }
 
-// fp16 plane(s) of eight consecutive elements j..j+7 of token t, scaled by sc (a power of two).
-__device__ __forceinline__ void convert8(const Cfg& c, const Ws& ws, const void* x, long long t, int j, float sc) {
-  float v[8];
-  load8(x, c.x_f32, t * c.d + j, v);
-  __align__(16) __half hi[8], lo[8];
-#pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    const float s = v[q] * sc;
-    hi[q] = __float2half_rn(s);
-    lo[q] = __float2half_rn(s - __half2float(hi[q]));
-  }
-  *reinterpret_cast<uint4*>(ws.xact + (t * c.xplanes) * c.d + j) = *reinterpret_cast<const uint4*>(hi);
-  if (c.xplanes == 2) *reinterpret_cast<uint4*>(ws.xact + (t * 2 + 1) * c.d + j) = *reinterpret_cast<const uint4*>(lo);
+// E4M3 terms of the 32-element block of token t starting at element j (lane = element).
+__device__ __forceinline__ void xterms_block(const Cfg& c, const Ws& ws, float v, long long t, int j, int lane) {
+  split_terms(v, c.xterms, ws.xq + (t * c.xterms) * c.d + j + lane, c.d,
+              ws.xs + (t * c.xterms) * (c.d / 32) + j / 32, c.d / 32, lane);
 }
 
-// Same, reading the eight elements from a token row staged in shared memory.
-__device__ __forceinline__ void convert8_shared(const Cfg& c, const Ws& ws, const uint8_t* xrow, long long t, int j,
-                                                float sc) {
-  float v[8];
-  if (c.x_f32) {
-    const float4 p = *reinterpret_cast<const float4*>(xrow + 4 * j);
-    const float4 q = *reinterpret_cast<const float4*>(xrow + 4 * j + 16);
-    v[0] = p.x; v[1] = p.y; v[2] = p.z; v[3] = p.w; v[4] = q.x; v[5] = q.y; v[6] = q.z; v[7] = q.w;
-  } else {
-    const uint4 p = *reinterpret_cast<const uint4*>(xrow + 2 * j);
-    const uint32_t w[4] = {p.x, p.y, p.z, p.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      v[2 * q] = __uint_as_float(w[q] << 16);
-      v[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
-    }
-  }
-  __align__(16) __half hi[8], lo[8];
-#pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    const float s = v[q] * sc;
-    hi[q] = __float2half_rn(s);
-    lo[q] = __float2half_rn(s - __half2float(hi[q]));
-  }
-  *reinterpret_cast<uint4*>(ws.xact + (t * c.xplanes) * c.d + j) = *reinterpret_cast<const uint4*>(hi);
-  if (c.xplanes == 2) *reinterpret_cast<uint4*>(ws.xact + (t * 2 + 1) * c.d + j) = *reinterpret_cast<const uint4*>(lo);
-}
-
-// One warp per token: the fp16 plane(s) of x scaled by one power of two per token, chosen so that
-// max|x_t| * 2^c lies in [2^14, 2^15). A bf16 token is exact in one plane; an fp32 token keeps
-// ~22 significant bits in the hi + lo planes.
-__device__ void xprep_rows(const Cfg& c, const Ws& ws, const void* x, long long T, long long first, long long step) {
+// One warp per token: all E4M3 terms of the token (used by k3moe_expert_ffn's preparation).
+__device__ void xterms_rows(const Cfg& c, const Ws& ws, const void* x, long long T, long long first, long long step) {
   const int lane = threadIdx.x & 31;
-  for (long long t = first; t < T; t += step) {
-    float a = 0.0f;
-    for (int j = lane * 8; j < c.d; j += 256) {
-      float v[8];
-      load8(x, c.x_f32, t * c.d + j, v);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) a = fmaxf(a, fabsf(v[q]));
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-    const int e = plane_exponent(a);
-    const float sc = pow2i(e);
-    for (int j = lane * 8; j < c.d; j += 256) convert8(c, ws, x, t, j, sc);
-    if (lane == 0) ws.xexp[t] = (int8_t)e;
-  }
+  for (long long t = first; t < T; t += step)
+    for (int j = 0; j < c.d; j += 32) xterms_block(c, ws, load_x(x, c.x_f32, t * c.d + j + lane), t, j, lane);
 }
 
 // Orderable 64-bit key: larger logit first, then lower expert id. Key 0 marks an empty entry.
@@ -286,8 +222,10 @@ __device__ void build_permutation(const Cfg& c, const Ws& ws, long long T, const
     ws.perm_tok[pr + q] = (int)(q % T);
     ws.perm_w[pr + q] = 1.0f;
   }
-  for (int rb = tid; rb < c.d / 32; rb += nt) ws.tilecnt[rb] = 0;
-  if (tid == 0) ws.ctrl[CTRL_NWG] = n_routed_wg + c.S * nwt;
+  if (tid == 0) {
+    ws.ctrl[CTRL_NWG] = n_routed_wg + c.S * nwt;
+    ws.ctrl[CTRL_NPOS] = offsets[E];
+  }
   __syncthreads();
 }
 
@@ -335,13 +273,12 @@ __global__ void __launch_bounds__(256) k_route(RouteArgs a) {
     __syncthreads();
   }
 
-  // logits of expert row e for the tile's tokens; the same pass finds max|x_t| of each token.
-  // Each segment issues all of its router-weight loads before any arithmetic.
+  // logits of expert row e for the tile's tokens. Each segment issues all of its router-weight loads before any arithmetic.
   constexpr int U = (TT == 1) ? 14 : 8;
   if (e < c.E) {
-    float acc[TT], am[TT];
+    float acc[TT];
 #pragma unroll
-    for (int tt = 0; tt < TT; ++tt) acc[tt] = am[tt] = 0.0f;
+    for (int tt = 0; tt < TT; ++tt) acc[tt] = 0.0f;
     const float* wrow = a.W + (long long)e * c.d;
     for (int j0 = 0; j0 < c.d; j0 += 128 * U) {
       uint4 wv[U];
@@ -370,10 +307,7 @@ __global__ void __launch_bounds__(256) k_route(RouteArgs a) {
                 xv[2] = __uint_as_float(q.y << 16); xv[3] = __uint_as_float(q.y & 0xFFFF0000u);
               }
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                acc[tt] = fmaf(w4[q], xv[q], acc[tt]);
-                am[tt] = fmaxf(am[tt], fabsf(xv[q]));
-              }
+              for (int q = 0; q < 4; ++q) acc[tt] = fmaf(w4[q], xv[q], acc[tt]);
             }
           }
         }
@@ -382,30 +316,26 @@ __global__ void __launch_bounds__(256) k_route(RouteArgs a) {
     const float b = a.bias ? a.bias[e] : 0.0f;
 #pragma unroll
     for (int tt = 0; tt < TT; ++tt) {
-      float v = acc[tt], m = am[tt];
+      float v = acc[tt];
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        v += __shfl_xor_sync(0xffffffffu, v, o);
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      }
-      am[tt] = m;
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
       if (lane == 0 && tt < ntt) a.ws.logits[(t0 + tt) * c.E + e] = v + b;
     }
-    // activation planes: warp e converts elements [256e, 256e + 256) of each token of the tile
-    if ((a.mode & RM_XPREP) && e * 256 < c.d) {
-      const int j = e * 256 + lane * 8;
-#pragma unroll
-      for (int tt = 0; tt < TT; ++tt) {
-        if (tt < ntt && j < c.d) {
-          const long long t = t0 + tt;
-          const int ex = plane_exponent(am[tt]);
-          convert8_shared(c, a.ws, smem + tt * row_bytes, t, j, pow2i(ex));
-          if (e == 0 && lane == 0) a.ws.xexp[t] = (int8_t)ex;
+  }
+  // E4M3 terms of x: each warp of the grid takes 256-element segments of the tile's tokens
+  if (a.mode & RM_XPREP) {
+    for (int sg = e; sg * 256 < c.d; sg += (int)gridDim.x * nw) {
+      for (int tt = 0; tt < ntt; ++tt) {
+        const uint8_t* xr = smem + tt * row_bytes;
+        for (int j = sg * 256; j < sg * 256 + 256 && j < c.d; j += 32) {
+          const float v = c.x_f32 ? reinterpret_cast<const float*>(xr)[j + lane]
+                                  : __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(xr)[j + lane] << 16);
+          xterms_block(c, a.ws, v, t0 + tt, j, lane);
         }
       }
     }
-    if (lane == 0) __threadfence();
   }
+  __threadfence();
 
   // the last CTA of each token tile selects the top-k of its tokens ...
   __syncthreads();
@@ -457,7 +387,7 @@ __global__ void __launch_bounds__(256) k_prep(PrepArgs a) {
     return;
   }
   const int warp = threadIdx.x >> 5;
-  xprep_rows(a.c, a.ws, a.x, a.T, (long long)(blockIdx.x - 1) * 8 + warp, (long long)(gridDim.x - 1) * 8);
+  xterms_rows(a.c, a.ws, a.x, a.T, (long long)(blockIdx.x - 1) * 8 + warp, (long long)(gridDim.x - 1) * 8);
 }
 
 __global__ void __launch_bounds__(256) k_rmsnorm(const float* x, long long T, int d, float eps, float* out) {

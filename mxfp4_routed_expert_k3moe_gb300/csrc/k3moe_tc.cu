@@ -1,0 +1,813 @@
+// Expert FFN of the MXFP4 MoE layer on the 5th-generation tensor cores (tcgen05, sm_103a):
+//   gate/up:  g = W_gate x, u = W_up x                  (k_tc<GATEUP>, partial sums per reduction part)
+//             h = SiLU(g) * u and its E4M3 terms          (k_glu)
+//   down:     o_p = w_p W_down h_p                       (k_tc<DOWN>, one row per position p)
+//             y[t] = sum_i o_(t,i) + sum_s o_(t,s)        (k_combine)
+// The MXFP4 records are consumed as stored (kimi-k3-in-c review, table "KDA·MLA·MoE": the
+// experts multiply the 4-bit codes directly): TMA copies 128 rows x 128 codes of a weight matrix
+// into shared memory (16U4_ALIGN16B: 16 codes per 16-byte slot, 128-byte swizzle), the E8M0 block
+// scales go to tensor memory, and tcgen05.mma.kind::mxf8f6f4.block_scale multiplies the E2M1
+// weights (A: M = 128 rows) by the activations (B: N = tokens x terms), applying both block scales.
+//
+// Activations enter as sums of E4M3 terms: each 32-element block of x (or h) is written as
+// v = sum_j q_j 2^{e_j} with q_j E4M3 and 2^{e_j} an E8M0 block scale, each term taking the
+// rounding residual of the previous ones. Two terms hold a bf16 block exactly (down to elements
+// 2^-13 below the block maximum); three terms leave at most ~2^-12 of the block maximum of an fp32
+// x or of h. The MMA columns of one token's terms are summed in the epilogue.
+//
+// CTA layout (one CTA per SM, persistent over work items, 384 threads):
+//   warps 0-3   epilogue: accumulators (double-buffered in tensor memory) -> per-position sums
+//   warps 4-7   loaders: the tensor copy of the weight tile (one lane) and cp.async of the B rows and
+//               of the scale words, each loader for its own ring slots. On this part one thread
+//               issues about one tensor copy per ~500 SM cycles, so a single issuing thread caps the
+//               weight stream near 3 TB/s; four reach the DRAM rate.
+//   warps 8-11  MMA issuers (one lane each): tcgen05.cp of the scale words into tensor memory, then
+//               the MMAs. One issuing thread sustains one MMA per ~120-230 SM cycles whatever N is,
+//               and MMAs into one accumulator follow each other only every ~450 cycles, so at small
+//               N (few tokens) up to four issuers share the stages and each alternates between two
+//               accumulators (TMEM columns of their own); the epilogue adds the partial sums.
+// Every ring slot has exactly one agent of each kind (loader v owns the slots s = v mod 4, issuer w
+// the slots s = w mod n_iss), so each agent waits on a slot's barriers round after round and a
+// parity wait never meets a barrier two phases away.
+// A pipeline stage holds `ch` consecutive 128-code chunks of the reduction axis, brought by one
+// tensor copy (the per-copy cost of the TMA unit is amortised over more bytes).
+// Every mbarrier wait is bounded; on a timeout the CTA raises the status word and stops early.
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "k3moe_kernels.h"
+
+namespace k3 {
+
+namespace {
+
+enum { GATEUP = 0, DOWN = 1 };
+constexpr int kMaxIss = 4;                // MMA-issuing warps
+constexpr int kLoaders = 4;               // loader warps
+constexpr int kWarpLoad = 4, kWarpIss = kWarpLoad + kLoaders;
+constexpr int kThreads = 32 * (kWarpIss + kMaxIss);
+constexpr int kMaxCh = 2;                 // chunks per stage
+constexpr int kTmemCols = 512;
+constexpr int kMaxN = 128;               // largest MMA N (B rows per tile)
+constexpr int kSfSlot = 32;              // TMEM columns per chunk: A scales at +0..3, B scales at +16..19
+constexpr int kMaxStages = 16;
+constexpr int kSfBytes = 1024;           // per stage in shared memory: A scale words, then B scale words
+constexpr int kATile = 128 * 128;        // 128 rows x 128 codes in 16-byte slots
+constexpr uint32_t kATileTx = 128 * 64;  // bytes delivered by the TMA (packed codes)
+constexpr uint32_t kWaitLimit = 1u << 24;
+
+// ------------------------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.b32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+      "[%6];" ::"r"(dst),
+      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void cp16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+// 4-byte copy; src_bytes 0 writes zeros
+__device__ __forceinline__ void cp4(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
+  return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                       uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%5], [%6], p;\n}\n" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb));
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+// smem -> TMEM copy of a 32 x 128-bit block, replicated into the four 32-lane quarters
+__device__ __forceinline__ void tc_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+// Descriptor of 32 rows x 16 bytes stored contiguously (no swizzle; 8-row groups 128 bytes apart).
+__device__ __forceinline__ uint64_t sf_desc(uint32_t addr) {
+  return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)(512 >> 4) << 16) | ((uint64_t)(128 >> 4) << 32) |
+         ((uint64_t)1 << 46);
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// 16 columns of the warp's 32 lanes; the registers are valid after tc_wait_ld.
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t* v) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+        "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// Shared-memory control block (after the pipeline stages).
+struct Ctl {
+  uint64_t full[kMaxStages];   // weight tiles (TMA bytes), B rows and scale words (cp.async) landed
+  uint64_t empty[kMaxStages];  // the stage's MMAs completed
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint64_t drain;
+  uint32_t tmem;
+  volatile int abort;
+  int last;
+};
+
+// Position in the ring of pipeline stages: slot s, phase parity of its current round, and whether
+// the ring has wrapped at least once.
+struct Ring {
+  int s = 0;
+  uint32_t ph = 0;
+  bool wrapped = false;
+  __device__ __forceinline__ void next(int S) {
+    if (++s == S) {
+      s = 0;
+      ph ^= 1u;
+      wrapped = true;
+    }
+  }
+};
+
+// Bounded wait; on timeout raises ST_TIMEOUT and the CTA-wide abort flag.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Ctl* ctl, int* status) {
+  for (uint32_t it = 0; it < kWaitLimit; ++it) {
+    if (mbar_try(bar, parity)) return true;
+    if (ctl->abort) return false;
+    if (it > 256) __nanosleep(64);
+  }
+  ctl->abort = 1;
+  atomicOr(&status[CTRL_STATUS], ST_TIMEOUT);
+  return false;
+}
+
+// ------------------------------------------------------------------------------- arguments
+// Division by a run-time invariant d through a multiply-high and shifts (the round-up method of
+// Granlund and Montgomery, "Division by invariant integers using multiplication", 1994): with
+// l = ceil(log2 d) and m = floor(2^32 (2^l - d) / d) + 1, n / d = (t + ((n - t) >> min(l,1))) >> max(l-1,0)
+// where t = (m n) >> 32, for every 32-bit n. Item decomposition runs per item in every role, where
+// the 64-bit divisions it replaces cost hundreds of cycles.
+struct FastDiv {
+  uint32_t d, m, s1, s2;
+  __host__ void init(uint32_t dv) {
+    d = dv;
+    uint32_t l = 0;
+    while ((1ull << l) < dv) ++l;
+    m = (uint32_t)(((1ull << 32) * ((1ull << l) - dv)) / dv + 1);
+    s1 = l < 1 ? l : 1;
+    s2 = l > 1 ? l - 1 : 0;
+  }
+  __device__ __forceinline__ uint32_t div(uint32_t n) const {
+    const uint32_t t = __umulhi(m, n);
+    return (t + ((n - t) >> s1)) >> s2;
+  }
+};
+
+struct TcArgs {
+  Cfg c;
+  Ws ws;
+  const uint8_t* routed;
+  const uint8_t* shared;
+  float* y;
+  long long T;
+  int n_tile;   // MMA N (multiple of 16, <= kMaxN)
+  int acc_cols; // tensor-memory columns per accumulator (>= n_tile, multiple of 16)
+  int n_iss;    // MMA-issuing threads
+  int n_acc;    // accumulators per issuer (the MMAs of a chunk alternate between them)
+  int sf_base;  // first column of the scale ring (after 2 buffers x n_iss x n_acc accumulators)
+  int b_bytes;  // shared-memory bytes of the B tile of a chunk
+  int ch;       // chunks per stage
+  int terms;    // B rows per token in this kernel (x terms for gate/up, h terms for down)
+  int hterms;   // h terms written by the gate/up finish
+  int parts;    // reduction parts per gate/up row tile
+  FastDiv div_parts, div_mtiles;
+  int stages;   // pipeline depth (<= kMaxStages)
+  int stage_bytes;  // ch x (A tile + B tile + scale words)
+};
+
+// Work item: (work group, matrix, 128-row tile, reduction part).
+struct Item {
+  int wgi, mat, mt, kp, j0, j1;
+  WorkGroup wg;
+};
+
+template <int MODE>
+__device__ __forceinline__ bool item_at(const TcArgs& a, long long it, long long n_items, Item& o) {
+  if (it >= n_items) return false;
+  const Cfg& c = a.c;
+  const int nch = (MODE == GATEUP ? c.d : c.f) / 128;
+  uint32_t r = (uint32_t)it;  // n_items < 2^31 (checked on the host)
+  uint32_t q = a.div_parts.div(r);
+  o.kp = (int)(r - q * a.div_parts.d);
+  r = q;
+  q = a.div_mtiles.div(r);
+  o.mt = (int)(r - q * a.div_mtiles.d);
+  r = q;
+  if (MODE == GATEUP) {
+    o.mat = (int)(r & 1u);
+    o.wgi = (int)(r >> 1);
+  } else {
+    o.mat = 0;
+    o.wgi = (int)r;
+  }
+  o.j0 = (int)a.div_parts.div((uint32_t)(o.kp * nch));
+  o.j1 = (int)a.div_parts.div((uint32_t)((o.kp + 1) * nch));
+  o.wg = a.ws.wgs[o.wgi];
+  return true;
+}
+
+// E8M0 scale bytes of weight row `row` (blocks 0 .. K/32-1) of the item's matrix.
+template <int MODE>
+__device__ __forceinline__ const uint8_t* scale_row(const TcArgs& a, const Item& it, int row) {
+  const Cfg& c = a.c;
+  const long long nc = (long long)c.d * c.f / 2, ns = (long long)c.d * c.f / 32;
+  const uint8_t* rec = it.wg.expert < c.E ? a.routed + (long long)it.wg.expert * c.stride
+                                          : a.shared + (long long)(it.wg.expert - c.E) * c.stride;
+  const int K = MODE == GATEUP ? c.d : c.f;
+  const long long off = MODE == GATEUP ? (it.mat == 0 ? nc : 2 * nc + ns) : 2 * (nc + ns) + nc;
+  return rec + off + (long long)row * (K / 32);
+}
+
+// B row n of the item (token i = n / terms, term j = n % terms): codes and E8M0 scales.
+template <int MODE>
+__device__ __forceinline__ bool b_row(const TcArgs& a, const Item& it, int n, const uint8_t*& codes,
+                                      const uint8_t*& scales) {
+  const Cfg& c = a.c;
+  const int i = n / a.terms, j = n - i * a.terms;
+  if (i >= it.wg.ntok) return false;
+  if (MODE == GATEUP) {
+    const long long r = (long long)a.ws.perm_tok[it.wg.pos0 + i] * a.terms + j;
+    codes = a.ws.xq + r * c.d;
+    scales = a.ws.xs + r * (c.d / 32);
+  } else {
+    const long long r = (long long)(it.wg.pos0 + i) * a.terms + j;
+    codes = a.ws.hq + r * c.f;
+    scales = a.ws.hs + r * (c.f / 32);
+  }
+  return true;
+}
+
+// What a loader reads ahead for one item: its work group and, for the B rows n = lane + 32 q, the
+// activation row they come from (the token for gate/up, the position for down; -1 past the work
+// group's tokens). The loads are only consumed an item later.
+struct LoadPlan {
+  Item it;
+  int bsrc[kMaxN / 32];
+};
+
+template <int MODE>
+__device__ __forceinline__ void make_plan(const TcArgs& a, const Item& it, int lane, LoadPlan& p) {
+  p.it = it;
+#pragma unroll
+  for (int q = 0; q < kMaxN / 32; ++q) {
+    const int n = lane + 32 * q;
+    const int i = n / a.terms;
+    p.bsrc[q] = -1;
+    if (n < a.n_tile && i < it.wg.ntok)
+      p.bsrc[q] = MODE == GATEUP ? __ldg(&a.ws.perm_tok[it.wg.pos0 + i]) : it.wg.pos0 + i;
+  }
+}
+
+// ------------------------------------------------------------------------------- the kernel
+// Shared memory of a stage: [A tiles: ch x 16 KB][B tiles: ch x b_bytes][scale words: ch x 1 KB].
+// Scale words of a chunk: 512 bytes for the 128 weight rows, then 512 for the B rows; the word of
+// row 32c + i (4 E8M0 bytes, one per 32-block of the chunk) sits at byte 16 i + 4 c, the layout
+// that the 32x128b.warpx4 copy spreads to TMEM lane 32q + i, column c of every quarter q.
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_tc(const __grid_constant__ CUtensorMap map_r0, const __grid_constant__ CUtensorMap map_r1,
+         const __grid_constant__ CUtensorMap map_s0, const __grid_constant__ CUtensorMap map_s1, TcArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  const int S = a.stages, CH = a.ch;
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + (size_t)S * a.stage_bytes);
+  const Cfg& c = a.c;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n_wg = a.ws.ctrl[CTRL_NWG];
+  const int nmat = MODE == GATEUP ? 2 : 1;
+  const int mtiles = (MODE == GATEUP ? c.f : c.d) / 128;
+  const long long n_items = (long long)n_wg * nmat * mtiles * a.parts;
+  int* status = a.ws.ctrl;
+  const int b_off = CH * kATile, sf_off = CH * (kATile + a.b_bytes);
+
+  if (n_wg == 0) return;  // nothing routed and no shared experts (k_combine writes y = 0)
+
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&ctl->tmem)),
+                 "r"(kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(su32(&ctl->full[s]), 1 + 32);
+      mbar_init(su32(&ctl->empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(su32(&ctl->acc_full[b]), a.n_iss);
+      mbar_init(su32(&ctl->acc_empty[b]), 128);
+    }
+    mbar_init(su32(&ctl->drain), a.n_iss);
+    ctl->abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem;
+
+  if (warp >= kWarpLoad && warp < kWarpIss) {
+    // ------------------------------------------------------------ loaders (one per slot class)
+    // The item two ahead has its work group read, the next one its B-row addresses resolved, so
+    // that neither dependent load sits in front of the next item's first copy.
+    const int lv = warp - kWarpLoad;
+    Ring rg;
+    bool ok = true;
+    LoadPlan cur, nxt;
+    Item it2;
+    long long ii = blockIdx.x;
+    bool has_nxt = item_at<MODE>(a, ii, n_items, it2);
+    if (has_nxt) make_plan<MODE>(a, it2, lane, nxt);
+    bool has_it2 = item_at<MODE>(a, ii + gridDim.x, n_items, it2);
+    while (ok && has_nxt) {
+      cur = nxt;
+      has_nxt = has_it2;
+      if (has_nxt) make_plan<MODE>(a, it2, lane, nxt);
+      ii += gridDim.x;
+      has_it2 = item_at<MODE>(a, ii + gridDim.x, n_items, it2);
+      const Item& it = cur.it;
+      const bool routed = it.wg.expert < c.E;
+      const CUtensorMap* map = routed ? (it.mat == 0 ? &map_r0 : &map_r1) : (it.mat == 0 ? &map_s0 : &map_s1);
+      const int ecoord = routed ? it.wg.expert : it.wg.expert - c.E;
+      const uint8_t* arow[4];
+      const uint8_t* bcodes[kMaxN / 32];
+      const uint8_t* bscales[kMaxN / 32];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) arow[q] = scale_row<MODE>(a, it, it.mt * 128 + lane + 32 * q);
+#pragma unroll
+      for (int q = 0; q < kMaxN / 32; ++q) {
+        bcodes[q] = nullptr;
+        bscales[q] = nullptr;
+        if (cur.bsrc[q] >= 0) {
+          const int n = lane + 32 * q;
+          const long long r = (long long)cur.bsrc[q] * a.terms + (n - (n / a.terms) * a.terms);
+          bcodes[q] = (MODE == GATEUP ? a.ws.xq : a.ws.hq) + r * (MODE == GATEUP ? c.d : c.f);
+          bscales[q] = (MODE == GATEUP ? a.ws.xs : a.ws.hs) + r * ((MODE == GATEUP ? c.d : c.f) / 32);
+        }
+      }
+      for (int j = it.j0; j < it.j1; j += CH, rg.next(S)) {
+        const int s = rg.s;
+        if (s % kLoaders != lv) continue;
+        if (rg.wrapped) ok = __all_sync(0xffffffffu, wait_bar(su32(&ctl->empty[s]), rg.ph ^ 1u, ctl, status));
+        if (!ok) break;
+        uint8_t* st = smem + (size_t)s * a.stage_bytes;
+        if (lane == 0) {
+          mbar_expect_tx(su32(&ctl->full[s]), kATileTx * CH);
+          tma_load_4d(su32(st), map, 0, it.mt * 128, j, ecoord, su32(&ctl->full[s]));
+        }
+        for (int cc = 0; cc < CH; ++cc) {
+          const int jj = j + cc;
+          const uint32_t sb = su32(st + b_off + cc * a.b_bytes), sc = su32(st + sf_off + cc * kSfBytes);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) cp4(sc + 16 * lane + 4 * q, arow[q] + 4 * jj, 4);
+#pragma unroll
+          for (int q = 0; q < kMaxN / 32; ++q) {
+            if (bcodes[q]) {
+              const int n = lane + 32 * q;
+              const uint8_t* src = bcodes[q] + (long long)jj * 128;
+#pragma unroll
+              for (int k16 = 0; k16 < 8; ++k16) cp16(sb + n * 128 + ((k16 ^ (n & 7)) << 4), src + k16 * 16);
+              cp4(sc + 512 + 16 * lane + 4 * q, bscales[q] + 4 * jj, 4);
+            }
+          }
+        }
+        cp_arrive_noinc(su32(&ctl->full[s]));
+      }
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    // after a timeout, give a weight tile still in flight time to land before the CTA exits
+    if (!ok && lane == 0)
+      for (int w = 0; w < 1000; ++w) __nanosleep(1000);
+  } else if (warp >= kWarpIss) {
+    // ------------------------------------------------------------ MMA issuers
+    const int w = warp - kWarpIss;
+    if (lane == 0 && w < a.n_iss) {
+      const uint32_t idesc =
+          (5u << 7) | (0u << 10) | ((uint32_t)(a.n_tile >> 3) << 17) | (1u << 23) | ((uint32_t)(128 >> 4) << 24);
+      // descriptors of stage 0, chunk 0; stage s / chunk cc add their byte offsets / 16 to the
+      // start-address field
+      const uint64_t da0 = sw128_desc(su32(smem)), db0 = sw128_desc(su32(smem) + b_off);
+      const uint64_t dsa0 = sf_desc(su32(smem) + sf_off), dsb0 = sf_desc(su32(smem) + sf_off + 512);
+      const uint32_t st16 = (uint32_t)a.stage_bytes >> 4, bb16 = (uint32_t)a.b_bytes >> 4;
+      long long i = 0;
+      Ring rg;
+      Item it;
+      bool ok = true;
+      for (long long ii = blockIdx.x; ok && item_at<MODE>(a, ii, n_items, it); ii += gridDim.x, ++i) {
+        const int b = (int)(i & 1);
+        const long long rb = i >> 1;
+        if (rb > 0 && !wait_bar(su32(&ctl->acc_empty[b]), (uint32_t)((rb - 1) & 1), ctl, status)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)((b * a.n_iss + w) * a.n_acc * a.acc_cols);
+        uint32_t started = 0;  // bit h: accumulator h already holds a partial sum of this item
+        for (int j = it.j0; j < it.j1; j += CH, rg.next(S)) {
+          const int s = rg.s;
+          if ((s & (a.n_iss - 1)) != w) continue;
+          if (!wait_bar(su32(&ctl->full[s]), rg.ph, ctl, status)) { ok = false; break; }
+          tc_fence_after();
+          fence_async_smem();  // B rows and scale words arrived through cp.async (generic proxy)
+          const uint64_t so = (uint64_t)(s * st16);
+          for (int cc = 0; cc < CH; ++cc) {
+            const uint32_t col = tmem + (uint32_t)(a.sf_base + (s * CH + cc) * kSfSlot);
+            tc_cp_32x128b_x4(col, dsa0 + so + (uint64_t)(cc * (kSfBytes >> 4)));
+            tc_cp_32x128b_x4(col + 16, dsb0 + so + (uint64_t)(cc * (kSfBytes >> 4)));
+            const uint64_t da = da0 + so + (uint64_t)(cc * (kATile >> 4)), db = db0 + so + (uint64_t)(cc * bb16);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int h = k & (a.n_acc - 1);
+              tc_mma(d + (uint32_t)(h * a.acc_cols), da + 2 * k, db + 2 * k,
+                     idesc | ((uint32_t)k << 4) | ((uint32_t)k << 29), col, col + 16, (started >> h) & 1u);
+              started |= 1u << h;
+            }
+          }
+          tc_commit(su32(&ctl->empty[s]));
+        }
+        if (!ok) break;
+        tc_commit(su32(&ctl->acc_full[b]));
+      }
+      tc_commit(su32(&ctl->drain));  // every MMA issued above has completed when this arrives
+      wait_bar(su32(&ctl->drain), 0, ctl, status);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 0-3)
+    // Per item: all partial accumulators of a 16-column block are read with one wait, the buffer is
+    // released right after the last block is read, and only then are the sums formed and stored.
+    const int q = warp;
+    long long i = 0;
+    int bad = 0;
+    int g0 = 0;  // ring slot of the item's first stage
+    Item it;
+    for (long long ii = blockIdx.x; item_at<MODE>(a, ii, n_items, it); ii += gridDim.x, ++i) {
+      const int b = (int)(i & 1);
+      // gate weight of token `lane` of the work group (down projection), fetched before the wait
+      const float wlane = (MODE == DOWN && lane < it.wg.ntok) ? __ldg(&a.ws.perm_w[it.wg.pos0 + lane]) : 0.0f;
+      if (!__all_sync(0xffffffffu, wait_bar(su32(&ctl->acc_full[b]), (uint32_t)((i >> 1) & 1), ctl, status))) break;
+      tc_fence_after();
+      const int row = it.mt * 128 + 32 * q + lane;
+      const int ncols = it.wg.ntok * a.terms;
+      const int nst = (it.j1 - it.j0) / CH;  // stages of the item
+      // the item's t-th stage sits in slot (g0 + t) mod S, owned by issuer slot mod n_iss; the
+      // issuers' partial sums are added in the order in which they first appear
+      int order[kMaxIss];
+      int nacc = 0;
+      {
+        unsigned seen = 0;
+        for (int t = 0, sl = g0; t < nst && t < S && nacc < a.n_iss; ++t, sl = (sl + 1 == S) ? 0 : sl + 1) {
+          const int w = sl & (a.n_iss - 1);
+          if (!(seen & (1u << w))) {
+            seen |= 1u << w;
+            order[nacc++] = w;
+          }
+        }
+      }
+      const uint32_t lane_base =
+          tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * a.n_iss * a.n_acc * a.acc_cols);
+      const int nparts = nacc * a.n_acc;  // (issuer, accumulator) pairs, issuer-major in first-use order
+      float run = 0.0f;
+      bool nan_row = false;
+      int tk = 0, jt = 0;  // token and term of the current column
+      for (int cb = 0; cb < ncols; cb += 16) {
+        float v[16];
+#pragma unroll
+        for (int cc = 0; cc < 16; ++cc) v[cc] = 0.0f;
+        for (int p0 = 0; p0 < nparts; p0 += 4) {
+          uint32_t u[4][16];
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            if (p0 + t < nparts) {
+              const int pp = p0 + t;
+              const int col0 = (order[pp / a.n_acc] * a.n_acc + (pp - (pp / a.n_acc) * a.n_acc)) * a.acc_cols;
+              tc_ld16(lane_base + (uint32_t)(col0 + cb), u[t]);
+            }
+          tc_wait_ld();
+          if (cb + 16 >= ncols && p0 + 4 >= nparts) {  // buffer read completely: hand it back
+            tc_fence_before();
+            mbar_arrive(su32(&ctl->acc_empty[b]));
+          }
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            if (p0 + t < nparts) {
+#pragma unroll
+              for (int cc = 0; cc < 16; ++cc) v[cc] += __uint_as_float(u[t][cc]);
+            }
+        }
+#pragma unroll
+        for (int cc = 0; cc < 16; ++cc) {
+          const int col = cb + cc;
+          if (col < ncols) {
+            run += v[cc];
+            if (++jt == a.terms) {
+              jt = 0;
+              const long long pos = it.wg.pos0 + tk;
+              nan_row |= (run != run);
+              if (MODE == GATEUP)
+                a.ws.gupart[((pos * c.ks + it.kp) * 2 + it.mat) * c.f + row] = run;
+              else
+                a.ws.part[pos * c.d + row] = run * __shfl_sync(0xffffffffu, wlane, tk & 31);
+              run = 0.0f;
+              ++tk;
+            }
+          }
+        }
+      }
+      g0 = (g0 + nst) % S;
+      // activations are finite by construction, so a NaN sum means a NaN weight scale: find it
+      if (nan_row) {
+        const uint8_t* sr = scale_row<MODE>(a, it, row);
+        for (int j = it.j0; j < it.j1; ++j)
+          bad |= (__vcmpeq4(__ldg(reinterpret_cast<const unsigned*>(sr) + j), 0xFFFFFFFFu) != 0u);
+      }
+    }
+    if (bad) atomicOr(&status[CTRL_STATUS], ST_NAN_SCALE);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+  }
+}
+
+// ------------------------------------------------------------------------------- GLU and combine
+// h = SiLU(g) * u per position and 32-row block of d_ff, the gate/up reduction parts summed in a fixed
+// order, written as E4M3 terms (one warp per (position, block); routed positions past the routed
+// count are skipped).
+__global__ void __launch_bounds__(256) k_glu(Cfg c, Ws ws, long long T) {
+  const int lane = threadIdx.x & 31;
+  const long long P_R = T * c.k, P = P_R + (long long)c.S * T;
+  const int nb = c.f / 32;
+  const long long n_routed_pos = ws.ctrl[CTRL_NPOS];
+  for (long long wi = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; wi < P * nb;
+       wi += ((long long)gridDim.x * blockDim.x) >> 5) {
+    const long long pos = wi / nb;
+    const int blk = (int)(wi - pos * nb);
+    if (pos < P_R && pos >= n_routed_pos) continue;
+    const int row = blk * 32 + lane;
+    const float* src = ws.gupart + pos * c.ks * 2 * c.f;
+    float g = 0.0f, u = 0.0f;
+    for (int kp = 0; kp < c.ks; ++kp) {
+      g += src[((long long)kp * 2 + 0) * c.f + row];
+      u += src[((long long)kp * 2 + 1) * c.f + row];
+    }
+    const float h = silu(g) * u;
+    split_terms(h, c.hterms, ws.hq + (pos * c.hterms) * c.f + row, c.f, ws.hs + (pos * c.hterms) * nb + blk, nb,
+                lane);
+  }
+}
+
+// y[t] = sum over the top-k slots of t (in slot order) of the gate-weighted expert outputs, then the
+// shared experts; one thread per (token, row of d_model).
+__global__ void __launch_bounds__(256) k_combine(Cfg c, Ws ws, float* y, long long T) {
+  const long long P_R = T * c.k;
+  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < T * c.d;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const long long tok = idx / c.d;
+    const int row = (int)(idx - tok * c.d);
+    float s = 0.0f;
+    for (int i = 0; i < c.k; ++i) {
+      const int p = ws.inv[tok * c.k + i];
+      if (p >= 0) s += ws.part[(long long)p * c.d + row];
+    }
+    for (int sh = 0; sh < c.S; ++sh) s += ws.part[(P_R + (long long)sh * T + tok) * c.d + row];
+    y[idx] = s;
+  }
+}
+
+// ------------------------------------------------------------------------------- host side
+int g_sms = 0;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::mutex g_mu;
+
+cudaError_t get_encode() {
+  if (g_encode) return cudaSuccess;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return e != cudaSuccess ? e : cudaErrorNotSupported;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return cudaSuccess;
+}
+
+// 3D map over expert records: {K codes, rows, experts}, 128 x 128 boxes of 16U4_ALIGN16B codes.
+struct MapKey {
+  const void* base;
+  long long K, rows, experts, stride;
+  int ch;
+};
+struct MapEntry {
+  MapKey key;
+  CUtensorMap map;
+  bool used;
+};
+constexpr int kMapCache = 64;
+MapEntry g_maps[kMapCache];
+int g_map_next = 0;
+
+// 4D map over one weight matrix of every expert record: {128 codes of a chunk, rows, K/128 chunks,
+// experts}, strides {K/2, 64, record stride} bytes; a box is 128 rows x `ch` chunks of 128 codes
+// (16U4_ALIGN16B: 16 codes per 16-byte slot, 128-byte swizzle), landing as ch tiles of 16 KB.
+cudaError_t weight_map(const uint8_t* base, long long K, long long rows, long long experts, long long stride, int ch,
+                       CUtensorMap* out) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  for (auto& m : g_maps)
+    if (m.used && m.key.base == base && m.key.K == K && m.key.rows == rows && m.key.experts == experts &&
+        m.key.stride == stride && m.key.ch == ch) {
+      *out = m.map;
+      return cudaSuccess;
+    }
+  cudaError_t e = get_encode();
+  if (e != cudaSuccess) return e;
+  MapEntry& m = g_maps[g_map_next];
+  g_map_next = (g_map_next + 1) % kMapCache;
+  cuuint64_t gdim[4] = {128, (cuuint64_t)rows, (cuuint64_t)(K / 128), (cuuint64_t)(experts > 0 ? experts : 1)};
+  cuuint64_t gstride[3] = {(cuuint64_t)(K / 2), 64, (cuuint64_t)stride};
+  cuuint32_t box[4] = {128, 128, (cuuint32_t)ch, 1}, estr[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(&m.map, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 4, const_cast<uint8_t*>(base), gdim, gstride,
+                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    m.used = false;
+    return cudaErrorInvalidValue;
+  }
+  m.key = MapKey{base, K, rows, experts, stride, ch};
+  m.used = true;
+  *out = m.map;
+  return cudaSuccess;
+}
+
+template <int MODE>
+cudaError_t launch_tc(const TcArgs& a, const CUtensorMap& r0, const CUtensorMap& r1, const CUtensorMap& s0,
+                      const CUtensorMap& s1, long long items_max, cudaStream_t st) {
+  if (items_max >= (1LL << 31)) return cudaErrorInvalidValue;  // item indices are decomposed in 32 bits
+  const size_t smem = (size_t)a.stages * a.stage_bytes + sizeof(Ctl) + 1024;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(k_tc<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  long long grid = items_max < g_sms ? items_max : g_sms;
+  if (grid < 1) grid = 1;
+  k_tc<MODE><<<(unsigned)grid, kThreads, smem, st>>>(r0, r1, s0, s1, a);
+  return cudaGetLastError();
+}
+
+// Tile geometry for an MMA N of n_tile: TMEM holds two accumulator buffers and then one scale slot
+// per stage; shared memory holds the stages and the control block.
+// Chunks per stage: kMaxCh when every item's chunk range divides evenly, else 1.
+int chunks_per_stage(long long nch, long long parts) {
+  return (nch % parts == 0 && (nch / parts) % kMaxCh == 0) ? kMaxCh : 1;
+}
+
+// With fewer than 4 stages of ch chunks the stage shrinks to one chunk.
+void size_tiles(TcArgs& a, int ch, int mtiles) {
+  a.div_parts.init((uint32_t)a.parts);
+  a.div_mtiles.init((uint32_t)mtiles);
+  a.acc_cols = (a.n_tile + 15) / 16 * 16;
+  a.n_iss = a.n_tile <= 32 ? 4 : (a.n_tile <= 64 ? 2 : 1);
+  a.n_acc = 1;  // two alternating accumulators measured no faster at any N
+  a.sf_base = (2 * a.n_iss * a.n_acc * a.acc_cols + 31) / 32 * 32;
+  a.b_bytes = (a.n_tile * 128 + 1023) / 1024 * 1024;
+  for (;; ch = 1) {
+    a.ch = ch;
+    a.stage_bytes = ch * (kATile + a.b_bytes + kSfBytes);
+    int st = (227 * 1024 - 1024 - (int)sizeof(Ctl)) / a.stage_bytes;
+    const int tm = (kTmemCols - a.sf_base) / (kSfSlot * ch);
+    if (st > tm) st = tm;
+    if (st > kMaxStages) st = kMaxStages;
+    a.stages = st;
+    if (st >= 4 || ch == 1) break;
+  }
+}
+
+int round16(int v) { return (v + 15) / 16 * 16; }
+
+}  // namespace
+
+namespace {
+
+struct TcMaps {
+  CUtensorMap gr, ur, gs, us, dr, ds;
+};
+
+cudaError_t setup(const Cfg& c, const uint8_t* routed, const uint8_t* shared, int ch_gu, int ch_dn, TcMaps& m,
+                  const uint8_t*& sh) {
+  if (g_sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (g_sms <= 0) g_sms = 1;
+  }
+  const long long nc = (long long)c.d * c.f / 2, ns = (long long)c.d * c.f / 32;
+  sh = (c.S > 0 && shared) ? shared : routed;
+  const long long sh_n = c.S > 0 ? c.S : 1;
+  cudaError_t e;
+  if (ch_gu > 0) {
+    if ((e = weight_map(routed, c.d, c.f, c.E, c.stride, ch_gu, &m.gr)) != cudaSuccess) return e;
+    if ((e = weight_map(routed + nc + ns, c.d, c.f, c.E, c.stride, ch_gu, &m.ur)) != cudaSuccess) return e;
+    if ((e = weight_map(sh, c.d, c.f, sh_n, c.stride, ch_gu, &m.gs)) != cudaSuccess) return e;
+    if ((e = weight_map(sh + nc + ns, c.d, c.f, sh_n, c.stride, ch_gu, &m.us)) != cudaSuccess) return e;
+  }
+  if (ch_dn > 0) {
+    if ((e = weight_map(routed + 2 * (nc + ns), c.f, c.d, c.E, c.stride, ch_dn, &m.dr)) != cudaSuccess) return e;
+    if ((e = weight_map(sh + 2 * (nc + ns), c.f, c.d, sh_n, c.stride, ch_dn, &m.ds)) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+TcArgs base_args(const Cfg& c, const Ws& ws, const uint8_t* routed, const uint8_t* sh, float* y, long long T) {
+  TcArgs a{};
+  a.c = c;
+  a.ws = ws;
+  a.routed = routed;
+  a.shared = sh;
+  a.y = y;
+  a.T = T;
+  a.hterms = c.hterms;
+  return a;
+}
+
+}  // namespace
+
+cudaError_t launch_gateup(const Cfg& c, const Ws& ws, const uint8_t* routed, const uint8_t* shared, float* y,
+                          long long T, long long wg_max, cudaStream_t st) {
+  TcArgs a = base_args(c, ws, routed, shared, y, T);
+  a.terms = c.xterms;
+  a.n_tile = round16(c.wgt * c.xterms);
+  a.parts = c.ks;
+  size_tiles(a, chunks_per_stage(c.d / 128, c.ks), c.f / 128);
+  if (a.stages < 2) return cudaErrorInvalidConfiguration;
+  TcMaps m;
+  cudaError_t e = setup(c, routed, shared, a.ch, 0, m, a.shared);
+  if (e != cudaSuccess) return e;
+  e = launch_tc<GATEUP>(a, m.gr, m.ur, m.gs, m.us, wg_max * 2 * (c.f / 128) * a.parts, st);
+  if (e != cudaSuccess) return e;
+  const long long warps = (T * (c.k + c.S)) * (c.f / 32);
+  long long blocks = (warps + 7) / 8;
+  if (blocks > 4LL * g_sms) blocks = 4LL * g_sms;
+  k_glu<<<(unsigned)(blocks > 0 ? blocks : 1), 256, 0, st>>>(c, ws, T);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_down(const Cfg& c, const Ws& ws, const uint8_t* routed, const uint8_t* shared, float* y,
+                        long long T, long long wg_max, cudaStream_t st) {
+  TcArgs a = base_args(c, ws, routed, shared, y, T);
+  a.terms = c.hterms;
+  a.n_tile = round16(c.wgt * c.hterms);
+  a.parts = 1;
+  size_tiles(a, chunks_per_stage(c.f / 128, 1), c.d / 128);
+  if (a.stages < 2) return cudaErrorInvalidConfiguration;
+  TcMaps m;
+  cudaError_t e = setup(c, routed, shared, 0, a.ch, m, a.shared);
+  if (e != cudaSuccess) return e;
+  e = launch_tc<DOWN>(a, m.dr, m.dr, m.ds, m.ds, wg_max * (c.d / 128), st);
+  if (e != cudaSuccess) return e;
+  long long blocks = (T * c.d + 255) / 256;
+  if (blocks > 8LL * g_sms) blocks = 8LL * g_sms;
+  k_combine<<<(unsigned)blocks, 256, 0, st>>>(c, ws, y, T);
+  return cudaGetLastError();
+}
+
+}  // namespace k3
