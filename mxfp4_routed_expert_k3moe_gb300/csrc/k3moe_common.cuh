@@ -77,6 +77,12 @@ __device__ __forceinline__ uint4 ld_v4(const void* p) {
   return v;
 }
 
+// Programmatic dependent launch: kernels of the layer are launched so that the next one may be
+// scheduled before the previous one ends; each waits here for its predecessor grid to complete
+// (and its memory to be visible) before it touches anything the predecessor writes.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
 // Split one 32-element block (one value per lane of the warp) into `terms` E4M3 terms with E8M0

@@ -229,6 +229,86 @@ __device__ void build_permutation(const Cfg& c, const Ws& ws, long long T, const
   __syncthreads();
 }
 
+// The same permutation for at most blockDim.x routed slots, without arrays over the experts: slot s
+// (thread s) finds its position by counting the valid slots that sort before it (expert id, then
+// slot order), and starts a work group when its rank within its expert is a multiple of wgt; the
+// work groups are numbered by a block-wide count of the starts before each position.
+__device__ void build_permutation_small(const Cfg& c, const Ws& ws, long long T, const int* idx, const float* w,
+                                        int* sm) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+  const int E = c.E, k = c.k, W = c.wgt;
+  const int n = (int)(T * k);
+  int* s_e = sm;               // [n] expert of each slot (-1 if invalid)
+  int* s_flag = sm + n;        // [n] by position: 1 if the position starts a work group
+  int* s_wsum = sm + 2 * n;    // [32] per-warp start counts
+  int e = -1;
+  if (tid < n) {
+    e = idx[tid];
+    if (e < 0 || e >= E) {
+      set_status(ws.ctrl, ST_BAD_EXPERT);
+      e = -1;
+    }
+    s_e[tid] = e;
+  }
+  const int npos = __syncthreads_count(tid < n && e >= 0);
+  int pos = -1, same_before = 0, cnt_e = 0;
+  if (tid < n && e >= 0) {
+    int before = 0;
+    for (int q = 0; q < n; ++q) {
+      const int eq = s_e[q];
+      if (eq < 0) continue;
+      before += (eq < e || (eq == e && q < tid)) ? 1 : 0;
+      cnt_e += (eq == e) ? 1 : 0;
+      same_before += (eq == e && q < tid) ? 1 : 0;
+    }
+    pos = before;
+    ws.perm_tok[pos] = tid / k;
+    ws.perm_w[pos] = w[tid];
+    s_flag[pos] = (same_before % W == 0) ? 1 : 0;
+  }
+  if (tid < n) ws.inv[tid] = pos;
+  __syncthreads();
+  // exclusive count of work-group starts before each position
+  const int f = (tid < npos) ? s_flag[tid] : 0;
+  const unsigned bal = __ballot_sync(0xffffffffu, f);
+  if (lane == 0) s_wsum[warp] = __popc(bal);
+  __syncthreads();
+  int base = 0, n_routed_wg = 0;
+  for (int q = 0; q < nw; ++q) {
+    base += (q < warp) ? s_wsum[q] : 0;
+    n_routed_wg += s_wsum[q];
+  }
+  const int g_at = base + __popc(bal & ((1u << lane) - 1u));  // group number of position tid
+  __syncthreads();
+  if (tid < npos) s_flag[tid] = g_at;  // now the group number of each position
+  __syncthreads();
+  if (tid < n && e >= 0 && same_before % W == 0) {
+    const int g = s_flag[pos];
+    ws.wgs[g] = WorkGroup{e, pos, min(W, cnt_e - same_before), 0};
+  }
+  const long long pr = (long long)n;  // shared positions start after all routed slots
+  const int nwt = (int)((T + W - 1) / W);
+  for (int q = tid; q < c.S * nwt; q += blockDim.x) {
+    const int sh = q / nwt, i = q % nwt;
+    const long long p0 = (long long)i * W;
+    ws.wgs[n_routed_wg + q] = WorkGroup{E + sh, (int)(pr + (long long)sh * T + p0), (int)min((long long)W, T - p0), 0};
+  }
+  for (long long q = tid; q < (long long)c.S * T; q += blockDim.x) {
+    ws.perm_tok[pr + q] = (int)(q % T);
+    ws.perm_w[pr + q] = 1.0f;
+  }
+  if (tid == 0) {
+    ws.ctrl[CTRL_NWG] = n_routed_wg + c.S * nwt;
+    ws.ctrl[CTRL_NPOS] = npos;
+  }
+  __syncthreads();
+}
+
+__device__ void permute(const Cfg& c, const Ws& ws, long long T, const int* idx, const float* w, int* sm) {
+  if (T * c.k <= (long long)blockDim.x) build_permutation_small(c, ws, T, idx, w, sm);
+  else build_permutation(c, ws, T, idx, w, sm);
+}
+
 struct RouteArgs {
   Cfg c;
   Ws ws;
@@ -249,89 +329,113 @@ __host__ __device__ __forceinline__ size_t route_tile_bytes(const Cfg& c, int tt
   return (m + 15) & ~(size_t)15;
 }
 
+// Router CTA: 8 warps, two expert rows, each row's reduction axis split in four quarters (one warp
+// each), so that every warp issues all router-weight loads of its quarter at once (the weights are
+// read once and stream; the latency of one batch is paid, not four). The token tile of x is staged
+// in shared memory meanwhile. Warps also produce the E4M3 terms of x, one 32-element block each.
 template <int TT>
-__global__ void __launch_bounds__(256) k_route(RouteArgs a) {
+__global__ void __launch_bounds__(256, 3) k_route(RouteArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ int s_last;
+  __shared__ float s_part[8][TT];
+  pdl_wait();  // the previous layer's kernels may still use the workspace and produce x
+  pdl_launch_dependents();
   const Cfg& c = a.c;
   const int nw = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int e = blockIdx.x * nw + warp;
+  const int r = warp >> 2, kq = warp & 3;
+  const int e = blockIdx.x * 2 + r;
   const long long t0 = (long long)blockIdx.y * TT;
   const int ntt = (int)min((long long)TT, a.T - t0);
   const int esz = c.x_f32 ? 4 : 2;
   const int row_bytes = c.d * esz;
   unsigned long long* cand = reinterpret_cast<unsigned long long*>(smem + route_tile_bytes(c, TT));
 
-  // the token tile of x goes to shared memory once per CTA
+  // the token tile of x goes to shared memory (asynchronously, waited for below)
   {
     const uint8_t* src = reinterpret_cast<const uint8_t*>(a.x) + t0 * row_bytes;
     const uint32_t dst = (uint32_t)__cvta_generic_to_shared(smem);
     const int bytes = ntt * row_bytes;
     for (int off = threadIdx.x * 16; off < bytes; off += blockDim.x * 16)
       asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + off), "l"(src + off) : "memory");
-    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
-    __syncthreads();
+    asm volatile("cp.async.commit_group;" ::: "memory");
   }
 
-  // logits of expert row e for the tile's tokens. Each segment issues all of its router-weight loads before any arithmetic.
-  constexpr int U = (TT == 1) ? 14 : 8;
-  if (e < c.E) {
-    float acc[TT];
+  // quarter [jb, je) of row e: U float4 loads per lane per batch, all issued before any arithmetic
+  constexpr int U = 14;
+  const int qlen = c.d / 4, jb = kq * qlen, je = jb + qlen;
+  float acc[TT];
 #pragma unroll
-    for (int tt = 0; tt < TT; ++tt) acc[tt] = 0.0f;
-    const float* wrow = a.W + (long long)e * c.d;
-    for (int j0 = 0; j0 < c.d; j0 += 128 * U) {
-      uint4 wv[U];
+  for (int tt = 0; tt < TT; ++tt) acc[tt] = 0.0f;
+  const float* wrow = a.W + (long long)(e < c.E ? e : 0) * c.d;
+  bool waited = false;
+  for (int j0 = jb; j0 < je; j0 += 128 * U) {
+    uint4 wv[U];
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int j = j0 + u * 128 + lane * 4;
-        wv[u] = (j < c.d) ? ld_stream_v4(wrow + j) : make_uint4(0, 0, 0, 0);
-      }
+    for (int u = 0; u < U; ++u) {
+      const int j = j0 + u * 128 + lane * 4;
+      wv[u] = (e < c.E && j < je) ? ld_stream_v4(wrow + j) : make_uint4(0, 0, 0, 0);
+    }
+    if (!waited) {
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+      __syncthreads();
+      waited = true;
+    }
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int j = j0 + u * 128 + lane * 4;
-        if (j < c.d) {
-          const float w4[4] = {__uint_as_float(wv[u].x), __uint_as_float(wv[u].y), __uint_as_float(wv[u].z),
-                               __uint_as_float(wv[u].w)};
+    for (int u = 0; u < U; ++u) {
+      const int j = j0 + u * 128 + lane * 4;
+      if (j < je) {
+        const float w4[4] = {__uint_as_float(wv[u].x), __uint_as_float(wv[u].y), __uint_as_float(wv[u].z),
+                             __uint_as_float(wv[u].w)};
 #pragma unroll
-          for (int tt = 0; tt < TT; ++tt) {
-            if (tt < ntt) {
-              float xv[4];
-              const uint8_t* xr = smem + tt * row_bytes;
-              if (c.x_f32) {
-                const float4 q = *reinterpret_cast<const float4*>(xr + 4 * j);
-                xv[0] = q.x; xv[1] = q.y; xv[2] = q.z; xv[3] = q.w;
-              } else {
-                const uint2 q = *reinterpret_cast<const uint2*>(xr + 2 * j);
-                xv[0] = __uint_as_float(q.x << 16); xv[1] = __uint_as_float(q.x & 0xFFFF0000u);
-                xv[2] = __uint_as_float(q.y << 16); xv[3] = __uint_as_float(q.y & 0xFFFF0000u);
-              }
-#pragma unroll
-              for (int q = 0; q < 4; ++q) acc[tt] = fmaf(w4[q], xv[q], acc[tt]);
+        for (int tt = 0; tt < TT; ++tt) {
+          if (tt < ntt) {
+            float xv[4];
+            const uint8_t* xr = smem + tt * row_bytes;
+            if (c.x_f32) {
+              const float4 q = *reinterpret_cast<const float4*>(xr + 4 * j);
+              xv[0] = q.x; xv[1] = q.y; xv[2] = q.z; xv[3] = q.w;
+            } else {
+              const uint2 q = *reinterpret_cast<const uint2*>(xr + 2 * j);
+              xv[0] = __uint_as_float(q.x << 16); xv[1] = __uint_as_float(q.x & 0xFFFF0000u);
+              xv[2] = __uint_as_float(q.y << 16); xv[3] = __uint_as_float(q.y & 0xFFFF0000u);
             }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[tt] = fmaf(w4[q], xv[q], acc[tt]);
           }
         }
       }
     }
-    const float b = a.bias ? a.bias[e] : 0.0f;
+  }
+  if (!waited) {  // (only when the quarter is empty)
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
+  }
 #pragma unroll
-    for (int tt = 0; tt < TT; ++tt) {
-      float v = acc[tt];
+  for (int tt = 0; tt < TT; ++tt) {
+    float v = acc[tt];
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      if (lane == 0 && tt < ntt) a.ws.logits[(t0 + tt) * c.E + e] = v + b;
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) s_part[warp][tt] = v;
+  }
+  __syncthreads();
+  // row sums of the four quarters, in quarter order
+  if (threadIdx.x < 2 * TT) {
+    const int rr = threadIdx.x / TT, tt = threadIdx.x - rr * TT;
+    const int er = blockIdx.x * 2 + rr;
+    if (er < c.E && tt < ntt) {
+      const float v = ((s_part[4 * rr][tt] + s_part[4 * rr + 1][tt]) + s_part[4 * rr + 2][tt]) + s_part[4 * rr + 3][tt];
+      a.ws.logits[(t0 + tt) * c.E + er] = v + (a.bias ? a.bias[er] : 0.0f);
     }
   }
-  // E4M3 terms of x: each warp of the grid takes 256-element segments of the tile's tokens
+  // E4M3 terms of x: warp gw of the grid takes the 32-element blocks gw, gw + 8 * gridDim.x, ...
   if (a.mode & RM_XPREP) {
-    for (int sg = e; sg * 256 < c.d; sg += (int)gridDim.x * nw) {
+    for (int blk = blockIdx.x * nw + warp; blk * 32 < c.d; blk += (int)gridDim.x * nw) {
+      const int j = blk * 32;
       for (int tt = 0; tt < ntt; ++tt) {
         const uint8_t* xr = smem + tt * row_bytes;
-        for (int j = sg * 256; j < sg * 256 + 256 && j < c.d; j += 32) {
-          const float v = c.x_f32 ? reinterpret_cast<const float*>(xr)[j + lane]
-                                  : __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(xr)[j + lane] << 16);
-          xterms_block(c, a.ws, v, t0 + tt, j, lane);
-        }
+        const float v = c.x_f32 ? reinterpret_cast<const float*>(xr)[j + lane]
+                                : __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(xr)[j + lane] << 16);
+        xterms_block(c, a.ws, v, t0 + tt, j, lane);
       }
     }
   }
@@ -366,8 +470,7 @@ __global__ void __launch_bounds__(256) k_route(RouteArgs a) {
     __threadfence();
     if (threadIdx.x == 0) a.ws.ctrl[CTRL_ROUTER_DONE] = 0;
   }
-  if (a.mode & RM_PERMUTE)
-    build_permutation(c, a.ws, a.T, a.ws.topk_idx, a.ws.topk_w, reinterpret_cast<int*>(smem));
+  if (a.mode & RM_PERMUTE) permute(c, a.ws, a.T, a.ws.topk_idx, a.ws.topk_w, reinterpret_cast<int*>(smem));
 }
 
 struct PrepArgs {
@@ -382,8 +485,10 @@ struct PrepArgs {
 // Activation planes for k3moe_expert_ffn (CTAs 1..), permutation of the given routing (CTA 0).
 __global__ void __launch_bounds__(256) k_prep(PrepArgs a) {
   extern __shared__ int s_perm[];  // 4E + 2 ints
+  pdl_wait();
+  pdl_launch_dependents();
   if (blockIdx.x == 0) {
-    build_permutation(a.c, a.ws, a.T, a.idx, a.w, s_perm);
+    permute(a.c, a.ws, a.T, a.idx, a.w, s_perm);
     return;
   }
   const int warp = threadIdx.x >> 5;
@@ -427,9 +532,8 @@ cudaError_t launch_route_tt(const RouteArgs& a, int warps, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  dim3 grid((a.c.E + warps - 1) / warps, (unsigned)((a.T + TT - 1) / TT));
-  k_route<TT><<<grid, warps * 32, smem, st>>>(a);
-  return cudaGetLastError();
+  dim3 grid((a.c.E + 1) / 2, (unsigned)((a.T + TT - 1) / TT));
+  return launch_pdl(k_route<TT>, grid, dim3(warps * 32), smem, st, a);
 }
 
 cudaError_t launch_route(const Cfg& c, const Ws& ws, const void* x, long long T, const float* W, const float* bias,
@@ -441,8 +545,8 @@ cudaError_t launch_route(const Cfg& c, const Ws& ws, const void* x, long long T,
   };
   if (T >= 8 && fits(8, 8)) return launch_route_tt<8>(a, 8, st);
   if (T >= 4 && fits(4, 8)) return launch_route_tt<4>(a, 8, st);
-  if (T >= 2 && fits(2, 4)) return launch_route_tt<2>(a, 4, st);
-  return launch_route_tt<1>(a, 4, st);
+  if (T >= 2 && fits(2, 8)) return launch_route_tt<2>(a, 8, st);
+  return launch_route_tt<1>(a, 8, st);
 }
 
 cudaError_t launch_prep(const Cfg& c, const Ws& ws, const void* x, long long T, const int* idx, const float* w,
@@ -456,8 +560,7 @@ cudaError_t launch_prep(const Cfg& c, const Ws& ws, const void* x, long long T, 
     if (e != cudaSuccess) return e;
     g_route_attr_set = true;
   }
-  k_prep<<<(unsigned)ctas, 256, sizeof(int) * (4 * (size_t)c.E + 2), st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(k_prep, dim3((unsigned)ctas), dim3(256), sizeof(int) * (4 * (size_t)c.E + 2), st, a);
 }
 
 cudaError_t launch_rmsnorm(const float* x, long long T, int d, float eps, float* out, cudaStream_t st) {

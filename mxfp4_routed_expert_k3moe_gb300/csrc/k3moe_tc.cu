@@ -315,6 +315,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + (size_t)S * a.stage_bytes);
   const Cfg& c = a.c;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_wait();  // the routing (or the gate/up results) come from the previous kernel
+  pdl_launch_dependents();
   const int n_wg = a.ws.ctrl[CTRL_NWG];
   const int nmat = MODE == GATEUP ? 2 : 1;
   const int mtiles = (MODE == GATEUP ? c.f : c.d) / 128;
@@ -575,6 +577,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // order, written as E4M3 terms (one warp per (position, block); routed positions past the routed
 // count are skipped).
 __global__ void __launch_bounds__(256) k_glu(Cfg c, Ws ws, long long T) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const long long P_R = T * c.k, P = P_R + (long long)c.S * T;
   const int nb = c.f / 32;
@@ -600,6 +604,8 @@ __global__ void __launch_bounds__(256) k_glu(Cfg c, Ws ws, long long T) {
 // y[t] = sum over the top-k slots of t (in slot order) of the gate-weighted expert outputs, then the
 // shared experts; one thread per (token, row of d_model).
 __global__ void __launch_bounds__(256) k_combine(Cfg c, Ws ws, float* y, long long T) {
+  pdl_wait();
+  pdl_launch_dependents();
   const long long P_R = T * c.k;
   for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < T * c.d;
        idx += (long long)gridDim.x * blockDim.x) {
@@ -690,8 +696,7 @@ cudaError_t launch_tc(const TcArgs& a, const CUtensorMap& r0, const CUtensorMap&
   }
   long long grid = items_max < g_sms ? items_max : g_sms;
   if (grid < 1) grid = 1;
-  k_tc<MODE><<<(unsigned)grid, kThreads, smem, st>>>(r0, r1, s0, s1, a);
-  return cudaGetLastError();
+  return launch_pdl(k_tc<MODE>, dim3((unsigned)grid), dim3(kThreads), smem, st, r0, r1, s0, s1, a);
 }
 
 // Tile geometry for an MMA N of n_tile: TMEM holds two accumulator buffers and then one scale slot
@@ -787,8 +792,7 @@ cudaError_t launch_gateup(const Cfg& c, const Ws& ws, const uint8_t* routed, con
   const long long warps = (T * (c.k + c.S)) * (c.f / 32);
   long long blocks = (warps + 7) / 8;
   if (blocks > 4LL * g_sms) blocks = 4LL * g_sms;
-  k_glu<<<(unsigned)(blocks > 0 ? blocks : 1), 256, 0, st>>>(c, ws, T);
-  return cudaGetLastError();
+  return launch_pdl(k_glu, dim3((unsigned)(blocks > 0 ? blocks : 1)), dim3(256), 0, st, c, ws, T);
 }
 
 cudaError_t launch_down(const Cfg& c, const Ws& ws, const uint8_t* routed, const uint8_t* shared, float* y,
@@ -806,8 +810,7 @@ cudaError_t launch_down(const Cfg& c, const Ws& ws, const uint8_t* routed, const
   if (e != cudaSuccess) return e;
   long long blocks = (T * c.d + 255) / 256;
   if (blocks > 8LL * g_sms) blocks = 8LL * g_sms;
-  k_combine<<<(unsigned)blocks, 256, 0, st>>>(c, ws, y, T);
-  return cudaGetLastError();
+  return launch_pdl(k_combine, dim3((unsigned)blocks), dim3(256), 0, st, c, ws, y, T);
 }
 
 }  // namespace k3
