@@ -16,12 +16,20 @@ constexpr long long kMaxK = 32;
 constexpr long long kMaxS = 8;
 constexpr int kMaxDModel = 25600;
 // Reduction parts of the gate/up projection: at a few tokens the (work group, row tile) items are
-// too few to spread over the SMs, so each is split along d into 4 parts summed by the last one.
-long long gateup_parts(long long T, long long d) {
-  const long long p = T <= 4 ? 4 : 1;
-  return p < d / 128 ? p : d / 128;
+// too few to spread over the SMs, so each is split along d into 4 parts (at most one per chunk of
+// the reduction axis: 256 codes in the E2M1 form, 128 in the E4M3 form), summed by the GLU kernel.
+long long gateup_parts(long long T, long long d, bool fp4) {
+  const long long p = T <= 4 ? 4 : 1, nch = d / (fp4 ? 256 : 128);
+  return p < nch ? p : nch;
 }
 constexpr long long kMaxTerms = 3;     // E4M3 terms per activation block (x: 2 bf16 / 3 fp32; h: 3)
+constexpr long long kMaxTermsFp4 = 8;  // E2M1 terms per activation block
+constexpr long long kFp4MaxT = 2;      // the E2M1 / mxf4 path serves up to this many tokens
+
+// E2M1 activation terms and kind::mxf4 MMAs for few tokens (d_model and d_ff multiples of 256).
+bool use_fp4(const k3moe_config* c, long long T) {
+  return T <= kFp4MaxT && c->d_model % 256 == 0 && c->d_ff % 256 == 0;
+}
 
 size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -85,12 +93,14 @@ Layout make_layout(const k3moe_config* c, long long T) {
   take(L.perm_w, sizeof(float) * P);
   take(L.inv, sizeof(int) * T * k);
   take(L.wgs, sizeof(k3::WorkGroup) * wg_bound(c, T));
-  take(L.xq, (size_t)(T * kMaxTerms * d));
-  take(L.xs, (size_t)(T * kMaxTerms * (d / 32)));
-  take(L.hq, (size_t)(P * kMaxTerms * f));
-  take(L.hs, (size_t)(P * kMaxTerms * (f / 32)));
+  const bool fp4 = use_fp4(c, T);
+  const long long terms = fp4 ? kMaxTermsFp4 : kMaxTerms;
+  take(L.xq, (size_t)(T * terms * (fp4 ? d / 2 : d)));
+  take(L.xs, (size_t)(T * terms * (d / 32)));
+  take(L.hq, (size_t)(P * terms * (fp4 ? f / 2 : f)));
+  take(L.hs, (size_t)(P * terms * (f / 32)));
   take(L.part, sizeof(float) * P * d);
-  take(L.gupart, sizeof(float) * P * gateup_parts(T, d) * 2 * f);
+  take(L.gupart, sizeof(float) * P * gateup_parts(T, d, fp4) * 2 * f);
   take(L.rtcnt, sizeof(int) * ((T + 7) / 8));
   L.total = o;
   return L;
@@ -129,10 +139,17 @@ Cfg make_cfg(const k3moe_config* c, long long T) {
   k.k = c->top_k;
   k.S = c->n_shared;
   k.x_f32 = c->x_dtype == K3MOE_X_F32 ? 1 : 0;
-  k.wgt = (int)(T < 32 ? T : 32);
-  k.ks = (int)gateup_parts(T, c->d_model);
-  k.xterms = k.x_f32 ? 3 : 2;
-  k.hterms = 3;
+  k.fp4 = use_fp4(c, T) ? 1 : 0;
+  const long long wmax = k.fp4 ? 16 : 32;
+  k.wgt = (int)(T < wmax ? T : wmax);
+  k.ks = (int)gateup_parts(T, c->d_model, k.fp4 != 0);
+  if (k.fp4) {
+    k.xterms = 8;  // at most 3^-8 of the block maximum per element; ~1e-7 of max|y| measured
+    k.hterms = 8;
+  } else {
+    k.xterms = k.x_f32 ? 3 : 2;
+    k.hterms = 3;
+  }
   k.stride = c->record_stride;
   return k;
 }
@@ -158,9 +175,14 @@ size_t k3moe_record_bytes(const k3moe_config* cfg) {
 size_t k3moe_workspace_bytes(const k3moe_config* cfg, int64_t max_tokens) {
   if (validate(cfg) != K3MOE_OK || !tokens_ok(cfg, max_tokens)) return 0;
   // the layout grows with T except where the gate/up split drops from 4 parts to 1 (above 4 tokens)
+  // and where the E2M1 activation form gives way to the E4M3 one (above kFp4MaxT tokens)
   const long long T = max_tokens < 1 ? 1 : max_tokens;
-  const size_t a = make_layout(cfg, T).total, b = make_layout(cfg, T < 4 ? T : 4).total;
-  return a > b ? a : b;
+  size_t best = make_layout(cfg, T).total;
+  for (long long t : {4LL, kFp4MaxT}) {
+    const size_t b = make_layout(cfg, T < t ? T : t).total;
+    best = b > best ? b : best;
+  }
+  return best;
 }
 
 k3moe_status k3moe_route(const k3moe_config* cfg, const void* x, int64_t T, const float* w_router, const float* bias,

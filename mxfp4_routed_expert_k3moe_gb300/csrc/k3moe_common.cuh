@@ -13,8 +13,9 @@ struct Cfg {
   int x_f32;          // 1 if x is fp32, 0 if bf16
   int wgt;            // max tokens per work group
   int ks;             // reduction parts of gate/up (allocated in the workspace)
-  int xterms;         // E4M3 terms per activation block of x (2 for bf16 x, 3 for fp32 x)
-  int hterms;         // E4M3 terms per block of h
+  int fp4;           // 1: activations as E2M1 terms and kind::mxf4 MMAs (few tokens); 0: E4M3 terms, mxf8f6f4
+  int xterms;         // terms per activation block of x (E4M3: 2 for bf16 x, 3 for fp32 x; E2M1: 8 or 16)
+  int hterms;         // terms per block of h
   long long stride;   // bytes between expert records
 };
 
@@ -47,9 +48,9 @@ struct Ws {
   float* perm_w;      // [P] gate weight of each position (1 for shared)
   int* inv;           // [T*k] position of routed slot (t, i), -1 if the slot was rejected
   WorkGroup* wgs;     // [WGmax]
-  uint8_t* xq;        // [T * xterms, d] E4M3 terms of x (row t*xterms + j)
+  uint8_t* xq;        // [T * xterms, d] E4M3 (or [.., d/2] packed E2M1) terms of x (row t*xterms + j)
   uint8_t* xs;        // [T * xterms, d/32] their E8M0 block scales
-  uint8_t* hq;        // [P * hterms, f] E4M3 terms of h (row p*hterms + j)
+  uint8_t* hq;        // [P * hterms, f] E4M3 (or [.., f/2] packed E2M1) terms of h (row p*hterms + j)
   uint8_t* hs;        // [P * hterms, f/32] their E8M0 block scales
   float* part;        // [P, d] gate-weighted down-projection outputs per position
   float* gupart;      // [P, ks, 2, f] partial gate/up sums of the reduction parts
@@ -75,6 +76,38 @@ __device__ __forceinline__ uint4 ld_v4(const void* p) {
   uint4 v;
   asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
   return v;
+}
+
+// The same split into E2M1 terms (values 0, 0.5, 1, 1.5, 2, 3, 4, 6 and signs) with E8M0 block
+// scales: e_j is chosen so that max|r_j| / 2^{e_j} lies in (3, 6] (no saturation), which makes each
+// rounding residual at most 2^{e_j} <= max|r_j| / 3, so n terms leave at most 3^-n of the block
+// maximum. Codes are packed two per byte (even element in the low nibble): lane l and l ^ 1 share a
+// byte, which the even lane writes to codes[j * code_stride + lane / 2]; lane 0 writes the scale.
+__device__ __forceinline__ void split_terms_fp4(float v, int terms, uint8_t* codes, long long code_stride,
+                                                uint8_t* scales, long long scale_stride, int lane) {
+  float r = v;
+  for (int j = 0; j < terms; ++j) {
+    float amax = fabsf(r);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    int e = 0;
+    if (amax > 0.0f && amax <= 3.402823466e38f) {
+      e = ilogbf(amax) - 2;                    // amax / 2^e in [4, 8)
+      if (amax * pow2i(-e) > 6.0f) e += 1;     // -> (3, 4)
+    }
+    e = e < -127 ? -127 : (e > 127 ? 127 : e);
+    const float s = r * pow2i(-e);
+    uint32_t code, dec;
+    asm("{\n .reg .b8 t;\n .reg .b16 h;\n cvt.rn.satfinite.e2m1x2.f32 t, %2, %3;\n mov.b16 h, {t, t};\n"
+        " cvt.u32.u16 %0, h;\n cvt.rn.f16x2.e2m1x2 %1, t;\n}\n"
+        : "=r"(code), "=r"(dec)
+        : "f"(0.0f), "f"(s));
+    code &= 0xFu;
+    r -= __half2float(__ushort_as_half((unsigned short)(dec & 0xFFFFu))) * pow2i(e);
+    const uint32_t hi = __shfl_down_sync(0xffffffffu, code, 1);
+    if ((lane & 1) == 0) codes[j * code_stride + (lane >> 1)] = (uint8_t)(code | (hi << 4));
+    if (lane == 0) scales[j * scale_stride] = (uint8_t)(e + 127);
+  }
 }
 
 // Programmatic dependent launch: kernels of the layer are launched so that the next one may be

@@ -25,10 +25,14 @@ __device__ __forceinline__ float load_x(const void* x, int x_f32, long long idx)
   return __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(x)[idx] << 16);
 }
 
-// E4M3 terms of the 32-element block of token t starting at element j (lane = element).
+// Activation terms of the 32-element block of token t starting at element j (lane = element).
 __device__ __forceinline__ void xterms_block(const Cfg& c, const Ws& ws, float v, long long t, int j, int lane) {
-  split_terms(v, c.xterms, ws.xq + (t * c.xterms) * c.d + j + lane, c.d,
-              ws.xs + (t * c.xterms) * (c.d / 32) + j / 32, c.d / 32, lane);
+  if (c.fp4)
+    split_terms_fp4(v, c.xterms, ws.xq + (t * c.xterms) * (c.d / 2) + j / 2, c.d / 2,
+                    ws.xs + (t * c.xterms) * (c.d / 32) + j / 32, c.d / 32, lane);
+  else
+    split_terms(v, c.xterms, ws.xq + (t * c.xterms) * c.d + j + lane, c.d,
+                ws.xs + (t * c.xterms) * (c.d / 32) + j / 32, c.d / 32, lane);
 }
 
 // One warp per token: all E4M3 terms of the token (used by k3moe_expert_ffn's preparation).

@@ -4,10 +4,14 @@
 //   down:     o_p = w_p W_down h_p                       (k_tc<DOWN>, one row per position p)
 //             y[t] = sum_i o_(t,i) + sum_s o_(t,s)        (k_combine)
 // The MXFP4 records are consumed as stored (kimi-k3-in-c review, table "KDA·MLA·MoE": the
-// experts multiply the 4-bit codes directly): TMA copies 128 rows x 128 codes of a weight matrix
-// into shared memory (16U4_ALIGN16B: 16 codes per 16-byte slot, 128-byte swizzle), the E8M0 block
-// scales go to tensor memory, and tcgen05.mma.kind::mxf8f6f4.block_scale multiplies the E2M1
-// weights (A: M = 128 rows) by the activations (B: N = tokens x terms), applying both block scales.
+// experts multiply the 4-bit codes directly): TMA copies 128 rows of a weight matrix into shared
+// memory, the E8M0 block scales go to tensor memory, and a block-scaled tcgen05.mma multiplies the
+// E2M1 weights (A: M = 128 rows) by the activations (B: N = tokens x terms), applying both scales.
+// Two forms, chosen by the token count:
+//   - few tokens (fp4): activations as E2M1 terms, kind::mxf4 (K = 64 per MMA); a chunk of the
+//     reduction axis is 256 codes = 128 packed bytes per row, copied as is (128-byte swizzle);
+//   - more tokens: activations as E4M3 terms, kind::mxf8f6f4 (K = 32 per MMA); a chunk is 128 codes,
+//     copied into 16-byte slots of 16 codes (16U4_ALIGN16B). Both chunks take 16 KB per 128 rows.
 //
 // Activations enter as sums of E4M3 terms: each 32-element block of x (or h) is written as
 // v = sum_j q_j 2^{e_j} with q_j E4M3 and 2^{e_j} an E8M0 block scale, each term taking the
@@ -48,16 +52,15 @@ namespace {
 enum { GATEUP = 0, DOWN = 1 };
 constexpr int kMaxIss = 4;                // MMA-issuing warps
 constexpr int kLoaders = 4;               // loader warps
-constexpr int kWarpLoad = 4, kWarpIss = kWarpLoad + kLoaders;
-constexpr int kThreads = 32 * (kWarpIss + kMaxIss);
+constexpr int kWarpLoad = 4, kWarpIss = kWarpLoad + kLoaders, kWarpEnd = kWarpIss + kMaxIss;
+constexpr int kThreads = 32 * kWarpEnd;
 constexpr int kMaxCh = 2;                 // chunks per stage
 constexpr int kTmemCols = 512;
 constexpr int kMaxN = 128;               // largest MMA N (B rows per tile)
-constexpr int kSfSlot = 32;              // TMEM columns per chunk: A scales at +0..3, B scales at +16..19
+// TMEM columns per chunk: E4M3 form: A scales at +0..3, B at +16..19 (32 columns); E2M1 form:
+// two scale words per row (8 blocks of 32): A at +0..3 and +16..19, B at +32.. and +48.. (64 columns)
 constexpr int kMaxStages = 16;
-constexpr int kSfBytes = 1024;           // per stage in shared memory: A scale words, then B scale words
-constexpr int kATile = 128 * 128;        // 128 rows x 128 codes in 16-byte slots
-constexpr uint32_t kATileTx = 128 * 64;  // bytes delivered by the TMA (packed codes)
+constexpr int kATile = 128 * 128;        // A tile of a chunk in shared memory (both forms)
 constexpr uint32_t kWaitLimit = 1u << 24;
 
 // ------------------------------------------------------------------------------- PTX helpers
@@ -107,6 +110,13 @@ __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint3
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%5], [%6], p;\n}\n" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb));
+}
+__device__ __forceinline__ void tc_mma_f4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                          uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], [%6], p;\n}\n" ::"r"(d),
       "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb));
 }
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
@@ -209,6 +219,10 @@ struct TcArgs {
   int sf_base;  // first column of the scale ring (after 2 buffers x n_iss x n_acc accumulators)
   int b_bytes;  // shared-memory bytes of the B tile of a chunk
   int ch;       // chunks per stage
+  int fp4;      // E2M1 form (kind::mxf4, 256-code chunks) or E4M3 form (kind::mxf8f6f4, 128-code chunks)
+  int nch;      // chunks along the reduction axis
+  int sf_slot;  // TMEM columns of the scales of a chunk
+  int sf_bytes; // shared-memory bytes of the scale words of a chunk
   int terms;    // B rows per token in this kernel (x terms for gate/up, h terms for down)
   int hterms;   // h terms written by the gate/up finish
   int parts;    // reduction parts per gate/up row tile
@@ -223,11 +237,34 @@ struct Item {
   WorkGroup wg;
 };
 
+// Item geometry only (no work-group read): what the MMA issuers and the epilogue's ring tracking need.
+template <int MODE>
+__device__ __forceinline__ bool item_geom(const TcArgs& a, long long it, long long n_items, Item& o) {
+  if (it >= n_items) return false;
+  const int nch = a.nch;
+  uint32_t r = (uint32_t)it;
+  uint32_t q = a.div_parts.div(r);
+  o.kp = (int)(r - q * a.div_parts.d);
+  r = q;
+  q = a.div_mtiles.div(r);
+  o.mt = (int)(r - q * a.div_mtiles.d);
+  r = q;
+  if (MODE == GATEUP) {
+    o.mat = (int)(r & 1u);
+    o.wgi = (int)(r >> 1);
+  } else {
+    o.mat = 0;
+    o.wgi = (int)r;
+  }
+  o.j0 = (int)a.div_parts.div((uint32_t)(o.kp * nch));
+  o.j1 = (int)a.div_parts.div((uint32_t)((o.kp + 1) * nch));
+  return true;
+}
+
 template <int MODE>
 __device__ __forceinline__ bool item_at(const TcArgs& a, long long it, long long n_items, Item& o) {
   if (it >= n_items) return false;
-  const Cfg& c = a.c;
-  const int nch = (MODE == GATEUP ? c.d : c.f) / 128;
+  const int nch = a.nch;
   uint32_t r = (uint32_t)it;  // n_items < 2^31 (checked on the host)
   uint32_t q = a.div_parts.div(r);
   o.kp = (int)(r - q * a.div_parts.d);
@@ -323,6 +360,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const long long n_items = (long long)n_wg * nmat * mtiles * a.parts;
   int* status = a.ws.ctrl;
   const int b_off = CH * kATile, sf_off = CH * (kATile + a.b_bytes);
+  const uint32_t tx_chunk = a.fp4 ? 128 * 128 : 128 * 64;  // bytes a chunk's tensor copy delivers
+  const int wpc = a.fp4 ? 2 : 1;                            // scale words per row per chunk
 
   if (n_wg == 0) return;  // nothing routed and no shared experts (k_combine writes y = 0)
 
@@ -384,7 +423,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (cur.bsrc[q] >= 0) {
           const int n = lane + 32 * q;
           const long long r = (long long)cur.bsrc[q] * a.terms + (n - (n / a.terms) * a.terms);
-          bcodes[q] = (MODE == GATEUP ? a.ws.xq : a.ws.hq) + r * (MODE == GATEUP ? c.d : c.f);
+          const int kk = MODE == GATEUP ? c.d : c.f;
+          bcodes[q] = (MODE == GATEUP ? a.ws.xq : a.ws.hq) + r * (a.fp4 ? kk / 2 : kk);
           bscales[q] = (MODE == GATEUP ? a.ws.xs : a.ws.hs) + r * ((MODE == GATEUP ? c.d : c.f) / 32);
         }
       }
@@ -395,14 +435,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         uint8_t* st = smem + (size_t)s * a.stage_bytes;
         if (lane == 0) {
-          mbar_expect_tx(su32(&ctl->full[s]), kATileTx * CH);
+          mbar_expect_tx(su32(&ctl->full[s]), tx_chunk * CH);
           tma_load_4d(su32(st), map, 0, it.mt * 128, j, ecoord, su32(&ctl->full[s]));
         }
         for (int cc = 0; cc < CH; ++cc) {
           const int jj = j + cc;
-          const uint32_t sb = su32(st + b_off + cc * a.b_bytes), sc = su32(st + sf_off + cc * kSfBytes);
+          const uint32_t sb = su32(st + b_off + cc * a.b_bytes), sc = su32(st + sf_off + cc * a.sf_bytes);
+          // scale words: A word h at sc + 512 h, B word h at sc + 512 (wpc + h)
+          for (int h = 0; h < wpc; ++h) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) cp4(sc + 16 * lane + 4 * q, arow[q] + 4 * jj, 4);
+            for (int q = 0; q < 4; ++q) cp4(sc + 512 * h + 16 * lane + 4 * q, arow[q] + 4 * (wpc * jj + h), 4);
+          }
 #pragma unroll
           for (int q = 0; q < kMaxN / 32; ++q) {
             if (bcodes[q]) {
@@ -410,7 +453,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint8_t* src = bcodes[q] + (long long)jj * 128;
 #pragma unroll
               for (int k16 = 0; k16 < 8; ++k16) cp16(sb + n * 128 + ((k16 ^ (n & 7)) << 4), src + k16 * 16);
-              cp4(sc + 512 + 16 * lane + 4 * q, bscales[q] + 4 * jj, 4);
+              for (int h = 0; h < wpc; ++h)
+                cp4(sc + 512 * (wpc + h) + 16 * lane + 4 * q, bscales[q] + 4 * (wpc * jj + h), 4);
             }
           }
         }
@@ -425,18 +469,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuers
     const int w = warp - kWarpIss;
     if (lane == 0 && w < a.n_iss) {
-      const uint32_t idesc =
-          (5u << 7) | (0u << 10) | ((uint32_t)(a.n_tile >> 3) << 17) | (1u << 23) | ((uint32_t)(128 >> 4) << 24);
+      // instruction descriptor: A/B formats (mxf4: E2M1 = 1; mxf8f6f4: A E2M1 = 5, B E4M3 = 0), N, UE8M0, M
+      const uint32_t idesc = (a.fp4 ? ((1u << 7) | (1u << 10)) : (5u << 7)) | ((uint32_t)(a.n_tile >> 3) << 17) |
+                             (1u << 23) | ((uint32_t)(128 >> 4) << 24);
       // descriptors of stage 0, chunk 0; stage s / chunk cc add their byte offsets / 16 to the
       // start-address field
       const uint64_t da0 = sw128_desc(su32(smem)), db0 = sw128_desc(su32(smem) + b_off);
-      const uint64_t dsa0 = sf_desc(su32(smem) + sf_off), dsb0 = sf_desc(su32(smem) + sf_off + 512);
+      const uint64_t dsa0 = sf_desc(su32(smem) + sf_off);
+      const int wpc = a.fp4 ? 2 : 1;
       const uint32_t st16 = (uint32_t)a.stage_bytes >> 4, bb16 = (uint32_t)a.b_bytes >> 4;
       long long i = 0;
       Ring rg;
       Item it;
       bool ok = true;
-      for (long long ii = blockIdx.x; ok && item_at<MODE>(a, ii, n_items, it); ii += gridDim.x, ++i) {
+      for (long long ii = blockIdx.x; ok && item_geom<MODE>(a, ii, n_items, it); ii += gridDim.x, ++i) {
         const int b = (int)(i & 1);
         const long long rb = i >> 1;
         if (rb > 0 && !wait_bar(su32(&ctl->acc_empty[b]), (uint32_t)((rb - 1) & 1), ctl, status)) break;
@@ -451,16 +497,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           fence_async_smem();  // B rows and scale words arrived through cp.async (generic proxy)
           const uint64_t so = (uint64_t)(s * st16);
           for (int cc = 0; cc < CH; ++cc) {
-            const uint32_t col = tmem + (uint32_t)(a.sf_base + (s * CH + cc) * kSfSlot);
-            tc_cp_32x128b_x4(col, dsa0 + so + (uint64_t)(cc * (kSfBytes >> 4)));
-            tc_cp_32x128b_x4(col + 16, dsb0 + so + (uint64_t)(cc * (kSfBytes >> 4)));
+            // scale words of the chunk: A word w to column col + 16 w, B word w to col + 16 (wpc + w)
+            const uint32_t col = tmem + (uint32_t)(a.sf_base + (s * CH + cc) * a.sf_slot);
+            const uint64_t dsc = dsa0 + so + (uint64_t)(cc * (a.sf_bytes >> 4));
+            for (int w2 = 0; w2 < 2 * wpc; ++w2) tc_cp_32x128b_x4(col + 16 * w2, dsc + (uint64_t)(w2 * (512 >> 4)));
             const uint64_t da = da0 + so + (uint64_t)(cc * (kATile >> 4)), db = db0 + so + (uint64_t)(cc * bb16);
+            if (a.fp4) {
+              // K = 64 per MMA; MMA k uses scale word k / 2, byte pair 2 (k % 2)
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const int h = k & (a.n_acc - 1);
-              tc_mma(d + (uint32_t)(h * a.acc_cols), da + 2 * k, db + 2 * k,
-                     idesc | ((uint32_t)k << 4) | ((uint32_t)k << 29), col, col + 16, (started >> h) & 1u);
-              started |= 1u << h;
+              for (int k = 0; k < 4; ++k) {
+                const uint32_t hw = (uint32_t)(k >> 1), sf = (uint32_t)(k & 1) * 2u;
+                tc_mma_f4(d, da + 2 * k, db + 2 * k, idesc | (sf << 4) | (sf << 29), col + 16 * hw, col + 32 + 16 * hw,
+                          started & 1u);
+                started = 1;
+              }
+            } else {
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const int h = k & (a.n_acc - 1);
+                tc_mma(d + (uint32_t)(h * a.acc_cols), da + 2 * k, db + 2 * k,
+                       idesc | ((uint32_t)k << 4) | ((uint32_t)k << 29), col, col + 16, (started >> h) & 1u);
+                started |= 1u << h;
+              }
             }
           }
           tc_commit(su32(&ctl->empty[s]));
@@ -473,67 +531,53 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue (warps 0-3)
-    // Per item: all partial accumulators of a 16-column block are read with one wait, the buffer is
-    // released right after the last block is read, and only then are the sums formed and stored.
+    // Per item: the partial accumulators of a 16-column block are read with one wait, the buffer is
+    // released right after the last block is read, and only then are the sums formed and stored. The
+    // next item's work group is read while the current one is waited for.
     const int q = warp;
     long long i = 0;
     int bad = 0;
     int g0 = 0;  // ring slot of the item's first stage
-    Item it;
-    for (long long ii = blockIdx.x; item_at<MODE>(a, ii, n_items, it); ii += gridDim.x, ++i) {
+    Item it, nx;
+    long long ii = blockIdx.x;
+    bool have = item_at<MODE>(a, ii, n_items, it);
+    for (; have; ++i) {
+      ii += gridDim.x;
+      const bool have_nx = item_at<MODE>(a, ii, n_items, nx);  // consumed next iteration
+      const int nst = (it.j1 - it.j0) / CH;  // stages of the item
       const int b = (int)(i & 1);
-      // gate weight of token `lane` of the work group (down projection), fetched before the wait
       const float wlane = (MODE == DOWN && lane < it.wg.ntok) ? __ldg(&a.ws.perm_w[it.wg.pos0 + lane]) : 0.0f;
       if (!__all_sync(0xffffffffu, wait_bar(su32(&ctl->acc_full[b]), (uint32_t)((i >> 1) & 1), ctl, status))) break;
       tc_fence_after();
       const int row = it.mt * 128 + 32 * q + lane;
       const int ncols = it.wg.ntok * a.terms;
-      const int nst = (it.j1 - it.j0) / CH;  // stages of the item
-      // the item's t-th stage sits in slot (g0 + t) mod S, owned by issuer slot mod n_iss; the
-      // issuers' partial sums are added in the order in which they first appear
-      int order[kMaxIss];
-      int nacc = 0;
-      {
-        unsigned seen = 0;
-        for (int t = 0, sl = g0; t < nst && t < S && nacc < a.n_iss; ++t, sl = (sl + 1 == S) ? 0 : sl + 1) {
-          const int w = sl & (a.n_iss - 1);
-          if (!(seen & (1u << w))) {
-            seen |= 1u << w;
-            order[nacc++] = w;
-          }
-        }
-      }
-      const uint32_t lane_base =
-          tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * a.n_iss * a.n_acc * a.acc_cols);
-      const int nparts = nacc * a.n_acc;  // (issuer, accumulator) pairs, issuer-major in first-use order
+      // issuers that received stages: owners (slot mod n_iss) of slots g0, g0 + 1, ...; their partial
+      // sums are added in issuer order
+      unsigned mask = 0;
+      for (int t = 0, sl = g0; t < nst && t < S; ++t, sl = (sl + 1 == S) ? 0 : sl + 1) mask |= 1u << (sl & (a.n_iss - 1));
+      const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * a.n_iss * a.acc_cols);
       float run = 0.0f;
       bool nan_row = false;
       int tk = 0, jt = 0;  // token and term of the current column
       for (int cb = 0; cb < ncols; cb += 16) {
+        uint32_t u[kMaxIss][16];
+#pragma unroll
+        for (int w = 0; w < kMaxIss; ++w)
+          if ((mask >> w) & 1u) tc_ld16(lane_base + (uint32_t)(w * a.acc_cols + cb), u[w]);
+        tc_wait_ld();
+        if (cb + 16 >= ncols) {  // buffer read completely: hand it back
+          tc_fence_before();
+          mbar_arrive(su32(&ctl->acc_empty[b]));
+        }
         float v[16];
 #pragma unroll
         for (int cc = 0; cc < 16; ++cc) v[cc] = 0.0f;
-        for (int p0 = 0; p0 < nparts; p0 += 4) {
-          uint32_t u[4][16];
 #pragma unroll
-          for (int t = 0; t < 4; ++t)
-            if (p0 + t < nparts) {
-              const int pp = p0 + t;
-              const int col0 = (order[pp / a.n_acc] * a.n_acc + (pp - (pp / a.n_acc) * a.n_acc)) * a.acc_cols;
-              tc_ld16(lane_base + (uint32_t)(col0 + cb), u[t]);
-            }
-          tc_wait_ld();
-          if (cb + 16 >= ncols && p0 + 4 >= nparts) {  // buffer read completely: hand it back
-            tc_fence_before();
-            mbar_arrive(su32(&ctl->acc_empty[b]));
+        for (int w = 0; w < kMaxIss; ++w)
+          if ((mask >> w) & 1u) {
+#pragma unroll
+            for (int cc = 0; cc < 16; ++cc) v[cc] += __uint_as_float(u[w][cc]);
           }
-#pragma unroll
-          for (int t = 0; t < 4; ++t)
-            if (p0 + t < nparts) {
-#pragma unroll
-              for (int cc = 0; cc < 16; ++cc) v[cc] += __uint_as_float(u[t][cc]);
-            }
-        }
 #pragma unroll
         for (int cc = 0; cc < 16; ++cc) {
           const int col = cb + cc;
@@ -553,13 +597,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      g0 = (g0 + nst) % S;
       // activations are finite by construction, so a NaN sum means a NaN weight scale: find it
       if (nan_row) {
         const uint8_t* sr = scale_row<MODE>(a, it, row);
         for (int j = it.j0; j < it.j1; ++j)
           bad |= (__vcmpeq4(__ldg(reinterpret_cast<const unsigned*>(sr) + j), 0xFFFFFFFFu) != 0u);
       }
+      g0 = (g0 + nst) % S;
+      have = have_nx;
+      it = nx;
     }
     if (bad) atomicOr(&status[CTRL_STATUS], ST_NAN_SCALE);
   }
@@ -596,8 +642,12 @@ __global__ void __launch_bounds__(256) k_glu(Cfg c, Ws ws, long long T) {
       u += src[((long long)kp * 2 + 1) * c.f + row];
     }
     const float h = silu(g) * u;
-    split_terms(h, c.hterms, ws.hq + (pos * c.hterms) * c.f + row, c.f, ws.hs + (pos * c.hterms) * nb + blk, nb,
-                lane);
+    if (c.fp4)
+      split_terms_fp4(h, c.hterms, ws.hq + (pos * c.hterms) * (c.f / 2) + blk * 16, c.f / 2,
+                      ws.hs + (pos * c.hterms) * nb + blk, nb, lane);
+    else
+      split_terms(h, c.hterms, ws.hq + (pos * c.hterms) * c.f + row, c.f, ws.hs + (pos * c.hterms) * nb + blk, nb,
+                  lane);
   }
 }
 
@@ -640,7 +690,7 @@ cudaError_t get_encode() {
 struct MapKey {
   const void* base;
   long long K, rows, experts, stride;
-  int ch;
+  int ch, fp4;
 };
 struct MapEntry {
   MapKey key;
@@ -651,15 +701,18 @@ constexpr int kMapCache = 64;
 MapEntry g_maps[kMapCache];
 int g_map_next = 0;
 
-// 4D map over one weight matrix of every expert record: {128 codes of a chunk, rows, K/128 chunks,
-// experts}, strides {K/2, 64, record stride} bytes; a box is 128 rows x `ch` chunks of 128 codes
-// (16U4_ALIGN16B: 16 codes per 16-byte slot, 128-byte swizzle), landing as ch tiles of 16 KB.
+// 4D map over one weight matrix of every expert record, boxes of 128 rows x `ch` chunks landing as
+// ch tiles of 16 KB with the 128-byte swizzle:
+//   E4M3 form: {128 codes of a chunk, rows, K/128 chunks, experts}, strides {K/2, 64, record} bytes,
+//              16U4_ALIGN16B (16 codes per 16-byte slot);
+//   E2M1 form: {128 bytes (256 codes) of a chunk, rows, K/256 chunks, experts}, strides {K/2, 128,
+//              record}, bytes as stored.
 cudaError_t weight_map(const uint8_t* base, long long K, long long rows, long long experts, long long stride, int ch,
-                       CUtensorMap* out) {
+                       int fp4, CUtensorMap* out) {
   std::lock_guard<std::mutex> lock(g_mu);
   for (auto& m : g_maps)
     if (m.used && m.key.base == base && m.key.K == K && m.key.rows == rows && m.key.experts == experts &&
-        m.key.stride == stride && m.key.ch == ch) {
+        m.key.stride == stride && m.key.ch == ch && m.key.fp4 == fp4) {
       *out = m.map;
       return cudaSuccess;
     }
@@ -667,17 +720,18 @@ cudaError_t weight_map(const uint8_t* base, long long K, long long rows, long lo
   if (e != cudaSuccess) return e;
   MapEntry& m = g_maps[g_map_next];
   g_map_next = (g_map_next + 1) % kMapCache;
-  cuuint64_t gdim[4] = {128, (cuuint64_t)rows, (cuuint64_t)(K / 128), (cuuint64_t)(experts > 0 ? experts : 1)};
-  cuuint64_t gstride[3] = {(cuuint64_t)(K / 2), 64, (cuuint64_t)stride};
+  cuuint64_t gdim[4] = {128, (cuuint64_t)rows, (cuuint64_t)(K / (fp4 ? 256 : 128)), (cuuint64_t)(experts > 0 ? experts : 1)};
+  cuuint64_t gstride[3] = {(cuuint64_t)(K / 2), (cuuint64_t)(fp4 ? 128 : 64), (cuuint64_t)stride};
   cuuint32_t box[4] = {128, 128, (cuuint32_t)ch, 1}, estr[4] = {1, 1, 1, 1};
-  CUresult r = g_encode(&m.map, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 4, const_cast<uint8_t*>(base), gdim, gstride,
+  CUresult r = g_encode(&m.map, fp4 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 4,
+                        const_cast<uint8_t*>(base), gdim, gstride,
                         box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     m.used = false;
     return cudaErrorInvalidValue;
   }
-  m.key = MapKey{base, K, rows, experts, stride, ch};
+  m.key = MapKey{base, K, rows, experts, stride, ch, fp4};
   m.used = true;
   *out = m.map;
   return cudaSuccess;
@@ -708,6 +762,8 @@ int chunks_per_stage(long long nch, long long parts) {
 
 // With fewer than 4 stages of ch chunks the stage shrinks to one chunk.
 void size_tiles(TcArgs& a, int ch, int mtiles) {
+  a.sf_slot = a.fp4 ? 64 : 32;
+  a.sf_bytes = a.fp4 ? 2048 : 1024;
   a.div_parts.init((uint32_t)a.parts);
   a.div_mtiles.init((uint32_t)mtiles);
   a.acc_cols = (a.n_tile + 15) / 16 * 16;
@@ -717,9 +773,9 @@ void size_tiles(TcArgs& a, int ch, int mtiles) {
   a.b_bytes = (a.n_tile * 128 + 1023) / 1024 * 1024;
   for (;; ch = 1) {
     a.ch = ch;
-    a.stage_bytes = ch * (kATile + a.b_bytes + kSfBytes);
+    a.stage_bytes = ch * (kATile + a.b_bytes + a.sf_bytes);
     int st = (227 * 1024 - 1024 - (int)sizeof(Ctl)) / a.stage_bytes;
-    const int tm = (kTmemCols - a.sf_base) / (kSfSlot * ch);
+    const int tm = (kTmemCols - a.sf_base) / (a.sf_slot * ch);
     if (st > tm) st = tm;
     if (st > kMaxStages) st = kMaxStages;
     a.stages = st;
@@ -739,6 +795,7 @@ struct TcMaps {
 
 cudaError_t setup(const Cfg& c, const uint8_t* routed, const uint8_t* shared, int ch_gu, int ch_dn, TcMaps& m,
                   const uint8_t*& sh) {
+  const int f4 = c.fp4;
   if (g_sms == 0) {
     int dev = 0;
     cudaGetDevice(&dev);
@@ -750,14 +807,14 @@ cudaError_t setup(const Cfg& c, const uint8_t* routed, const uint8_t* shared, in
   const long long sh_n = c.S > 0 ? c.S : 1;
   cudaError_t e;
   if (ch_gu > 0) {
-    if ((e = weight_map(routed, c.d, c.f, c.E, c.stride, ch_gu, &m.gr)) != cudaSuccess) return e;
-    if ((e = weight_map(routed + nc + ns, c.d, c.f, c.E, c.stride, ch_gu, &m.ur)) != cudaSuccess) return e;
-    if ((e = weight_map(sh, c.d, c.f, sh_n, c.stride, ch_gu, &m.gs)) != cudaSuccess) return e;
-    if ((e = weight_map(sh + nc + ns, c.d, c.f, sh_n, c.stride, ch_gu, &m.us)) != cudaSuccess) return e;
+    if ((e = weight_map(routed, c.d, c.f, c.E, c.stride, ch_gu, f4, &m.gr)) != cudaSuccess) return e;
+    if ((e = weight_map(routed + nc + ns, c.d, c.f, c.E, c.stride, ch_gu, f4, &m.ur)) != cudaSuccess) return e;
+    if ((e = weight_map(sh, c.d, c.f, sh_n, c.stride, ch_gu, f4, &m.gs)) != cudaSuccess) return e;
+    if ((e = weight_map(sh + nc + ns, c.d, c.f, sh_n, c.stride, ch_gu, f4, &m.us)) != cudaSuccess) return e;
   }
   if (ch_dn > 0) {
-    if ((e = weight_map(routed + 2 * (nc + ns), c.f, c.d, c.E, c.stride, ch_dn, &m.dr)) != cudaSuccess) return e;
-    if ((e = weight_map(sh + 2 * (nc + ns), c.f, c.d, sh_n, c.stride, ch_dn, &m.ds)) != cudaSuccess) return e;
+    if ((e = weight_map(routed + 2 * (nc + ns), c.f, c.d, c.E, c.stride, ch_dn, f4, &m.dr)) != cudaSuccess) return e;
+    if ((e = weight_map(sh + 2 * (nc + ns), c.f, c.d, sh_n, c.stride, ch_dn, f4, &m.ds)) != cudaSuccess) return e;
   }
   return cudaSuccess;
 }
@@ -782,7 +839,9 @@ cudaError_t launch_gateup(const Cfg& c, const Ws& ws, const uint8_t* routed, con
   a.terms = c.xterms;
   a.n_tile = round16(c.wgt * c.xterms);
   a.parts = c.ks;
-  size_tiles(a, chunks_per_stage(c.d / 128, c.ks), c.f / 128);
+  a.fp4 = c.fp4;
+  a.nch = c.d / (c.fp4 ? 256 : 128);
+  size_tiles(a, chunks_per_stage(a.nch, c.ks), c.f / 128);
   if (a.stages < 2) return cudaErrorInvalidConfiguration;
   TcMaps m;
   cudaError_t e = setup(c, routed, shared, a.ch, 0, m, a.shared);
@@ -801,7 +860,9 @@ cudaError_t launch_down(const Cfg& c, const Ws& ws, const uint8_t* routed, const
   a.terms = c.hterms;
   a.n_tile = round16(c.wgt * c.hterms);
   a.parts = 1;
-  size_tiles(a, chunks_per_stage(c.f / 128, 1), c.d / 128);
+  a.fp4 = c.fp4;
+  a.nch = c.f / (c.fp4 ? 256 : 128);
+  size_tiles(a, chunks_per_stage(a.nch, 1), c.d / 128);
   if (a.stages < 2) return cudaErrorInvalidConfiguration;
   TcMaps m;
   cudaError_t e = setup(c, routed, shared, 0, a.ch, m, a.shared);

@@ -170,9 +170,15 @@ def test_repeatable_and_batch_invariant():
     y1, i1, _ = run_layer(L, xd, 9)
     y2, i2, _ = run_layer(L, xd, 9)
     assert np.array_equal(i1, i2) and np.array_equal(y1, y2)
+    # one token alone takes the E2M1-term form (error ~1e-7 of max|y|), nine tokens the E4M3-term form
+    # (~2e-5): the same token agrees to within those bounds, not bit for bit
     y3, i3, _ = run_layer(L, xd[4:5].contiguous(), 1)
     assert np.array_equal(i3[0], i1[4])
-    assert rel_err(y3[0], y1[4]) < 1e-6
+    assert rel_err(y3[0], y1[4]) < 5e-5
+    # within one form (three and nine tokens, E4M3 terms) only the accumulation order differs
+    y4, i4, _ = run_layer(L, xd[2:5].contiguous(), 3)
+    assert np.array_equal(i4[2], i1[4])
+    assert rel_err(y4[2], y1[4]) < 1e-6
 
 
 # ------------------------------------------------------------------ device-side data checks
