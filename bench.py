@@ -41,7 +41,12 @@ FALLBACK_HBM_GBS = 6800.0
 
 # DRAM traffic per launch from an ncu capture, keyed by kernel; valid only while the kernel sources
 # hash to the recorded value (see profiles/).
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # dram__bytes_read.sum + dram__bytes_write.sum of one launch (decode b=1: 16 routed + 2 shared
+    # records, the same per launch at any expert count), profiles/k_tc_ffn_decode_b1.md
+    "k_tc<gate/up>": (214172672, "9e004338329c9ed4"),
+    "k_tc<down>": (108428800, "9e004338329c9ed4"),
+}
 
 
 def parse():
@@ -239,7 +244,7 @@ def run_ours(args, rank, world, local_rank):
 
     # phase events for sampled steps (all recorded inside the timed region, on the launching stream)
     n_samp = (args.steps + args.sample_every - 1) // args.sample_every
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_samp)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(n_samp)]
     st = torch.cuda.current_stream()
     for e4 in ev:  # materialise the handles
         for e in e4:
@@ -273,20 +278,22 @@ def run_ours(args, rank, world, local_rank):
     if k3.check_device_status(ws) != k3.OK:
         raise RuntimeError("device status check failed in the timed region")
 
-    ph = np.array([[ev[s][0].elapsed_time(ev[s][1]), ev[s][1].elapsed_time(ev[s][2]), ev[s][2].elapsed_time(ev[s][3])]
-                   for s in range(n_samp)])
-    route_ms, gateup_ms, down_ms = ph.mean(axis=0)
+    # per-kernel device times of the sampled steps (events between the five kernels)
+    ph = np.array([[ev[s][j].elapsed_time(ev[s][j + 1]) for j in range(5)] for s in range(n_samp)])
+    route_ms, gateup_ms, glu_ms, down_ms, combine_ms = ph.mean(axis=0)
     idxs = idx_samples.cpu().numpy()
     U = float(np.mean([len(np.unique(idxs[s])) for s in range(n_samp)]))
     rec = shape.record_bytes
     mat = f * d // 2 + f * d // 32
-    P = T * (k + S)
-    bytes_gateup = (U + S) * 2 * mat + T * d * 2 + P * f * 4
-    bytes_down = (U + S) * mat + P * f * 4 + T * d * 4
-    bytes_route = E * d * 4 + T * d * 2 + T * k * 8
+    # algorithmic bytes: the expert records the step must read, the router weights, x read once and
+    # y written once; activation terms, partial sums and h are implementation traffic (not counted)
+    bytes_gateup = (U + S) * 2 * mat
+    bytes_down = (U + S) * mat
+    bytes_route = E * d * 4 + T * d * 2
     bytes_layer = (U + S) * rec + E * d * 4 + T * d * 2 + T * d * 4
     peak, peak_kind = hbm_peak()
-    kernels = {"k_gateup": (gateup_ms, bytes_gateup), "k_down": (down_ms, bytes_down), "k_route": (route_ms, bytes_route)}
+    kernels = {"k_tc<gate/up>": (gateup_ms, bytes_gateup), "k_tc<down>": (down_ms, bytes_down),
+               "k_route": (route_ms, bytes_route)}
     dom = max(kernels, key=lambda n: kernels[n][0])
     dom_ms, dom_bytes = kernels[dom]
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
@@ -310,11 +317,13 @@ def run_ours(args, rank, world, local_rank):
                      "frac": achieved / peak, "traffic": traffic, "peak_kind": f"{peak_kind} (MEASURED_PEAKS hbm_gbs)"
                      if peak_kind == "measured" else "fallback",
                      "algorithmic_bytes_per_launch": dom_bytes, "avg_launch_ms": dom_ms},
-        "phases_ms": {"route": route_ms, "gateup": gateup_ms, "down": down_ms, "sampled_steps": n_samp},
+        "kernels_ms": {"k_route": route_ms, "k_tc<gate/up>": gateup_ms, "k_glu": glu_ms, "k_tc<down>": down_ms,
+                       "k_combine": combine_ms, "sampled_steps": n_samp,
+                       "note": "events between the kernels remove their launch overlap in the sampled steps"},
         "layer_roofline": {"bytes_per_step": bytes_layer, "achieved_gbs": bytes_layer / (ms_per_step * 1e-3) / 1e9,
                            "frac": bytes_layer / (ms_per_step * 1e-3) / 1e9 / peak},
         "distinct_experts_per_step": U,
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 5 * args.steps,
         "clocks": clk,
     }
 

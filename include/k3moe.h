@@ -132,9 +132,10 @@ K3MOE_API k3moe_status k3moe_layer(const k3moe_config* cfg /* host */, const voi
                          float* topk_w_out, void* ws, size_t ws_bytes, void* stream);
 
 /*
- * k3moe_layer with phase timing, for profiling: `events` points to 4 cudaEvent_t handles created by
+ * k3moe_layer with phase timing, for profiling: `events` points to 6 cudaEvent_t handles created by
  * the caller; they are recorded on `stream` before the router kernel, before the gate/up kernel,
- * before the down-projection kernel and after it. Same kernels and results as k3moe_layer.
+ * before the GLU kernel, before the down-projection kernel, before the combine kernel and after it.
+ * Same kernels and results as k3moe_layer (an event between two kernels only removes their overlap).
  */
 K3MOE_API k3moe_status k3moe_layer_timed(const k3moe_config* cfg /* host */, const void* x, int64_t T,
                                          const float* w_router, const float* bias,

@@ -132,8 +132,10 @@ def layer(cfg, x, T, w_router, bias, routed, shared, y, ws, topk_idx=None, topk_
 
 
 def layer_timed(cfg, x, T, w_router, bias, routed, shared, y, ws, events, topk_idx=None, topk_w=None, stream=None):
-    """k3moe_layer recording 4 caller-created cudaEvent_t handles (ints) around its three kernels."""
-    ev = (ctypes.c_void_p * 4)(*events)
+    """k3moe_layer recording 6 caller-created cudaEvent_t handles (ints) around its five kernels."""
+    if len(events) != 6:
+        raise ValueError("layer_timed needs 6 events")
+    ev = (ctypes.c_void_p * 6)(*events)
     _check(load().k3moe_layer_timed(ctypes.byref(cfg), _ptr(x), T, _ptr(w_router), _ptr(bias), _ptr(routed),
                                     _ptr(shared), _ptr(y), _ptr(topk_idx), _ptr(topk_w), _ptr(ws),
                                     ws.numel() * ws.element_size(), _stream(stream), ev), "k3moe_layer_timed")

@@ -241,7 +241,9 @@ k3moe_status layer_impl(const k3moe_config* cfg, const void* x, int64_t T, const
       !aligned16(y) || (shared_records && !aligned16(shared_records)) || (topk_idx_out && !aligned16(topk_idx_out)) ||
       (topk_w_out && !aligned16(topk_w_out)))
     return K3MOE_ERR_INVALID_ARGUMENT;
-  if (events && (!events[0] || !events[1] || !events[2] || !events[3])) return K3MOE_ERR_INVALID_ARGUMENT;
+  if (events)
+    for (int i = 0; i < 6; ++i)
+      if (!events[i]) return K3MOE_ERR_INVALID_ARGUMENT;
   if (T == 0) return K3MOE_OK;
   Layout L;
   if ((s = check_ws(cfg, T, ws, ws_bytes, &L)) != K3MOE_OK) return s;
@@ -255,10 +257,11 @@ k3moe_status layer_impl(const k3moe_config* cfg, const void* x, int64_t T, const
     e = k3::launch_route(c, w, x, T, w_router, bias, topk_idx_out, topk_w_out,
                          k3::RM_USER_OUT | k3::RM_XPREP | k3::RM_PERMUTE, st);
   if (e == cudaSuccess && events) e = cudaEventRecord(static_cast<cudaEvent_t>(events[1]), st);
-  if (e == cudaSuccess) e = k3::launch_gateup(c, w, routed_records, shared_records, y, T, wgb, st);
-  if (e == cudaSuccess && events) e = cudaEventRecord(static_cast<cudaEvent_t>(events[2]), st);
-  if (e == cudaSuccess) e = k3::launch_down(c, w, routed_records, shared_records, y, T, wgb, st);
-  if (e == cudaSuccess && events) e = cudaEventRecord(static_cast<cudaEvent_t>(events[3]), st);
+  auto evt = [&](int i) { return events ? static_cast<cudaEvent_t>(events[i]) : nullptr; };
+  if (e == cudaSuccess) e = k3::launch_gateup(c, w, routed_records, shared_records, y, T, wgb, st, evt(2));
+  if (e == cudaSuccess && events) e = cudaEventRecord(evt(3), st);
+  if (e == cudaSuccess) e = k3::launch_down(c, w, routed_records, shared_records, y, T, wgb, st, evt(4));
+  if (e == cudaSuccess && events) e = cudaEventRecord(evt(5), st);
   return cuda_status(e);
 }
 

@@ -35,9 +35,10 @@ cudaError_t launch_rmsnorm(const float* x, long long T, int d, float eps, float*
 cudaError_t launch_residual_add(float* x, const float* y, long long n, cudaStream_t st);
 
 // k3moe_tc.cu (tcgen05 expert FFN)
+// `mid` (optional) is recorded between the projection kernel and the GLU / combine kernel.
 cudaError_t launch_gateup(const Cfg& c, const Ws& ws, const uint8_t* routed, const uint8_t* shared, float* y,
-                          long long T, long long wg_max, cudaStream_t st);
+                          long long T, long long wg_max, cudaStream_t st, cudaEvent_t mid = nullptr);
 cudaError_t launch_down(const Cfg& c, const Ws& ws, const uint8_t* routed, const uint8_t* shared, float* y,
-                        long long T, long long wg_max, cudaStream_t st);
+                        long long T, long long wg_max, cudaStream_t st, cudaEvent_t mid = nullptr);
 
 }  // namespace k3

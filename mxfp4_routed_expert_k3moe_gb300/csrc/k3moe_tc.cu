@@ -834,7 +834,7 @@ TcArgs base_args(const Cfg& c, const Ws& ws, const uint8_t* routed, const uint8_
 }  // namespace
 
 cudaError_t launch_gateup(const Cfg& c, const Ws& ws, const uint8_t* routed, const uint8_t* shared, float* y,
-                          long long T, long long wg_max, cudaStream_t st) {
+                          long long T, long long wg_max, cudaStream_t st, cudaEvent_t mid) {
   TcArgs a = base_args(c, ws, routed, shared, y, T);
   a.terms = c.xterms;
   a.n_tile = round16(c.wgt * c.xterms);
@@ -847,6 +847,7 @@ cudaError_t launch_gateup(const Cfg& c, const Ws& ws, const uint8_t* routed, con
   cudaError_t e = setup(c, routed, shared, a.ch, 0, m, a.shared);
   if (e != cudaSuccess) return e;
   e = launch_tc<GATEUP>(a, m.gr, m.ur, m.gs, m.us, wg_max * 2 * (c.f / 128) * a.parts, st);
+  if (e == cudaSuccess && mid) e = cudaEventRecord(mid, st);
   if (e != cudaSuccess) return e;
   const long long warps = (T * (c.k + c.S)) * (c.f / 32);
   long long blocks = (warps + 7) / 8;
@@ -855,7 +856,7 @@ cudaError_t launch_gateup(const Cfg& c, const Ws& ws, const uint8_t* routed, con
 }
 
 cudaError_t launch_down(const Cfg& c, const Ws& ws, const uint8_t* routed, const uint8_t* shared, float* y,
-                        long long T, long long wg_max, cudaStream_t st) {
+                        long long T, long long wg_max, cudaStream_t st, cudaEvent_t mid) {
   TcArgs a = base_args(c, ws, routed, shared, y, T);
   a.terms = c.hterms;
   a.n_tile = round16(c.wgt * c.hterms);
@@ -868,6 +869,7 @@ cudaError_t launch_down(const Cfg& c, const Ws& ws, const uint8_t* routed, const
   cudaError_t e = setup(c, routed, shared, 0, a.ch, m, a.shared);
   if (e != cudaSuccess) return e;
   e = launch_tc<DOWN>(a, m.dr, m.dr, m.ds, m.ds, wg_max * (c.d / 128), st);
+  if (e == cudaSuccess && mid) e = cudaEventRecord(mid, st);
   if (e != cudaSuccess) return e;
   long long blocks = (T * c.d + 255) / 256;
   if (blocks > 8LL * g_sms) blocks = 8LL * g_sms;
