@@ -56,7 +56,8 @@ def parse():
     p.add_argument("--warmup", type=int, default=50)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", choices=list(WORKLOADS), default="decode_b1")
-    p.add_argument("--layers", type=int, default=4, help="independent weight sets rotated across steps")
+    p.add_argument("--layers", type=int, default=8,
+                   help="independent weight sets rotated across steps (8: the router weights alone, 206 MB, exceed L2)")
     p.add_argument("--experts", type=int, default=None, help="override routed experts (small profiling case)")
     p.add_argument("--batches", type=int, default=64, help="distinct token batches rotated across steps")
     p.add_argument("--sample-every", type=int, default=8, help="phase-timed step every N steps")
@@ -204,6 +205,12 @@ class LayerWeights:
         st = torch.cuda.current_stream().cuda_stream
         synth.records_device(shape, seed, layer, 0, shape.n_routed, self.routed.data_ptr(), stride, st)
         synth.records_device(shape, seed, layer, shape.n_routed, shape.n_shared, self.shared.data_ptr(), stride, st)
+        # weight loading: scale bytes into the device order the kernels read (once, not timed)
+        import mxfp4_routed_expert_k3moe_gb300 as k3
+        cfg = k3.Config.make(shape.d_model, shape.d_ff, shape.n_routed, shape.top_k, shape.n_shared,
+                             record_stride=stride)
+        k3.pack_records(cfg, self.routed, shape.n_routed)
+        k3.pack_records(cfg, self.shared, shape.n_shared)
 
 
 def run_ours(args, rank, world, local_rank):

@@ -17,7 +17,9 @@
  *   [gate codes f x d/2][gate scales f x d/32][up codes f x d/2][up scales f x d/32]
  *   [down codes d x f/2][down scales d x f/32]
  * Codes are row-major, two per byte, the even column in the low nibble. A record of the
- * d_model 7168 / d_ff 1536 shape is 17,547,264 bytes (the census figure).
+ * d_model 7168 / d_ff 1536 shape is 17,547,264 bytes (the census figure). This is the stored
+ * order; the compute calls read records whose scale bytes were put in the device order by
+ * k3moe_pack_records (see there), once, when the records are loaded onto the GPU.
  *
  * Conventions shared by every call below:
  *  - Pointers are DEVICE pointers unless marked "host". The caller owns all memory; nothing is
@@ -87,6 +89,23 @@ typedef struct {
   int64_t record_stride; /* bytes between expert records (>= record size, multiple of 256) */
 } k3moe_config;
 
+/*
+ * Scale order of device-resident records. The block-scaled MMA of the tensor cores reads the E8M0
+ * scales of 128 weight rows x 4 blocks as one 32 x 16-byte image (lane i of each 32-row quarter c
+ * holds the 4 scale bytes of row 32 c + i). In the device order every 128-row tile of a matrix
+ * (rows 128 t .. 128 t + 127, whose scale bytes are one contiguous range in either order) stores
+ * the byte of tile row r = 32 c + i and block b = 4 g + e at
+ *     tile_start + 512 g + 16 i + 4 c + e,
+ * so that the scales of one chunk of the reduction axis are a single contiguous copy. Codes are
+ * unchanged. The record size and all offsets of the stored order are unchanged.
+ * k3moe_pack_records converts `n_records` records (record_stride bytes apart, 16-byte aligned
+ * base) in place: to_device = 1 stored -> device order, 0 device -> stored order. Only d_model,
+ * d_ff and record_stride of `cfg` are used (any valid config of that geometry). Asynchronous on
+ * `stream`; the records must not be in use by another call meanwhile.
+ */
+K3MOE_API k3moe_status k3moe_pack_records(const k3moe_config* cfg /* host */, uint8_t* records, int64_t n_records,
+                                          int32_t to_device, void* stream);
+
 /* Bytes of one expert record for this config: 3 * d_model * d_ff * 17 / 32 (host only; 0 if invalid). */
 K3MOE_API size_t k3moe_record_bytes(const k3moe_config* cfg /* host */);
 
@@ -113,8 +132,10 @@ K3MOE_API k3moe_status k3moe_route(const k3moe_config* cfg /* host */, const voi
  *   x              [T, d_model] bf16 or fp32
  *   topk_idx       [T, top_k] int32 expert ids in [0, n_routed) (checked on the device)
  *   topk_w         [T, top_k] fp32 gate weights
- *   routed_records n_routed records, record_stride bytes apart (16-byte aligned base)
- *   shared_records n_shared records, record_stride bytes apart (may be NULL if n_shared == 0)
+ *   routed_records n_routed records, record_stride bytes apart (16-byte aligned base), in the
+ *                  device scale order (k3moe_pack_records)
+ *   shared_records n_shared records, record_stride bytes apart, device scale order (may be NULL
+ *                  if n_shared == 0)
  *   y              [T, d_model] fp32 out, overwritten
  */
 K3MOE_API k3moe_status k3moe_expert_ffn(const k3moe_config* cfg /* host */, const void* x, int64_t T,

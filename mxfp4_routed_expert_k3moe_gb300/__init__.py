@@ -22,8 +22,8 @@ ACT_EXACT, ACT_MXFP4 = 0, 1
 X_BF16, X_F32 = 0, 1
 
 EXPORTS = ["k3moe_record_bytes", "k3moe_workspace_bytes", "k3moe_route", "k3moe_expert_ffn", "k3moe_layer",
-           "k3moe_layer_timed", "k3moe_layer_static", "k3moe_rmsnorm", "k3moe_residual_add",
-           "k3moe_check_device_status", "k3moe_status_string"]
+           "k3moe_layer_timed", "k3moe_layer_static", "k3moe_pack_records", "k3moe_rmsnorm",
+           "k3moe_residual_add", "k3moe_check_device_status", "k3moe_status_string"]
 
 
 class Config(ctypes.Structure):
@@ -70,13 +70,14 @@ def load(path: str | None = None):
         L.k3moe_layer_timed.argtypes = [cfgp, _P, _I64, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]
         L.k3moe_layer_static.argtypes = [cfgp, _P, _I64, _P, _P, _P, _P, _P, _P]
         L.k3moe_layer_static.restype = ctypes.c_int
+        L.k3moe_pack_records.argtypes = [cfgp, _P, _I64, ctypes.c_int32, _P]
         L.k3moe_rmsnorm.argtypes = [_P, _I64, ctypes.c_int32, ctypes.c_float, _P, _P]
         L.k3moe_residual_add.argtypes = [_P, _P, _I64, _P]
         L.k3moe_check_device_status.argtypes = [_P, _P]
         L.k3moe_status_string.argtypes = [ctypes.c_int]
         L.k3moe_status_string.restype = ctypes.c_char_p
-        for name in ["k3moe_route", "k3moe_expert_ffn", "k3moe_layer", "k3moe_layer_timed", "k3moe_rmsnorm", "k3moe_residual_add",
-                     "k3moe_check_device_status"]:
+        for name in ["k3moe_route", "k3moe_expert_ffn", "k3moe_layer", "k3moe_layer_timed", "k3moe_pack_records",
+                     "k3moe_rmsnorm", "k3moe_residual_add", "k3moe_check_device_status"]:
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -146,6 +147,13 @@ def layer_static(cfg, x, T, w_router, bias, routed, shared, y, stream=None):
     device memory; its scratch is a fixed 4 MiB array inside the library (see include/k3moe.h)."""
     _check(load().k3moe_layer_static(ctypes.byref(cfg), _ptr(x), T, _ptr(w_router), _ptr(bias), _ptr(routed),
                                      _ptr(shared), _ptr(y), _stream(stream)), "k3moe_layer_static")
+
+
+def pack_records(cfg, records, n_records, to_device=True, stream=None):
+    """k3moe_pack_records: put the scale bytes of n records (in place) into the device order that the
+    compute calls read (to_device=True), or back into the stored order."""
+    _check(load().k3moe_pack_records(ctypes.byref(cfg), _ptr(records), n_records, 1 if to_device else 0,
+                                     _stream(stream)), "k3moe_pack_records")
 
 
 def rmsnorm(x, T, d, eps, xn, stream=None):

@@ -285,6 +285,17 @@ k3moe_status k3moe_layer_timed(const k3moe_config* cfg, const void* x, int64_t T
                     ws_bytes, stream, events);
 }
 
+k3moe_status k3moe_pack_records(const k3moe_config* cfg, uint8_t* records, int64_t n_records, int32_t to_device,
+                                void* stream) {
+  k3moe_status s = validate(cfg);
+  if (s != K3MOE_OK && s != K3MOE_ERR_UNSUPPORTED) return s;  // only the record geometry matters here
+  if (!records || !aligned16(records) || n_records < 0 || (to_device != 0 && to_device != 1))
+    return K3MOE_ERR_INVALID_ARGUMENT;
+  if (n_records == 0) return K3MOE_OK;
+  return cuda_status(k3::launch_pack_scales(records, n_records, cfg->record_stride, cfg->d_model, cfg->d_ff, to_device,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
 k3moe_status k3moe_rmsnorm(const float* x, int64_t T, int32_t d, float eps, float* xn, void* stream) {
   if (!x || !xn || T < 0 || d <= 0 || !(eps >= 0.0f)) return K3MOE_ERR_INVALID_ARGUMENT;
   if (T == 0) return K3MOE_OK;

@@ -64,6 +64,14 @@ __device__ __forceinline__ unsigned long long local_max(const unsigned long long
   return t[0];
 }
 
+// Warp-wide maximum of one 64-bit key per lane: the high words first, then the low words of the
+// lanes that hold the maximal high word (two single-instruction reductions).
+__device__ __forceinline__ unsigned long long warp_max_key(unsigned long long v) {
+  const uint32_t hi = __reduce_max_sync(0xffffffffu, (uint32_t)(v >> 32));
+  const uint32_t lo = __reduce_max_sync(0xffffffffu, (uint32_t)(v >> 32) == hi ? (uint32_t)v : 0u);
+  return ((unsigned long long)hi << 32) | lo;
+}
+
 // One warp: the k largest keys held in registers (R per lane), in descending order; lane r < k
 // returns the r-th (0 if fewer than r+1 keys exist). Each round takes the warp-wide maximum of the
 // lanes' cached local maxima; only the lane that owned it clears the key and recomputes its maximum.
@@ -73,12 +81,7 @@ __device__ unsigned long long warp_topk(unsigned long long (&key)[R], int k) {
   unsigned long long lm = local_max<R>(key);
   unsigned long long mine = 0;
   for (int r = 0; r < k; ++r) {
-    unsigned long long best = lm;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
-      best = other > best ? other : best;
-    }
+    const unsigned long long best = warp_max_key(lm);
     if (lane == r) mine = best;
     if (best != 0ull && lm == best) {  // keys are unique: exactly one owner
 #pragma unroll
@@ -89,40 +92,92 @@ __device__ unsigned long long warp_topk(unsigned long long (&key)[R], int k) {
   return mine;
 }
 
-// Stage 1 of the block top-k: warp w takes experts lane + 32 (w + nw q), q < R.
+// Keys of one thread for the block top-k: experts lane + 32 (warp + nw q), q < R.
 template <int R>
-__device__ __forceinline__ unsigned long long topk_stage1(int E, int k, const float* logits_t) {
+__device__ __forceinline__ void load_keys(int E, const float* logits_t, unsigned long long (&key)[R]) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  unsigned long long key[R];
 #pragma unroll
   for (int q = 0; q < R; ++q) {
     const int e = lane + 32 * (warp + nw * q);
     key[q] = (e < E) ? topk_key(__ldcg(&logits_t[e]), e) : 0ull;
   }
-  return warp_topk<R>(key, k);
 }
 
-// Top-k and renormalised softmax gates of one token, by the whole CTA (2 to 8 warps): every warp
-// selects the k best of its share of the experts, then warp 0 selects the k best of those
-// candidates. `cand` is shared memory for 32 keys per warp. Ends with __syncthreads.
+// The k largest keys of one token, in descending order, into sel[0..k). `cand` holds blockDim.x keys,
+// `s_thr` 64.
+//
+// Threshold pass: every warp takes its m = ceil(k / nw) largest keys; these nw m distinct keys are
+// all >= their minimum tau, so the k-th largest key is >= tau and the selection lies among the keys
+// >= tau. Those candidates (the warps' own picks plus the rest of the keys >= tau; typically a few
+// more than k) are gathered in shared memory and each is ranked by counting the candidates above
+// it. If more candidates than threads turn up (ties at the threshold's scale, or tiny E), the
+// two-stage selection runs instead: every warp's k best, then the k best of those.
+template <int R>
+__device__ void topk_select(int E, int k, const float* logits_t, unsigned long long* cand, unsigned long long* sel,
+                            unsigned long long* s_thr, int* s_n) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int m = (k + nw - 1) / nw;
+  unsigned long long key[R];
+  load_keys<R>(E, logits_t, key);
+  const unsigned long long mine = warp_topk<R>(key, m);  // clears the picked keys in `key`
+  if (lane < m) s_thr[warp * m + lane] = mine;
+  if (threadIdx.x == 0) *s_n = 0;
+  __syncthreads();
+  unsigned long long tau = ~0ull;
+  for (int i = 0; i < nw * m; ++i) tau = s_thr[i] < tau ? s_thr[i] : tau;
+  const int cap = blockDim.x;
+  if (lane < m && mine != 0ull) {
+    const int at = atomicAdd(s_n, 1);
+    if (at < cap) cand[at] = mine;
+  }
+#pragma unroll
+  for (int q = 0; q < R; ++q)
+    if (key[q] != 0ull && key[q] >= tau) {
+      const int at = atomicAdd(s_n, 1);
+      if (at < cap) cand[at] = key[q];
+    }
+  __syncthreads();
+  const int n = *s_n;
+  if (n <= cap) {
+    if ((int)threadIdx.x < n) {
+      const unsigned long long v = cand[threadIdx.x];
+      int rank = 0;
+      for (int j = 0; j < n; ++j) rank += (cand[j] > v) ? 1 : 0;
+      if (rank < k) sel[rank] = v;
+    }
+    if ((int)threadIdx.x < k && (int)threadIdx.x >= n) sel[threadIdx.x] = 0ull;  // fewer than k experts
+  } else {
+    load_keys<R>(E, logits_t, key);
+    const unsigned long long top = warp_topk<R>(key, k);
+    cand[warp * 32 + lane] = (lane < k) ? top : 0ull;
+    __syncthreads();
+    if (warp == 0) {
+      unsigned long long c8[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) c8[q] = (q < nw) ? cand[q * 32 + lane] : 0ull;
+      const unsigned long long best = warp_topk<8>(c8, k);
+      if (lane < k) sel[lane] = best;
+    }
+  }
+  __syncthreads();
+}
+
+// Top-k and renormalised softmax gates of one token, by the whole CTA (2 to 8 warps). `cand` is
+// shared memory for blockDim.x keys. Ends with __syncthreads.
 __device__ void topk_block(int E, int k, const float* logits_t, unsigned long long* cand, int* idx_out, float* w_out,
                            int* idx_user, float* w_user) {
+  __shared__ unsigned long long s_sel[32], s_thr[64];
+  __shared__ int s_n;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   const int per_lane = (E + 32 * nw - 1) / (32 * nw);
-  unsigned long long m;
-  if (per_lane <= 1) m = topk_stage1<1>(E, k, logits_t);
-  else if (per_lane <= 2) m = topk_stage1<2>(E, k, logits_t);
-  else if (per_lane <= 4) m = topk_stage1<4>(E, k, logits_t);
-  else if (per_lane <= 8) m = topk_stage1<8>(E, k, logits_t);
-  else if (per_lane <= 16) m = topk_stage1<16>(E, k, logits_t);
-  else m = topk_stage1<32>(E, k, logits_t);
-  cand[warp * 32 + lane] = (lane < k) ? m : 0ull;
-  __syncthreads();
+  if (per_lane <= 1) topk_select<1>(E, k, logits_t, cand, s_sel, s_thr, &s_n);
+  else if (per_lane <= 2) topk_select<2>(E, k, logits_t, cand, s_sel, s_thr, &s_n);
+  else if (per_lane <= 4) topk_select<4>(E, k, logits_t, cand, s_sel, s_thr, &s_n);
+  else if (per_lane <= 8) topk_select<8>(E, k, logits_t, cand, s_sel, s_thr, &s_n);
+  else if (per_lane <= 16) topk_select<16>(E, k, logits_t, cand, s_sel, s_thr, &s_n);
+  else topk_select<32>(E, k, logits_t, cand, s_sel, s_thr, &s_n);
   if (warp == 0) {
-    unsigned long long key[8];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) key[q] = (q < nw) ? cand[q * 32 + lane] : 0ull;
-    const unsigned long long best = warp_topk<8>(key, k);
+    const unsigned long long best = (lane < k) ? s_sel[lane] : 0ull;
     const int my_e = key_expert(best);
     const float my_l = (lane < k) ? __ldcg(&logits_t[my_e]) : 0.0f;
     const float lmax = __shfl_sync(0xffffffffu, my_l, 0);
@@ -342,8 +397,6 @@ __global__ void __launch_bounds__(256, 3) k_route(RouteArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ int s_last;
   __shared__ float s_part[8][TT];
-  pdl_wait();  // the previous layer's kernels may still use the workspace and produce x
-  pdl_launch_dependents();
   const Cfg& c = a.c;
   const int nw = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = warp >> 2, kq = warp & 3;
@@ -353,6 +406,24 @@ __global__ void __launch_bounds__(256, 3) k_route(RouteArgs a) {
   const int esz = c.x_f32 ? 4 : 2;
   const int row_bytes = c.d * esz;
   unsigned long long* cand = reinterpret_cast<unsigned long long*>(smem + route_tile_bytes(c, TT));
+
+  // quarter [jb, je) of row e: U float4 loads per lane per batch, all issued before any arithmetic
+  constexpr int U = 14;
+  const int qlen = c.d / 4, jb = kq * qlen, je = jb + qlen;
+  const float* wrow = a.W + (long long)(e < c.E ? e : 0) * c.d;
+  uint4 wv[U];
+  auto load_batch = [&](int j0) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int j = j0 + u * 128 + lane * 4;
+      wv[u] = (e < c.E && j < je) ? ld_stream_v4(wrow + j) : make_uint4(0, 0, 0, 0);
+    }
+  };
+  // The router weights are not written by earlier kernels: the first batch is in flight before the
+  // wait for the previous kernels, which may still use the workspace and produce x.
+  load_batch(jb);
+  pdl_wait();
+  pdl_launch_dependents();
 
   // the token tile of x goes to shared memory (asynchronously, waited for below)
   {
@@ -364,21 +435,12 @@ __global__ void __launch_bounds__(256, 3) k_route(RouteArgs a) {
     asm volatile("cp.async.commit_group;" ::: "memory");
   }
 
-  // quarter [jb, je) of row e: U float4 loads per lane per batch, all issued before any arithmetic
-  constexpr int U = 14;
-  const int qlen = c.d / 4, jb = kq * qlen, je = jb + qlen;
   float acc[TT];
 #pragma unroll
   for (int tt = 0; tt < TT; ++tt) acc[tt] = 0.0f;
-  const float* wrow = a.W + (long long)(e < c.E ? e : 0) * c.d;
   bool waited = false;
   for (int j0 = jb; j0 < je; j0 += 128 * U) {
-    uint4 wv[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int j = j0 + u * 128 + lane * 4;
-      wv[u] = (e < c.E && j < je) ? ld_stream_v4(wrow + j) : make_uint4(0, 0, 0, 0);
-    }
+    if (j0 != jb) load_batch(j0);
     if (!waited) {
       asm volatile("cp.async.wait_group 0;" ::: "memory");
       __syncthreads();

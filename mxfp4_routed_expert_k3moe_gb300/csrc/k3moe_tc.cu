@@ -26,13 +26,15 @@
 //               issues about one tensor copy per ~500 SM cycles, so a single issuing thread caps the
 //               weight stream near 3 TB/s; four reach the DRAM rate.
 //   warps 8-11  MMA issuers (one lane each): tcgen05.cp of the scale words into tensor memory, then
-//               the MMAs. One issuing thread sustains one MMA per ~120-230 SM cycles whatever N is,
-//               and MMAs into one accumulator follow each other only every ~450 cycles, so at small
-//               N (few tokens) up to four issuers share the stages and each alternates between two
-//               accumulators (TMEM columns of their own); the epilogue adds the partial sums.
+//               the MMAs. One issuing thread sustains one tcgen05 instruction per ~120-230 SM cycles
+//               whatever N is, so at small N (few tokens) four issuers share the stages, each with
+//               its own accumulators in tensor memory; the epilogue adds the partial sums of an item.
 // Every ring slot has exactly one agent of each kind (loader v owns the slots s = v mod 4, issuer w
 // the slots s = w mod n_iss), so each agent waits on a slot's barriers round after round and a
 // parity wait never meets a barrier two phases away.
+// The E8M0 scales of the weights are read in the device order (k3moe_pack_records): the scales of a
+// chunk of 128 rows are one contiguous block, brought by one bulk copy with the tensor copy of the
+// codes. (Fetched row by row, 4 bytes per request, they took a quarter of the DRAM rate.)
 // A pipeline stage holds `ch` consecutive 128-code chunks of the reduction axis, brought by one
 // tensor copy (the per-copy cost of the TMA unit is amortised over more bytes).
 // Every mbarrier wait is bounded; on a timeout the CTA raises the status word and stops early.
@@ -83,12 +85,20 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// L2 policy for data read once (the weight stream): evicted first, so that the small arrays that
+// every CTA reads repeatedly (work groups, activation terms) stay in L2 instead of queueing behind
+// the stream at the DRAM.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
-                                            uint32_t bar) {
+                                            uint32_t bar, uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
-      "[%6];" ::"r"(dst),
-      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
+      "%3, %4, %5}], [%6], %7;" ::"r"(dst),
+      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar), "l"(policy)
       : "memory");
 }
 __device__ __forceinline__ void cp16(uint32_t dst, const void* src) {
@@ -97,6 +107,14 @@ __device__ __forceinline__ void cp16(uint32_t dst, const void* src) {
 // 4-byte copy; src_bytes 0 writes zeros
 __device__ __forceinline__ void cp4(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+// Bulk copy (16-byte aligned, multiple of 16 bytes) completing on an mbarrier, with an L2 policy.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
 }
 __device__ __forceinline__ void cp_arrive_noinc(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
@@ -216,7 +234,8 @@ struct TcArgs {
   int acc_cols; // tensor-memory columns per accumulator (>= n_tile, multiple of 16)
   int n_iss;    // MMA-issuing threads
   int n_acc;    // accumulators per issuer (the MMAs of a chunk alternate between them)
-  int sf_base;  // first column of the scale ring (after 2 buffers x n_iss x n_acc accumulators)
+  int sf_base;  // first column of the scale slots, one per chunk of every stage (after 2 buffers x
+                // n_iss x n_acc accumulators)
   int b_bytes;  // shared-memory bytes of the B tile of a chunk
   int ch;       // chunks per stage
   int fp4;      // E2M1 form (kind::mxf4, 256-code chunks) or E4M3 form (kind::mxf8f6f4, 128-code chunks)
@@ -285,16 +304,19 @@ __device__ __forceinline__ bool item_at(const TcArgs& a, long long it, long long
   return true;
 }
 
-// E8M0 scale bytes of weight row `row` (blocks 0 .. K/32-1) of the item's matrix.
+// E8M0 scale bytes of the item's 128-row tile, in the device order (k3moe_pack_records): the tile's
+// 128 x K/32 bytes form groups of 512 bytes, one per 4 consecutive blocks; inside a group, the byte
+// of row 32c + i and block 4g + e sits at 16 i + 4 c + e. A group is thus the 32 x 16-byte image
+// that tcgen05.cp 32x128b.warpx4 spreads to TMEM lane 32q + i, column c: the MMA's scale layout.
 template <int MODE>
-__device__ __forceinline__ const uint8_t* scale_row(const TcArgs& a, const Item& it, int row) {
+__device__ __forceinline__ const uint8_t* scale_tile(const TcArgs& a, const Item& it) {
   const Cfg& c = a.c;
   const long long nc = (long long)c.d * c.f / 2, ns = (long long)c.d * c.f / 32;
   const uint8_t* rec = it.wg.expert < c.E ? a.routed + (long long)it.wg.expert * c.stride
                                           : a.shared + (long long)(it.wg.expert - c.E) * c.stride;
   const int K = MODE == GATEUP ? c.d : c.f;
   const long long off = MODE == GATEUP ? (it.mat == 0 ? nc : 2 * nc + ns) : 2 * (nc + ns) + nc;
-  return rec + off + (long long)row * (K / 32);
+  return rec + off + (long long)it.mt * 128 * (K / 32);
 }
 
 // B row n of the item (token i = n / terms, term j = n % terms): codes and E8M0 scales.
@@ -393,6 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The item two ahead has its work group read, the next one its B-row addresses resolved, so
     // that neither dependent load sits in front of the next item's first copy.
     const int lv = warp - kWarpLoad;
+    const uint64_t pol = policy_evict_first();
     Ring rg;
     bool ok = true;
     LoadPlan cur, nxt;
@@ -411,11 +434,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool routed = it.wg.expert < c.E;
       const CUtensorMap* map = routed ? (it.mat == 0 ? &map_r0 : &map_r1) : (it.mat == 0 ? &map_s0 : &map_s1);
       const int ecoord = routed ? it.wg.expert : it.wg.expert - c.E;
-      const uint8_t* arow[4];
+      const uint8_t* atile = scale_tile<MODE>(a, it);
       const uint8_t* bcodes[kMaxN / 32];
       const uint8_t* bscales[kMaxN / 32];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) arow[q] = scale_row<MODE>(a, it, it.mt * 128 + lane + 32 * q);
 #pragma unroll
       for (int q = 0; q < kMaxN / 32; ++q) {
         bcodes[q] = nullptr;
@@ -435,17 +456,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         uint8_t* st = smem + (size_t)s * a.stage_bytes;
         if (lane == 0) {
-          mbar_expect_tx(su32(&ctl->full[s]), tx_chunk * CH);
-          tma_load_4d(su32(st), map, 0, it.mt * 128, j, ecoord, su32(&ctl->full[s]));
+          // weight codes (tensor copy) and the chunks' A scale groups (one bulk copy each: the
+          // groups of a chunk are contiguous in the device order) complete on the same barrier
+          mbar_expect_tx(su32(&ctl->full[s]), (tx_chunk + 512 * wpc) * CH);
+          tma_load_4d(su32(st), map, 0, it.mt * 128, j, ecoord, su32(&ctl->full[s]), pol);
+          for (int cc = 0; cc < CH; ++cc)
+            bulk_load(su32(st + sf_off + cc * a.sf_bytes), atile + (size_t)512 * wpc * (j + cc), 512 * wpc,
+                      su32(&ctl->full[s]), pol);
         }
         for (int cc = 0; cc < CH; ++cc) {
           const int jj = j + cc;
           const uint32_t sb = su32(st + b_off + cc * a.b_bytes), sc = su32(st + sf_off + cc * a.sf_bytes);
-          // scale words: A word h at sc + 512 h, B word h at sc + 512 (wpc + h)
-          for (int h = 0; h < wpc; ++h) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) cp4(sc + 512 * h + 16 * lane + 4 * q, arow[q] + 4 * (wpc * jj + h), 4);
-          }
+          // scale words: A word h at sc + 512 h (bulk copy above), B word h at sc + 512 (wpc + h)
 #pragma unroll
           for (int q = 0; q < kMaxN / 32; ++q) {
             if (bcodes[q]) {
@@ -491,13 +513,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t started = 0;  // bit h: accumulator h already holds a partial sum of this item
         for (int j = it.j0; j < it.j1; j += CH, rg.next(S)) {
           const int s = rg.s;
-          if ((s & (a.n_iss - 1)) != w) continue;
+          if (s % a.n_iss != w) continue;
           if (!wait_bar(su32(&ctl->full[s]), rg.ph, ctl, status)) { ok = false; break; }
           tc_fence_after();
           fence_async_smem();  // B rows and scale words arrived through cp.async (generic proxy)
           const uint64_t so = (uint64_t)(s * st16);
           for (int cc = 0; cc < CH; ++cc) {
             // scale words of the chunk: A word w to column col + 16 w, B word w to col + 16 (wpc + w)
+            // The scale slot belongs to the stage: it is rewritten only after the stage's previous MMAs
+            // completed (the loader refilled the stage after its empty barrier).
             const uint32_t col = tmem + (uint32_t)(a.sf_base + (s * CH + cc) * a.sf_slot);
             const uint64_t dsc = dsa0 + so + (uint64_t)(cc * (a.sf_bytes >> 4));
             for (int w2 = 0; w2 < 2 * wpc; ++w2) tc_cp_32x128b_x4(col + 16 * w2, dsc + (uint64_t)(w2 * (512 >> 4)));
@@ -533,20 +557,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue (warps 0-3)
     // Per item: the partial accumulators of a 16-column block are read with one wait, the buffer is
     // released right after the last block is read, and only then are the sums formed and stored. The
-    // next item's work group is read while the current one is waited for.
+    // work group of the item two ahead (and the gate weights of the next one) are read while the
+    // current one is waited for: while the weight stream saturates the DRAM, a read that misses L2
+    // waits microseconds.
     const int q = warp;
     long long i = 0;
     int bad = 0;
     int g0 = 0;  // ring slot of the item's first stage
-    Item it, nx;
+    Item it, nx, nx2;
     long long ii = blockIdx.x;
     bool have = item_at<MODE>(a, ii, n_items, it);
+    bool have_nx = item_at<MODE>(a, ii + gridDim.x, n_items, nx);
+    float wlane = (MODE == DOWN && have && lane < it.wg.ntok) ? __ldg(&a.ws.perm_w[it.wg.pos0 + lane]) : 0.0f;
     for (; have; ++i) {
       ii += gridDim.x;
-      const bool have_nx = item_at<MODE>(a, ii, n_items, nx);  // consumed next iteration
+      const bool have_nx2 = item_at<MODE>(a, ii + gridDim.x, n_items, nx2);  // consumed two iterations later
+      const float wnext = (MODE == DOWN && have_nx && lane < nx.wg.ntok) ? __ldg(&a.ws.perm_w[nx.wg.pos0 + lane]) : 0.0f;
       const int nst = (it.j1 - it.j0) / CH;  // stages of the item
       const int b = (int)(i & 1);
-      const float wlane = (MODE == DOWN && lane < it.wg.ntok) ? __ldg(&a.ws.perm_w[it.wg.pos0 + lane]) : 0.0f;
       if (!__all_sync(0xffffffffu, wait_bar(su32(&ctl->acc_full[b]), (uint32_t)((i >> 1) & 1), ctl, status))) break;
       tc_fence_after();
       const int row = it.mt * 128 + 32 * q + lane;
@@ -554,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // issuers that received stages: owners (slot mod n_iss) of slots g0, g0 + 1, ...; their partial
       // sums are added in issuer order
       unsigned mask = 0;
-      for (int t = 0, sl = g0; t < nst && t < S; ++t, sl = (sl + 1 == S) ? 0 : sl + 1) mask |= 1u << (sl & (a.n_iss - 1));
+      for (int t = 0, sl = g0; t < nst && t < S; ++t, sl = (sl + 1 == S) ? 0 : sl + 1) mask |= 1u << (sl % a.n_iss);
       const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * a.n_iss * a.acc_cols);
       float run = 0.0f;
       bool nan_row = false;
@@ -599,13 +627,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // activations are finite by construction, so a NaN sum means a NaN weight scale: find it
       if (nan_row) {
-        const uint8_t* sr = scale_row<MODE>(a, it, row);
-        for (int j = it.j0; j < it.j1; ++j)
-          bad |= (__vcmpeq4(__ldg(reinterpret_cast<const unsigned*>(sr) + j), 0xFFFFFFFFu) != 0u);
+        const uint8_t* sg = scale_tile<MODE>(a, it) + 16 * lane + 4 * q;  // row 32 q + lane of the tile
+        for (int g = it.j0 * wpc; g < it.j1 * wpc; ++g)
+          bad |= (__vcmpeq4(__ldg(reinterpret_cast<const unsigned*>(sg + (size_t)512 * g)), 0xFFFFFFFFu) != 0u);
       }
       g0 = (g0 + nst) % S;
       have = have_nx;
+      have_nx = have_nx2;
       it = nx;
+      nx = nx2;
+      wlane = wnext;
     }
     if (bad) atomicOr(&status[CTRL_STATUS], ST_NAN_SCALE);
   }
@@ -668,6 +699,43 @@ __global__ void __launch_bounds__(256) k_combine(Cfg c, Ws ws, float* y, long lo
     }
     for (int sh = 0; sh < c.S; ++sh) s += ws.part[(P_R + (long long)sh * T + tok) * c.d + row];
     y[idx] = s;
+  }
+}
+
+// ------------------------------------------------------------------------------- scale order
+// Converts the E8M0 scale bytes of whole records between the stored order ([rows][K/32] per matrix)
+// and the device order read by k_tc (scale_tile). Both orders keep each 128-row tile of a matrix in
+// the same contiguous byte range, so one CTA per tile stages the range in shared memory and writes
+// it back permuted, in place.
+__global__ void __launch_bounds__(256) k_pack_scales(uint8_t* records, long long n_rec, long long stride, int d, int f,
+                                                      int to_device) {
+  extern __shared__ __align__(16) uint8_t sbuf[];
+  const int tiles_gu = f / 128, tiles_dn = d / 128;
+  const long long per_rec = 2LL * tiles_gu + tiles_dn;
+  const long long nc = (long long)d * f / 2, ns = (long long)d * f / 32;
+  for (long long u = blockIdx.x; u < n_rec * per_rec; u += gridDim.x) {
+    const long long r = u / per_rec;
+    int t = (int)(u - r * per_rec), m = 0, K = d;
+    if (t >= 2 * tiles_gu) { m = 2; t -= 2 * tiles_gu; K = f; }
+    else if (t >= tiles_gu) { m = 1; t -= tiles_gu; }
+    const int nb = K / 32;  // blocks per row, a multiple of 4
+    uint8_t* base = records + r * stride + m * (nc + ns) + nc + (long long)t * 128 * nb;
+    const int n = 128 * nb;
+    for (int o = threadIdx.x * 16; o < n; o += blockDim.x * 16)
+      *reinterpret_cast<uint4*>(sbuf + o) = *reinterpret_cast<const uint4*>(base + o);
+    __syncthreads();
+    for (int o = threadIdx.x; o < n; o += blockDim.x) {
+      int src;
+      if (to_device) {  // o = 512 g + 16 i + 4 c + e holds row 32 c + i, block 4 g + e
+        const int g = o >> 9, i = (o >> 4) & 31, c = (o >> 2) & 3, e = o & 3;
+        src = (32 * c + i) * nb + 4 * g + e;
+      } else {  // o = row * nb + block
+        const int row = o / nb, b = o - row * nb;
+        src = 512 * (b >> 2) + 16 * (row & 31) + 4 * (row >> 5) + (b & 3);
+      }
+      base[o] = sbuf[src];
+    }
+    __syncthreads();
   }
 }
 
@@ -753,8 +821,10 @@ cudaError_t launch_tc(const TcArgs& a, const CUtensorMap& r0, const CUtensorMap&
   return launch_pdl(k_tc<MODE>, dim3((unsigned)grid), dim3(kThreads), smem, st, r0, r1, s0, s1, a);
 }
 
-// Tile geometry for an MMA N of n_tile: TMEM holds two accumulator buffers and then one scale slot
-// per stage; shared memory holds the stages and the control block.
+// Tile geometry for an MMA N of n_tile: TMEM holds two accumulator buffers per issuer and then one
+// scale slot per chunk of every stage, which bounds the ring's depth; shared memory holds the stages
+// and the control block. (Scale slots owned by the issuers instead, with a deeper ring in shared
+// memory, measured slower: an issuer then waits for its own earlier MMAs.)
 // Chunks per stage: kMaxCh when every item's chunk range divides evenly, else 1.
 int chunks_per_stage(long long nch, long long parts) {
   return (nch % parts == 0 && (nch / parts) % kMaxCh == 0) ? kMaxCh : 1;
@@ -874,6 +944,25 @@ cudaError_t launch_down(const Cfg& c, const Ws& ws, const uint8_t* routed, const
   long long blocks = (T * c.d + 255) / 256;
   if (blocks > 8LL * g_sms) blocks = 8LL * g_sms;
   return launch_pdl(k_combine, dim3((unsigned)blocks), dim3(256), 0, st, c, ws, y, T);
+}
+
+cudaError_t launch_pack_scales(uint8_t* records, long long n_rec, long long stride, int d, int f, int to_device,
+                               cudaStream_t st) {
+  const size_t smem = (size_t)128 * ((d > f ? d : f) / 32);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(k_pack_scales, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  const long long units = n_rec * (2LL * (f / 128) + d / 128);
+  if (g_sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (g_sms <= 0) g_sms = 1;
+  }
+  const long long grid = units < 8LL * g_sms ? units : 8LL * g_sms;
+  k_pack_scales<<<(unsigned)(grid > 0 ? grid : 1), 256, smem, st>>>(records, n_rec, stride, d, f, to_device);
+  return cudaGetLastError();
 }
 
 }  // namespace k3

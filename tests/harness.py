@@ -13,11 +13,26 @@ INDEX_GAP = 1e-5   # near-tie rule for top-k indices (oracle 16th vs 17th logit)
 REL_TOL = 2e-3     # max|y_gpu - y_ref| / max|y_ref|
 
 
+def device_order(records: np.ndarray, d: int, f: int) -> np.ndarray:
+    """Host restatement of the device scale order (include/k3moe.h, k3moe_pack_records) for records in
+    the stored order, one per row of `records`: in every 128-row tile of each matrix, the scale byte
+    of tile row 32c + i and block 4g + e moves to 512g + 16i + 4c + e of the tile's range."""
+    out = records.copy()
+    nc, ns = d * f // 2, d * f // 32
+    for m, (rows, cols) in enumerate(((f, d), (f, d), (d, f))):
+        nb = cols // 32
+        off = m * (nc + ns) + nc
+        sc = records[:, off:off + ns].reshape(len(records), rows // 128, 4, 32, nb // 4, 4)  # [t][c][i][g][e]
+        out[:, off:off + ns] = sc.transpose(0, 1, 4, 3, 2, 5).reshape(len(records), ns)    # [t][g][i][c][e]
+    return out
+
+
 class DeviceLayer:
-    """One layer's inputs on the GPU (records generated on the device) plus the host copies the oracle needs."""
+    """One layer's inputs on the GPU (records generated on the device, then put in the device scale
+    order unless pack=False) plus the host copies (stored order) the oracle needs."""
 
     def __init__(self, shape: synth.LayerShape, seed: int, layer: int = 0, zipf_s: float | None = None,
-                 x_dtype: str = "bf16", stride: int | None = None):
+                 x_dtype: str = "bf16", stride: int | None = None, pack: bool = True):
         import torch
         import mxfp4_routed_expert_k3moe_gb300 as k3
         self.shape, self.seed, self.layer, self.x_dtype = shape, seed, layer, x_dtype
@@ -36,6 +51,10 @@ class DeviceLayer:
             synth.records_device(shape, seed, layer, E, S, self.shared.data_ptr(), self.stride, st)
         self.cfg = k3.Config.make(shape.d_model, shape.d_ff, E, shape.top_k, S,
                                   x_dtype=k3.X_BF16 if x_dtype == "bf16" else k3.X_F32, record_stride=self.stride)
+        if pack:
+            k3.pack_records(self.cfg, self.routed, E)
+            if S:
+                k3.pack_records(self.cfg, self.shared, S)
         self._host_records = {}
 
     def host_records(self, experts):

@@ -78,6 +78,20 @@ def test_invalid_pointers_rejected_on_host():
     assert lib.k3moe_layer(ctypes.byref(cfg), a, 4, a, None, a, a, a, None, None, a, 1024, None) == k3.ERR_WORKSPACE
 
 
+def test_pack_records_rejects_bad_arguments_on_host():
+    cfg = k3.Config.make(**K3CFG)
+    lib = k3.load()
+    a = ctypes.c_void_p(1 << 20)
+    assert lib.k3moe_pack_records(ctypes.byref(cfg), None, 1, 1, None) == k3.ERR_INVALID_ARGUMENT
+    assert lib.k3moe_pack_records(ctypes.byref(cfg), ctypes.c_void_p((1 << 20) + 8), 1, 1, None) == 1
+    assert lib.k3moe_pack_records(ctypes.byref(cfg), a, -1, 1, None) == k3.ERR_INVALID_ARGUMENT
+    assert lib.k3moe_pack_records(ctypes.byref(cfg), a, 1, 2, None) == k3.ERR_INVALID_ARGUMENT
+    assert lib.k3moe_pack_records(ctypes.byref(cfg), a, 0, 1, None) == k3.OK
+    bad = k3.Config.make(**K3CFG)
+    bad.d_ff = 100
+    assert lib.k3moe_pack_records(ctypes.byref(bad), a, 1, 1, None) == k3.ERR_INVALID_ARGUMENT
+
+
 def test_zero_tokens_launches_nothing():
     cfg = k3.Config.make(**K3CFG)
     lib = k3.load()

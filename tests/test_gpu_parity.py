@@ -7,7 +7,7 @@ import numpy as np
 import pytest
 
 import synth
-from harness import REL_TOL, DeviceLayer, gate_err, index_parity, rel_err
+from harness import REL_TOL, DeviceLayer, device_order, gate_err, index_parity, rel_err
 
 pytestmark = pytest.mark.gpu
 
@@ -52,7 +52,7 @@ def check_layer(L: DeviceLayer, T: int, sample=None, batch=0):
 
 def test_device_generator_matches_host():
     sh = synth.TINY
-    L = DeviceLayer(sh, seed=0)
+    L = DeviceLayer(sh, seed=0, pack=False)
     dev = L.routed.cpu().numpy().reshape(sh.n_routed, L.stride)
     host = synth.records_host(sh, 0, 0, range(sh.n_routed), L.stride)
     assert np.array_equal(dev, host)
@@ -71,10 +71,27 @@ def k3_decode_b64():
 
 
 def test_device_generator_matches_host_k3(k3_decode_b1):
+    """The fixture's records are generated on the device and put in the device scale order there."""
     L = k3_decode_b1
+    d, f = L.shape.d_model, L.shape.d_ff
     for e in (0, 517, 895):
         dev = L.routed[e * L.stride:(e + 1) * L.stride].cpu().numpy()
-        assert np.array_equal(dev, synth.records_host(L.shape, 1, 0, [e], L.stride)[0])
+        host = synth.records_host(L.shape, 1, 0, [e], L.stride)
+        assert np.array_equal(dev, device_order(host, d, f)[0])
+
+
+@pytest.mark.parametrize("shape", [synth.TINY, MID])
+def test_pack_records_round_trip(shape):
+    """Stored -> device order matches the host restatement; device -> stored restores every byte."""
+    L = DeviceLayer(shape, seed=4, pack=False)
+    E, d, f = shape.n_routed, shape.d_model, shape.d_ff
+    stored = L.routed.cpu().numpy().reshape(E, L.stride)
+    k3.pack_records(L.cfg, L.routed, E)
+    packed = L.routed.cpu().numpy().reshape(E, L.stride)
+    assert np.array_equal(packed, device_order(stored, d, f))
+    assert not np.array_equal(packed, stored)
+    k3.pack_records(L.cfg, L.routed, E, to_device=False)
+    assert np.array_equal(L.routed.cpu().numpy().reshape(E, L.stride), stored)
 
 
 # ------------------------------------------------------------------ layer parity
