@@ -144,7 +144,7 @@ Cfg make_cfg(const k3moe_config* c, long long T) {
   k.wgt = (int)(T < wmax ? T : wmax);
   k.ks = (int)gateup_parts(T, c->d_model, k.fp4 != 0);
   if (k.fp4) {
-    k.xterms = 8;  // at most 3^-8 of the block maximum per element; ~1e-7 of max|y| measured
+    k.xterms = 8;  // at most 2^-23 of the block maximum per element
     k.hterms = 8;
   } else {
     k.xterms = k.x_f32 ? 3 : 2;

@@ -78,23 +78,25 @@ __device__ __forceinline__ uint4 ld_v4(const void* p) {
   return v;
 }
 
-// The same split into E2M1 terms (values 0, 0.5, 1, 1.5, 2, 3, 4, 6 and signs) with E8M0 block
-// scales: e_j is chosen so that max|r_j| / 2^{e_j} lies in (3, 6] (no saturation), which makes each
-// rounding residual at most 2^{e_j} <= max|r_j| / 3, so n terms leave at most 3^-n of the block
-// maximum. Codes are packed two per byte (even element in the low nibble): lane l and l ^ 1 share a
-// byte, which the even lane writes to codes[j * code_stride + lane / 2]; lane 0 writes the scale.
+// The same kind of split into E2M1 terms (values 0, 0.5, 1, 1.5, 2, 3, 4, 6 and signs) with E8M0
+// block scales, on a fixed exponent schedule: with E = floor(log2 max|v|) of the block, term j uses
+// the scale 2^{E - 3j}. Every scaled residual then lies within [-2, 2], where E2M1 is spaced by 0.5,
+// so each rounding leaves at most a quarter of the term's scale: |r_{j+1}| <= 2^{E - 3j - 2}, and the
+// next term sees |r_{j+1}| / 2^{E - 3j - 3} <= 2 again. n terms leave at most 2^{E - 3n + 1}, i.e.
+// 2^-23 of the block maximum for 8 terms, with one reduction for the block maximum in all. (Scales
+// are clamped at 2^-127; elements below that stay unresolved.) Codes are packed two per byte (even
+// element in the low nibble): lane l and l ^ 1 share a byte, which the even lane writes to
+// codes[j * code_stride + lane / 2]; lane 0 writes the scales.
 __device__ __forceinline__ void split_terms_fp4(float v, int terms, uint8_t* codes, long long code_stride,
                                                 uint8_t* scales, long long scale_stride, int lane) {
+  float amax = fabsf(v);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  int E = 0;
+  if (amax > 0.0f && amax <= 3.402823466e38f) E = ilogbf(amax);  // max|v| / 2^E in [1, 2)
   float r = v;
   for (int j = 0; j < terms; ++j) {
-    float amax = fabsf(r);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    int e = 0;
-    if (amax > 0.0f && amax <= 3.402823466e38f) {
-      e = ilogbf(amax) - 2;                    // amax / 2^e in [4, 8)
-      if (amax * pow2i(-e) > 6.0f) e += 1;     // -> (3, 4)
-    }
+    int e = E - 3 * j;
     e = e < -127 ? -127 : (e > 127 ? 127 : e);
     const float s = r * pow2i(-e);
     uint32_t code, dec;

@@ -51,6 +51,10 @@ __device__ __forceinline__ unsigned long long topk_key(float l, int e) {
 __device__ __forceinline__ int key_expert(unsigned long long key) {
   return (int)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
 }
+__device__ __forceinline__ float key_logit(unsigned long long key) {
+  const uint32_t o = (uint32_t)(key >> 32);
+  return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
+}
 
 template <int R>
 __device__ __forceinline__ unsigned long long local_max(const unsigned long long (&key)[R]) {
@@ -164,8 +168,9 @@ __device__ void topk_select(int E, int k, const float* logits_t, unsigned long l
 
 // Top-k and renormalised softmax gates of one token, by the whole CTA (2 to 8 warps). `cand` is
 // shared memory for blockDim.x keys. Ends with __syncthreads.
+// `idx_sm` / `w_sm` (shared memory, or NULL) receive a copy of the selection for the permutation.
 __device__ void topk_block(int E, int k, const float* logits_t, unsigned long long* cand, int* idx_out, float* w_out,
-                           int* idx_user, float* w_user) {
+                           int* idx_user, float* w_user, int* idx_sm, float* w_sm) {
   __shared__ unsigned long long s_sel[32], s_thr[64];
   __shared__ int s_n;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -174,12 +179,11 @@ __device__ void topk_block(int E, int k, const float* logits_t, unsigned long lo
   else if (per_lane <= 2) topk_select<2>(E, k, logits_t, cand, s_sel, s_thr, &s_n);
   else if (per_lane <= 4) topk_select<4>(E, k, logits_t, cand, s_sel, s_thr, &s_n);
   else if (per_lane <= 8) topk_select<8>(E, k, logits_t, cand, s_sel, s_thr, &s_n);
-  else if (per_lane <= 16) topk_select<16>(E, k, logits_t, cand, s_sel, s_thr, &s_n);
-  else topk_select<32>(E, k, logits_t, cand, s_sel, s_thr, &s_n);
+  else topk_select<16>(E, k, logits_t, cand, s_sel, s_thr, &s_n);  // E <= 4096 with 8 warps
   if (warp == 0) {
     const unsigned long long best = (lane < k) ? s_sel[lane] : 0ull;
     const int my_e = key_expert(best);
-    const float my_l = (lane < k) ? __ldcg(&logits_t[my_e]) : 0.0f;
+    const float my_l = (lane < k) ? key_logit(best) : 0.0f;  // the key holds the logit's bits
     const float lmax = __shfl_sync(0xffffffffu, my_l, 0);
     const float ex = (lane < k) ? expf(my_l - lmax) : 0.0f;
     float sum = ex;
@@ -191,6 +195,8 @@ __device__ void topk_block(int E, int k, const float* logits_t, unsigned long lo
       w_out[lane] = w;
       if (idx_user) idx_user[lane] = my_e;
       if (w_user) w_user[lane] = w;
+      if (idx_sm) idx_sm[lane] = my_e;
+      if (w_sm) w_sm[lane] = w;
     }
   }
   __syncthreads();
@@ -397,6 +403,8 @@ __global__ void __launch_bounds__(256, 3) k_route(RouteArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ int s_last;
   __shared__ float s_part[8][TT];
+  __shared__ int s_tk_idx[8 * 32];  // the selection of a single token tile, for the permutation
+  __shared__ float s_tk_w[8 * 32];
   const Cfg& c = a.c;
   const int nw = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = warp >> 2, kq = warp & 3;
@@ -516,11 +524,14 @@ __global__ void __launch_bounds__(256, 3) k_route(RouteArgs a) {
   __syncthreads();
   if (!s_last) return;
   __threadfence();
+  // one token tile whose routed slots fit the block: the permutation reads the selection from shared memory
+  const bool tile_sm = gridDim.y == 1 && (long long)ntt * c.k <= (long long)blockDim.x && ntt * c.k <= 8 * 32;
   for (int tt = 0; tt < ntt; ++tt) {
     const long long t = t0 + tt;
     topk_block(c.E, c.k, a.ws.logits + t * c.E, cand, a.ws.topk_idx + t * c.k, a.ws.topk_w + t * c.k,
                (a.mode & RM_USER_OUT) && a.out_idx ? a.out_idx + t * c.k : nullptr,
-               (a.mode & RM_USER_OUT) && a.out_w ? a.out_w + t * c.k : nullptr);
+               (a.mode & RM_USER_OUT) && a.out_w ? a.out_w + t * c.k : nullptr, tile_sm ? s_tk_idx + tt * c.k : nullptr,
+               tile_sm ? s_tk_w + tt * c.k : nullptr);
   }
   if (threadIdx.x == 0) a.ws.rtcnt[blockIdx.y] = 0;
   // ... and the last token tile to finish builds the permutation (directly when there is one tile)
@@ -536,7 +547,10 @@ __global__ void __launch_bounds__(256, 3) k_route(RouteArgs a) {
     __threadfence();
     if (threadIdx.x == 0) a.ws.ctrl[CTRL_ROUTER_DONE] = 0;
   }
-  if (a.mode & RM_PERMUTE) permute(c, a.ws, a.T, a.ws.topk_idx, a.ws.topk_w, reinterpret_cast<int*>(smem));
+  if (a.mode & RM_PERMUTE) {
+    if (tile_sm) permute(c, a.ws, a.T, s_tk_idx, s_tk_w, reinterpret_cast<int*>(smem));
+    else permute(c, a.ws, a.T, a.ws.topk_idx, a.ws.topk_w, reinterpret_cast<int*>(smem));
+  }
 }
 
 struct PrepArgs {
