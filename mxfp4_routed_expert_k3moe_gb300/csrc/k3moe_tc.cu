@@ -62,6 +62,7 @@ constexpr int kMaxN = 128;               // largest MMA N (B rows per tile)
 // TMEM columns per chunk: E4M3 form: A scales at +0..3, B at +16..19 (32 columns); E2M1 form:
 // two scale words per row (8 blocks of 32): A at +0..3 and +16..19, B at +32.. and +48.. (64 columns)
 constexpr int kMaxStages = 16;
+constexpr int kMaxBuf = 4;               // accumulator buffers per issuer
 constexpr int kATile = 128 * 128;        // A tile of a chunk in shared memory (both forms)
 constexpr uint32_t kWaitLimit = 1u << 24;
 
@@ -159,6 +160,13 @@ __device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t* v) {
         "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
       : "r"(taddr));
 }
+// 64 columns of the warp's 32 lanes in one instruction (every issuer's 16-column partial at once)
+__device__ __forceinline__ void tc_ld64(uint32_t taddr, uint32_t* v) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31]), "=r"(v[32]), "=r"(v[33]), "=r"(v[34]), "=r"(v[35]), "=r"(v[36]), "=r"(v[37]), "=r"(v[38]), "=r"(v[39]), "=r"(v[40]), "=r"(v[41]), "=r"(v[42]), "=r"(v[43]), "=r"(v[44]), "=r"(v[45]), "=r"(v[46]), "=r"(v[47]), "=r"(v[48]), "=r"(v[49]), "=r"(v[50]), "=r"(v[51]), "=r"(v[52]), "=r"(v[53]), "=r"(v[54]), "=r"(v[55]), "=r"(v[56]), "=r"(v[57]), "=r"(v[58]), "=r"(v[59]), "=r"(v[60]), "=r"(v[61]), "=r"(v[62]), "=r"(v[63])
+      : "r"(taddr));
+}
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
@@ -166,8 +174,8 @@ __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.a
 struct Ctl {
   uint64_t full[kMaxStages];   // weight tiles (TMA bytes), B rows and scale words (cp.async) landed
   uint64_t empty[kMaxStages];  // the stage's MMAs completed
-  uint64_t acc_full[2];
-  uint64_t acc_empty[2];
+  uint64_t acc_full[kMaxBuf];
+  uint64_t acc_empty[kMaxBuf];
   uint64_t drain;
   uint32_t tmem;
   volatile int abort;
@@ -234,6 +242,7 @@ struct TcArgs {
   int acc_cols; // tensor-memory columns per accumulator (>= n_tile, multiple of 16)
   int n_iss;    // MMA-issuing threads
   int n_acc;    // accumulators per issuer (the MMAs of a chunk alternate between them)
+  int n_buf;    // accumulator buffers (items in flight between the issuers and the epilogue)
   int sf_base;  // first column of the scale slots, one per chunk of every stage (after 2 buffers x
                 // n_iss x n_acc accumulators)
   int b_bytes;  // shared-memory bytes of the B tile of a chunk
@@ -397,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(su32(&ctl->full[s]), 1 + 32);
       mbar_init(su32(&ctl->empty[s]), 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < a.n_buf; ++b) {
       mbar_init(su32(&ctl->acc_full[b]), a.n_iss);
       mbar_init(su32(&ctl->acc_empty[b]), 128);
     }
@@ -505,8 +514,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       Item it;
       bool ok = true;
       for (long long ii = blockIdx.x; ok && item_geom<MODE>(a, ii, n_items, it); ii += gridDim.x, ++i) {
-        const int b = (int)(i & 1);
-        const long long rb = i >> 1;
+        const long long rb = i / a.n_buf;  // the buffer's round
+        const int b = (int)(i - rb * a.n_buf);
         if (rb > 0 && !wait_bar(su32(&ctl->acc_empty[b]), (uint32_t)((rb - 1) & 1), ctl, status)) break;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)((b * a.n_iss + w) * a.n_acc * a.acc_cols);
@@ -574,8 +583,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool have_nx2 = item_at<MODE>(a, ii + gridDim.x, n_items, nx2);  // consumed two iterations later
       const float wnext = (MODE == DOWN && have_nx && lane < nx.wg.ntok) ? __ldg(&a.ws.perm_w[nx.wg.pos0 + lane]) : 0.0f;
       const int nst = (it.j1 - it.j0) / CH;  // stages of the item
-      const int b = (int)(i & 1);
-      if (!__all_sync(0xffffffffu, wait_bar(su32(&ctl->acc_full[b]), (uint32_t)((i >> 1) & 1), ctl, status))) break;
+      const long long rb = i / a.n_buf;
+      const int b = (int)(i - rb * a.n_buf);
+      if (!__all_sync(0xffffffffu, wait_bar(su32(&ctl->acc_full[b]), (uint32_t)(rb & 1), ctl, status))) break;
       tc_fence_after();
       const int row = it.mt * 128 + 32 * q + lane;
       const int ncols = it.wg.ntok * a.terms;
@@ -587,11 +597,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       float run = 0.0f;
       bool nan_row = false;
       int tk = 0, jt = 0;  // token and term of the current column
+      // at the smallest N (four issuers of 16 columns, one token's terms) one load takes all partials:
+      // every tensor-memory load waits in the tensor pipe with the MMAs, so fewer loads cost less
+      const bool one_load = a.n_iss * a.acc_cols == 64 && ncols <= 16;
       for (int cb = 0; cb < ncols; cb += 16) {
         uint32_t u[kMaxIss][16];
+        if (one_load) {
+          tc_ld64(lane_base, &u[0][0]);
+        } else {
 #pragma unroll
-        for (int w = 0; w < kMaxIss; ++w)
-          if ((mask >> w) & 1u) tc_ld16(lane_base + (uint32_t)(w * a.acc_cols + cb), u[w]);
+          for (int w = 0; w < kMaxIss; ++w)
+            if ((mask >> w) & 1u) tc_ld16(lane_base + (uint32_t)(w * a.acc_cols + cb), u[w]);
+        }
         tc_wait_ld();
         if (cb + 16 >= ncols) {  // buffer read completely: hand it back
           tc_fence_before();
@@ -839,7 +856,9 @@ void size_tiles(TcArgs& a, int ch, int mtiles) {
   a.acc_cols = (a.n_tile + 15) / 16 * 16;
   a.n_iss = a.n_tile <= 32 ? 4 : (a.n_tile <= 64 ? 2 : 1);
   a.n_acc = 1;  // two alternating accumulators measured no faster at any N
-  a.sf_base = (2 * a.n_iss * a.n_acc * a.acc_cols + 31) / 32 * 32;
+  // two accumulator buffers (three, with a stage fewer, measured no faster)
+  a.n_buf = 2;
+  a.sf_base = (a.n_buf * a.n_iss * a.n_acc * a.acc_cols + 31) / 32 * 32;
   a.b_bytes = (a.n_tile * 128 + 1023) / 1024 * 1024;
   for (;; ch = 1) {
     a.ch = ch;
