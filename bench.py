@@ -44,8 +44,8 @@ FALLBACK_HBM_GBS = 6800.0
 NCU_TRAFFIC = {
     # dram__bytes_read.sum + dram__bytes_write.sum of one launch (decode b=1: 16 routed + 2 shared
     # records, the same per launch at any expert count), profiles/k_tc_ffn_decode_b1.md
-    "k_tc<gate/up>": (214172672, "9e004338329c9ed4"),
-    "k_tc<down>": (108428800, "9e004338329c9ed4"),
+    "k_tc<gate/up>": (213737216, "050bbdb703b59061"),
+    "k_tc<down>": (107933184, "050bbdb703b59061"),
 }
 
 
@@ -59,6 +59,7 @@ def parse():
     p.add_argument("--layers", type=int, default=8,
                    help="independent weight sets rotated across steps (8: the router weights alone, 206 MB, exceed L2)")
     p.add_argument("--experts", type=int, default=None, help="override routed experts (small profiling case)")
+    p.add_argument("--tokens", type=int, default=None, help="override tokens per layer call (small profiling case)")
     p.add_argument("--batches", type=int, default=64, help="distinct token batches rotated across steps")
     p.add_argument("--sample-every", type=int, default=8, help="phase-timed step every N steps")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -220,6 +221,7 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     T, seed, zipf_s = WORKLOADS[args.workload]
+    T = args.tokens or T
     base = synth.K3
     E = args.experts or base.n_routed
     shape = synth.LayerShape(base.d_model, base.d_ff, E, base.top_k, base.n_shared)

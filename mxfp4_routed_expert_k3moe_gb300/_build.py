@@ -10,7 +10,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libk3moe.so")
-SOURCES = ["k3moe_api.cu", "k3moe_route.cu", "k3moe_tc.cu", "k3moe_static.cu"]
+SOURCES = ["k3moe_api.cu", "k3moe_route.cu", "k3moe_tc.cu", "k3moe_router_tc.cu", "k3moe_static.cu"]
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
               "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden", "--expt-relaxed-constexpr"]
 

@@ -33,6 +33,11 @@ bool use_fp4(const k3moe_config* c, long long T) {
 
 size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Router logits on the tensor cores (bf16 tokens, prefill-sized T), else on the CUDA cores.
+bool router_tc(const k3moe_config* c, long long T) {
+  return T >= k3::kRouterTcMinT && c->x_dtype == K3MOE_X_BF16 && c->d_model % 64 == 0;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 long long record_bytes_of(const k3moe_config* c) {
@@ -69,7 +74,7 @@ long long wg_bound(const k3moe_config* c, long long T) {
 
 struct Layout {
   size_t ctrl, logits, topk_idx, topk_w, counts, cursor, offsets, wgoff, perm_tok, perm_w, inv, wgs, xq, xs, hq, hs,
-      part, gupart, rtcnt, total;
+      part, gupart, rtcnt, w3, total;
 };
 
 Layout make_layout(const k3moe_config* c, long long T) {
@@ -102,6 +107,7 @@ Layout make_layout(const k3moe_config* c, long long T) {
   take(L.part, sizeof(float) * P * d);
   take(L.gupart, sizeof(float) * P * gateup_parts(T, d, fp4) * 2 * f);
   take(L.rtcnt, sizeof(int) * ((T + 7) / 8));
+  take(L.w3, router_tc(c, T) ? (size_t)3 * E * d * 2 : 0);  // bf16 parts of the router weights
   L.total = o;
   return L;
 }
@@ -140,6 +146,8 @@ Cfg make_cfg(const k3moe_config* c, long long T) {
   k.S = c->n_shared;
   k.x_f32 = c->x_dtype == K3MOE_X_F32 ? 1 : 0;
   k.fp4 = use_fp4(c, T) ? 1 : 0;
+  // tokens per work group (42 at prefill sizes, which reads an expert's record fewer times, measured
+  // slower: the projections there are not bound by the record reads)
   const long long wmax = k.fp4 ? 16 : 32;
   k.wgt = (int)(T < wmax ? T : wmax);
   k.ks = (int)gateup_parts(T, c->d_model, k.fp4 != 0);
@@ -198,8 +206,15 @@ k3moe_status k3moe_route(const k3moe_config* cfg, const void* x, int64_t T, cons
   Layout L;
   if ((s = check_ws(cfg, T, ws, ws_bytes, &L)) != K3MOE_OK) return s;
   const Cfg c = make_cfg(cfg, T);
-  return cuda_status(k3::launch_route(c, bind(L, ws), x, T, w_router, bias, topk_idx, topk_w, k3::RM_USER_OUT,
-                                      static_cast<cudaStream_t>(stream)));
+  const Ws w = bind(L, ws);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int mode = k3::RM_USER_OUT;
+  if (router_tc(cfg, T)) {
+    cudaError_t e = k3::launch_router_tc(c, w, x, T, w_router, bias, static_cast<char*>(ws) + L.w3, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    mode |= k3::RM_LOGITS_READY;
+  }
+  return cuda_status(k3::launch_route(c, w, x, T, w_router, bias, topk_idx, topk_w, mode, st));
 }
 
 k3moe_status k3moe_expert_ffn(const k3moe_config* cfg, const void* x, int64_t T, const int32_t* topk_idx,
@@ -253,9 +268,12 @@ k3moe_status layer_impl(const k3moe_config* cfg, const void* x, int64_t T, const
   const long long wgb = wg_bound(cfg, T);
   cudaError_t e = cudaSuccess;
   if (events) e = cudaEventRecord(static_cast<cudaEvent_t>(events[0]), st);
-  if (e == cudaSuccess)
-    e = k3::launch_route(c, w, x, T, w_router, bias, topk_idx_out, topk_w_out,
-                         k3::RM_USER_OUT | k3::RM_XPREP | k3::RM_PERMUTE, st);
+  int mode = k3::RM_USER_OUT | k3::RM_XPREP | k3::RM_PERMUTE;
+  if (e == cudaSuccess && router_tc(cfg, T)) {
+    e = k3::launch_router_tc(c, w, x, T, w_router, bias, static_cast<char*>(ws) + L.w3, st);
+    mode |= k3::RM_LOGITS_READY;
+  }
+  if (e == cudaSuccess) e = k3::launch_route(c, w, x, T, w_router, bias, topk_idx_out, topk_w_out, mode, st);
   if (e == cudaSuccess && events) e = cudaEventRecord(static_cast<cudaEvent_t>(events[1]), st);
   auto evt = [&](int i) { return events ? static_cast<cudaEvent_t>(events[i]) : nullptr; };
   if (e == cudaSuccess) e = k3::launch_gateup(c, w, routed_records, shared_records, y, T, wgb, st, evt(2));

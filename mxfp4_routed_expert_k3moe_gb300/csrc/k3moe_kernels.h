@@ -26,12 +26,18 @@ inline cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, 
 }
 
 // k3moe_route.cu
-enum RouteMode { RM_USER_OUT = 1, RM_XPREP = 2, RM_PERMUTE = 4 };
+enum RouteMode { RM_USER_OUT = 1, RM_XPREP = 2, RM_PERMUTE = 4, RM_LOGITS_READY = 8 };
 cudaError_t launch_route(const Cfg& c, const Ws& ws, const void* x, long long T, const float* W, const float* bias,
                          int* out_idx, float* out_w, int mode, cudaStream_t st);
 cudaError_t launch_prep(const Cfg& c, const Ws& ws, const void* x, long long T, const int* idx, const float* w,
                         cudaStream_t st);
 cudaError_t launch_rmsnorm(const float* x, long long T, int d, float eps, float* out, cudaStream_t st);
+
+// k3moe_router_tc.cu: router logits of bf16 tokens on the tensor cores (large T). `w3` is workspace
+// for the three bf16 parts of the router weights ([3, E, d]).
+constexpr long long kRouterTcMinT = 512;
+cudaError_t launch_router_tc(const Cfg& c, const Ws& ws, const void* x, long long T, const float* W, const float* bias,
+                             void* w3, cudaStream_t st);
 cudaError_t launch_residual_add(float* x, const float* y, long long n, cudaStream_t st);
 
 // k3moe_tc.cu (tcgen05 expert FFN)

@@ -408,7 +408,8 @@ __global__ void __launch_bounds__(256, 3) k_route(RouteArgs a) {
   const Cfg& c = a.c;
   const int nw = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = warp >> 2, kq = warp & 3;
-  const int e = blockIdx.x * 2 + r;
+  const bool dots = !(a.mode & RM_LOGITS_READY);  // else the logits were computed by the tensor cores
+  const int e = dots ? blockIdx.x * 2 + r : c.E;
   const long long t0 = (long long)blockIdx.y * TT;
   const int ntt = (int)min((long long)TT, a.T - t0);
   const int esz = c.x_f32 ? 4 : 2;
@@ -496,7 +497,7 @@ __global__ void __launch_bounds__(256, 3) k_route(RouteArgs a) {
   if (threadIdx.x < 2 * TT) {
     const int rr = threadIdx.x / TT, tt = threadIdx.x - rr * TT;
     const int er = blockIdx.x * 2 + rr;
-    if (er < c.E && tt < ntt) {
+    if (dots && er < c.E && tt < ntt) {
       const float v = ((s_part[4 * rr][tt] + s_part[4 * rr + 1][tt]) + s_part[4 * rr + 2][tt]) + s_part[4 * rr + 3][tt];
       a.ws.logits[(t0 + tt) * c.E + er] = v + (a.bias ? a.bias[er] : 0.0f);
     }
@@ -612,7 +613,8 @@ cudaError_t launch_route_tt(const RouteArgs& a, int warps, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  dim3 grid((a.c.E + 1) / 2, (unsigned)((a.T + TT - 1) / TT));
+  // with precomputed logits one CTA per token tile selects, writes the activation terms and permutes
+  dim3 grid((a.mode & RM_LOGITS_READY) ? 1u : (unsigned)((a.c.E + 1) / 2), (unsigned)((a.T + TT - 1) / TT));
   return launch_pdl(k_route<TT>, grid, dim3(warps * 32), smem, st, a);
 }
 

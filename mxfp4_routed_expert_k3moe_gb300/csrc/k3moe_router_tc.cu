@@ -1,0 +1,217 @@
+// Router logits of many tokens on the 5th-generation tensor cores (tcgen05 kind::f16, sm_103a):
+//   logits[t, e] = sum_j x[t, j] W[e, j] (+ b[e])
+// (kimi-k3-in-c review, table "한눈에 보는 kimi-k3-in-c": 896 routed experts scored per token.)
+// The tokens x are bf16, so they enter the MMA exactly. The fp32 router weights are split into three
+// bf16 parts, W = W_hi + W_mid + W_lo, each the bf16 rounding of what the previous parts leave (the
+// differences are exact in fp32), which keeps 24 significant bits of every weight; the parts go to
+// the workspace as W3[3][E][d] and the GEMM runs over K = 3 d, reusing each token tile for all three,
+// with fp32 accumulation in tensor memory. At prefill sizes this replaces the CUDA-core dot products,
+// which read the whole router matrix once per tile of 8 tokens.
+//
+// One CTA per (128-token tile, 256-expert tile): warp 0 lane 0 issues the tensor copies of a 4-stage
+// ring (x tile 128 x 64 and W part tile 256 x 64, bf16, 128-byte swizzle), warp 1 lane 0 issues the
+// MMAs (M = 128 tokens, N = 256 experts, K = 16 each), and the four warps then read the accumulator
+// (lane = token) and store the logits with the bias added. Every wait is bounded.
+#include <cstdint>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include "k3moe_kernels.h"
+#include "k3moe_ptx.cuh"
+
+namespace k3 {
+
+namespace {
+
+using namespace ptx;
+
+constexpr int kRM = 128;                  // tokens per tile (MMA M)
+constexpr int kRN = 256;                  // experts per tile (MMA N)
+constexpr int kRK = 64;                   // bf16 elements per stage along the reduction axis (one 128-byte row)
+constexpr int kRStages = 4;
+constexpr int kRThreads = 128;
+constexpr int kRA = kRM * kRK * 2;        // 16 KB
+constexpr int kRB = kRN * kRK * 2;        // 32 KB
+constexpr uint32_t kRWaitLimit = 1u << 24;
+
+struct RCtl {
+  uint64_t full[kRStages];
+  uint64_t empty[kRStages];
+  uint64_t done;
+  uint32_t tmem;
+  volatile int abort;
+};
+
+__device__ __forceinline__ bool rwait(uint32_t bar, uint32_t parity, RCtl* ctl, int* status) {
+  for (uint32_t it = 0; it < kRWaitLimit; ++it) {
+    if (mbar_try(bar, parity)) return true;
+    if (ctl->abort) return false;
+    if (it > 256) __nanosleep(64);
+  }
+  ctl->abort = 1;
+  atomicOr(&status[CTRL_STATUS], ST_TIMEOUT);
+  return false;
+}
+
+// W3[p][e][j], p = 0, 1, 2: the three bf16 parts of W[e][j].
+__global__ void __launch_bounds__(256) k_split_w(const float* W, long long n, __nv_bfloat16* w3) {
+  pdl_wait();
+  pdl_launch_dependents();
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const float w = W[i];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+    const float r1 = w - __bfloat162float(hi);
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const float r2 = r1 - __bfloat162float(mid);
+    w3[i] = hi;
+    w3[n + i] = mid;
+    w3[2 * n + i] = __float2bfloat16_rn(r2);
+  }
+}
+
+__global__ void __launch_bounds__(kRThreads, 1)
+    k_router_mma(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
+                 const float* bias, float* logits, long long T, int E, int d, int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  RCtl* ctl = reinterpret_cast<RCtl*>(smem + kRStages * (kRA + kRB));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int mt = blockIdx.x, nt = blockIdx.y;
+  pdl_wait();  // the weight parts come from the split kernel just before
+  pdl_launch_dependents();
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&ctl->tmem)), "r"(kRN));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  if (tid == 0) {
+    for (int s = 0; s < kRStages; ++s) {
+      mbar_init(su32(&ctl->full[s]), 1);
+      mbar_init(su32(&ctl->empty[s]), 1);
+    }
+    mbar_init(su32(&ctl->done), 1);
+    ctl->abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem;
+  const int kpp = d / kRK, nk = 3 * kpp;  // k-steps per part, in all
+  bool ok = true;
+  if (warp == 0) {
+    if (lane == 0) {  // tensor copies
+      for (int ks = 0, s = 0; ks < nk && ok; ++ks) {
+        const uint32_t round = (uint32_t)(ks / kRStages);
+        if (ks >= kRStages && !rwait(su32(&ctl->empty[s]), (round - 1) & 1u, ctl, status)) { ok = false; break; }
+        const int part = ks / kpp, k0 = (ks - part * kpp) * kRK;
+        uint8_t* st = smem + (size_t)s * (kRA + kRB);
+        mbar_expect_tx(su32(&ctl->full[s]), kRA + kRB);
+        tma_load_2d(su32(st), &map_x, k0, mt * kRM, su32(&ctl->full[s]));
+        tma_load_3d(su32(st + kRA), &map_w, k0, nt * kRN, part, su32(&ctl->full[s]));
+        if (++s == kRStages) s = 0;
+      }
+      // after a timeout, give copies still in flight time to land before the CTA exits
+      if (!ok)
+        for (int w = 0; w < 1000; ++w) __nanosleep(1000);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // MMAs
+      const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kRN >> 3) << 17) | ((uint32_t)(kRM >> 4) << 24);
+      for (int ks = 0, s = 0; ks < nk; ++ks) {
+        if (!rwait(su32(&ctl->full[s]), (uint32_t)(ks / kRStages) & 1u, ctl, status)) { ok = false; break; }
+        tc_fence_after();
+        const uint8_t* st = smem + (size_t)s * (kRA + kRB);
+        const uint64_t da = sw128_desc(su32(st)), db = sw128_desc(su32(st + kRA));
+#pragma unroll
+        for (int k = 0; k < kRK / 16; ++k) tc_mma_bf16(tmem, da + 2 * k, db + 2 * k, idesc, (ks | k) ? 1u : 0u);
+        tc_commit(su32(&ctl->empty[s]));
+        if (++s == kRStages) s = 0;
+      }
+      tc_commit(su32(&ctl->done));  // arrives when every MMA issued above has completed
+    }
+  }
+  __syncwarp();
+  // epilogue: lane = token, 32 expert columns per load
+  const bool have = __all_sync(0xffffffffu, rwait(su32(&ctl->done), 0, ctl, status));
+  tc_fence_after();
+  if (have) {
+    const long long t = (long long)mt * kRM + 32 * warp + lane;
+    for (int c0 = 0; c0 < kRN; c0 += 32) {
+      uint32_t v[32];
+      tc_ld32(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)c0, v);
+      tc_wait_ld();
+      const int e0 = nt * kRN + c0;
+      if (t < T) {
+        float* dst = logits + t * E + e0;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (e0 + j < E) dst[j] = __uint_as_float(v[j]) + (bias ? __ldg(&bias[e0 + j]) : 0.0f);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kRN));
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode_r = nullptr;
+std::mutex g_mu_r;
+
+cudaError_t encode_fn() {
+  std::lock_guard<std::mutex> lock(g_mu_r);
+  if (g_encode_r) return cudaSuccess;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return e != cudaSuccess ? e : cudaErrorNotSupported;
+  g_encode_r = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_router_tc(const Cfg& c, const Ws& ws, const void* x, long long T, const float* W, const float* bias,
+                             void* w3, cudaStream_t st) {
+  if (c.x_f32 || c.d % kRK != 0 || T > (1LL << 31) - kRM) return cudaErrorInvalidValue;
+  cudaError_t e = encode_fn();
+  if (e != cudaSuccess) return e;
+  const long long n = (long long)c.E * c.d;
+  e = launch_pdl(k_split_w, dim3(4 * 152), dim3(256), 0, st, W, n, static_cast<__nv_bfloat16*>(w3));
+  if (e != cudaSuccess) return e;
+  CUtensorMap mx, mw;
+  {
+    cuuint64_t gdim[2] = {(cuuint64_t)c.d, (cuuint64_t)T};
+    cuuint64_t gstr[1] = {(cuuint64_t)c.d * 2};
+    cuuint32_t box[2] = {kRK, kRM}, es[2] = {1, 1};
+    if (g_encode_r(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), gdim, gstr, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    cuuint64_t gdim[3] = {(cuuint64_t)c.d, (cuuint64_t)c.E, 3};
+    cuuint64_t gstr[2] = {(cuuint64_t)c.d * 2, (cuuint64_t)n * 2};
+    cuuint32_t box[3] = {kRK, kRN, 1}, es[3] = {1, 1, 1};
+    if (g_encode_r(&mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, w3, gdim, gstr, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  static bool attr = false;
+  const size_t smem = (size_t)kRStages * (kRA + kRB) + sizeof(RCtl) + 1024;
+  if (!attr) {
+    if ((e = cudaFuncSetAttribute(k_router_mma, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
+      return e;
+    attr = true;
+  }
+  dim3 grid((unsigned)((T + kRM - 1) / kRM), (unsigned)((c.E + kRN - 1) / kRN));
+  return launch_pdl(k_router_mma, grid, dim3(kRThreads), smem, st, mx, mw, bias, ws.logits, T, c.E, c.d, ws.ctrl);
+}
+
+}  // namespace k3

@@ -46,6 +46,7 @@
 #include <cudaTypedefs.h>
 
 #include "k3moe_kernels.h"
+#include "k3moe_ptx.cuh"
 
 namespace k3 {
 
@@ -66,109 +67,7 @@ constexpr int kMaxBuf = 4;               // accumulator buffers per issuer
 constexpr int kATile = 128 * 128;        // A tile of a chunk in shared memory (both forms)
 constexpr uint32_t kWaitLimit = 1u << 24;
 
-// ------------------------------------------------------------------------------- PTX helpers
-__device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.b32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// L2 policy for data read once (the weight stream): evicted first, so that the small arrays that
-// every CTA reads repeatedly (work groups, activation terms) stay in L2 instead of queueing behind
-// the stream at the DRAM.
-__device__ __forceinline__ uint64_t policy_evict_first() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
-                                            uint32_t bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
-      "%3, %4, %5}], [%6], %7;" ::"r"(dst),
-      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar), "l"(policy)
-      : "memory");
-}
-__device__ __forceinline__ void cp16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-// 4-byte copy; src_bytes 0 writes zeros
-__device__ __forceinline__ void cp4(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
-// Bulk copy (16-byte aligned, multiple of 16 bytes) completing on an mbarrier, with an L2 policy.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
-          dst),
-      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
-      : "memory");
-}
-__device__ __forceinline__ void cp_arrive_noinc(uint32_t bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
-  return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
-         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa, uint32_t sfb,
-                                       uint32_t acc) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%5], [%6], p;\n}\n" ::"r"(d),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb));
-}
-__device__ __forceinline__ void tc_mma_f4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa, uint32_t sfb,
-                                          uint32_t acc) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], [%6], p;\n}\n" ::"r"(d),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb));
-}
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-// smem -> TMEM copy of a 32 x 128-bit block, replicated into the four 32-lane quarters
-__device__ __forceinline__ void tc_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
-// Descriptor of 32 rows x 16 bytes stored contiguously (no swizzle; 8-row groups 128 bytes apart).
-__device__ __forceinline__ uint64_t sf_desc(uint32_t addr) {
-  return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)(512 >> 4) << 16) | ((uint64_t)(128 >> 4) << 32) |
-         ((uint64_t)1 << 46);
-}
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-// 16 columns of the warp's 32 lanes; the registers are valid after tc_wait_ld.
-__device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t* v) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
-        "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
-      : "r"(taddr));
-}
-// 64 columns of the warp's 32 lanes in one instruction (every issuer's 16-column partial at once)
-__device__ __forceinline__ void tc_ld64(uint32_t taddr, uint32_t* v) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
-      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31]), "=r"(v[32]), "=r"(v[33]), "=r"(v[34]), "=r"(v[35]), "=r"(v[36]), "=r"(v[37]), "=r"(v[38]), "=r"(v[39]), "=r"(v[40]), "=r"(v[41]), "=r"(v[42]), "=r"(v[43]), "=r"(v[44]), "=r"(v[45]), "=r"(v[46]), "=r"(v[47]), "=r"(v[48]), "=r"(v[49]), "=r"(v[50]), "=r"(v[51]), "=r"(v[52]), "=r"(v[53]), "=r"(v[54]), "=r"(v[55]), "=r"(v[56]), "=r"(v[57]), "=r"(v[58]), "=r"(v[59]), "=r"(v[60]), "=r"(v[61]), "=r"(v[62]), "=r"(v[63])
-      : "r"(taddr));
-}
-__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+using namespace ptx;
 
 // Shared-memory control block (after the pipeline stages).
 struct Ctl {
@@ -635,7 +534,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (MODE == GATEUP)
                 a.ws.gupart[((pos * c.ks + it.kp) * 2 + it.mat) * c.f + row] = run;
               else
-                a.ws.part[pos * c.d + row] = run * __shfl_sync(0xffffffffu, wlane, tk & 31);
+                a.ws.part[pos * c.d + row] =
+                    run * (tk < 32 ? __shfl_sync(0xffffffffu, wlane, tk & 31) : __ldg(&a.ws.perm_w[pos]));
               run = 0.0f;
               ++tk;
             }
@@ -853,11 +753,14 @@ void size_tiles(TcArgs& a, int ch, int mtiles) {
   a.sf_bytes = a.fp4 ? 2048 : 1024;
   a.div_parts.init((uint32_t)a.parts);
   a.div_mtiles.init((uint32_t)mtiles);
-  a.acc_cols = (a.n_tile + 15) / 16 * 16;
-  a.n_iss = a.n_tile <= 32 ? 4 : (a.n_tile <= 64 ? 2 : 1);
+  a.acc_cols = 16;  // a power of two >= n_tile: every accumulator starts at a multiple of its width
+  while (a.acc_cols < a.n_tile) a.acc_cols *= 2;
+  // issuers and accumulator buffers: small N needs several issuers (issue rate). Above 64 columns:
+  // with few tokens per work group (T < 256) two issuers with one buffer each (measured faster), at
+  // prefill sizes one issuer with two buffers (measured faster: deeper ring, overlapped epilogue)
+  a.n_iss = a.n_tile <= 32 ? 4 : (a.n_tile <= 64 || a.T < 256 ? 2 : 1);
   a.n_acc = 1;  // two alternating accumulators measured no faster at any N
-  // two accumulator buffers (three, with a stage fewer, measured no faster)
-  a.n_buf = 2;
+  a.n_buf = (a.n_tile <= 64 || a.T >= 256) ? 2 : 1;  // (three, with a stage fewer, measured no faster)
   a.sf_base = (a.n_buf * a.n_iss * a.n_acc * a.acc_cols + 31) / 32 * 32;
   a.b_bytes = (a.n_tile * 128 + 1023) / 1024 * 1024;
   for (;; ch = 1) {

@@ -155,6 +155,33 @@ def test_route_only():
     assert gate_err(idx.cpu().numpy(), wn, idx_ref, w_ref) < 1e-6
 
 
+@pytest.mark.parametrize("T", [512, 700])
+def test_route_tensor_core_router(T):
+    """From 512 bf16 tokens the logits come from the tensor cores (the fp32 router weights in three
+    bf16 parts, fp32 accumulation): same selection (near-tie rule) and gates as the oracle."""
+    L = DeviceLayer(MID, seed=12, zipf_s=1.1)
+    xh, xd = L.tokens(T)
+    idx = torch.empty((T, MID.top_k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, MID.top_k), dtype=torch.float32, device="cuda")
+    ws = torch.zeros(k3.workspace_bytes(L.cfg, T), dtype=torch.uint8, device="cuda")
+    k3.route(L.cfg, xd, T, L.W, L.bias, idx, w, ws)
+    torch.cuda.synchronize()
+    assert k3.check_device_status(ws) == k3.OK
+    _, idx_ref, w_ref, logits_ref = L.oracle(xh)
+    ok, near = index_parity(idx.cpu().numpy(), idx_ref, logits_ref, MID.top_k)
+    assert ok
+    wn = w.cpu().numpy()
+    keep = [t for t in range(T) if t not in near]
+    assert np.allclose(wn.sum(axis=1), 1.0, atol=1e-6)
+    assert gate_err(idx.cpu().numpy()[keep], wn[keep], idx_ref[keep], w_ref[keep]) < 1e-5
+
+
+def test_layer_mid_large_T_sampled():
+    """The whole layer at 700 tokens: tensor-core router, E4M3 activation terms."""
+    L = DeviceLayer(MID, seed=13)
+    check_layer(L, 700, sample=[0, 5, 333, 512, 699])
+
+
 def test_expert_ffn_given_routing():
     L = DeviceLayer(MID, seed=11, x_dtype="f32")
     T = 13
