@@ -171,7 +171,7 @@ K3MOE_API k3moe_status k3moe_layer_timed(const k3moe_config* cfg /* host */, con
  * cudaMalloc's device synchronisation; this call needs no workspace from them. Its scratch is a
  * fixed K3MOE_STATIC_SCRATCH_BYTES array in device memory declared by the library (resident on
  * every GPU that loads it until exit); calls needing more (k3moe_workspace_bytes(cfg, T) larger,
- * i.e. T > 2 at the 7168/1536/896 shape) return K3MOE_ERR_WORKSPACE. It allocates nothing,
+ * i.e. T > 4 at the 7168/1536/896 shape) return K3MOE_ERR_WORKSPACE. It allocates nothing,
  * clears the scratch it uses at the start of each call, and otherwise behaves like k3moe_layer
  * without the optional top-k outputs. All calls on a device share the array: calls that overlap
  * on the GPU race and give wrong results. The first call on a device looks up the array's

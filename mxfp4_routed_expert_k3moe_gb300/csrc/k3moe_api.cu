@@ -15,12 +15,15 @@ constexpr long long kMaxE = 4096;
 constexpr long long kMaxK = 32;
 constexpr long long kMaxS = 8;
 constexpr int kMaxDModel = 25600;
-// Reduction parts of the gate/up projection: at a few tokens the (work group, row tile) items are
-// too few to spread over the SMs, so each is split along d into 4 parts (at most one per chunk of
-// the reduction axis: 256 codes in the E2M1 form, 128 in the E4M3 form), summed by the GLU kernel.
+// Reduction parts of the gate/up projection (summed by the GLU kernel). At decode, splitting each
+// (work group, row tile) item along d into 2, 3, 4, 7 or 14 parts, to spread the few items over the
+// SMs more evenly, measured slower than whole items (per-item costs outweigh the balance: 52 us
+// for 1 part, 60 us for 4, 116 us for 14 at one token), so one part is used.
 long long gateup_parts(long long T, long long d, bool fp4) {
-  const long long p = T <= 4 ? 4 : 1, nch = d / (fp4 ? 256 : 128);
-  return p < nch ? p : nch;
+  (void)T;
+  (void)d;
+  (void)fp4;
+  return 1;
 }
 constexpr long long kMaxTerms = 3;     // E4M3 terms per activation block (x: 2 bf16 / 3 fp32; h: 3)
 constexpr long long kMaxTermsFp4 = 8;  // E2M1 terms per activation block
