@@ -55,7 +55,9 @@ def parse():
     p.add_argument("--steps", type=int, default=20000)
     p.add_argument("--warmup", type=int, default=50)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=list(WORKLOADS), default="decode_b1")
+    p.add_argument("--workload", choices=list(WORKLOADS) + ["stack4_zipf"], default="decode_b1")
+    p.add_argument("--sweep", default="1,8,64,512,4096,16384",
+                   help="stack4_zipf: token counts per layer call (one JSON line each)")
     p.add_argument("--layers", type=int, default=8,
                    help="independent weight sets rotated across steps (8: the router weights alone, 206 MB, exceed L2)")
     p.add_argument("--experts", type=int, default=None, help="override routed experts (small profiling case)")
@@ -380,6 +382,69 @@ def e2e(args, k3, cfg, layers, xs_host, T, d, dev):
             "d2h_bytes_per_step": T * d * 4, "steps": steps}
 
 
+def run_stack(args, rank, world, local_rank):
+    """stack4_zipf: 4 independent layers (seeds 40-43, Zipf 1.1 routing bias), pre-norm residual
+    x <- x + Layer_l(RMSNorm(x)) with fp32 activations, for each token count of --sweep. One step =
+    the 4 layers on one batch; one JSON line per token count (a curve, not the headline)."""
+    import torch
+    import mxfp4_routed_expert_k3moe_gb300 as k3
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    shape = synth.K3
+    stride = shape.record_stride
+    d, E, k, S = shape.d_model, shape.n_routed, shape.top_k, shape.n_shared
+    layers = [LayerWeights(shape, 40 + l, l, 1.1, stride, dev) for l in range(4)]
+    cfg = k3.Config.make(d, shape.d_ff, E, k, S, x_dtype=k3.X_F32, record_stride=stride)
+    peak, peak_kind = hbm_peak()
+    for T in [int(t) for t in args.sweep.split(",")]:
+        x = torch.from_numpy(synth.tokens(shape, 40, T, "f32")).to(dev)
+        xn = torch.empty_like(x)
+        y = torch.empty_like(x)
+        ws = torch.zeros(k3.workspace_bytes(cfg, T), dtype=torch.uint8, device=dev)
+        idx = [torch.empty((T, k), dtype=torch.int32, device=dev) for _ in range(4)]
+
+        def step(keep_idx=False):
+            for l, L in enumerate(layers):
+                k3.rmsnorm(x, T, d, 1e-6, xn)
+                k3.layer(cfg, xn, T, L.W, L.bias, L.routed, L.shared, y, ws, topk_idx=idx[l] if keep_idx else None)
+                k3.residual_add(x, y, T * d)
+
+        steps = max(3, min(args.steps, int(2e5 // max(T, 1))))
+        for _ in range(max(3, min(args.warmup, 5))):
+            step()
+        step(keep_idx=True)
+        torch.cuda.synchronize()
+        if k3.check_device_status(ws) != k3.OK:
+            raise RuntimeError("device status check failed in the stack")
+        U = [int(torch.unique(i).numel()) for i in idx]
+        clocks = ClockSampler(local_rank)
+        clocks.start()
+        time.sleep(0.2)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(steps):
+            step()
+        b.record()
+        torch.cuda.synchronize()
+        clk = clocks.stop()
+        ms = a.elapsed_time(b) / steps
+        rec = shape.record_bytes
+        bytes_step = sum((u + S) * rec + E * d * 4 + T * d * 4 * 2 for u in U)
+        line = {"metric": "MoE-layer tokens/s (K3 shape, 4-layer stack with pre-norm residual)",
+                "value": 4 * T / (ms * 1e-3), "unit": "layer-tokens/s", "stack_tokens_per_s": T / (ms * 1e-3),
+                "ms_per_step": ms, "steps": steps, "higher_is_better": True, "dtype": "mxfp4 weights x fp32 activations, fp32 accumulate",
+                "data": "synthetic", "config": {"workload": "stack4_zipf", "tokens_per_layer_call": T, "layers": 4},
+                "distinct_experts_per_layer": U,
+                "layer_roofline": {"bytes_per_step": bytes_step, "achieved_gbs": bytes_step / (ms * 1e-3) / 1e9,
+                                   "frac": bytes_step / (ms * 1e-3) / 1e9 / peak, "peak": peak, "peak_kind": peak_kind},
+                "clocks": clk}
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        del ws, x, xn, y
+        torch.cuda.empty_cache()
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -393,7 +458,10 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
-    run_ours(args, rank, world, local_rank)
+    if args.workload == "stack4_zipf":
+        run_stack(args, rank, world, local_rank)
+    else:
+        run_ours(args, rank, world, local_rank)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

@@ -36,9 +36,9 @@ bool use_fp4(const k3moe_config* c, long long T) {
 
 size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Router logits on the tensor cores (bf16 tokens, prefill-sized T), else on the CUDA cores.
+// Router logits on the tensor cores at prefill-sized T, else on the CUDA cores.
 bool router_tc(const k3moe_config* c, long long T) {
-  return T >= k3::kRouterTcMinT && c->x_dtype == K3MOE_X_BF16 && c->d_model % 64 == 0;
+  return T >= k3::kRouterTcMinT && c->d_model % 64 == 0;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -77,7 +77,7 @@ long long wg_bound(const k3moe_config* c, long long T) {
 
 struct Layout {
   size_t ctrl, logits, topk_idx, topk_w, counts, cursor, offsets, wgoff, perm_tok, perm_w, inv, wgs, xq, xs, hq, hs,
-      part, gupart, rtcnt, w3, total;
+      part, gupart, rtcnt, w3, x3, total;
 };
 
 Layout make_layout(const k3moe_config* c, long long T) {
@@ -109,8 +109,9 @@ Layout make_layout(const k3moe_config* c, long long T) {
   take(L.hs, (size_t)(P * terms * (f / 32)));
   take(L.part, sizeof(float) * P * d);
   take(L.gupart, sizeof(float) * P * gateup_parts(T, d, fp4) * 2 * f);
-  take(L.rtcnt, sizeof(int) * ((T + 7) / 8));
+  take(L.rtcnt, sizeof(int) * T);  // one counter per router token tile (tiles of 1 to 8 tokens)
   take(L.w3, router_tc(c, T) ? (size_t)3 * E * d * 2 : 0);  // bf16 parts of the router weights
+  take(L.x3, router_tc(c, T) && c->x_dtype == K3MOE_X_F32 ? (size_t)3 * T * d * 2 : 0);  // ... of fp32 tokens
   L.total = o;
   return L;
 }
@@ -213,7 +214,8 @@ k3moe_status k3moe_route(const k3moe_config* cfg, const void* x, int64_t T, cons
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int mode = k3::RM_USER_OUT;
   if (router_tc(cfg, T)) {
-    cudaError_t e = k3::launch_router_tc(c, w, x, T, w_router, bias, static_cast<char*>(ws) + L.w3, st);
+    cudaError_t e = k3::launch_router_tc(c, w, x, T, w_router, bias, static_cast<char*>(ws) + L.w3,
+                                         static_cast<char*>(ws) + L.x3, st);
     if (e != cudaSuccess) return cuda_status(e);
     mode |= k3::RM_LOGITS_READY;
   }
@@ -273,7 +275,8 @@ k3moe_status layer_impl(const k3moe_config* cfg, const void* x, int64_t T, const
   if (events) e = cudaEventRecord(static_cast<cudaEvent_t>(events[0]), st);
   int mode = k3::RM_USER_OUT | k3::RM_XPREP | k3::RM_PERMUTE;
   if (e == cudaSuccess && router_tc(cfg, T)) {
-    e = k3::launch_router_tc(c, w, x, T, w_router, bias, static_cast<char*>(ws) + L.w3, st);
+    e = k3::launch_router_tc(c, w, x, T, w_router, bias, static_cast<char*>(ws) + L.w3, static_cast<char*>(ws) + L.x3,
+                             st);
     mode |= k3::RM_LOGITS_READY;
   }
   if (e == cudaSuccess) e = k3::launch_route(c, w, x, T, w_router, bias, topk_idx_out, topk_w_out, mode, st);

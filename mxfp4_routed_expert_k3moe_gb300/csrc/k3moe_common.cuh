@@ -54,7 +54,7 @@ struct Ws {
   uint8_t* hs;        // [P * hterms, f/32] their E8M0 block scales
   float* part;        // [P, d] gate-weighted down-projection outputs per position
   float* gupart;      // [P, ks, 2, f] partial gate/up sums of the reduction parts
-  int* rtcnt;         // [ceil(T/8)] router CTAs finished per token tile
+  int* rtcnt;         // [T] router CTAs finished per token tile (tiles of 1 to 8 tokens)
 };
 
 // ----------------------------------------------------------------------------- small helpers

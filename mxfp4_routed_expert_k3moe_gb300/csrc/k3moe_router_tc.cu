@@ -1,12 +1,14 @@
 // Router logits of many tokens on the 5th-generation tensor cores (tcgen05 kind::f16, sm_103a):
 //   logits[t, e] = sum_j x[t, j] W[e, j] (+ b[e])
 // (kimi-k3-in-c review, table "한눈에 보는 kimi-k3-in-c": 896 routed experts scored per token.)
-// The tokens x are bf16, so they enter the MMA exactly. The fp32 router weights are split into three
-// bf16 parts, W = W_hi + W_mid + W_lo, each the bf16 rounding of what the previous parts leave (the
-// differences are exact in fp32), which keeps 24 significant bits of every weight; the parts go to
-// the workspace as W3[3][E][d] and the GEMM runs over K = 3 d, reusing each token tile for all three,
-// with fp32 accumulation in tensor memory. At prefill sizes this replaces the CUDA-core dot products,
-// which read the whole router matrix once per tile of 8 tokens.
+// The fp32 router weights are split into three bf16 parts, W = W0 + W1 + W2, each the bf16 rounding
+// of what the previous parts leave (the differences are exact in fp32), which keeps 24 significant
+// bits of every weight; the parts go to the workspace as W3[3][E][d]. bf16 tokens enter the MMA
+// exactly and meet the three parts: K = 3 d. fp32 tokens are split the same way into X3[3][T][d], and
+// the products X_a W_b with a + b <= 2 are accumulated (6 pairs, K = 6 d); the pairs left out are
+// below 2^-24 of the dot product's terms. Accumulation is fp32 in tensor memory. At prefill sizes
+// this replaces the CUDA-core dot products, which read the whole router matrix once per tile of 8
+// tokens.
 //
 // One CTA per (128-token tile, 256-expert tile): warp 0 lane 0 issues the tensor copies of a 4-stage
 // ring (x tile 128 x 64 and W part tile 256 x 64, bf16, 128-byte swizzle), warp 1 lane 0 issues the
@@ -56,7 +58,11 @@ __device__ __forceinline__ bool rwait(uint32_t bar, uint32_t parity, RCtl* ctl, 
   return false;
 }
 
-// W3[p][e][j], p = 0, 1, 2: the three bf16 parts of W[e][j].
+// Pairs (token part, weight part) of the reduction, in order: bf16 tokens use the first three.
+__constant__ int kPairA[6] = {0, 0, 0, 1, 1, 2};
+__constant__ int kPairB[6] = {0, 1, 2, 0, 1, 0};
+
+// W3[p][i], p = 0, 1, 2: the three bf16 parts of W[i] (router weights or fp32 tokens).
 __global__ void __launch_bounds__(256) k_split_w(const float* W, long long n, __nv_bfloat16* w3) {
   pdl_wait();
   pdl_launch_dependents();
@@ -74,7 +80,7 @@ __global__ void __launch_bounds__(256) k_split_w(const float* W, long long n, __
 
 __global__ void __launch_bounds__(kRThreads, 1)
     k_router_mma(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
-                 const float* bias, float* logits, long long T, int E, int d, int* status) {
+                 const float* bias, float* logits, long long T, int E, int d, int npairs, int* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   RCtl* ctl = reinterpret_cast<RCtl*>(smem + kRStages * (kRA + kRB));
@@ -99,18 +105,18 @@ __global__ void __launch_bounds__(kRThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem;
-  const int kpp = d / kRK, nk = 3 * kpp;  // k-steps per part, in all
+  const int kpp = d / kRK, nk = npairs * kpp;  // k-steps per (token part, weight part) pair, in all
   bool ok = true;
   if (warp == 0) {
     if (lane == 0) {  // tensor copies
       for (int ks = 0, s = 0; ks < nk && ok; ++ks) {
         const uint32_t round = (uint32_t)(ks / kRStages);
         if (ks >= kRStages && !rwait(su32(&ctl->empty[s]), (round - 1) & 1u, ctl, status)) { ok = false; break; }
-        const int part = ks / kpp, k0 = (ks - part * kpp) * kRK;
+        const int pair = ks / kpp, k0 = (ks - pair * kpp) * kRK;
         uint8_t* st = smem + (size_t)s * (kRA + kRB);
         mbar_expect_tx(su32(&ctl->full[s]), kRA + kRB);
-        tma_load_2d(su32(st), &map_x, k0, mt * kRM, su32(&ctl->full[s]));
-        tma_load_3d(su32(st + kRA), &map_w, k0, nt * kRN, part, su32(&ctl->full[s]));
+        tma_load_3d(su32(st), &map_x, k0, mt * kRM, kPairA[pair], su32(&ctl->full[s]));
+        tma_load_3d(su32(st + kRA), &map_w, k0, nt * kRN, kPairB[pair], su32(&ctl->full[s]));
         if (++s == kRStages) s = 0;
       }
       // after a timeout, give copies still in flight time to land before the CTA exits
@@ -177,19 +183,24 @@ cudaError_t encode_fn() {
 }  // namespace
 
 cudaError_t launch_router_tc(const Cfg& c, const Ws& ws, const void* x, long long T, const float* W, const float* bias,
-                             void* w3, cudaStream_t st) {
-  if (c.x_f32 || c.d % kRK != 0 || T > (1LL << 31) - kRM) return cudaErrorInvalidValue;
+                             void* w3, void* x3, cudaStream_t st) {
+  if (c.d % kRK != 0 || T > (1LL << 31) - kRM || (c.x_f32 && !x3)) return cudaErrorInvalidValue;
   cudaError_t e = encode_fn();
   if (e != cudaSuccess) return e;
   const long long n = (long long)c.E * c.d;
   e = launch_pdl(k_split_w, dim3(4 * 152), dim3(256), 0, st, W, n, static_cast<__nv_bfloat16*>(w3));
   if (e != cudaSuccess) return e;
+  if (c.x_f32) {  // fp32 tokens: three bf16 parts as well
+    e = launch_pdl(k_split_w, dim3(4 * 152), dim3(256), 0, st, static_cast<const float*>(x), T * c.d,
+                   static_cast<__nv_bfloat16*>(x3));
+    if (e != cudaSuccess) return e;
+  }
   CUtensorMap mx, mw;
   {
-    cuuint64_t gdim[2] = {(cuuint64_t)c.d, (cuuint64_t)T};
-    cuuint64_t gstr[1] = {(cuuint64_t)c.d * 2};
-    cuuint32_t box[2] = {kRK, kRM}, es[2] = {1, 1};
-    if (g_encode_r(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), gdim, gstr, box, es,
+    cuuint64_t gdim[3] = {(cuuint64_t)c.d, (cuuint64_t)T, (cuuint64_t)(c.x_f32 ? 3 : 1)};
+    cuuint64_t gstr[2] = {(cuuint64_t)c.d * 2, (cuuint64_t)(T * c.d * 2)};
+    cuuint32_t box[3] = {kRK, kRM, 1}, es[3] = {1, 1, 1};
+    if (g_encode_r(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, c.x_f32 ? x3 : const_cast<void*>(x), gdim, gstr, box, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
@@ -211,7 +222,8 @@ cudaError_t launch_router_tc(const Cfg& c, const Ws& ws, const void* x, long lon
     attr = true;
   }
   dim3 grid((unsigned)((T + kRM - 1) / kRM), (unsigned)((c.E + kRN - 1) / kRN));
-  return launch_pdl(k_router_mma, grid, dim3(kRThreads), smem, st, mx, mw, bias, ws.logits, T, c.E, c.d, ws.ctrl);
+  return launch_pdl(k_router_mma, grid, dim3(kRThreads), smem, st, mx, mw, bias, ws.logits, T, c.E, c.d,
+                    c.x_f32 ? 6 : 3, ws.ctrl);
 }
 
 }  // namespace k3

@@ -27,7 +27,7 @@
 //               weight stream near 3 TB/s; four reach the DRAM rate.
 //   warps 8-11  MMA issuers (one lane each): tcgen05.cp of the scale words into tensor memory, then
 //               the MMAs. One issuing thread sustains one tcgen05 instruction per ~120-230 SM cycles
-//               whatever N is, so at small N (few tokens) four issuers share the stages, each with
+//               whatever N is, so at small N (few tokens) three issuers share the stages, each with
 //               its own accumulators in tensor memory; the epilogue adds the partial sums of an item.
 // Every ring slot has exactly one agent of each kind (loader v owns the slots s = v mod 4, issuer w
 // the slots s = w mod n_iss), so each agent waits on a slot's barriers round after round and a
@@ -755,10 +755,11 @@ void size_tiles(TcArgs& a, int ch, int mtiles) {
   a.div_mtiles.init((uint32_t)mtiles);
   a.acc_cols = 16;  // a power of two >= n_tile: every accumulator starts at a multiple of its width
   while (a.acc_cols < a.n_tile) a.acc_cols *= 2;
-  // issuers and accumulator buffers: small N needs several issuers (issue rate). Above 64 columns:
-  // with few tokens per work group (T < 256) two issuers with one buffer each (measured faster), at
-  // prefill sizes one issuer with two buffers (measured faster: deeper ring, overlapped epilogue)
-  a.n_iss = a.n_tile <= 32 ? 4 : (a.n_tile <= 64 || a.T < 256 ? 2 : 1);
+  // issuers and accumulator buffers: small N needs several issuers (issue rate); three (each owning
+  // two of the six stages at N = 16) measured faster than four (two owning two, two owning one) or
+  // two. Above 64 columns: with few tokens per work group (T < 256) two issuers with one buffer each
+  // (measured faster), at prefill sizes one issuer with two buffers (deeper ring, overlapped epilogue)
+  a.n_iss = a.n_tile <= 32 ? 3 : (a.n_tile <= 64 || a.T < 256 ? 2 : 1);
   a.n_acc = 1;  // two alternating accumulators measured no faster at any N
   a.n_buf = (a.n_tile <= 64 || a.T >= 256) ? 2 : 1;  // (three, with a stage fewer, measured no faster)
   a.sf_base = (a.n_buf * a.n_iss * a.n_acc * a.acc_cols + 31) / 32 * 32;

@@ -130,6 +130,13 @@ def test_layer_decode_b64_zipf_full_size(k3_decode_b64):
     check_layer(k3_decode_b64, 64, sample=list(range(0, 64, 4)))
 
 
+def test_layer_k3_f32_tokens_many_tiles_sampled():
+    """fp32 tokens at the K3 width stage 4 tokens per router tile: 600 tokens make 150 tiles, each
+    with its own arrival counter; tokens far past the first tiles are checked."""
+    L = DeviceLayer(synth.K3, seed=14, x_dtype="f32")
+    check_layer(L, 600, sample=[0, 259, 420, 599])
+
+
 def test_layer_prefill_4096_sampled():
     L = DeviceLayer(synth.K3, seed=3)
     check_layer(L, 4096, sample=[0, 1, 777, 2048, 4095])
@@ -155,11 +162,11 @@ def test_route_only():
     assert gate_err(idx.cpu().numpy(), wn, idx_ref, w_ref) < 1e-6
 
 
-@pytest.mark.parametrize("T", [512, 700])
-def test_route_tensor_core_router(T):
-    """From 512 bf16 tokens the logits come from the tensor cores (the fp32 router weights in three
-    bf16 parts, fp32 accumulation): same selection (near-tie rule) and gates as the oracle."""
-    L = DeviceLayer(MID, seed=12, zipf_s=1.1)
+@pytest.mark.parametrize("T,x_dtype", [(512, "bf16"), (700, "bf16"), (600, "f32")])
+def test_route_tensor_core_router(T, x_dtype):
+    """From 512 tokens the logits come from the tensor cores (the fp32 router weights, and fp32 tokens,
+    in three bf16 parts; fp32 accumulation): same selection (near-tie rule) and gates as the oracle."""
+    L = DeviceLayer(MID, seed=12, zipf_s=1.1, x_dtype=x_dtype)
     xh, xd = L.tokens(T)
     idx = torch.empty((T, MID.top_k), dtype=torch.int32, device="cuda")
     w = torch.empty((T, MID.top_k), dtype=torch.float32, device="cuda")
