@@ -64,6 +64,7 @@ constexpr int kMaxN = 128;               // largest MMA N (B rows per tile)
 // two scale words per row (8 blocks of 32): A at +0..3 and +16..19, B at +32.. and +48.. (64 columns)
 constexpr int kMaxStages = 16;
 constexpr int kMaxBuf = 4;               // accumulator buffers per issuer
+constexpr int kEpRing = 4;               // work groups the epilogue fetches ahead (cp.async)
 constexpr int kATile = 128 * 128;        // A tile of a chunk in shared memory (both forms)
 constexpr uint32_t kWaitLimit = 1u << 24;
 
@@ -79,6 +80,7 @@ struct Ctl {
   uint32_t tmem;
   volatile int abort;
   int last;
+  alignas(16) WorkGroup ep_wg[4][kEpRing];  // epilogue warp q's copies of the work groups of its next items (cp.async)
 };
 
 // Position in the ring of pipeline stages: slot s, phase parity of its current round, and whether
@@ -472,15 +474,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     long long i = 0;
     int bad = 0;
     int g0 = 0;  // ring slot of the item's first stage
-    Item it, nx, nx2;
-    long long ii = blockIdx.x;
-    bool have = item_at<MODE>(a, ii, n_items, it);
-    bool have_nx = item_at<MODE>(a, ii + gridDim.x, n_items, nx);
-    float wlane = (MODE == DOWN && have && lane < it.wg.ntok) ? __ldg(&a.ws.perm_w[it.wg.pos0 + lane]) : 0.0f;
-    for (; have; ++i) {
-      ii += gridDim.x;
-      const bool have_nx2 = item_at<MODE>(a, ii + gridDim.x, n_items, nx2);  // consumed two iterations later
-      const float wnext = (MODE == DOWN && have_nx && lane < nx.wg.ntok) ? __ldg(&a.ws.perm_w[nx.wg.pos0 + lane]) : 0.0f;
+    Item it;
+    // the work groups of the next kEpRing items arrive by cp.async into this warp's ring, so that
+    // no load sits in the epilogue's path (with the DRAM saturated a plain load waited ~2 us)
+    auto fetch_wg = [&](long long idx, int slot) {
+      if (lane == 0 && idx < n_items) {
+        Item g;
+        item_geom<MODE>(a, idx, n_items, g);
+        cp16(su32(&ctl->ep_wg[q][slot]), &a.ws.wgs[g.wgi]);
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    for (int r = 0; r < kEpRing; ++r) fetch_wg(blockIdx.x + (long long)r * gridDim.x, r);
+    for (long long ii = blockIdx.x; item_geom<MODE>(a, ii, n_items, it); ii += gridDim.x, ++i) {
+      const int slot = (int)(i % kEpRing);
+      asm volatile("cp.async.wait_group %0;" ::"n"(kEpRing - 1) : "memory");
+      __syncwarp();
+      it.wg = ctl->ep_wg[q][slot];
+      __syncwarp();
+      fetch_wg(ii + (long long)kEpRing * gridDim.x, slot);  // reuses the slot just read
       const int nst = (it.j1 - it.j0) / CH;  // stages of the item
       const long long rb = i / a.n_buf;
       const int b = (int)(i - rb * a.n_buf);
@@ -534,8 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (MODE == GATEUP)
                 a.ws.gupart[((pos * c.ks + it.kp) * 2 + it.mat) * c.f + row] = run;
               else
-                a.ws.part[pos * c.d + row] =
-                    run * (tk < 32 ? __shfl_sync(0xffffffffu, wlane, tk & 31) : __ldg(&a.ws.perm_w[pos]));
+                a.ws.part[pos * c.d + row] = run;  // the gate weight is applied by the combine
               run = 0.0f;
               ++tk;
             }
@@ -549,12 +560,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           bad |= (__vcmpeq4(__ldg(reinterpret_cast<const unsigned*>(sg + (size_t)512 * g)), 0xFFFFFFFFu) != 0u);
       }
       g0 = (g0 + nst) % S;
-      have = have_nx;
-      have_nx = have_nx2;
-      it = nx;
-      nx = nx2;
-      wlane = wnext;
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");
     if (bad) atomicOr(&status[CTRL_STATUS], ST_NAN_SCALE);
   }
 
@@ -612,7 +619,7 @@ __global__ void __launch_bounds__(256) k_combine(Cfg c, Ws ws, float* y, long lo
     float s = 0.0f;
     for (int i = 0; i < c.k; ++i) {
       const int p = ws.inv[tok * c.k + i];
-      if (p >= 0) s += ws.part[(long long)p * c.d + row];
+      if (p >= 0) s += ws.perm_w[p] * ws.part[(long long)p * c.d + row];
     }
     for (int sh = 0; sh < c.S; ++sh) s += ws.part[(P_R + (long long)sh * T + tok) * c.d + row];
     y[idx] = s;
