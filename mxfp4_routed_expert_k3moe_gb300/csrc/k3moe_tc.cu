@@ -80,7 +80,9 @@ struct Ctl {
   uint32_t tmem;
   volatile int abort;
   int last;
-  alignas(16) WorkGroup ep_wg[4][kEpRing];  // epilogue warp q's copies of the work groups of its next items (cp.async)
+  alignas(16) WorkGroup ep_wg[4][kEpRing];
+  alignas(16) WorkGroup ld_wg[kLoaders][kEpRing];  // loader v's copies of its next items' work groups
+  int ld_tok[kLoaders][kEpRing][32];               // ... and the tokens of their positions (gate/up)  // epilogue warp q's copies of the work groups of its next items (cp.async)
 };
 
 // Position in the ring of pipeline stages: slot s, phase parity of its current round, and whether
@@ -248,27 +250,6 @@ __device__ __forceinline__ bool b_row(const TcArgs& a, const Item& it, int n, co
   return true;
 }
 
-// What a loader reads ahead for one item: its work group and, for the B rows n = lane + 32 q, the
-// activation row they come from (the token for gate/up, the position for down; -1 past the work
-// group's tokens). The loads are only consumed an item later.
-struct LoadPlan {
-  Item it;
-  int bsrc[kMaxN / 32];
-};
-
-template <int MODE>
-__device__ __forceinline__ void make_plan(const TcArgs& a, const Item& it, int lane, LoadPlan& p) {
-  p.it = it;
-#pragma unroll
-  for (int q = 0; q < kMaxN / 32; ++q) {
-    const int n = lane + 32 * q;
-    const int i = n / a.terms;
-    p.bsrc[q] = -1;
-    if (n < a.n_tile && i < it.wg.ntok)
-      p.bsrc[q] = MODE == GATEUP ? __ldg(&a.ws.perm_tok[it.wg.pos0 + i]) : it.wg.pos0 + i;
-  }
-}
-
 // ------------------------------------------------------------------------------- the kernel
 // Shared memory of a stage: [A tiles: ch x 16 KB][B tiles: ch x b_bytes][scale words: ch x 1 KB].
 // Scale words of a chunk: 512 bytes for the 128 weight rows, then 512 for the B rows; the word of
@@ -322,25 +303,57 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp >= kWarpLoad && warp < kWarpIss) {
     // ------------------------------------------------------------ loaders (one per slot class)
-    // The item two ahead has its work group read, the next one its B-row addresses resolved, so
-    // that neither dependent load sits in front of the next item's first copy.
+    // Work groups (kEpRing items ahead) and the tokens of their positions (two items ahead) arrive by
+    // cp.async into this loader's ring, so that no load stalls the loader between items (with the
+    // DRAM saturated by the weight stream a dependent load waits microseconds).
     const int lv = warp - kWarpLoad;
     const uint64_t pol = policy_evict_first();
     Ring rg;
     bool ok = true;
-    LoadPlan cur, nxt;
-    Item it2;
-    long long ii = blockIdx.x;
-    bool has_nxt = item_at<MODE>(a, ii, n_items, it2);
-    if (has_nxt) make_plan<MODE>(a, it2, lane, nxt);
-    bool has_it2 = item_at<MODE>(a, ii + gridDim.x, n_items, it2);
-    while (ok && has_nxt) {
-      cur = nxt;
-      has_nxt = has_it2;
-      if (has_nxt) make_plan<MODE>(a, it2, lane, nxt);
-      ii += gridDim.x;
-      has_it2 = item_at<MODE>(a, ii + gridDim.x, n_items, it2);
-      const Item& it = cur.it;
+    WorkGroup* rwg = ctl->ld_wg[lv];
+    auto fetch_wg = [&](long long idx, int slot) {  // the work group of item idx, if any
+      if (lane == 0 && idx < n_items) {
+        Item g;
+        item_geom<MODE>(a, idx, n_items, g);
+        cp16(su32(&rwg[slot]), &a.ws.wgs[g.wgi]);
+      }
+    };
+    auto fetch_tok = [&](long long idx, int slot) {  // tokens of item idx's positions (its work group is in `slot`)
+      if (MODE == GATEUP && idx < n_items) {
+        const WorkGroup g = rwg[slot];
+        if (lane < g.ntok && lane < 32) cp4(su32(&ctl->ld_tok[lv][slot][lane]), &a.ws.perm_tok[g.pos0 + lane], 4);
+      }
+    };
+    // prologue: work groups of the first kEpRing items and tokens of the first two, waited for here
+    for (int r = 0; r < kEpRing; ++r) fetch_wg(blockIdx.x + (long long)r * gridDim.x, r);
+    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+    __syncwarp();
+    fetch_tok(blockIdx.x, 0);
+    fetch_tok(blockIdx.x + (long long)gridDim.x, 1);
+    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+    __syncwarp();
+    Item it;
+    long long kk = 0;
+    for (long long ii = blockIdx.x; ok && item_geom<MODE>(a, ii, n_items, it); ii += gridDim.x, ++kk) {
+      const int slot = (int)(kk % kEpRing);
+      // the group committed two items ago holds this item's tokens and the work group two ahead
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+      __syncwarp();
+      it.wg = rwg[slot];
+      int bsrc[kMaxN / 32];
+#pragma unroll
+      for (int q = 0; q < kMaxN / 32; ++q) {
+        const int n = lane + 32 * q;
+        const int i = n / a.terms;
+        bsrc[q] = -1;
+        if (n < a.n_tile && i < it.wg.ntok)
+          bsrc[q] = MODE == GATEUP ? ctl->ld_tok[lv][slot][i] : it.wg.pos0 + i;
+      }
+      __syncwarp();
+      // refill: the work group kEpRing ahead into this slot, the tokens of the item two ahead
+      fetch_wg(ii + (long long)kEpRing * gridDim.x, slot);
+      fetch_tok(ii + 2LL * gridDim.x, (int)((kk + 2) % kEpRing));
+      asm volatile("cp.async.commit_group;" ::: "memory");
       const bool routed = it.wg.expert < c.E;
       const CUtensorMap* map = routed ? (it.mat == 0 ? &map_r0 : &map_r1) : (it.mat == 0 ? &map_s0 : &map_s1);
       const int ecoord = routed ? it.wg.expert : it.wg.expert - c.E;
@@ -351,9 +364,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int q = 0; q < kMaxN / 32; ++q) {
         bcodes[q] = nullptr;
         bscales[q] = nullptr;
-        if (cur.bsrc[q] >= 0) {
+        if (bsrc[q] >= 0) {
           const int n = lane + 32 * q;
-          const long long r = (long long)cur.bsrc[q] * a.terms + (n - (n / a.terms) * a.terms);
+          const long long r = (long long)bsrc[q] * a.terms + (n - (n / a.terms) * a.terms);
           const int kk = MODE == GATEUP ? c.d : c.f;
           bcodes[q] = (MODE == GATEUP ? a.ws.xq : a.ws.hq) + r * (a.fp4 ? kk / 2 : kk);
           bscales[q] = (MODE == GATEUP ? a.ws.xs : a.ws.hs) + r * ((MODE == GATEUP ? c.d : c.f) / 32);
