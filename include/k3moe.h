@@ -18,8 +18,8 @@
  *   [down codes d x f/2][down scales d x f/32]
  * Codes are row-major, two per byte, the even column in the low nibble. A record of the
  * d_model 7168 / d_ff 1536 shape is 17,547,264 bytes (the census figure). This is the stored
- * order; the compute calls read records whose scale bytes were put in the device order by
- * k3moe_pack_records (see there), once, when the records are loaded onto the GPU.
+ * order; the compute calls read records put in the device order by k3moe_pack_records (see
+ * there), once, when the records are loaded onto the GPU.
  *
  * Conventions shared by every call below:
  *  - Pointers are DEVICE pointers unless marked "host". The caller owns all memory; nothing is
@@ -90,14 +90,20 @@ typedef struct {
 } k3moe_config;
 
 /*
- * Scale order of device-resident records. The block-scaled MMA of the tensor cores reads the E8M0
- * scales of 128 weight rows x 4 blocks as one 32 x 16-byte image (lane i of each 32-row quarter c
- * holds the 4 scale bytes of row 32 c + i). In the device order every 128-row tile of a matrix
- * (rows 128 t .. 128 t + 127, whose scale bytes are one contiguous range in either order) stores
- * the byte of tile row r = 32 c + i and block b = 4 g + e at
- *     tile_start + 512 g + 16 i + 4 c + e,
- * so that the scales of one chunk of the reduction axis are a single contiguous copy. Codes are
- * unchanged. The record size and all offsets of the stored order are unchanged.
+ * Device order of records. The block-scaled MMA of the tensor cores reads the E8M0 scales of 128
+ * weight rows x 4 blocks as one 32 x 16-byte image (lane i of each 32-row quarter c holds the 4
+ * scale bytes of row 32 c + i), and the gate/up kernel finishes h = SiLU(g) * u in its epilogue,
+ * which needs the gate and up rows of the same h indices in one 128-row tile. In the device order:
+ *  - gate/up: for u = 0 .. d_ff/128 - 1 and half h = 0, 1, the stacked tile 2u + h consists of gate
+ *    rows 128u + 64h .. 128u + 64h + 63 (its rows 0-63) and up rows 128u + 64h .. +63 (rows
+ *    64-127); stacked tile 2u takes the place of gate rows 128u .. 128u + 127 and stacked tile 2u + 1
+ *    that of up rows 128u .. 128u + 127, for the codes and for the scale bytes. (For the codes this
+ *    swaps gate rows 128u + 64 .. 128u + 127 with up rows 128u .. 128u + 63.)
+ *  - down: codes unchanged.
+ *  - every 128-row tile (stacked, or of the down matrix) stores its scale bytes as its image: the
+ *    byte of tile row r = 32 c + i and block b = 4 g + e at tile_start + 512 g + 16 i + 4 c + e,
+ *    so that the scales of one chunk of the reduction axis are a single contiguous copy.
+ * The record size and the offsets of the six regions are those of the stored order.
  * k3moe_pack_records converts `n_records` records (record_stride bytes apart, 16-byte aligned
  * base) in place: to_device = 1 stored -> device order, 0 device -> stored order. Only d_model,
  * d_ff and record_stride of `cfg` are used (any valid config of that geometry). Asynchronous on
@@ -133,8 +139,8 @@ K3MOE_API k3moe_status k3moe_route(const k3moe_config* cfg /* host */, const voi
  *   topk_idx       [T, top_k] int32 expert ids in [0, n_routed) (checked on the device)
  *   topk_w         [T, top_k] fp32 gate weights
  *   routed_records n_routed records, record_stride bytes apart (16-byte aligned base), in the
- *                  device scale order (k3moe_pack_records)
- *   shared_records n_shared records, record_stride bytes apart, device scale order (may be NULL
+ *                  device order (k3moe_pack_records)
+ *   shared_records n_shared records, record_stride bytes apart, device order (may be NULL
  *                  if n_shared == 0)
  *   y              [T, d_model] fp32 out, overwritten
  */
@@ -154,8 +160,9 @@ K3MOE_API k3moe_status k3moe_layer(const k3moe_config* cfg /* host */, const voi
 
 /*
  * k3moe_layer with phase timing, for profiling: `events` points to 6 cudaEvent_t handles created by
- * the caller; they are recorded on `stream` before the router kernel, before the gate/up kernel,
- * before the GLU kernel, before the down-projection kernel, before the combine kernel and after it.
+ * the caller; they are recorded on `stream` before the router kernel, before the gate/up kernel
+ * (which also finishes h), twice after it (once where a separate GLU kernel would end), before the
+ * combine kernel and after it.
  * Same kernels and results as k3moe_layer (an event between two kernels only removes their overlap).
  */
 K3MOE_API k3moe_status k3moe_layer_timed(const k3moe_config* cfg /* host */, const void* x, int64_t T,

@@ -150,8 +150,8 @@ def layer_static(cfg, x, T, w_router, bias, routed, shared, y, stream=None):
 
 
 def pack_records(cfg, records, n_records, to_device=True, stream=None):
-    """k3moe_pack_records: put the scale bytes of n records (in place) into the device order that the
-    compute calls read (to_device=True), or back into the stored order."""
+    """k3moe_pack_records: put n records (in place) into the device order that the compute calls
+    read (to_device=True), or back into the stored order."""
     _check(load().k3moe_pack_records(ctypes.byref(cfg), _ptr(records), n_records, 1 if to_device else 0,
                                      _stream(stream)), "k3moe_pack_records")
 

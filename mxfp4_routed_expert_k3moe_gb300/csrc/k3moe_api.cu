@@ -15,16 +15,6 @@ constexpr long long kMaxE = 4096;
 constexpr long long kMaxK = 32;
 constexpr long long kMaxS = 8;
 constexpr int kMaxDModel = 25600;
-// Reduction parts of the gate/up projection (summed by the GLU kernel). At decode, splitting each
-// (work group, row tile) item along d into 2, 3, 4, 7 or 14 parts, to spread the few items over the
-// SMs more evenly, measured slower than whole items (per-item costs outweigh the balance: 52 us
-// for 1 part, 60 us for 4, 116 us for 14 at one token), so one part is used.
-long long gateup_parts(long long T, long long d, bool fp4) {
-  (void)T;
-  (void)d;
-  (void)fp4;
-  return 1;
-}
 constexpr long long kMaxTerms = 3;     // E4M3 terms per activation block (x: 2 bf16 / 3 fp32; h: 3)
 constexpr long long kMaxTermsFp4 = 8;  // E2M1 terms per activation block
 constexpr long long kFp4MaxT = 2;      // the E2M1 / mxf4 path serves up to this many tokens
@@ -77,7 +67,7 @@ long long wg_bound(const k3moe_config* c, long long T) {
 
 struct Layout {
   size_t ctrl, logits, topk_idx, topk_w, counts, cursor, offsets, wgoff, perm_tok, perm_w, inv, wgs, xq, xs, hq, hs,
-      part, gupart, rtcnt, w3, x3, total;
+      part, rtcnt, w3, x3, total;
 };
 
 Layout make_layout(const k3moe_config* c, long long T) {
@@ -108,7 +98,6 @@ Layout make_layout(const k3moe_config* c, long long T) {
   take(L.hq, (size_t)(P * terms * (fp4 ? f / 2 : f)));
   take(L.hs, (size_t)(P * terms * (f / 32)));
   take(L.part, sizeof(float) * P * d);
-  take(L.gupart, sizeof(float) * P * gateup_parts(T, d, fp4) * 2 * f);
   take(L.rtcnt, sizeof(int) * T);  // one counter per router token tile (tiles of 1 to 8 tokens)
   take(L.w3, router_tc(c, T) ? (size_t)3 * E * d * 2 : 0);  // bf16 parts of the router weights
   take(L.x3, router_tc(c, T) && c->x_dtype == K3MOE_X_F32 ? (size_t)3 * T * d * 2 : 0);  // ... of fp32 tokens
@@ -136,7 +125,6 @@ Ws bind(const Layout& L, void* base) {
   w.hq = reinterpret_cast<uint8_t*>(b + L.hq);
   w.hs = reinterpret_cast<uint8_t*>(b + L.hs);
   w.part = reinterpret_cast<float*>(b + L.part);
-  w.gupart = reinterpret_cast<float*>(b + L.gupart);
   w.rtcnt = reinterpret_cast<int*>(b + L.rtcnt);
   return w;
 }
@@ -154,7 +142,6 @@ Cfg make_cfg(const k3moe_config* c, long long T) {
   // slower: the projections there are not bound by the record reads)
   const long long wmax = k.fp4 ? 16 : 32;
   k.wgt = (int)(T < wmax ? T : wmax);
-  k.ks = (int)gateup_parts(T, c->d_model, k.fp4 != 0);
   if (k.fp4) {
     k.xterms = 8;  // at most 2^-23 of the block maximum per element
     k.hterms = 8;
@@ -186,15 +173,11 @@ size_t k3moe_record_bytes(const k3moe_config* cfg) {
 
 size_t k3moe_workspace_bytes(const k3moe_config* cfg, int64_t max_tokens) {
   if (validate(cfg) != K3MOE_OK || !tokens_ok(cfg, max_tokens)) return 0;
-  // the layout grows with T except where the gate/up split drops from 4 parts to 1 (above 4 tokens)
-  // and where the E2M1 activation form gives way to the E4M3 one (above kFp4MaxT tokens)
+  // the layout grows with T except, possibly, where the E2M1 activation form gives way to the E4M3
+  // one (above kFp4MaxT tokens)
   const long long T = max_tokens < 1 ? 1 : max_tokens;
-  size_t best = make_layout(cfg, T).total;
-  for (long long t : {4LL, kFp4MaxT}) {
-    const size_t b = make_layout(cfg, T < t ? T : t).total;
-    best = b > best ? b : best;
-  }
-  return best;
+  const size_t a = make_layout(cfg, T).total, b = make_layout(cfg, T < kFp4MaxT ? T : kFp4MaxT).total;
+  return a > b ? a : b;
 }
 
 k3moe_status k3moe_route(const k3moe_config* cfg, const void* x, int64_t T, const float* w_router, const float* bias,
@@ -316,7 +299,7 @@ k3moe_status k3moe_pack_records(const k3moe_config* cfg, uint8_t* records, int64
   if (!records || !aligned16(records) || n_records < 0 || (to_device != 0 && to_device != 1))
     return K3MOE_ERR_INVALID_ARGUMENT;
   if (n_records == 0) return K3MOE_OK;
-  return cuda_status(k3::launch_pack_scales(records, n_records, cfg->record_stride, cfg->d_model, cfg->d_ff, to_device,
+  return cuda_status(k3::launch_pack_records(records, n_records, cfg->record_stride, cfg->d_model, cfg->d_ff, to_device,
                                             static_cast<cudaStream_t>(stream)));
 }
 

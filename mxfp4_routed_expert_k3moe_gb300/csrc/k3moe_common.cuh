@@ -12,7 +12,6 @@ struct Cfg {
   int d, f, E, k, S;  // d_model, d_ff, routed experts, top-k, shared experts
   int x_f32;          // 1 if x is fp32, 0 if bf16
   int wgt;            // max tokens per work group
-  int ks;             // reduction parts of gate/up (allocated in the workspace)
   int fp4;           // 1: activations as E2M1 terms and kind::mxf4 MMAs (few tokens); 0: E4M3 terms, mxf8f6f4
   int xterms;         // terms per activation block of x (E4M3: 2 for bf16 x, 3 for fp32 x; E2M1: 8 or 16)
   int hterms;         // terms per block of h
@@ -52,8 +51,7 @@ struct Ws {
   uint8_t* xs;        // [T * xterms, d/32] their E8M0 block scales
   uint8_t* hq;        // [P * hterms, f] E4M3 (or [.., f/2] packed E2M1) terms of h (row p*hterms + j)
   uint8_t* hs;        // [P * hterms, f/32] their E8M0 block scales
-  float* part;        // [P, d] gate-weighted down-projection outputs per position
-  float* gupart;      // [P, ks, 2, f] partial gate/up sums of the reduction parts
+  float* part;        // [P, d] down-projection outputs per position (the combine weights them)
   int* rtcnt;         // [T] router CTAs finished per token tile (tiles of 1 to 8 tokens)
 };
 

@@ -48,7 +48,7 @@ cudaError_t launch_down(const Cfg& c, const Ws& ws, const uint8_t* routed, const
                         long long T, long long wg_max, cudaStream_t st, cudaEvent_t mid = nullptr);
 
 // In-place conversion of the records' scale bytes between the stored and the device order.
-cudaError_t launch_pack_scales(uint8_t* records, long long n_rec, long long stride, int d, int f, int to_device,
+cudaError_t launch_pack_records(uint8_t* records, long long n_rec, long long stride, int d, int f, int to_device,
                                cudaStream_t st);
 
 }  // namespace k3

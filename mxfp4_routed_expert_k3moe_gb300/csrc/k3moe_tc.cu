@@ -1,6 +1,6 @@
 // Expert FFN of the MXFP4 MoE layer on the 5th-generation tensor cores (tcgen05, sm_103a):
-//   gate/up:  g = W_gate x, u = W_up x                  (k_tc<GATEUP>, partial sums per reduction part)
-//             h = SiLU(g) * u and its E4M3 terms          (k_glu)
+//   gate/up:  g = W_gate x, u = W_up x                  (k_tc<GATEUP>)
+//             h = SiLU(g) * u and its terms               (the same kernel's epilogue)
 //   down:     o_p = w_p W_down h_p                       (k_tc<DOWN>, one row per position p)
 //             y[t] = sum_i o_(t,i) + sum_s o_(t,s)        (k_combine)
 // The MXFP4 records are consumed as stored (kimi-k3-in-c review, table "KDA·MLA·MoE": the
@@ -82,8 +82,11 @@ struct Ctl {
   int last;
   alignas(16) WorkGroup ep_wg[4][kEpRing];
   alignas(16) WorkGroup ld_wg[kLoaders][kEpRing];  // loader v's copies of its next items' work groups
-  int ld_tok[kLoaders][kEpRing][32];               // ... and the tokens of their positions (gate/up)  // epilogue warp q's copies of the work groups of its next items (cp.async)
+  int ld_tok[kLoaders][kEpRing][32];               // ... and the tokens of their positions (gate/up)
+  uint32_t ld_row[kLoaders][kMaxN];                // B row n of loader v's current item: activation row, or ~0
 };
+// Gate/up exchange area after the control block: float [4 epilogue warps][xb_tok tokens][32 lanes].
+__host__ __device__ constexpr size_t ctl_bytes() { return (sizeof(Ctl) + 15) / 16 * 16; }
 
 // Position in the ring of pipeline stages: slot s, phase parity of its current round, and whether
 // the ring has wrapped at least once.
@@ -155,8 +158,9 @@ struct TcArgs {
   int sf_slot;  // TMEM columns of the scales of a chunk
   int sf_bytes; // shared-memory bytes of the scale words of a chunk
   int terms;    // B rows per token in this kernel (x terms for gate/up, h terms for down)
-  int hterms;   // h terms written by the gate/up finish
-  int parts;    // reduction parts per gate/up row tile
+  int hterms;   // h terms written by the gate/up epilogue
+  int xb_tok;   // tokens per item in the gate/up exchange area (0 for the down projection)
+  int parts;    // reduction parts per row tile (1: whole items)
   FastDiv div_parts, div_mtiles;
   int stages;   // pipeline depth (<= kMaxStages)
   int stage_bytes;  // ch x (A tile + B tile + scale words)
@@ -358,20 +362,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       const CUtensorMap* map = routed ? (it.mat == 0 ? &map_r0 : &map_r1) : (it.mat == 0 ? &map_s0 : &map_s1);
       const int ecoord = routed ? it.wg.expert : it.wg.expert - c.E;
       const uint8_t* atile = scale_tile<MODE>(a, it);
-      const uint8_t* bcodes[kMaxN / 32];
+      // B row n of the tile = activation row (token or position) * terms + term; the rows' indices go
+      // to this loader's table, which the code copies below read, and the scale pointers of rows
+      // lane + 32 q stay in registers
+      const int kk = MODE == GATEUP ? c.d : c.f;
+      const long long row_bytes = a.fp4 ? kk / 2 : kk;
+      const uint8_t* bbase = MODE == GATEUP ? a.ws.xq : a.ws.hq;
+      uint32_t* rtab = ctl->ld_row[lv];
+      const int nrows = min(a.n_tile, it.wg.ntok * a.terms);  // rows past these are not read
       const uint8_t* bscales[kMaxN / 32];
 #pragma unroll
       for (int q = 0; q < kMaxN / 32; ++q) {
-        bcodes[q] = nullptr;
         bscales[q] = nullptr;
+        const int n = lane + 32 * q;
+        uint32_t r = ~0u;  // (rows < 3 * 2^30: positions < 2^30, at most 3 terms above 2 tokens)
         if (bsrc[q] >= 0) {
-          const int n = lane + 32 * q;
-          const long long r = (long long)bsrc[q] * a.terms + (n - (n / a.terms) * a.terms);
-          const int kk = MODE == GATEUP ? c.d : c.f;
-          bcodes[q] = (MODE == GATEUP ? a.ws.xq : a.ws.hq) + r * (a.fp4 ? kk / 2 : kk);
-          bscales[q] = (MODE == GATEUP ? a.ws.xs : a.ws.hs) + r * ((MODE == GATEUP ? c.d : c.f) / 32);
+          r = (uint32_t)bsrc[q] * (uint32_t)a.terms + (uint32_t)(n - (n / a.terms) * a.terms);
+          bscales[q] = (MODE == GATEUP ? a.ws.xs : a.ws.hs) + (long long)r * (kk / 32);
         }
+        if (n < a.n_tile) rtab[n] = r;
       }
+      __syncwarp();
       for (int j = it.j0; j < it.j1; j += CH, rg.next(S)) {
         const int s = rg.s;
         if (s % kLoaders != lv) continue;
@@ -391,17 +402,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int jj = j + cc;
           const uint32_t sb = su32(st + b_off + cc * a.b_bytes), sc = su32(st + sf_off + cc * a.sf_bytes);
           // scale words: A word h at sc + 512 h (bulk copy above), B word h at sc + 512 (wpc + h)
+          // codes: lane = 16-byte segment k16 of row 4 it + lane / 8, so that one copy instruction
+          // reads four 128-byte rows (one row per lane read 32 rows: a quarter of the L1 rate)
+          // (four rows per lane at a time: their table reads are issued before the copies)
+          const int k16 = lane & 7;
+          for (int n0 = lane >> 3; n0 < nrows; n0 += 16) {
+            uint32_t r[4];
 #pragma unroll
-          for (int q = 0; q < kMaxN / 32; ++q) {
-            if (bcodes[q]) {
-              const int n = lane + 32 * q;
-              const uint8_t* src = bcodes[q] + (long long)jj * 128;
+            for (int u = 0; u < 4; ++u) r[u] = n0 + 4 * u < nrows ? rtab[n0 + 4 * u] : ~0u;
 #pragma unroll
-              for (int k16 = 0; k16 < 8; ++k16) cp16(sb + n * 128 + ((k16 ^ (n & 7)) << 4), src + k16 * 16);
-              for (int h = 0; h < wpc; ++h)
-                cp4(sc + 512 * (wpc + h) + 16 * lane + 4 * q, bscales[q] + 4 * (wpc * jj + h), 4);
+            for (int u = 0; u < 4; ++u) {
+              const int n = n0 + 4 * u;
+              if (r[u] != ~0u)
+                cp16(sb + n * 128 + ((k16 ^ (n & 7)) << 4), bbase + (long long)r[u] * row_bytes + jj * 128 + k16 * 16);
             }
           }
+#pragma unroll
+          for (int q = 0; q < kMaxN / 32; ++q)
+            if (bscales[q])
+              for (int h = 0; h < wpc; ++h)
+                cp4(sc + 512 * (wpc + h) + 16 * lane + 4 * q, bscales[q] + 4 * (wpc * jj + h), 4);
         }
         cp_arrive_noinc(su32(&ctl->full[s]));
       }
@@ -484,6 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // current one is waited for: while the weight stream saturates the DRAM, a read that misses L2
     // waits microseconds.
     const int q = warp;
+    float* xb = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ctl) + ctl_bytes());  // gate/up exchange
     long long i = 0;
     int bad = 0;
     int g0 = 0;  // ring slot of the item's first stage
@@ -509,7 +530,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nst = (it.j1 - it.j0) / CH;  // stages of the item
       const long long rb = i / a.n_buf;
       const int b = (int)(i - rb * a.n_buf);
-      if (!__all_sync(0xffffffffu, wait_bar(su32(&ctl->acc_full[b]), (uint32_t)(rb & 1), ctl, status))) break;
+      bool okw = __all_sync(0xffffffffu, wait_bar(su32(&ctl->acc_full[b]), (uint32_t)(rb & 1), ctl, status));
+      // gate/up: the four warps agree (they meet at a barrier below); this also keeps the exchange
+      // area of the previous item until every warp has read it
+      if (MODE == GATEUP) okw = bar_and(1, 128, okw);
+      if (!okw) break;
       tc_fence_after();
       const int row = it.mt * 128 + 32 * q + lane;
       const int ncols = it.wg.ntok * a.terms;
@@ -557,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const long long pos = it.wg.pos0 + tk;
               nan_row |= (run != run);
               if (MODE == GATEUP)
-                a.ws.gupart[((pos * c.ks + it.kp) * 2 + it.mat) * c.f + row] = run;
+                xb[(q * a.xb_tok + tk) * 32 + lane] = run;
               else
                 a.ws.part[pos * c.d + row] = run;  // the gate weight is applied by the combine
               run = 0.0f;
@@ -571,6 +596,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint8_t* sg = scale_tile<MODE>(a, it) + 16 * lane + 4 * q;  // row 32 q + lane of the tile
         for (int g = it.j0 * wpc; g < it.j1 * wpc; ++g)
           bad |= (__vcmpeq4(__ldg(reinterpret_cast<const unsigned*>(sg + (size_t)512 * g)), 0xFFFFFFFFu) != 0u);
+      }
+      if (MODE == GATEUP) {
+        // The stacked tile's rows 0-63 are gate rows and 64-127 the up rows of the same 64 rows of h
+        // (k3moe_pack_records): warp q and warp q ^ 2 hold g and u of h rows 32 (q & 1) + lane of
+        // them. After the exchange, warps 0-1 finish the even tokens of the item, warps 2-3 the odd.
+        bar_sync(1, 128);
+        const int p = q & 1;
+        const int nb = c.f / 32, blk = 4 * it.mt + 2 * it.mat + p;  // 32-block of h
+        for (int i = q >> 1; i < it.wg.ntok; i += 2) {
+          const float g = xb[(p * a.xb_tok + i) * 32 + lane], u = xb[((p + 2) * a.xb_tok + i) * 32 + lane];
+          const float h = silu(g) * u;
+          const long long pos = it.wg.pos0 + i;
+          if (c.fp4)
+            split_terms_fp4(h, c.hterms, a.ws.hq + (pos * c.hterms) * (c.f / 2) + blk * 16, c.f / 2,
+                            a.ws.hs + (pos * c.hterms) * nb + blk, nb, lane);
+          else
+            split_terms(h, c.hterms, a.ws.hq + (pos * c.hterms) * c.f + blk * 32 + lane, c.f,
+                        a.ws.hs + (pos * c.hterms) * nb + blk, nb, lane);
+        }
       }
       g0 = (g0 + nst) % S;
     }
@@ -586,39 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// ------------------------------------------------------------------------------- GLU and combine
-// h = SiLU(g) * u per position and 32-row block of d_ff, the gate/up reduction parts summed in a fixed
-// order, written as E4M3 terms (one warp per (position, block); routed positions past the routed
-// count are skipped).
-__global__ void __launch_bounds__(256) k_glu(Cfg c, Ws ws, long long T) {
-  pdl_wait();
-  pdl_launch_dependents();
-  const int lane = threadIdx.x & 31;
-  const long long P_R = T * c.k, P = P_R + (long long)c.S * T;
-  const int nb = c.f / 32;
-  const long long n_routed_pos = ws.ctrl[CTRL_NPOS];
-  for (long long wi = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; wi < P * nb;
-       wi += ((long long)gridDim.x * blockDim.x) >> 5) {
-    const long long pos = wi / nb;
-    const int blk = (int)(wi - pos * nb);
-    if (pos < P_R && pos >= n_routed_pos) continue;
-    const int row = blk * 32 + lane;
-    const float* src = ws.gupart + pos * c.ks * 2 * c.f;
-    float g = 0.0f, u = 0.0f;
-    for (int kp = 0; kp < c.ks; ++kp) {
-      g += src[((long long)kp * 2 + 0) * c.f + row];
-      u += src[((long long)kp * 2 + 1) * c.f + row];
-    }
-    const float h = silu(g) * u;
-    if (c.fp4)
-      split_terms_fp4(h, c.hterms, ws.hq + (pos * c.hterms) * (c.f / 2) + blk * 16, c.f / 2,
-                      ws.hs + (pos * c.hterms) * nb + blk, nb, lane);
-    else
-      split_terms(h, c.hterms, ws.hq + (pos * c.hterms) * c.f + row, c.f, ws.hs + (pos * c.hterms) * nb + blk, nb,
-                  lane);
-  }
-}
-
+// ------------------------------------------------------------------------------- combine
 // y[t] = sum over the top-k slots of t (in slot order) of the gate-weighted expert outputs, then the
 // shared experts; one thread per (token, row of d_model).
 __global__ void __launch_bounds__(256) k_combine(Cfg c, Ws ws, float* y, long long T) {
@@ -639,40 +651,83 @@ __global__ void __launch_bounds__(256) k_combine(Cfg c, Ws ws, float* y, long lo
   }
 }
 
-// ------------------------------------------------------------------------------- scale order
-// Converts the E8M0 scale bytes of whole records between the stored order ([rows][K/32] per matrix)
-// and the device order read by k_tc (scale_tile). Both orders keep each 128-row tile of a matrix in
-// the same contiguous byte range, so one CTA per tile stages the range in shared memory and writes
-// it back permuted, in place.
-__global__ void __launch_bounds__(256) k_pack_scales(uint8_t* records, long long n_rec, long long stride, int d, int f,
-                                                      int to_device) {
+// ------------------------------------------------------------------------------- device order
+// Byte of row r (of 128) and 32-block b inside the scale image of one 128-row tile (k3moe.h): the
+// 512-byte group of blocks 4g..4g+3 holds, at 16 i + 4 c + e, row 32 c + i and block 4 g + e.
+__device__ __forceinline__ int img_at(int r, int b) { return 512 * (b >> 2) + 16 * (r & 31) + 4 * (r >> 5) + (b & 3); }
+
+// Converts whole records between the stored order and the device order read by k_tc. One CTA per
+// unit, in place:
+//   gate/up pair u (gate rows 128u..128u+127 and up rows 128u..128u+127): the codes of gate rows
+//     128u+64.. and up rows 128u.. swap places (64 rows each; the swap is its own inverse), and the
+//     scale bytes of both tiles, staged in shared memory, are written as the images of the stacked
+//     tiles 2u (gate rows 128u.., then up rows 128u..) and 2u+1 (gate rows 128u+64.., up rows
+//     128u+64..) into the ranges of gate tile u and up tile u (or back);
+//   down tile t: its scale bytes are written as the tile's image (or back).
+__global__ void __launch_bounds__(256) k_pack_records(uint8_t* records, long long n_rec, long long stride, int d,
+                                                       int f, int to_device) {
   extern __shared__ __align__(16) uint8_t sbuf[];
-  const int tiles_gu = f / 128, tiles_dn = d / 128;
-  const long long per_rec = 2LL * tiles_gu + tiles_dn;
+  const int pairs = f / 128, tiles_dn = d / 128;
+  const long long per_rec = (long long)pairs + tiles_dn;
   const long long nc = (long long)d * f / 2, ns = (long long)d * f / 32;
-  for (long long u = blockIdx.x; u < n_rec * per_rec; u += gridDim.x) {
-    const long long r = u / per_rec;
-    int t = (int)(u - r * per_rec), m = 0, K = d;
-    if (t >= 2 * tiles_gu) { m = 2; t -= 2 * tiles_gu; K = f; }
-    else if (t >= tiles_gu) { m = 1; t -= tiles_gu; }
-    const int nb = K / 32;  // blocks per row, a multiple of 4
-    uint8_t* base = records + r * stride + m * (nc + ns) + nc + (long long)t * 128 * nb;
-    const int n = 128 * nb;
-    for (int o = threadIdx.x * 16; o < n; o += blockDim.x * 16)
-      *reinterpret_cast<uint4*>(sbuf + o) = *reinterpret_cast<const uint4*>(base + o);
-    __syncthreads();
-    for (int o = threadIdx.x; o < n; o += blockDim.x) {
-      int src;
-      if (to_device) {  // o = 512 g + 16 i + 4 c + e holds row 32 c + i, block 4 g + e
-        const int g = o >> 9, i = (o >> 4) & 31, c = (o >> 2) & 3, e = o & 3;
-        src = (32 * c + i) * nb + 4 * g + e;
-      } else {  // o = row * nb + block
-        const int row = o / nb, b = o - row * nb;
-        src = 512 * (b >> 2) + 16 * (row & 31) + 4 * (row >> 5) + (b & 3);
+  for (long long unit = blockIdx.x; unit < n_rec * per_rec; unit += gridDim.x) {
+    const long long rr = unit / per_rec;
+    const int t = (int)(unit - rr * per_rec);
+    uint8_t* rec = records + rr * stride;
+    if (t < pairs) {
+      const int nb = d / 32;  // blocks per row, a multiple of 4
+      const int n = 128 * nb;
+      uint8_t* gs = rec + nc + (long long)t * n;            // gate tile t's scale range
+      uint8_t* us = rec + 2 * nc + ns + (long long)t * n;   // up tile t's scale range
+      uint8_t* gc = rec + ((long long)t * 128 + 64) * (d / 2);     // gate rows 128t+64.. (codes)
+      uint8_t* uc = rec + nc + ns + (long long)t * 128 * (d / 2);  // up rows 128t..
+      for (int o = threadIdx.x * 16; o < 64 * (d / 2); o += blockDim.x * 16) {
+        const uint4 x = *reinterpret_cast<const uint4*>(gc + o), y = *reinterpret_cast<const uint4*>(uc + o);
+        *reinterpret_cast<uint4*>(gc + o) = y;
+        *reinterpret_cast<uint4*>(uc + o) = x;
       }
-      base[o] = sbuf[src];
+      for (int o = threadIdx.x * 16; o < n; o += blockDim.x * 16) {
+        *reinterpret_cast<uint4*>(sbuf + o) = *reinterpret_cast<const uint4*>(gs + o);
+        *reinterpret_cast<uint4*>(sbuf + n + o) = *reinterpret_cast<const uint4*>(us + o);
+      }
+      __syncthreads();
+      for (int o = threadIdx.x; o < 2 * n; o += blockDim.x) {
+        const int h = o >= n, oo = o - h * n;  // destination: gate range (h 0) or up range (h 1)
+        int src;
+        if (to_device) {  // oo is byte img_at(r, b) of stacked tile 2t + h
+          const int g = oo >> 9, i = (oo >> 4) & 31, c = (oo >> 2) & 3, e = oo & 3;
+          const int r = 32 * c + i, b = 4 * g + e;
+          const int row = 64 * h + (r & 63);   // row of the gate (r < 64) or up tile
+          src = (r < 64 ? 0 : n) + row * nb + b;
+        } else {  // oo = row * nb + b of the gate (h 0) or up (h 1) tile t
+          const int row = oo / nb, b = oo - row * nb;
+          const int st = row >> 6;             // stacked tile 2t + st holds the row ...
+          const int r = 64 * h + (row & 63);   // ... as its row r
+          src = st * n + img_at(r, b);
+        }
+        (h ? us : gs)[oo] = sbuf[src];
+      }
+      __syncthreads();
+    } else {
+      const int nb = f / 32;
+      const int n = 128 * nb;
+      uint8_t* base = rec + 2 * (nc + ns) + nc + (long long)(t - pairs) * n;
+      for (int o = threadIdx.x * 16; o < n; o += blockDim.x * 16)
+        *reinterpret_cast<uint4*>(sbuf + o) = *reinterpret_cast<const uint4*>(base + o);
+      __syncthreads();
+      for (int o = threadIdx.x; o < n; o += blockDim.x) {
+        int src;
+        if (to_device) {
+          const int g = o >> 9, i = (o >> 4) & 31, c = (o >> 2) & 3, e = o & 3;
+          src = (32 * c + i) * nb + 4 * g + e;
+        } else {
+          const int row = o / nb, b = o - row * nb;
+          src = img_at(row, b);
+        }
+        base[o] = sbuf[src];
+      }
+      __syncthreads();
     }
-    __syncthreads();
   }
 }
 
@@ -742,11 +797,14 @@ cudaError_t weight_map(const uint8_t* base, long long K, long long rows, long lo
   return cudaSuccess;
 }
 
+// Bytes of the gate/up exchange area (float per epilogue warp, token and lane).
+size_t xb_bytes(const TcArgs& a) { return (size_t)4 * a.xb_tok * 32 * sizeof(float); }
+
 template <int MODE>
 cudaError_t launch_tc(const TcArgs& a, const CUtensorMap& r0, const CUtensorMap& r1, const CUtensorMap& s0,
                       const CUtensorMap& s1, long long items_max, cudaStream_t st) {
   if (items_max >= (1LL << 31)) return cudaErrorInvalidValue;  // item indices are decomposed in 32 bits
-  const size_t smem = (size_t)a.stages * a.stage_bytes + sizeof(Ctl) + 1024;
+  const size_t smem = (size_t)a.stages * a.stage_bytes + ctl_bytes() + xb_bytes(a) + 1024;
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(k_tc<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
@@ -787,7 +845,7 @@ void size_tiles(TcArgs& a, int ch, int mtiles) {
   for (;; ch = 1) {
     a.ch = ch;
     a.stage_bytes = ch * (kATile + a.b_bytes + a.sf_bytes);
-    int st = (227 * 1024 - 1024 - (int)sizeof(Ctl)) / a.stage_bytes;
+    int st = (227 * 1024 - 1024 - (int)ctl_bytes() - (int)xb_bytes(a)) / a.stage_bytes;
     const int tm = (kTmemCols - a.sf_base) / (a.sf_slot * ch);
     if (st > tm) st = tm;
     if (st > kMaxStages) st = kMaxStages;
@@ -851,21 +909,18 @@ cudaError_t launch_gateup(const Cfg& c, const Ws& ws, const uint8_t* routed, con
   TcArgs a = base_args(c, ws, routed, shared, y, T);
   a.terms = c.xterms;
   a.n_tile = round16(c.wgt * c.xterms);
-  a.parts = c.ks;
+  a.xb_tok = c.wgt;
+  a.parts = 1;  // the epilogue needs whole sums (splitting items along d measured slower at decode too)
   a.fp4 = c.fp4;
   a.nch = c.d / (c.fp4 ? 256 : 128);
-  size_tiles(a, chunks_per_stage(a.nch, c.ks), c.f / 128);
+  size_tiles(a, chunks_per_stage(a.nch, 1), c.f / 128);
   if (a.stages < 2) return cudaErrorInvalidConfiguration;
   TcMaps m;
   cudaError_t e = setup(c, routed, shared, a.ch, 0, m, a.shared);
   if (e != cudaSuccess) return e;
-  e = launch_tc<GATEUP>(a, m.gr, m.ur, m.gs, m.us, wg_max * 2 * (c.f / 128) * a.parts, st);
+  e = launch_tc<GATEUP>(a, m.gr, m.ur, m.gs, m.us, wg_max * 2 * (c.f / 128), st);
   if (e == cudaSuccess && mid) e = cudaEventRecord(mid, st);
-  if (e != cudaSuccess) return e;
-  const long long warps = (T * (c.k + c.S)) * (c.f / 32);
-  long long blocks = (warps + 7) / 8;
-  if (blocks > 4LL * g_sms) blocks = 4LL * g_sms;
-  return launch_pdl(k_glu, dim3((unsigned)(blocks > 0 ? blocks : 1)), dim3(256), 0, st, c, ws, T);
+  return e;
 }
 
 cudaError_t launch_down(const Cfg& c, const Ws& ws, const uint8_t* routed, const uint8_t* shared, float* y,
@@ -889,14 +944,16 @@ cudaError_t launch_down(const Cfg& c, const Ws& ws, const uint8_t* routed, const
   return launch_pdl(k_combine, dim3((unsigned)blocks), dim3(256), 0, st, c, ws, y, T);
 }
 
-cudaError_t launch_pack_scales(uint8_t* records, long long n_rec, long long stride, int d, int f, int to_device,
-                               cudaStream_t st) {
-  const size_t smem = (size_t)128 * ((d > f ? d : f) / 32);
+cudaError_t launch_pack_records(uint8_t* records, long long n_rec, long long stride, int d, int f, int to_device,
+                                cudaStream_t st) {
+  // a gate/up pair stages two tiles of d/32 scale bytes per row, a down tile one of f/32
+  const size_t smem = (size_t)128 * (2 * (d / 32) > f / 32 ? 2 * (d / 32) : f / 32);
+  if (smem > 227 * 1024) return cudaErrorInvalidValue;
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(k_pack_scales, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(k_pack_records, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  const long long units = n_rec * (2LL * (f / 128) + d / 128);
+  const long long units = n_rec * ((long long)(f / 128) + d / 128);
   if (g_sms == 0) {
     int dev = 0;
     cudaGetDevice(&dev);
@@ -904,7 +961,7 @@ cudaError_t launch_pack_scales(uint8_t* records, long long n_rec, long long stri
     if (g_sms <= 0) g_sms = 1;
   }
   const long long grid = units < 8LL * g_sms ? units : 8LL * g_sms;
-  k_pack_scales<<<(unsigned)(grid > 0 ? grid : 1), 256, smem, st>>>(records, n_rec, stride, d, f, to_device);
+  k_pack_records<<<(unsigned)(grid > 0 ? grid : 1), 256, smem, st>>>(records, n_rec, stride, d, f, to_device);
   return cudaGetLastError();
 }
 

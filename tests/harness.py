@@ -13,17 +13,36 @@ INDEX_GAP = 1e-5   # near-tie rule for top-k indices (oracle 16th vs 17th logit)
 REL_TOL = 2e-3     # max|y_gpu - y_ref| / max|y_ref|
 
 
+def _image(tile: np.ndarray) -> np.ndarray:
+    """Scale image of one 128-row tile ([..., 128, nb] bytes): row 32c + i, block 4g + e -> 512g + 16i + 4c + e."""
+    lead, nb = tile.shape[:-2], tile.shape[-1]
+    t = tile.reshape(*lead, 4, 32, nb // 4, 4)                      # [c][i][g][e]
+    k = len(lead)
+    return t.transpose(*range(k), k + 2, k + 1, k, k + 3).reshape(*lead, 128 * nb)  # [g][i][c][e]
+
+
 def device_order(records: np.ndarray, d: int, f: int) -> np.ndarray:
-    """Host restatement of the device scale order (include/k3moe.h, k3moe_pack_records) for records in
-    the stored order, one per row of `records`: in every 128-row tile of each matrix, the scale byte
-    of tile row 32c + i and block 4g + e moves to 512g + 16i + 4c + e of the tile's range."""
+    """Host restatement of the device order (include/k3moe.h, k3moe_pack_records) for records in the
+    stored order, one per row of `records`. Gate/up: stacked tile 2u + h (rows 0-63: gate rows
+    128u + 64h.., rows 64-127: up rows 128u + 64h..) replaces gate tile u (h = 0) or up tile u (h = 1),
+    codes and scales; down: each tile's scales. Every tile's scales are stored as its image."""
     out = records.copy()
+    n = len(records)
     nc, ns = d * f // 2, d * f // 32
-    for m, (rows, cols) in enumerate(((f, d), (f, d), (d, f))):
-        nb = cols // 32
-        off = m * (nc + ns) + nc
-        sc = records[:, off:off + ns].reshape(len(records), rows // 128, 4, 32, nb // 4, 4)  # [t][c][i][g][e]
-        out[:, off:off + ns] = sc.transpose(0, 1, 4, 3, 2, 5).reshape(len(records), ns)    # [t][g][i][c][e]
+    u = f // 128
+    g_c, u_c = slice(0, nc), slice(nc + ns, 2 * nc + ns)
+    g_s, u_s = slice(nc, nc + ns), slice(2 * nc + ns, 2 * (nc + ns))
+    gc = records[:, g_c].reshape(n, u, 2, 64, d // 2)   # [tile][half][row][bytes]
+    uc = records[:, u_c].reshape(n, u, 2, 64, d // 2)
+    out[:, g_c] = np.stack([gc[:, :, 0], uc[:, :, 0]], axis=2).reshape(n, nc)   # stacked tiles 2u
+    out[:, u_c] = np.stack([gc[:, :, 1], uc[:, :, 1]], axis=2).reshape(n, nc)   # stacked tiles 2u + 1
+    gs = records[:, g_s].reshape(n, u, 2, 64, d // 32)
+    us = records[:, u_s].reshape(n, u, 2, 64, d // 32)
+    out[:, g_s] = _image(np.concatenate([gs[:, :, 0], us[:, :, 0]], axis=2)).reshape(n, ns)
+    out[:, u_s] = _image(np.concatenate([gs[:, :, 1], us[:, :, 1]], axis=2)).reshape(n, ns)
+    off = 2 * (nc + ns) + nc
+    ds = records[:, off:off + ns].reshape(n, d // 128, 128, f // 32)
+    out[:, off:off + ns] = _image(ds).reshape(n, ns)
     return out
 
 

@@ -71,7 +71,7 @@ def k3_decode_b64():
 
 
 def test_device_generator_matches_host_k3(k3_decode_b1):
-    """The fixture's records are generated on the device and put in the device scale order there."""
+    """The fixture's records are generated on the device and put in the device order there."""
     L = k3_decode_b1
     d, f = L.shape.d_model, L.shape.d_ff
     for e in (0, 517, 895):
