@@ -26,9 +26,22 @@ bool use_fp4(const k3moe_config* c, long long T) {
 
 size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Router logits on the tensor cores at prefill-sized T, else on the CUDA cores.
+// Router logits on the tensor cores from kRouterTcMinT tokens, else on the CUDA cores.
 bool router_tc(const k3moe_config* c, long long T) {
   return T >= k3::kRouterTcMinT && c->d_model % 64 == 0;
+}
+
+// Parts of the tensor-core router's reduction axis: enough (128 token x 256 expert) tiles x parts to
+// fill the 152 SMs once, each part at least 16 of the 64-wide k-steps (the router kernel adds the
+// parts up: fewer parts, fewer loads there); 1 on the CUDA-core path.
+constexpr long long kRouterSplitSms = 152;
+long long router_splits(const k3moe_config* c, long long T) {
+  if (!router_tc(c, T)) return 1;
+  const long long tiles = ((T + 127) / 128) * ((c->n_routed + 255) / 256);
+  const long long nk = (c->x_dtype == K3MOE_X_F32 ? 6 : 3) * (c->d_model / 64);
+  long long p = kRouterSplitSms / tiles;
+  if (p > nk / 16) p = nk / 16;
+  return p < 1 ? 1 : p;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -80,7 +93,15 @@ Layout make_layout(const k3moe_config* c, long long T) {
     o = align_up(o + (bytes ? bytes : 1));
   };
   take(L.ctrl, sizeof(int) * k3::CTRL_WORDS);
-  take(L.logits, sizeof(float) * T * E);
+  // partial logits: T x parts rows. Within a run of equal tile counts the parts are constant, so the
+  // largest row count over T' <= T is at T or at a run's end (a multiple of 128; parts are 1 beyond
+  // kRouterSplitSms runs): sized for that, the layout never shrinks as T grows
+  long long lrows = T * router_splits(c, T);
+  for (long long j = 1; j <= kRouterSplitSms && 128 * j < T; ++j) {
+    const long long r = 128 * j * router_splits(c, 128 * j);
+    lrows = r > lrows ? r : lrows;
+  }
+  take(L.logits, sizeof(float) * lrows * E);
   take(L.topk_idx, sizeof(int) * T * k);
   take(L.topk_w, sizeof(float) * T * k);
   take(L.counts, sizeof(int) * E);
@@ -138,9 +159,11 @@ Cfg make_cfg(const k3moe_config* c, long long T) {
   k.S = c->n_shared;
   k.x_f32 = c->x_dtype == K3MOE_X_F32 ? 1 : 0;
   k.fp4 = use_fp4(c, T) ? 1 : 0;
-  // tokens per work group (42 at prefill sizes, which reads an expert's record fewer times, measured
-  // slower: the projections there are not bound by the record reads)
-  const long long wmax = k.fp4 ? 16 : 32;
+  // tokens per work group. Below 256 tokens most routed experts get one or two tokens and only the
+  // shared experts fill a group: 16 keeps the down projection's MMA N at 48, with two accumulator
+  // buffers (32 measured 35 % slower there at 64 tokens, 8 slower than 16). At prefill sizes 32 (42,
+  // which reads an expert's record fewer times, measured slower)
+  const long long wmax = (k.fp4 || T < 256) ? 16 : 32;
   k.wgt = (int)(T < wmax ? T : wmax);
   if (k.fp4) {
     k.xterms = 8;  // at most 2^-23 of the block maximum per element
@@ -149,6 +172,7 @@ Cfg make_cfg(const k3moe_config* c, long long T) {
     k.xterms = k.x_f32 ? 3 : 2;
     k.hterms = 3;
   }
+  k.rsplit = (int)router_splits(c, T);
   k.stride = c->record_stride;
   return k;
 }

@@ -15,6 +15,7 @@ struct Cfg {
   int fp4;           // 1: activations as E2M1 terms and kind::mxf4 MMAs (few tokens); 0: E4M3 terms, mxf8f6f4
   int xterms;         // terms per activation block of x (E4M3: 2 for bf16 x, 3 for fp32 x; E2M1: 8 or 16)
   int hterms;         // terms per block of h
+  int rsplit;         // partial logits the router kernel adds up (parts of the tensor-core reduction; 1: final)
   long long stride;   // bytes between expert records
 };
 
@@ -36,7 +37,7 @@ struct WorkGroup {
 // Device pointers into the caller's workspace (offsets computed on the host, see ws_layout).
 struct Ws {
   int* ctrl;
-  float* logits;      // [T, E]
+  float* logits;      // [rsplit, T, E] partial logits (one part: the logits)
   int* topk_idx;      // [T, k]
   float* topk_w;      // [T, k]
   int* counts;        // [E] tokens per routed expert

@@ -96,14 +96,38 @@ __device__ unsigned long long warp_topk(unsigned long long (&key)[R], int k) {
   return mine;
 }
 
-// Keys of one thread for the block top-k: experts lane + 32 (warp + nw q), q < R.
+// Keys of one thread for the block top-k: experts lane + 32 (warp + nw q), q < R. The logits are the
+// sums of `np` partial logits `ls` floats apart, added in part order.
 template <int R>
-__device__ __forceinline__ void load_keys(int E, const float* logits_t, unsigned long long (&key)[R]) {
+__device__ __forceinline__ void load_keys(int E, const float* logits_t, long long ls, int np,
+                                          unsigned long long (&key)[R]) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  float l[R];
 #pragma unroll
   for (int q = 0; q < R; ++q) {
     const int e = lane + 32 * (warp + nw * q);
-    key[q] = (e < E) ? topk_key(__ldcg(&logits_t[e]), e) : 0ull;
+    l[q] = (e < E) ? __ldcg(&logits_t[e]) : 0.0f;
+  }
+  constexpr int kZ = 2;  // parts loaded per round (all loads of a round are in flight together)
+  for (int z0 = 1; z0 < np; z0 += kZ) {
+    float pv[kZ][R];
+#pragma unroll
+    for (int u = 0; u < kZ; ++u)
+#pragma unroll
+      for (int q = 0; q < R; ++q) {
+        const int e = lane + 32 * (warp + nw * q);
+        pv[u][q] = (z0 + u < np && e < E) ? __ldcg(&logits_t[(z0 + u) * ls + e]) : 0.0f;
+      }
+#pragma unroll
+    for (int u = 0; u < kZ; ++u)
+      if (z0 + u < np)
+#pragma unroll
+        for (int q = 0; q < R; ++q) l[q] += pv[u][q];
+  }
+#pragma unroll
+  for (int q = 0; q < R; ++q) {
+    const int e = lane + 32 * (warp + nw * q);
+    key[q] = (e < E) ? topk_key(l[q], e) : 0ull;
   }
 }
 
@@ -117,12 +141,12 @@ __device__ __forceinline__ void load_keys(int E, const float* logits_t, unsigned
 // it. If more candidates than threads turn up (ties at the threshold's scale, or tiny E), the
 // two-stage selection runs instead: every warp's k best, then the k best of those.
 template <int R>
-__device__ void topk_select(int E, int k, const float* logits_t, unsigned long long* cand, unsigned long long* sel,
-                            unsigned long long* s_thr, int* s_n) {
+__device__ void topk_select(int E, int k, const float* logits_t, long long ls, int np, unsigned long long* cand,
+                            unsigned long long* sel, unsigned long long* s_thr, int* s_n) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   const int m = (k + nw - 1) / nw;
   unsigned long long key[R];
-  load_keys<R>(E, logits_t, key);
+  load_keys<R>(E, logits_t, ls, np, key);
   const unsigned long long mine = warp_topk<R>(key, m);  // clears the picked keys in `key`
   if (lane < m) s_thr[warp * m + lane] = mine;
   if (threadIdx.x == 0) *s_n = 0;
@@ -151,7 +175,7 @@ __device__ void topk_select(int E, int k, const float* logits_t, unsigned long l
     }
     if ((int)threadIdx.x < k && (int)threadIdx.x >= n) sel[threadIdx.x] = 0ull;  // fewer than k experts
   } else {
-    load_keys<R>(E, logits_t, key);
+    load_keys<R>(E, logits_t, ls, np, key);
     const unsigned long long top = warp_topk<R>(key, k);
     cand[warp * 32 + lane] = (lane < k) ? top : 0ull;
     __syncthreads();
@@ -166,20 +190,20 @@ __device__ void topk_select(int E, int k, const float* logits_t, unsigned long l
   __syncthreads();
 }
 
-// Top-k and renormalised softmax gates of one token, by the whole CTA (2 to 8 warps). `cand` is
-// shared memory for blockDim.x keys. Ends with __syncthreads.
+// Top-k and renormalised softmax gates of one token, by the whole CTA (2 to 8 warps), from `np` partial
+// logits `ls` floats apart. `cand` is shared memory for blockDim.x keys. Ends with __syncthreads.
 // `idx_sm` / `w_sm` (shared memory, or NULL) receive a copy of the selection for the permutation.
-__device__ void topk_block(int E, int k, const float* logits_t, unsigned long long* cand, int* idx_out, float* w_out,
-                           int* idx_user, float* w_user, int* idx_sm, float* w_sm) {
+__device__ void topk_block(int E, int k, const float* logits_t, long long ls, int np, unsigned long long* cand,
+                           int* idx_out, float* w_out, int* idx_user, float* w_user, int* idx_sm, float* w_sm) {
   __shared__ unsigned long long s_sel[32], s_thr[64];
   __shared__ int s_n;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   const int per_lane = (E + 32 * nw - 1) / (32 * nw);
-  if (per_lane <= 1) topk_select<1>(E, k, logits_t, cand, s_sel, s_thr, &s_n);
-  else if (per_lane <= 2) topk_select<2>(E, k, logits_t, cand, s_sel, s_thr, &s_n);
-  else if (per_lane <= 4) topk_select<4>(E, k, logits_t, cand, s_sel, s_thr, &s_n);
-  else if (per_lane <= 8) topk_select<8>(E, k, logits_t, cand, s_sel, s_thr, &s_n);
-  else topk_select<16>(E, k, logits_t, cand, s_sel, s_thr, &s_n);  // E <= 4096 with 8 warps
+  if (per_lane <= 1) topk_select<1>(E, k, logits_t, ls, np, cand, s_sel, s_thr, &s_n);
+  else if (per_lane <= 2) topk_select<2>(E, k, logits_t, ls, np, cand, s_sel, s_thr, &s_n);
+  else if (per_lane <= 4) topk_select<4>(E, k, logits_t, ls, np, cand, s_sel, s_thr, &s_n);
+  else if (per_lane <= 8) topk_select<8>(E, k, logits_t, ls, np, cand, s_sel, s_thr, &s_n);
+  else topk_select<16>(E, k, logits_t, ls, np, cand, s_sel, s_thr, &s_n);  // E <= 4096 with 8 warps
   if (warp == 0) {
     const unsigned long long best = (lane < k) ? s_sel[lane] : 0ull;
     const int my_e = key_expert(best);
@@ -239,7 +263,10 @@ __device__ void block_scan2(const int* in0, const int* in1, int* out0, int* out1
 }
 
 // One CTA: positions, inverse map and work groups for T tokens' routed slots plus the shared experts.
-// `sm` is shared-memory scratch of 4E + 2 ints (counts, cursors, offsets, work-group offsets).
+// `sm` is shared-memory scratch of 4E + 2 ints (counts, cursors, offsets, work-group offsets). The
+// slot loops read kPermBatch slots per thread before acting on them (one load latency per batch).
+// The order of an expert's positions follows the shared-memory atomics; no result depends on it (the
+// projections treat positions independently and the combine adds each token's slots in slot order).
 __device__ void build_permutation(const Cfg& c, const Ws& ws, long long T, const int* idx, const float* w, int* sm) {
   __shared__ int s_tmp[64];
   const int tid = threadIdx.x, nt = blockDim.x;
@@ -251,10 +278,20 @@ __device__ void build_permutation(const Cfg& c, const Ws& ws, long long T, const
   const long long nslot = T * k;
   for (int e = tid; e < E; e += nt) { counts[e] = 0; cursor[e] = 0; }
   __syncthreads();
-  for (long long s = tid; s < nslot; s += nt) {
-    const int e = idx[s];
-    if (e < 0 || e >= E) set_status(ws.ctrl, ST_BAD_EXPERT);
-    else atomicAdd(&counts[e], 1);
+  constexpr int kPermBatch = 8;
+  for (long long s0 = tid; s0 < nslot; s0 += (long long)kPermBatch * nt) {
+    int ev[kPermBatch];
+#pragma unroll
+    for (int u = 0; u < kPermBatch; ++u) {
+      const long long s = s0 + (long long)u * nt;
+      ev[u] = s < nslot ? __ldcg(&idx[s]) : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < kPermBatch; ++u) {
+      if (s0 + (long long)u * nt >= nslot) continue;
+      if (ev[u] < 0 || ev[u] >= E) set_status(ws.ctrl, ST_BAD_EXPERT);
+      else atomicAdd(&counts[ev[u]], 1);
+    }
   }
   __syncthreads();
   for (int e = tid; e < E; e += nt) cursor[e] = (counts[e] + W - 1) / W;  // work groups per expert
@@ -262,13 +299,26 @@ __device__ void build_permutation(const Cfg& c, const Ws& ws, long long T, const
   block_scan2(counts, cursor, offsets, wgoff, E, s_tmp);
   for (int e = tid; e < E; e += nt) cursor[e] = 0;
   __syncthreads();
-  for (long long s = tid; s < nslot; s += nt) {
-    const int e = idx[s];
-    if (e < 0 || e >= E) { ws.inv[s] = -1; continue; }
-    const int pos = offsets[e] + atomicAdd(&cursor[e], 1);
-    ws.perm_tok[pos] = (int)(s / k);
-    ws.perm_w[pos] = w[s];
-    ws.inv[s] = pos;
+  for (long long s0 = tid; s0 < nslot; s0 += (long long)kPermBatch * nt) {
+    int ev[kPermBatch];
+    float wv[kPermBatch];
+#pragma unroll
+    for (int u = 0; u < kPermBatch; ++u) {
+      const long long s = s0 + (long long)u * nt;
+      ev[u] = s < nslot ? __ldcg(&idx[s]) : -1;
+      wv[u] = s < nslot ? __ldcg(&w[s]) : 0.0f;
+    }
+#pragma unroll
+    for (int u = 0; u < kPermBatch; ++u) {
+      const long long s = s0 + (long long)u * nt;
+      if (s >= nslot) continue;
+      const int e = ev[u];
+      if (e < 0 || e >= E) { ws.inv[s] = -1; continue; }
+      const int pos = offsets[e] + atomicAdd(&cursor[e], 1);
+      ws.perm_tok[pos] = (int)(s / k);
+      ws.perm_w[pos] = wv[u];
+      ws.inv[s] = pos;
+    }
   }
   for (int e = tid; e < E; e += nt) {
     const int n = counts[e];
@@ -387,8 +437,9 @@ struct RouteArgs {
 };
 
 // Shared-memory layout of the router CTA: [x tile | permutation scratch (aliased)][top-k candidates].
-__host__ __device__ __forceinline__ size_t route_tile_bytes(const Cfg& c, int tt) {
-  const size_t xt = (size_t)tt * c.d * (c.x_f32 ? 4 : 2);
+// The x tile is staged only when the CTA computes logits (stage_x).
+__host__ __device__ __forceinline__ size_t route_tile_bytes(const Cfg& c, int tt, bool stage_x) {
+  const size_t xt = stage_x ? (size_t)tt * c.d * (c.x_f32 ? 4 : 2) : 0;
   const size_t perm = sizeof(int) * (4 * (size_t)c.E + 2);
   const size_t m = xt > perm ? xt : perm;
   return (m + 15) & ~(size_t)15;
@@ -414,11 +465,11 @@ __global__ void __launch_bounds__(256, 3) k_route(RouteArgs a) {
   const int ntt = (int)min((long long)TT, a.T - t0);
   const int esz = c.x_f32 ? 4 : 2;
   const int row_bytes = c.d * esz;
-  unsigned long long* cand = reinterpret_cast<unsigned long long*>(smem + route_tile_bytes(c, TT));
+  unsigned long long* cand = reinterpret_cast<unsigned long long*>(smem + route_tile_bytes(c, TT, dots));
 
   // quarter [jb, je) of row e: U float4 loads per lane per batch, all issued before any arithmetic
   constexpr int U = 14;
-  const int qlen = c.d / 4, jb = kq * qlen, je = jb + qlen;
+  const int qlen = c.d / 4, jb = kq * qlen, je = dots ? jb + qlen : jb;
   const float* wrow = a.W + (long long)(e < c.E ? e : 0) * c.d;
   uint4 wv[U];
   auto load_batch = [&](int j0) {
@@ -435,7 +486,7 @@ __global__ void __launch_bounds__(256, 3) k_route(RouteArgs a) {
   pdl_launch_dependents();
 
   // the token tile of x goes to shared memory (asynchronously, waited for below)
-  {
+  if (dots) {
     const uint8_t* src = reinterpret_cast<const uint8_t*>(a.x) + t0 * row_bytes;
     const uint32_t dst = (uint32_t)__cvta_generic_to_shared(smem);
     const int bytes = ntt * row_bytes;
@@ -507,9 +558,14 @@ __global__ void __launch_bounds__(256, 3) k_route(RouteArgs a) {
     for (int blk = blockIdx.x * nw + warp; blk * 32 < c.d; blk += (int)gridDim.x * nw) {
       const int j = blk * 32;
       for (int tt = 0; tt < ntt; ++tt) {
-        const uint8_t* xr = smem + tt * row_bytes;
-        const float v = c.x_f32 ? reinterpret_cast<const float*>(xr)[j + lane]
-                                : __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(xr)[j + lane] << 16);
+        float v;
+        if (dots) {  // from the staged tile
+          const uint8_t* xr = smem + tt * row_bytes;
+          v = c.x_f32 ? reinterpret_cast<const float*>(xr)[j + lane]
+                      : __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(xr)[j + lane] << 16);
+        } else {
+          v = load_x(a.x, c.x_f32, (t0 + tt) * c.d + j + lane);
+        }
         xterms_block(c, a.ws, v, t0 + tt, j, lane);
       }
     }
@@ -529,7 +585,8 @@ __global__ void __launch_bounds__(256, 3) k_route(RouteArgs a) {
   const bool tile_sm = gridDim.y == 1 && (long long)ntt * c.k <= (long long)blockDim.x && ntt * c.k <= 8 * 32;
   for (int tt = 0; tt < ntt; ++tt) {
     const long long t = t0 + tt;
-    topk_block(c.E, c.k, a.ws.logits + t * c.E, cand, a.ws.topk_idx + t * c.k, a.ws.topk_w + t * c.k,
+    topk_block(c.E, c.k, a.ws.logits + t * c.E, a.T * c.E, dots ? 1 : c.rsplit, cand, a.ws.topk_idx + t * c.k,
+               a.ws.topk_w + t * c.k,
                (a.mode & RM_USER_OUT) && a.out_idx ? a.out_idx + t * c.k : nullptr,
                (a.mode & RM_USER_OUT) && a.out_w ? a.out_w + t * c.k : nullptr, tile_sm ? s_tk_idx + tt * c.k : nullptr,
                tile_sm ? s_tk_w + tt * c.k : nullptr);
@@ -605,7 +662,7 @@ bool g_route_attr_set = false;
 
 template <int TT>
 cudaError_t launch_route_tt(const RouteArgs& a, int warps, cudaStream_t st) {
-  const size_t smem = route_tile_bytes(a.c, TT) + sizeof(unsigned long long) * 32 * warps;
+  const size_t smem = route_tile_bytes(a.c, TT, !(a.mode & RM_LOGITS_READY)) + sizeof(unsigned long long) * 32 * warps;
   if (smem > (size_t)kRouteMaxSmem) return cudaErrorInvalidValue;
   static bool attr = false;
   if (!attr) {
@@ -623,8 +680,11 @@ cudaError_t launch_route(const Cfg& c, const Ws& ws, const void* x, long long T,
   RouteArgs a{c, ws, x, T, W, bias, out_idx, out_w, mode};
   // largest token tile (<= T) whose staged activations fit in shared memory
   auto fits = [&](int tt, int warps) {
-    return route_tile_bytes(c, tt) + sizeof(unsigned long long) * 32 * warps <= (size_t)kRouteMaxSmem;
+    return route_tile_bytes(c, tt, !(mode & RM_LOGITS_READY)) + sizeof(unsigned long long) * 32 * warps <=
+           (size_t)kRouteMaxSmem;
   };
+  // with precomputed logits every token has its own CTA (its top-k is the CTA's only serial work)
+  if (mode & RM_LOGITS_READY) return launch_route_tt<1>(a, 8, st);
   if (T >= 8 && fits(8, 8)) return launch_route_tt<8>(a, 8, st);
   if (T >= 4 && fits(4, 8)) return launch_route_tt<4>(a, 8, st);
   if (T >= 2 && fits(2, 8)) return launch_route_tt<2>(a, 8, st);

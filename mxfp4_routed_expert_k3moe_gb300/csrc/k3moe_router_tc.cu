@@ -10,10 +10,12 @@
 // this replaces the CUDA-core dot products, which read the whole router matrix once per tile of 8
 // tokens.
 //
-// One CTA per (128-token tile, 256-expert tile): warp 0 lane 0 issues the tensor copies of a 4-stage
-// ring (x tile 128 x 64 and W part tile 256 x 64, bf16, 128-byte swizzle), warp 1 lane 0 issues the
-// MMAs (M = 128 tokens, N = 256 experts, K = 16 each), and the four warps then read the accumulator
-// (lane = token) and store the logits with the bias added. Every wait is bounded.
+// One CTA per (128-token tile, 256-expert tile, part of the reduction axis): warp 0 lane 0 issues the
+// tensor copies of a 4-stage ring (x tile 128 x 64 and W part tile 256 x 64, bf16, 128-byte swizzle),
+// warp 1 lane 0 issues the MMAs (M = 128 tokens, N = 256 experts, K = 16 each), and the four warps
+// then read the accumulator (lane = token) and store the partial logits (the bias added to part 0).
+// With few tokens the reduction axis is cut into parts so that the grid fills the SMs; the router
+// kernel adds the parts, in part order, when it reads the logits. Every wait is bounded.
 #include <cstdint>
 #include <mutex>
 
@@ -80,12 +82,12 @@ __global__ void __launch_bounds__(256) k_split_w(const float* W, long long n, __
 
 __global__ void __launch_bounds__(kRThreads, 1)
     k_router_mma(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
-                 const float* bias, float* logits, long long T, int E, int d, int npairs, int* status) {
+                 const float* bias, float* logits, long long T, int E, int d, int npairs, int nsplit, int* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   RCtl* ctl = reinterpret_cast<RCtl*>(smem + kRStages * (kRA + kRB));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int mt = blockIdx.x, nt = blockIdx.y;
+  const int mt = blockIdx.x, nt = blockIdx.y, z = blockIdx.z;
   pdl_wait();  // the weight parts come from the split kernel just before
   pdl_launch_dependents();
   if (warp == 0) {
@@ -106,12 +108,14 @@ __global__ void __launch_bounds__(kRThreads, 1)
   tc_fence_after();
   const uint32_t tmem = ctl->tmem;
   const int kpp = d / kRK, nk = npairs * kpp;  // k-steps per (token part, weight part) pair, in all
+  const int kb = (int)((long long)nk * z / nsplit), ke = (int)((long long)nk * (z + 1) / nsplit);  // this part
   bool ok = true;
   if (warp == 0) {
     if (lane == 0) {  // tensor copies
-      for (int ks = 0, s = 0; ks < nk && ok; ++ks) {
-        const uint32_t round = (uint32_t)(ks / kRStages);
-        if (ks >= kRStages && !rwait(su32(&ctl->empty[s]), (round - 1) & 1u, ctl, status)) { ok = false; break; }
+      for (int ks = kb, s = 0; ks < ke && ok; ++ks) {
+        const int i = ks - kb;
+        const uint32_t round = (uint32_t)(i / kRStages);
+        if (i >= kRStages && !rwait(su32(&ctl->empty[s]), (round - 1) & 1u, ctl, status)) { ok = false; break; }
         const int pair = ks / kpp, k0 = (ks - pair * kpp) * kRK;
         uint8_t* st = smem + (size_t)s * (kRA + kRB);
         mbar_expect_tx(su32(&ctl->full[s]), kRA + kRB);
@@ -126,13 +130,13 @@ __global__ void __launch_bounds__(kRThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {  // MMAs
       const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kRN >> 3) << 17) | ((uint32_t)(kRM >> 4) << 24);
-      for (int ks = 0, s = 0; ks < nk; ++ks) {
-        if (!rwait(su32(&ctl->full[s]), (uint32_t)(ks / kRStages) & 1u, ctl, status)) { ok = false; break; }
+      for (int ks = kb, s = 0; ks < ke; ++ks) {
+        if (!rwait(su32(&ctl->full[s]), (uint32_t)((ks - kb) / kRStages) & 1u, ctl, status)) { ok = false; break; }
         tc_fence_after();
         const uint8_t* st = smem + (size_t)s * (kRA + kRB);
         const uint64_t da = sw128_desc(su32(st)), db = sw128_desc(su32(st + kRA));
 #pragma unroll
-        for (int k = 0; k < kRK / 16; ++k) tc_mma_bf16(tmem, da + 2 * k, db + 2 * k, idesc, (ks | k) ? 1u : 0u);
+        for (int k = 0; k < kRK / 16; ++k) tc_mma_bf16(tmem, da + 2 * k, db + 2 * k, idesc, (ks != kb || k) ? 1u : 0u);
         tc_commit(su32(&ctl->empty[s]));
         if (++s == kRStages) s = 0;
       }
@@ -151,10 +155,11 @@ __global__ void __launch_bounds__(kRThreads, 1)
       tc_wait_ld();
       const int e0 = nt * kRN + c0;
       if (t < T) {
-        float* dst = logits + t * E + e0;
+        float* dst = logits + (long long)z * T * E + t * E + e0;
+        const bool addb = bias && z == 0;
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-          if (e0 + j < E) dst[j] = __uint_as_float(v[j]) + (bias ? __ldg(&bias[e0 + j]) : 0.0f);
+          if (e0 + j < E) dst[j] = __uint_as_float(v[j]) + (addb ? __ldg(&bias[e0 + j]) : 0.0f);
       }
     }
   }
@@ -184,7 +189,9 @@ cudaError_t encode_fn() {
 
 cudaError_t launch_router_tc(const Cfg& c, const Ws& ws, const void* x, long long T, const float* W, const float* bias,
                              void* w3, void* x3, cudaStream_t st) {
-  if (c.d % kRK != 0 || T > (1LL << 31) - kRM || (c.x_f32 && !x3)) return cudaErrorInvalidValue;
+  if (c.d % kRK != 0 || T > (1LL << 31) - kRM || (c.x_f32 && !x3) || c.rsplit < 1 ||
+      c.rsplit > (c.x_f32 ? 6 : 3) * (c.d / kRK))
+    return cudaErrorInvalidValue;
   cudaError_t e = encode_fn();
   if (e != cudaSuccess) return e;
   const long long n = (long long)c.E * c.d;
@@ -221,9 +228,9 @@ cudaError_t launch_router_tc(const Cfg& c, const Ws& ws, const void* x, long lon
       return e;
     attr = true;
   }
-  dim3 grid((unsigned)((T + kRM - 1) / kRM), (unsigned)((c.E + kRN - 1) / kRN));
+  dim3 grid((unsigned)((T + kRM - 1) / kRM), (unsigned)((c.E + kRN - 1) / kRN), (unsigned)c.rsplit);
   return launch_pdl(k_router_mma, grid, dim3(kRThreads), smem, st, mx, mw, bias, ws.logits, T, c.E, c.d,
-                    c.x_f32 ? 6 : 3, ws.ctrl);
+                    c.x_f32 ? 6 : 3, c.rsplit, ws.ctrl);
 }
 
 }  // namespace k3

@@ -145,9 +145,11 @@ def test_layer_prefill_4096_sampled():
 # ------------------------------------------------------------------ separate entry points
 
 
-def test_route_only():
+@pytest.mark.parametrize("T,tol", [(5, 1e-6), (29, 1e-5)])
+def test_route_only(T, tol):
+    """Below 8 tokens the logits are fp32 dot products on the CUDA cores (gates to 1e-6); from 8 on
+    they come from the tensor cores as partial sums over parts of d (gates to 1e-5, as below)."""
     L = DeviceLayer(MID, seed=10, zipf_s=1.1)
-    T = 29
     xh, xd = L.tokens(T)
     idx = torch.empty((T, MID.top_k), dtype=torch.int32, device="cuda")
     w = torch.empty((T, MID.top_k), dtype=torch.float32, device="cuda")
@@ -159,13 +161,14 @@ def test_route_only():
     assert ok
     wn = w.cpu().numpy()
     assert np.allclose(wn.sum(axis=1), 1.0, atol=1e-6)
-    assert gate_err(idx.cpu().numpy(), wn, idx_ref, w_ref) < 1e-6
+    assert gate_err(idx.cpu().numpy(), wn, idx_ref, w_ref) < tol
 
 
-@pytest.mark.parametrize("T,x_dtype", [(512, "bf16"), (700, "bf16"), (600, "f32")])
+@pytest.mark.parametrize("T,x_dtype", [(8, "bf16"), (40, "f32"), (512, "bf16"), (700, "bf16"), (600, "f32")])
 def test_route_tensor_core_router(T, x_dtype):
-    """From 512 tokens the logits come from the tensor cores (the fp32 router weights, and fp32 tokens,
-    in three bf16 parts; fp32 accumulation): same selection (near-tie rule) and gates as the oracle."""
+    """From 8 tokens the logits come from the tensor cores (the fp32 router weights, and fp32 tokens,
+    in three bf16 parts; fp32 accumulation; below ~600 tokens as partial sums over parts of d): same
+    selection (near-tie rule) and gates as the oracle."""
     L = DeviceLayer(MID, seed=12, zipf_s=1.1, x_dtype=x_dtype)
     xh, xd = L.tokens(T)
     idx = torch.empty((T, MID.top_k), dtype=torch.int32, device="cuda")
