@@ -79,7 +79,7 @@ long long wg_bound(const k3moe_config* c, long long T) {
 }
 
 struct Layout {
-  size_t ctrl, logits, topk_idx, topk_w, counts, cursor, offsets, wgoff, perm_tok, perm_w, inv, wgs, xq, xs, hq, hs,
+  size_t ctrl, logits, topk_idx, topk_w, counts, cursor, offsets, wgoff, perm_tok, perm_w, inv, wgs, wgs_dn, xq, xs, hq, hs,
       part, rtcnt, w3, x3, total;
 };
 
@@ -112,6 +112,7 @@ Layout make_layout(const k3moe_config* c, long long T) {
   take(L.perm_w, sizeof(float) * P);
   take(L.inv, sizeof(int) * T * k);
   take(L.wgs, sizeof(k3::WorkGroup) * wg_bound(c, T));
+  take(L.wgs_dn, sizeof(k3::WorkGroup) * wg_bound(c, T));
   const bool fp4 = use_fp4(c, T);
   const long long terms = fp4 ? kMaxTermsFp4 : kMaxTerms;
   take(L.xq, (size_t)(T * terms * (fp4 ? d / 2 : d)));
@@ -141,6 +142,7 @@ Ws bind(const Layout& L, void* base) {
   w.perm_w = reinterpret_cast<float*>(b + L.perm_w);
   w.inv = reinterpret_cast<int*>(b + L.inv);
   w.wgs = reinterpret_cast<k3::WorkGroup*>(b + L.wgs);
+  w.wgs_dn = reinterpret_cast<k3::WorkGroup*>(b + L.wgs_dn);
   w.xq = reinterpret_cast<uint8_t*>(b + L.xq);
   w.xs = reinterpret_cast<uint8_t*>(b + L.xs);
   w.hq = reinterpret_cast<uint8_t*>(b + L.hq);
@@ -159,12 +161,13 @@ Cfg make_cfg(const k3moe_config* c, long long T) {
   k.S = c->n_shared;
   k.x_f32 = c->x_dtype == K3MOE_X_F32 ? 1 : 0;
   k.fp4 = use_fp4(c, T) ? 1 : 0;
-  // tokens per work group. Below 256 tokens most routed experts get one or two tokens and only the
-  // shared experts fill a group: 16 keeps the down projection's MMA N at 48, with two accumulator
-  // buffers (32 measured 35 % slower there at 64 tokens, 8 slower than 16). At prefill sizes 32 (42,
-  // which reads an expert's record fewer times, measured slower)
-  const long long wmax = (k.fp4 || T < 256) ? 16 : 32;
+  // tokens per work group. Gate/up: 32 (16 with the E2M1 terms; 42, which reads an expert's record
+  // fewer times, measured slower at prefill sizes, 16 slower from 256 tokens on). Down: 16, which
+  // keeps its MMA N at 48 with two issuers and two accumulator buffers (32, N = 96 with one of
+  // either, measured 35 % slower at 64 tokens, 45 % at 512, 9 % at 4096; 8 slower than 16)
+  const long long wmax = k.fp4 ? 16 : 32, wmax_dn = 16;
   k.wgt = (int)(T < wmax ? T : wmax);
+  k.wgt_dn = (int)(T < wmax_dn ? T : wmax_dn);
   if (k.fp4) {
     k.xterms = 8;  // at most 2^-23 of the block maximum per element
     k.hterms = 8;

@@ -11,7 +11,8 @@ namespace k3 {
 struct Cfg {
   int d, f, E, k, S;  // d_model, d_ff, routed experts, top-k, shared experts
   int x_f32;          // 1 if x is fp32, 0 if bf16
-  int wgt;            // max tokens per work group
+  int wgt;            // max tokens per work group of the gate/up projection
+  int wgt_dn;         // ... of the down projection (the permutation writes both lists)
   int fp4;           // 1: activations as E2M1 terms and kind::mxf4 MMAs (few tokens); 0: E4M3 terms, mxf8f6f4
   int xterms;         // terms per activation block of x (E4M3: 2 for bf16 x, 3 for fp32 x; E2M1: 8 or 16)
   int hterms;         // terms per block of h
@@ -25,6 +26,7 @@ enum CtrlSlot {
   CTRL_ROUTER_DONE = 1,  // router token tiles whose top-k is done (the last builds the permutation)
   CTRL_NWG = 2,          // number of work groups built by the permutation
   CTRL_NPOS = 3,         // number of routed positions (slots with a valid expert id)
+  CTRL_NWG_DN = 4,       // number of work groups of the down projection's list
   CTRL_WORDS = 64
 };
 enum StatusBits { ST_BAD_EXPERT = 1, ST_NAN_SCALE = 2, ST_TIMEOUT = 4 };
@@ -47,7 +49,8 @@ struct Ws {
   int* perm_tok;      // [P] token of each position (P = T*k routed + T*S shared)
   float* perm_w;      // [P] gate weight of each position (1 for shared)
   int* inv;           // [T*k] position of routed slot (t, i), -1 if the slot was rejected
-  WorkGroup* wgs;     // [WGmax]
+  WorkGroup* wgs;     // [WGmax] work groups of the gate/up projection (wgt positions at most)
+  WorkGroup* wgs_dn;  // [WGmax] work groups of the down projection (wgt_dn positions at most)
   uint8_t* xq;        // [T * xterms, d] E4M3 (or [.., d/2] packed E2M1) terms of x (row t*xterms + j)
   uint8_t* xs;        // [T * xterms, d/32] their E8M0 block scales
   uint8_t* hq;        // [P * hterms, f] E4M3 (or [.., f/2] packed E2M1) terms of h (row p*hterms + j)

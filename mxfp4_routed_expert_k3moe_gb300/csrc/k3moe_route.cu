@@ -262,8 +262,20 @@ __device__ void block_scan2(const int* in0, const int* in1, int* out0, int* out1
   __syncthreads();
 }
 
-// One CTA: positions, inverse map and work groups for T tokens' routed slots plus the shared experts.
-// `sm` is shared-memory scratch of 4E + 2 ints (counts, cursors, offsets, work-group offsets). The
+// Ints of permutation scratch in shared memory (256-thread CTAs): the general builder's 6E + 4, the
+// small one's 3 x 256 slots + 64.
+__host__ __device__ constexpr size_t perm_ints(int E) {
+  return 6 * (size_t)E + 4 > 3 * 256 + 64 ? 6 * (size_t)E + 4 : 3 * 256 + 64;
+}
+
+// Work groups of one run of n positions from p0 (expert e), at most W positions each, from list slot g.
+__device__ __forceinline__ void write_groups(WorkGroup* list, int g, int e, long long p0, long long n, int W) {
+  for (long long p = 0; p < n; p += W, ++g) list[g] = WorkGroup{e, (int)(p0 + p), (int)min((long long)W, n - p), 0};
+}
+
+// One CTA: positions, inverse map and the two work-group lists (wgt positions each for gate/up,
+// wgt_dn for down) for T tokens' routed slots plus the shared experts. `sm` is shared-memory scratch
+// of kPermInts(E) ints (counts, cursors, offsets, the two lists' group offsets, scan scratch). The
 // slot loops read kPermBatch slots per thread before acting on them (one load latency per batch).
 // The order of an expert's positions follows the shared-memory atomics; no result depends on it (the
 // projections treat positions independently and the combine adds each token's slots in slot order).
@@ -271,10 +283,13 @@ __device__ void build_permutation(const Cfg& c, const Ws& ws, long long T, const
   __shared__ int s_tmp[64];
   const int tid = threadIdx.x, nt = blockDim.x;
   const int E = c.E, k = c.k, W = c.wgt;
+  const int Wd = c.wgt_dn;
   int* counts = sm;
   int* cursor = sm + E;
   int* offsets = sm + 2 * E;      // E + 1
   int* wgoff = sm + 3 * E + 1;    // E + 1
+  int* wgoff_dn = sm + 4 * E + 2; // E + 1
+  int* scratch = sm + 5 * E + 3;  // E + 1
   const long long nslot = T * k;
   for (int e = tid; e < E; e += nt) { counts[e] = 0; cursor[e] = 0; }
   __syncthreads();
@@ -297,6 +312,9 @@ __device__ void build_permutation(const Cfg& c, const Ws& ws, long long T, const
   for (int e = tid; e < E; e += nt) cursor[e] = (counts[e] + W - 1) / W;  // work groups per expert
   __syncthreads();
   block_scan2(counts, cursor, offsets, wgoff, E, s_tmp);
+  for (int e = tid; e < E; e += nt) cursor[e] = (counts[e] + Wd - 1) / Wd;  // down work groups per expert
+  __syncthreads();
+  block_scan2(cursor, cursor, wgoff_dn, scratch, E, s_tmp);
   for (int e = tid; e < E; e += nt) cursor[e] = 0;
   __syncthreads();
   for (long long s0 = tid; s0 < nslot; s0 += (long long)kPermBatch * nt) {
@@ -321,24 +339,24 @@ __device__ void build_permutation(const Cfg& c, const Ws& ws, long long T, const
     }
   }
   for (int e = tid; e < E; e += nt) {
-    const int n = counts[e];
-    int g = wgoff[e];
-    for (int p = 0; p < n; p += W, ++g) ws.wgs[g] = WorkGroup{e, offsets[e] + p, min(W, n - p), 0};
+    write_groups(ws.wgs, wgoff[e], e, offsets[e], counts[e], W);
+    write_groups(ws.wgs_dn, wgoff_dn[e], e, offsets[e], counts[e], Wd);
   }
-  const int n_routed_wg = wgoff[E];
   const long long pr = nslot;  // shared positions start after all routed slots
-  const int nwt = (int)((T + W - 1) / W);
-  for (int q = tid; q < c.S * nwt; q += nt) {
-    const int s = q / nwt, i = q % nwt;
-    const long long p0 = (long long)i * W;
-    ws.wgs[n_routed_wg + q] = WorkGroup{E + s, (int)(pr + (long long)s * T + p0), (int)min((long long)W, T - p0), 0};
-  }
+  const int nwt = (int)((T + W - 1) / W), nwt_d = (int)((T + Wd - 1) / Wd);
+  for (int q = tid; q < c.S * nwt; q += nt)
+    write_groups(ws.wgs, wgoff[E] + q, E + q / nwt, pr + (long long)(q / nwt) * T + (long long)(q % nwt) * W,
+                 min((long long)W, T - (long long)(q % nwt) * W), W);
+  for (int q = tid; q < c.S * nwt_d; q += nt)
+    write_groups(ws.wgs_dn, wgoff_dn[E] + q, E + q / nwt_d, pr + (long long)(q / nwt_d) * T + (long long)(q % nwt_d) * Wd,
+                 min((long long)Wd, T - (long long)(q % nwt_d) * Wd), Wd);
   for (long long q = tid; q < (long long)c.S * T; q += nt) {
     ws.perm_tok[pr + q] = (int)(q % T);
     ws.perm_w[pr + q] = 1.0f;
   }
   if (tid == 0) {
-    ws.ctrl[CTRL_NWG] = n_routed_wg + c.S * nwt;
+    ws.ctrl[CTRL_NWG] = wgoff[E] + c.S * nwt;
+    ws.ctrl[CTRL_NWG_DN] = wgoff_dn[E] + c.S * nwt_d;
     ws.ctrl[CTRL_NPOS] = offsets[E];
   }
   __syncthreads();
@@ -346,16 +364,18 @@ __device__ void build_permutation(const Cfg& c, const Ws& ws, long long T, const
 
 // The same permutation for at most blockDim.x routed slots, without arrays over the experts: slot s
 // (thread s) finds its position by counting the valid slots that sort before it (expert id, then
-// slot order), and starts a work group when its rank within its expert is a multiple of wgt; the
-// work groups are numbered by a block-wide count of the starts before each position.
+// slot order), and starts a work group of either list when its rank within its expert is a multiple
+// of that list's size; the groups are numbered by a block-wide count of the starts before each
+// position.
 __device__ void build_permutation_small(const Cfg& c, const Ws& ws, long long T, const int* idx, const float* w,
                                         int* sm) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
-  const int E = c.E, k = c.k, W = c.wgt;
+  const int E = c.E, k = c.k, W = c.wgt, Wd = c.wgt_dn;
   const int n = (int)(T * k);
-  int* s_e = sm;               // [n] expert of each slot (-1 if invalid)
-  int* s_flag = sm + n;        // [n] by position: 1 if the position starts a work group
-  int* s_wsum = sm + 2 * n;    // [32] per-warp start counts
+  int* s_e = sm;                // [n] expert of each slot (-1 if invalid)
+  int* s_flag = sm + n;         // [n] by position: 1 if the position starts a gate/up group (then its number)
+  int* s_flag_dn = sm + 2 * n;  // [n] the same for the down groups
+  int* s_wsum = sm + 3 * n;     // [2][32] per-warp start counts
   int e = -1;
   if (tid < n) {
     e = idx[tid];
@@ -380,40 +400,50 @@ __device__ void build_permutation_small(const Cfg& c, const Ws& ws, long long T,
     ws.perm_tok[pos] = tid / k;
     ws.perm_w[pos] = w[tid];
     s_flag[pos] = (same_before % W == 0) ? 1 : 0;
+    s_flag_dn[pos] = (same_before % Wd == 0) ? 1 : 0;
   }
   if (tid < n) ws.inv[tid] = pos;
   __syncthreads();
-  // exclusive count of work-group starts before each position
-  const int f = (tid < npos) ? s_flag[tid] : 0;
-  const unsigned bal = __ballot_sync(0xffffffffu, f);
-  if (lane == 0) s_wsum[warp] = __popc(bal);
+  // exclusive counts of the work-group starts before each position
+  const unsigned bal = __ballot_sync(0xffffffffu, tid < npos && s_flag[tid]);
+  const unsigned bal_dn = __ballot_sync(0xffffffffu, tid < npos && s_flag_dn[tid]);
+  if (lane == 0) {
+    s_wsum[warp] = __popc(bal);
+    s_wsum[32 + warp] = __popc(bal_dn);
+  }
   __syncthreads();
-  int base = 0, n_routed_wg = 0;
+  int base = 0, base_dn = 0, n_routed_wg = 0, n_routed_wg_dn = 0;
   for (int q = 0; q < nw; ++q) {
     base += (q < warp) ? s_wsum[q] : 0;
+    base_dn += (q < warp) ? s_wsum[32 + q] : 0;
     n_routed_wg += s_wsum[q];
+    n_routed_wg_dn += s_wsum[32 + q];
   }
-  const int g_at = base + __popc(bal & ((1u << lane) - 1u));  // group number of position tid
+  const unsigned below = (1u << lane) - 1u;
   __syncthreads();
-  if (tid < npos) s_flag[tid] = g_at;  // now the group number of each position
-  __syncthreads();
-  if (tid < n && e >= 0 && same_before % W == 0) {
-    const int g = s_flag[pos];
-    ws.wgs[g] = WorkGroup{e, pos, min(W, cnt_e - same_before), 0};
+  if (tid < npos) {  // now the group numbers of each position
+    s_flag[tid] = base + __popc(bal & below);
+    s_flag_dn[tid] = base_dn + __popc(bal_dn & below);
   }
+  __syncthreads();
+  if (tid < n && e >= 0 && same_before % W == 0) ws.wgs[s_flag[pos]] = WorkGroup{e, pos, min(W, cnt_e - same_before), 0};
+  if (tid < n && e >= 0 && same_before % Wd == 0)
+    ws.wgs_dn[s_flag_dn[pos]] = WorkGroup{e, pos, min(Wd, cnt_e - same_before), 0};
   const long long pr = (long long)n;  // shared positions start after all routed slots
-  const int nwt = (int)((T + W - 1) / W);
-  for (int q = tid; q < c.S * nwt; q += blockDim.x) {
-    const int sh = q / nwt, i = q % nwt;
-    const long long p0 = (long long)i * W;
-    ws.wgs[n_routed_wg + q] = WorkGroup{E + sh, (int)(pr + (long long)sh * T + p0), (int)min((long long)W, T - p0), 0};
-  }
+  const int nwt = (int)((T + W - 1) / W), nwt_d = (int)((T + Wd - 1) / Wd);
+  for (int q = tid; q < c.S * nwt; q += blockDim.x)
+    write_groups(ws.wgs, n_routed_wg + q, E + q / nwt, pr + (long long)(q / nwt) * T + (long long)(q % nwt) * W,
+                 min((long long)W, T - (long long)(q % nwt) * W), W);
+  for (int q = tid; q < c.S * nwt_d; q += blockDim.x)
+    write_groups(ws.wgs_dn, n_routed_wg_dn + q, E + q / nwt_d, pr + (long long)(q / nwt_d) * T + (long long)(q % nwt_d) * Wd,
+                 min((long long)Wd, T - (long long)(q % nwt_d) * Wd), Wd);
   for (long long q = tid; q < (long long)c.S * T; q += blockDim.x) {
     ws.perm_tok[pr + q] = (int)(q % T);
     ws.perm_w[pr + q] = 1.0f;
   }
   if (tid == 0) {
     ws.ctrl[CTRL_NWG] = n_routed_wg + c.S * nwt;
+    ws.ctrl[CTRL_NWG_DN] = n_routed_wg_dn + c.S * nwt_d;
     ws.ctrl[CTRL_NPOS] = npos;
   }
   __syncthreads();
@@ -440,7 +470,7 @@ struct RouteArgs {
 // The x tile is staged only when the CTA computes logits (stage_x).
 __host__ __device__ __forceinline__ size_t route_tile_bytes(const Cfg& c, int tt, bool stage_x) {
   const size_t xt = stage_x ? (size_t)tt * c.d * (c.x_f32 ? 4 : 2) : 0;
-  const size_t perm = sizeof(int) * (4 * (size_t)c.E + 2);
+  const size_t perm = sizeof(int) * perm_ints(c.E);
   const size_t m = xt > perm ? xt : perm;
   return (m + 15) & ~(size_t)15;
 }
@@ -622,7 +652,7 @@ struct PrepArgs {
 
 // Activation planes for k3moe_expert_ffn (CTAs 1..), permutation of the given routing (CTA 0).
 __global__ void __launch_bounds__(256) k_prep(PrepArgs a) {
-  extern __shared__ int s_perm[];  // 4E + 2 ints
+  extern __shared__ int s_perm[];  // perm_ints(E) ints
   pdl_wait();
   pdl_launch_dependents();
   if (blockIdx.x == 0) {
@@ -698,11 +728,11 @@ cudaError_t launch_prep(const Cfg& c, const Ws& ws, const void* x, long long T, 
   if (ctas > 1 + 152 * 8) ctas = 1 + 152 * 8;
   if (!g_route_attr_set) {
     cudaError_t e = cudaFuncSetAttribute(k_prep, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(sizeof(int) * (4 * kMaxE + 2)));
+                                         (int)(sizeof(int) * perm_ints(kMaxE)));
     if (e != cudaSuccess) return e;
     g_route_attr_set = true;
   }
-  return launch_pdl(k_prep, dim3((unsigned)ctas), dim3(256), sizeof(int) * (4 * (size_t)c.E + 2), st, a);
+  return launch_pdl(k_prep, dim3((unsigned)ctas), dim3(256), sizeof(int) * perm_ints(c.E), st, a);
 }
 
 cudaError_t launch_rmsnorm(const float* x, long long T, int d, float eps, float* out, cudaStream_t st) {

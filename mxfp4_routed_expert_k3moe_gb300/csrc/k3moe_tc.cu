@@ -196,30 +196,6 @@ __device__ __forceinline__ bool item_geom(const TcArgs& a, long long it, long lo
   return true;
 }
 
-template <int MODE>
-__device__ __forceinline__ bool item_at(const TcArgs& a, long long it, long long n_items, Item& o) {
-  if (it >= n_items) return false;
-  const int nch = a.nch;
-  uint32_t r = (uint32_t)it;  // n_items < 2^31 (checked on the host)
-  uint32_t q = a.div_parts.div(r);
-  o.kp = (int)(r - q * a.div_parts.d);
-  r = q;
-  q = a.div_mtiles.div(r);
-  o.mt = (int)(r - q * a.div_mtiles.d);
-  r = q;
-  if (MODE == GATEUP) {
-    o.mat = (int)(r & 1u);
-    o.wgi = (int)(r >> 1);
-  } else {
-    o.mat = 0;
-    o.wgi = (int)r;
-  }
-  o.j0 = (int)a.div_parts.div((uint32_t)(o.kp * nch));
-  o.j1 = (int)a.div_parts.div((uint32_t)((o.kp + 1) * nch));
-  o.wg = a.ws.wgs[o.wgi];
-  return true;
-}
-
 // E8M0 scale bytes of the item's 128-row tile, in the device order (k3moe_pack_records): the tile's
 // 128 x K/32 bytes form groups of 512 bytes, one per 4 consecutive blocks; inside a group, the byte
 // of row 32c + i and block 4g + e sits at 16 i + 4 c + e. A group is thus the 32 x 16-byte image
@@ -271,7 +247,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   pdl_wait();  // the routing (or the gate/up results) come from the previous kernel
   pdl_launch_dependents();
-  const int n_wg = a.ws.ctrl[CTRL_NWG];
+  const int n_wg = a.ws.ctrl[MODE == GATEUP ? CTRL_NWG : CTRL_NWG_DN];
+  const WorkGroup* wgs = MODE == GATEUP ? a.ws.wgs : a.ws.wgs_dn;
   const int nmat = MODE == GATEUP ? 2 : 1;
   const int mtiles = (MODE == GATEUP ? c.f : c.d) / 128;
   const long long n_items = (long long)n_wg * nmat * mtiles * a.parts;
@@ -319,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0 && idx < n_items) {
         Item g;
         item_geom<MODE>(a, idx, n_items, g);
-        cp16(su32(&rwg[slot]), &a.ws.wgs[g.wgi]);
+        cp16(su32(&rwg[slot]), &wgs[g.wgi]);
       }
     };
     auto fetch_tok = [&](long long idx, int slot) {  // tokens of item idx's positions (its work group is in `slot`)
@@ -515,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0 && idx < n_items) {
         Item g;
         item_geom<MODE>(a, idx, n_items, g);
-        cp16(su32(&ctl->ep_wg[q][slot]), &a.ws.wgs[g.wgi]);
+        cp16(su32(&ctl->ep_wg[q][slot]), &wgs[g.wgi]);
       }
       asm volatile("cp.async.commit_group;" ::: "memory");
     };
@@ -927,7 +904,7 @@ cudaError_t launch_down(const Cfg& c, const Ws& ws, const uint8_t* routed, const
                         long long T, long long wg_max, cudaStream_t st, cudaEvent_t mid) {
   TcArgs a = base_args(c, ws, routed, shared, y, T);
   a.terms = c.hterms;
-  a.n_tile = round16(c.wgt * c.hterms);
+  a.n_tile = round16(c.wgt_dn * c.hterms);
   a.parts = 1;
   a.fp4 = c.fp4;
   a.nch = c.f / (c.fp4 ? 256 : 128);
