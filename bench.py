@@ -141,9 +141,9 @@ class ClockSampler:
 # ----------------------------------------------------------------------------- oracle (CPU baseline)
 def kernels_per_layer(T, x_dtype):
     """Kernels one layer call launches: router, gate/up (with the GLU), down, combine, plus the
-    tensor-core router GEMM and the bf16 splits of its operands from 512 tokens on."""
+    tensor-core router GEMM and the bf16 splits of its operands from 8 tokens on."""
     n = 4
-    if T >= 512:
+    if T >= 8:
         n += 2 + (1 if x_dtype == "f32" else 0)
     return n
 
