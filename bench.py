@@ -44,8 +44,8 @@ FALLBACK_HBM_GBS = 6800.0
 NCU_TRAFFIC = {
     # dram__bytes_read.sum + dram__bytes_write.sum of one launch (decode b=1: 16 routed + 2 shared
     # records, the same per launch at any expert count), profiles/k_tc_ffn_decode_b1.md
-    "k_tc<gate/up>": (213737216, "050bbdb703b59061"),
-    "k_tc<down>": (107933184, "050bbdb703b59061"),
+    "k_tc<gate/up>": (213603328, "3db708856b9ff277"),
+    "k_tc<down>": (107830016, "3db708856b9ff277"),
 }
 
 
@@ -71,9 +71,10 @@ def parse():
 
 
 def kernel_hash():
+    """Hash of the sources of the projection kernels (k_tc and what it includes)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mxfp4_routed_expert_k3moe_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in ("k3moe_tc.cu", "k3moe_ptx.cuh", "k3moe_kernels.h", "k3moe_common.cuh"):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -141,9 +142,9 @@ class ClockSampler:
 # ----------------------------------------------------------------------------- oracle (CPU baseline)
 def kernels_per_layer(T, x_dtype):
     """Kernels one layer call launches: router, gate/up (with the GLU), down, combine, plus the
-    tensor-core router GEMM and the bf16 splits of its operands from 8 tokens on."""
+    tensor-core router GEMM and the bf16 splits of its operands from 16 tokens on."""
     n = 4
-    if T >= 8:
+    if T >= 16:
         n += 2 + (1 if x_dtype == "f32" else 0)
     return n
 

@@ -33,10 +33,10 @@ cudaError_t launch_prep(const Cfg& c, const Ws& ws, const void* x, long long T, 
                         cudaStream_t st);
 cudaError_t launch_rmsnorm(const float* x, long long T, int d, float eps, float* out, cudaStream_t st);
 
-// k3moe_router_tc.cu: router logits on the tensor cores (from kRouterTcMinT tokens). `w3` is workspace
-// for the three bf16 parts of the router weights ([3, E, d]), `x3` for those of fp32 tokens ([3, T, d]);
-// the logits are written as c.rsplit partial sums ([rsplit, T, E], see Cfg).
-constexpr long long kRouterTcMinT = 8;
+// k3moe_router_tc.cu: router logits on the tensor cores (the token counts where this runs are chosen
+// in k3moe_api.cu). `w3` is workspace for the three bf16 parts of the router weights ([3, E, d]), `x3`
+// for those of fp32 tokens ([3, T, d]); the logits are written as c.rsplit partial sums ([rsplit, T, E],
+// see Cfg).
 cudaError_t launch_router_tc(const Cfg& c, const Ws& ws, const void* x, long long T, const float* W, const float* bias,
                              void* w3, void* x3, cudaStream_t st);
 cudaError_t launch_residual_add(float* x, const float* y, long long n, cudaStream_t st);

@@ -147,7 +147,7 @@ def test_layer_prefill_4096_sampled():
 
 @pytest.mark.parametrize("T,tol", [(5, 1e-6), (29, 1e-5)])
 def test_route_only(T, tol):
-    """Below 8 tokens the logits are fp32 dot products on the CUDA cores (gates to 1e-6); from 8 on
+    """Below 16 tokens the logits are fp32 dot products on the CUDA cores (gates to 1e-6); from 16 on
     they come from the tensor cores as partial sums over parts of d (gates to 1e-5, as below)."""
     L = DeviceLayer(MID, seed=10, zipf_s=1.1)
     xh, xd = L.tokens(T)
@@ -164,9 +164,9 @@ def test_route_only(T, tol):
     assert gate_err(idx.cpu().numpy(), wn, idx_ref, w_ref) < tol
 
 
-@pytest.mark.parametrize("T,x_dtype", [(8, "bf16"), (40, "f32"), (512, "bf16"), (700, "bf16"), (600, "f32")])
+@pytest.mark.parametrize("T,x_dtype", [(16, "bf16"), (40, "f32"), (512, "bf16"), (700, "bf16"), (600, "f32")])
 def test_route_tensor_core_router(T, x_dtype):
-    """From 8 tokens the logits come from the tensor cores (the fp32 router weights, and fp32 tokens,
+    """From 16 tokens the logits come from the tensor cores (the fp32 router weights, and fp32 tokens,
     in three bf16 parts; fp32 accumulation; below ~600 tokens as partial sums over parts of d): same
     selection (near-tie rule) and gates as the oracle."""
     L = DeviceLayer(MID, seed=12, zipf_s=1.1, x_dtype=x_dtype)
