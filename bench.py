@@ -320,7 +320,8 @@ def run_ours(args, rank, world, local_rank):
     dom_ms, dom_bytes = kernels[dom]
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
     traffic = None
-    if dom in NCU_TRAFFIC and NCU_TRAFFIC[dom][1] == kernel_hash():
+    # (the recorded counters are those of the decode b=1 launch; other workloads report none)
+    if args.workload == "decode_b1" and T == 1 and dom in NCU_TRAFFIC and NCU_TRAFFIC[dom][1] == kernel_hash():
         traffic = NCU_TRAFFIC[dom][0]
     ms_per_step = elapsed_ms / args.steps
     value = world * T * args.steps / (elapsed_ms * 1e-3)

@@ -35,11 +35,19 @@ __device__ __forceinline__ void xterms_block(const Cfg& c, const Ws& ws, float v
                 ws.xs + (t * c.xterms) * (c.d / 32) + j / 32, c.d / 32, lane);
 }
 
-// One warp per token: all E4M3 terms of the token (used by k3moe_expert_ffn's preparation).
+// One warp per token: all activation terms of the token (used by k3moe_expert_ffn's preparation);
+// eight blocks' elements are loaded before their terms are formed.
 __device__ void xterms_rows(const Cfg& c, const Ws& ws, const void* x, long long T, long long first, long long step) {
   const int lane = threadIdx.x & 31;
   for (long long t = first; t < T; t += step)
-    for (int j = 0; j < c.d; j += 32) xterms_block(c, ws, load_x(x, c.x_f32, t * c.d + j + lane), t, j, lane);
+    for (int j0 = 0; j0 < c.d; j0 += 8 * 32) {
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = j0 + 32 * u < c.d ? load_x(x, c.x_f32, t * c.d + j0 + 32 * u + lane) : 0.0f;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (j0 + 32 * u < c.d) xterms_block(c, ws, v[u], t, j0 + 32 * u, lane);
+    }
 }
 
 // Orderable 64-bit key: larger logit first, then lower expert id. Key 0 marks an empty entry.
@@ -97,8 +105,8 @@ __device__ unsigned long long warp_topk(unsigned long long (&key)[R], int k) {
 }
 
 // Keys of one thread for the block top-k: experts lane + 32 (warp + nw q), q < R. The logits are the
-// sums of `np` partial logits `ls` floats apart, added in part order.
-template <int R>
+// sums of `np` partial logits `ls` floats apart, added in part order, the loads of KZ parts at a time.
+template <int R, int KZ>
 __device__ __forceinline__ void load_keys(int E, const float* logits_t, long long ls, int np,
                                           unsigned long long (&key)[R]) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -108,18 +116,17 @@ __device__ __forceinline__ void load_keys(int E, const float* logits_t, long lon
     const int e = lane + 32 * (warp + nw * q);
     l[q] = (e < E) ? __ldcg(&logits_t[e]) : 0.0f;
   }
-  constexpr int kZ = 2;  // parts loaded per round (all loads of a round are in flight together)
-  for (int z0 = 1; z0 < np; z0 += kZ) {
-    float pv[kZ][R];
+  for (int z0 = 1; z0 < np; z0 += KZ) {
+    float pv[KZ][R];
 #pragma unroll
-    for (int u = 0; u < kZ; ++u)
+    for (int u = 0; u < KZ; ++u)
 #pragma unroll
       for (int q = 0; q < R; ++q) {
         const int e = lane + 32 * (warp + nw * q);
         pv[u][q] = (z0 + u < np && e < E) ? __ldcg(&logits_t[(z0 + u) * ls + e]) : 0.0f;
       }
 #pragma unroll
-    for (int u = 0; u < kZ; ++u)
+    for (int u = 0; u < KZ; ++u)
       if (z0 + u < np)
 #pragma unroll
         for (int q = 0; q < R; ++q) l[q] += pv[u][q];
@@ -140,13 +147,13 @@ __device__ __forceinline__ void load_keys(int E, const float* logits_t, long lon
 // more than k) are gathered in shared memory and each is ranked by counting the candidates above
 // it. If more candidates than threads turn up (ties at the threshold's scale, or tiny E), the
 // two-stage selection runs instead: every warp's k best, then the k best of those.
-template <int R>
+template <int R, int KZ>
 __device__ void topk_select(int E, int k, const float* logits_t, long long ls, int np, unsigned long long* cand,
                             unsigned long long* sel, unsigned long long* s_thr, int* s_n) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   const int m = (k + nw - 1) / nw;
   unsigned long long key[R];
-  load_keys<R>(E, logits_t, ls, np, key);
+  load_keys<R, KZ>(E, logits_t, ls, np, key);
   const unsigned long long mine = warp_topk<R>(key, m);  // clears the picked keys in `key`
   if (lane < m) s_thr[warp * m + lane] = mine;
   if (threadIdx.x == 0) *s_n = 0;
@@ -175,7 +182,7 @@ __device__ void topk_select(int E, int k, const float* logits_t, long long ls, i
     }
     if ((int)threadIdx.x < k && (int)threadIdx.x >= n) sel[threadIdx.x] = 0ull;  // fewer than k experts
   } else {
-    load_keys<R>(E, logits_t, ls, np, key);
+    load_keys<R, KZ>(E, logits_t, ls, np, key);
     const unsigned long long top = warp_topk<R>(key, k);
     cand[warp * 32 + lane] = (lane < k) ? top : 0ull;
     __syncthreads();
@@ -193,17 +200,18 @@ __device__ void topk_select(int E, int k, const float* logits_t, long long ls, i
 // Top-k and renormalised softmax gates of one token, by the whole CTA (2 to 8 warps), from `np` partial
 // logits `ls` floats apart. `cand` is shared memory for blockDim.x keys. Ends with __syncthreads.
 // `idx_sm` / `w_sm` (shared memory, or NULL) receive a copy of the selection for the permutation.
+template <int KZ>
 __device__ void topk_block(int E, int k, const float* logits_t, long long ls, int np, unsigned long long* cand,
                            int* idx_out, float* w_out, int* idx_user, float* w_user, int* idx_sm, float* w_sm) {
   __shared__ unsigned long long s_sel[32], s_thr[64];
   __shared__ int s_n;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   const int per_lane = (E + 32 * nw - 1) / (32 * nw);
-  if (per_lane <= 1) topk_select<1>(E, k, logits_t, ls, np, cand, s_sel, s_thr, &s_n);
-  else if (per_lane <= 2) topk_select<2>(E, k, logits_t, ls, np, cand, s_sel, s_thr, &s_n);
-  else if (per_lane <= 4) topk_select<4>(E, k, logits_t, ls, np, cand, s_sel, s_thr, &s_n);
-  else if (per_lane <= 8) topk_select<8>(E, k, logits_t, ls, np, cand, s_sel, s_thr, &s_n);
-  else topk_select<16>(E, k, logits_t, ls, np, cand, s_sel, s_thr, &s_n);  // E <= 4096 with 8 warps
+  if (per_lane <= 1) topk_select<1, KZ>(E, k, logits_t, ls, np, cand, s_sel, s_thr, &s_n);
+  else if (per_lane <= 2) topk_select<2, KZ>(E, k, logits_t, ls, np, cand, s_sel, s_thr, &s_n);
+  else if (per_lane <= 4) topk_select<4, KZ>(E, k, logits_t, ls, np, cand, s_sel, s_thr, &s_n);
+  else if (per_lane <= 8) topk_select<8, KZ>(E, k, logits_t, ls, np, cand, s_sel, s_thr, &s_n);
+  else topk_select<16, KZ>(E, k, logits_t, ls, np, cand, s_sel, s_thr, &s_n);  // E <= 4096 with 8 warps
   if (warp == 0) {
     const unsigned long long best = (lane < k) ? s_sel[lane] : 0ull;
     const int my_e = key_expert(best);
@@ -489,7 +497,9 @@ __global__ void __launch_bounds__(256, 3) k_route(RouteArgs a) {
   const Cfg& c = a.c;
   const int nw = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = warp >> 2, kq = warp & 3;
-  const bool dots = !(a.mode & RM_LOGITS_READY);  // else the logits were computed by the tensor cores
+  // (launch_route gives precomputed logits to k_select; the mode flag is kept here, where the compiled
+  // form of the dot-product path measured best, without spills)
+  const bool dots = !(a.mode & RM_LOGITS_READY);
   const int e = dots ? blockIdx.x * 2 + r : c.E;
   const long long t0 = (long long)blockIdx.y * TT;
   const int ntt = (int)min((long long)TT, a.T - t0);
@@ -615,7 +625,7 @@ __global__ void __launch_bounds__(256, 3) k_route(RouteArgs a) {
   const bool tile_sm = gridDim.y == 1 && (long long)ntt * c.k <= (long long)blockDim.x && ntt * c.k <= 8 * 32;
   for (int tt = 0; tt < ntt; ++tt) {
     const long long t = t0 + tt;
-    topk_block(c.E, c.k, a.ws.logits + t * c.E, a.T * c.E, dots ? 1 : c.rsplit, cand, a.ws.topk_idx + t * c.k,
+    topk_block<2>(c.E, c.k, a.ws.logits + t * c.E, a.T * c.E, dots ? 1 : c.rsplit, cand, a.ws.topk_idx + t * c.k,
                a.ws.topk_w + t * c.k,
                (a.mode & RM_USER_OUT) && a.out_idx ? a.out_idx + t * c.k : nullptr,
                (a.mode & RM_USER_OUT) && a.out_w ? a.out_w + t * c.k : nullptr, tile_sm ? s_tk_idx + tt * c.k : nullptr,
@@ -686,7 +696,75 @@ __global__ void k_residual_add(float* x, const float* y, long long n) {
     x[i] += y[i];
 }
 
+// Selection with logits computed by the tensor cores (k_router_mma): grid (G, T). CTA (0, t) selects
+// token t's top-k from the partial logits (added in part order) and the last of these CTAs builds the
+// permutation; token t's activation terms are formed by CTAs (1 .. G-1, t), sharing its 32-blocks, or
+// with G = 1 by CTA (0, t) first. G by token count (router phase, K3 shape): 5 below 256 tokens (one
+// CTA per token spent ~18 us on the terms at 64 tokens, its warps taking 28 blocks in turn each), 2
+// below 1024 (512 tokens: 112 us against 133 with G = 1), 1 from 1024 (4096 tokens: 557 us against
+// 594 with G = 2 and 638 with G = 5).
+__host__ __forceinline__ unsigned select_ctas(long long T) { return T < 256 ? 5u : (T < 1024 ? 2u : 1u); }
+// KZ: partial logits loaded per round; MINB: CTAs per SM the registers are sized for (with one part,
+// three CTAs per SM; with several, two, whose registers hold four parts' loads without spilling).
+template <int KZ, int MINB>
+__global__ void __launch_bounds__(256, MINB) k_select(RouteArgs a) {
+  extern __shared__ __align__(16) uint8_t smem[];  // [x row | permutation scratch][top-k candidates]
+  __shared__ int s_last;
+  const Cfg& c = a.c;
+  const int nw = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long t = blockIdx.y;
+  pdl_wait();
+  pdl_launch_dependents();
+  const int tc0 = gridDim.x > 1 ? 1 : 0;  // first term-forming CTA
+  if (blockIdx.x >= tc0 && (a.mode & RM_XPREP)) {
+    const int esz = c.x_f32 ? 4 : 2;
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(a.x) + t * c.d * esz;
+    const uint32_t dst = (uint32_t)__cvta_generic_to_shared(smem);
+    for (int off = threadIdx.x * 16; off < c.d * esz; off += blockDim.x * 16)
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + off), "l"(src + off) : "memory");
+    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
+    const int n = (int)gridDim.x - tc0;
+    for (int blk = ((int)blockIdx.x - tc0) * nw + warp; blk * 32 < c.d; blk += n * nw) {
+      const int j = blk * 32;
+      const float v = c.x_f32 ? reinterpret_cast<const float*>(smem)[j + lane]
+                              : __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(smem)[j + lane] << 16);
+      xterms_block(c, a.ws, v, t, j, lane);
+    }
+    __syncthreads();  // (with G = 1 the x row's shared memory is reused below)
+  }
+  if (blockIdx.x > 0) return;
+  unsigned long long* cand = reinterpret_cast<unsigned long long*>(smem + route_tile_bytes(c, 1, true));
+  topk_block<KZ>(c.E, c.k, a.ws.logits + t * c.E, a.T * c.E, c.rsplit, cand, a.ws.topk_idx + t * c.k,
+                a.ws.topk_w + t * c.k, (a.mode & RM_USER_OUT) && a.out_idx ? a.out_idx + t * c.k : nullptr,
+                (a.mode & RM_USER_OUT) && a.out_w ? a.out_w + t * c.k : nullptr, nullptr, nullptr);
+  // the last selecting CTA builds the permutation
+  if (threadIdx.x < 32) __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int prev = atomicAdd(&a.ws.ctrl[CTRL_ROUTER_DONE], 1);
+    s_last = (prev == (int)gridDim.y - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (threadIdx.x == 0) a.ws.ctrl[CTRL_ROUTER_DONE] = 0;
+  if (a.mode & RM_PERMUTE) permute(c, a.ws, a.T, a.ws.topk_idx, a.ws.topk_w, reinterpret_cast<int*>(smem));
+}
+
 bool g_route_attr_set = false;
+template <int KZ, int MINB>
+cudaError_t launch_select(const RouteArgs& a, cudaStream_t st) {
+  const size_t smem = route_tile_bytes(a.c, 1, true) + sizeof(unsigned long long) * 256;
+  if (smem > (size_t)kRouteMaxSmem) return cudaErrorInvalidValue;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(k_select<KZ, MINB>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRouteMaxSmem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  return launch_pdl(k_select<KZ, MINB>, dim3(select_ctas(a.T), (unsigned)a.T), dim3(256), smem, st, a);
+}
 
 }  // namespace
 
@@ -713,8 +791,8 @@ cudaError_t launch_route(const Cfg& c, const Ws& ws, const void* x, long long T,
     return route_tile_bytes(c, tt, !(mode & RM_LOGITS_READY)) + sizeof(unsigned long long) * 32 * warps <=
            (size_t)kRouteMaxSmem;
   };
-  // with precomputed logits every token has its own CTA (its top-k is the CTA's only serial work)
-  if (mode & RM_LOGITS_READY) return launch_route_tt<1>(a, 8, st);
+  if (mode & RM_LOGITS_READY)  // selection and activation terms from the tensor cores' partial logits
+    return c.rsplit > 1 ? launch_select<4, 2>(a, st) : launch_select<1, 3>(a, st);
   if (T >= 8 && fits(8, 8)) return launch_route_tt<8>(a, 8, st);
   if (T >= 4 && fits(4, 8)) return launch_route_tt<4>(a, 8, st);
   if (T >= 2 && fits(2, 8)) return launch_route_tt<2>(a, 8, st);

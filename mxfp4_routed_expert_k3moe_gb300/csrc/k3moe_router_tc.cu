@@ -64,19 +64,25 @@ __device__ __forceinline__ bool rwait(uint32_t bar, uint32_t parity, RCtl* ctl, 
 __constant__ int kPairA[6] = {0, 0, 0, 1, 1, 2};
 __constant__ int kPairB[6] = {0, 1, 2, 0, 1, 0};
 
-// W3[p][i], p = 0, 1, 2: the three bf16 parts of W[i] (router weights or fp32 tokens).
+// W3[p][i], p = 0, 1, 2: the three bf16 parts of W[i] (router weights or fp32 tokens); n a multiple of
+// 4, W 16-byte aligned: four elements per thread and step (one 16-byte load, three 8-byte stores).
 __global__ void __launch_bounds__(256) k_split_w(const float* W, long long n, __nv_bfloat16* w3) {
   pdl_wait();
   pdl_launch_dependents();
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
-    const float w = W[i];
-    const __nv_bfloat16 hi = __float2bfloat16_rn(w);
-    const float r1 = w - __bfloat162float(hi);
-    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
-    const float r2 = r1 - __bfloat162float(mid);
-    w3[i] = hi;
-    w3[n + i] = mid;
-    w3[2 * n + i] = __float2bfloat16_rn(r2);
+  for (long long i = 4 * ((long long)blockIdx.x * blockDim.x + threadIdx.x); i < n;
+       i += 4LL * gridDim.x * blockDim.x) {
+    const float4 w4 = __ldcs(reinterpret_cast<const float4*>(W + i));
+    const float w[4] = {w4.x, w4.y, w4.z, w4.w};
+    __nv_bfloat16 p[3][4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      p[0][u] = __float2bfloat16_rn(w[u]);
+      const float r1 = w[u] - __bfloat162float(p[0][u]);
+      p[1][u] = __float2bfloat16_rn(r1);
+      p[2][u] = __float2bfloat16_rn(r1 - __bfloat162float(p[1][u]));
+    }
+#pragma unroll
+    for (int q = 0; q < 3; ++q) *reinterpret_cast<uint2*>(w3 + q * n + i) = *reinterpret_cast<const uint2*>(p[q]);
   }
 }
 
@@ -144,22 +150,33 @@ __global__ void __launch_bounds__(kRThreads, 1)
     }
   }
   __syncwarp();
-  // epilogue: lane = token, 32 expert columns per load
-  const bool have = __all_sync(0xffffffffu, rwait(su32(&ctl->done), 0, ctl, status));
+  // epilogue: the accumulator (lane = token, column = expert) goes through shared memory, whose stages
+  // are free once every MMA completed (rows of kRN + 1 floats: conflict-free both ways), and each warp
+  // then stores whole rows of logits (a thread per accumulator row stored 32 scattered rows per
+  // instruction)
+  const bool have = __syncthreads_and(__all_sync(0xffffffffu, rwait(su32(&ctl->done), 0, ctl, status)));
   tc_fence_after();
+  float* tile = reinterpret_cast<float*>(smem);
   if (have) {
-    const long long t = (long long)mt * kRM + 32 * warp + lane;
+    const int r = 32 * warp + lane;
     for (int c0 = 0; c0 < kRN; c0 += 32) {
       uint32_t v[32];
       tc_ld32(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)c0, v);
       tc_wait_ld();
-      const int e0 = nt * kRN + c0;
-      if (t < T) {
-        float* dst = logits + (long long)z * T * E + t * E + e0;
-        const bool addb = bias && z == 0;
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (e0 + j < E) dst[j] = __uint_as_float(v[j]) + (addb ? __ldg(&bias[e0 + j]) : 0.0f);
+      for (int j = 0; j < 32; ++j) tile[r * (kRN + 1) + c0 + j] = __uint_as_float(v[j]);
+    }
+  }
+  __syncthreads();
+  if (have) {
+    const bool addb = bias && z == 0;
+    for (int rr = warp; rr < kRM; rr += kRThreads / 32) {
+      const long long t = (long long)mt * kRM + rr;
+      if (t >= T) break;
+      float* dst = logits + (long long)z * T * E + t * E + (long long)nt * kRN;
+      for (int cc = lane; cc < kRN; cc += 32) {
+        const int e = nt * kRN + cc;
+        if (e < E) dst[cc] = tile[rr * (kRN + 1) + cc] + (addb ? __ldg(&bias[e]) : 0.0f);
       }
     }
   }

@@ -164,7 +164,7 @@ def test_route_only(T, tol):
     assert gate_err(idx.cpu().numpy(), wn, idx_ref, w_ref) < tol
 
 
-@pytest.mark.parametrize("T,x_dtype", [(16, "bf16"), (40, "f32"), (512, "bf16"), (700, "bf16"), (600, "f32")])
+@pytest.mark.parametrize("T,x_dtype", [(16, "bf16"), (40, "f32"), (512, "bf16"), (700, "bf16"), (600, "f32"), (1100, "bf16")])
 def test_route_tensor_core_router(T, x_dtype):
     """From 16 tokens the logits come from the tensor cores (the fp32 router weights, and fp32 tokens,
     in three bf16 parts; fp32 accumulation; below ~600 tokens as partial sums over parts of d): same
@@ -190,6 +190,12 @@ def test_layer_mid_large_T_sampled():
     """The whole layer at 700 tokens: tensor-core router, E4M3 activation terms."""
     L = DeviceLayer(MID, seed=13)
     check_layer(L, 700, sample=[0, 5, 333, 512, 699])
+
+
+def test_layer_mid_1100_tokens_sampled():
+    """From 1024 tokens each token's selecting CTA also forms its activation terms."""
+    L = DeviceLayer(MID, seed=15)
+    check_layer(L, 1100, sample=[0, 1, 640, 1023, 1099])
 
 
 def test_expert_ffn_given_routing():
