@@ -609,7 +609,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------------------- combine
 // y[t] = sum over the top-k slots of t (in slot order) of the gate-weighted expert outputs, then the
-// shared experts; one thread per (token, row of d_model).
+// shared experts; one thread per (token, row of d_model). BATCH (few tokens, where the kernel is one
+// chain of dependent loads): a thread issues all its loads before the sums, in two rounds (the slots'
+// positions, then their gate weights and outputs), and adds in the same order; measured 0.9 us
+// faster per layer at one token, but its registers halve the occupancy, which made it slower from
+// 64 tokens on (4096 tokens: 0.33 ms).
+constexpr int kCombMaxK = 32, kCombMaxS = 8;  // top_k <= 32, n_shared <= 8 (checked by the API)
+constexpr long long kCombBatchMaxT = 2;
+template <bool BATCH>
 __global__ void __launch_bounds__(256) k_combine(Cfg c, Ws ws, float* y, long long T) {
   pdl_wait();
   pdl_launch_dependents();
@@ -618,12 +625,39 @@ __global__ void __launch_bounds__(256) k_combine(Cfg c, Ws ws, float* y, long lo
        idx += (long long)gridDim.x * blockDim.x) {
     const long long tok = idx / c.d;
     const int row = (int)(idx - tok * c.d);
-    float s = 0.0f;
-    for (int i = 0; i < c.k; ++i) {
-      const int p = ws.inv[tok * c.k + i];
-      if (p >= 0) s += ws.perm_w[p] * ws.part[(long long)p * c.d + row];
+    if (!BATCH) {
+      float s = 0.0f;
+      for (int i = 0; i < c.k; ++i) {
+        const int p = ws.inv[tok * c.k + i];
+        if (p >= 0) s += ws.perm_w[p] * ws.part[(long long)p * c.d + row];
+      }
+      for (int sh = 0; sh < c.S; ++sh) s += ws.part[(P_R + (long long)sh * T + tok) * c.d + row];
+      y[idx] = s;
+      continue;
     }
-    for (int sh = 0; sh < c.S; ++sh) s += ws.part[(P_R + (long long)sh * T + tok) * c.d + row];
+    int p[kCombMaxK];
+#pragma unroll
+    for (int i = 0; i < kCombMaxK; ++i) p[i] = i < c.k ? __ldcg(&ws.inv[tok * c.k + i]) : -1;
+    float w[kCombMaxK], o[kCombMaxK], so[kCombMaxS];
+#pragma unroll
+    for (int i = 0; i < kCombMaxK; ++i) {
+      w[i] = 0.0f;
+      o[i] = 0.0f;
+      if (p[i] >= 0) {
+        w[i] = __ldcg(&ws.perm_w[p[i]]);
+        o[i] = __ldcg(&ws.part[(long long)p[i] * c.d + row]);
+      }
+    }
+#pragma unroll
+    for (int sh = 0; sh < kCombMaxS; ++sh)
+      so[sh] = sh < c.S ? __ldcg(&ws.part[(P_R + (long long)sh * T + tok) * c.d + row]) : 0.0f;
+    float s = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kCombMaxK; ++i)
+      if (p[i] >= 0) s += w[i] * o[i];
+#pragma unroll
+    for (int sh = 0; sh < kCombMaxS; ++sh)
+      if (sh < c.S) s += so[sh];
     y[idx] = s;
   }
 }
@@ -918,7 +952,8 @@ cudaError_t launch_down(const Cfg& c, const Ws& ws, const uint8_t* routed, const
   if (e != cudaSuccess) return e;
   long long blocks = (T * c.d + 255) / 256;
   if (blocks > 8LL * g_sms) blocks = 8LL * g_sms;
-  return launch_pdl(k_combine, dim3((unsigned)blocks), dim3(256), 0, st, c, ws, y, T);
+  if (T <= kCombBatchMaxT) return launch_pdl(k_combine<true>, dim3((unsigned)blocks), dim3(256), 0, st, c, ws, y, T);
+  return launch_pdl(k_combine<false>, dim3((unsigned)blocks), dim3(256), 0, st, c, ws, y, T);
 }
 
 cudaError_t launch_pack_records(uint8_t* records, long long n_rec, long long stride, int d, int f, int to_device,
