@@ -44,8 +44,8 @@ FALLBACK_HBM_GBS = 6800.0
 NCU_TRAFFIC = {
     # dram__bytes_read.sum + dram__bytes_write.sum of one launch (decode b=1: 16 routed + 2 shared
     # records, the same per launch at any expert count), profiles/k_tc_ffn_decode_b1.md
-    "k_tc<gate/up>": (213603328, "3db708856b9ff277"),
-    "k_tc<down>": (107830016, "3db708856b9ff277"),
+    "k_tc<gate/up>": (213776128, "010f64675472a078"),
+    "k_tc<down>": (107876352, "010f64675472a078"),
 }
 
 
