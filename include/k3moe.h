@@ -68,7 +68,8 @@ typedef enum {
   K3MOE_ERR_TIMEOUT = 6
 } k3moe_status;
 
-/* Router score function. Only the softmax score is implemented. */
+/* Router score function: softmax over the logits (the bias, if given, is added to the logits), or
+   sigmoid of the unbiased logit with a selection-only bias (see k3moe_route). */
 enum { K3MOE_SCORE_SOFTMAX = 0, K3MOE_SCORE_SIGMOID_BIAS = 1 };
 /* Legal but not implemented: d_model > 25600 (the router stages whole rows in shared memory). */
 /* Activation handling in the expert FFN. Only the exact mode is implemented: activations keep
@@ -120,12 +121,15 @@ K3MOE_API size_t k3moe_workspace_bytes(const k3moe_config* cfg /* host */, int64
 
 /*
  * Router: softmax over the n_routed logits of each token, top-k, renormalised gates.
- * (The review's list of header invariants describes a sigmoid score whose bias changes only
- * the selection; that score is K3MOE_SCORE_SIGMOID_BIAS and returns K3MOE_ERR_UNSUPPORTED.)
+ * With score_func K3MOE_SCORE_SIGMOID_BIAS (the review's list of public-header invariants: the
+ * routing bias skews only the selection, the combine weights come from the unbiased sigmoid score):
+ * s_e = sigmoid(x . W_e), the k largest s_e + b_e are selected (equal values -> lower index first),
+ * and the gates are s_e / sum over the selected of s.
  *   x        [T, d_model] bf16 or fp32 (cfg->x_dtype), row-major
  *   w_router [n_routed, d_model] fp32, row-major
- *   bias     [n_routed] fp32 added to every logit before selection and softmax, or NULL
- *   topk_idx [T, top_k] int32 out: expert ids, descending logit, ties to the lower id
+ *   bias     [n_routed] fp32, or NULL: softmax score: added to every logit before selection and
+ *            softmax; sigmoid score: added to the sigmoid scores for the selection only
+ *   topk_idx [T, top_k] int32 out: expert ids, descending ranked value, ties to the lower id
  *   topk_w   [T, top_k] fp32 out: gates, summing to 1 per token
  */
 K3MOE_API k3moe_status k3moe_route(const k3moe_config* cfg /* host */, const void* x, int64_t T,

@@ -66,7 +66,7 @@ k3moe_status validate(const k3moe_config* c) {
   if (c->x_dtype != K3MOE_X_BF16 && c->x_dtype != K3MOE_X_F32) return K3MOE_ERR_INVALID_ARGUMENT;
   if (c->record_stride < record_bytes_of(c) || c->record_stride % 256) return K3MOE_ERR_INVALID_ARGUMENT;
   if ((long long)c->d_model * c->d_ff > (1LL << 40)) return K3MOE_ERR_INVALID_ARGUMENT;
-  if (c->score_func != K3MOE_SCORE_SOFTMAX || c->act_mode != K3MOE_ACT_EXACT) return K3MOE_ERR_UNSUPPORTED;
+  if (c->act_mode != K3MOE_ACT_EXACT) return K3MOE_ERR_UNSUPPORTED;
   if (c->d_model > kMaxDModel) return K3MOE_ERR_UNSUPPORTED;  // router rows are staged in shared memory
   return K3MOE_OK;
 }
@@ -180,6 +180,7 @@ Cfg make_cfg(const k3moe_config* c, long long T) {
     k.hterms = 3;
   }
   k.rsplit = (int)router_splits(c, T);
+  k.sigmoid = c->score_func == K3MOE_SCORE_SIGMOID_BIAS ? 1 : 0;
   k.stride = c->record_stride;
   return k;
 }

@@ -106,9 +106,13 @@ __device__ unsigned long long warp_topk(unsigned long long (&key)[R], int k) {
 
 // Keys of one thread for the block top-k: experts lane + 32 (warp + nw q), q < R. The logits are the
 // sums of `np` partial logits `ls` floats apart, added in part order, the loads of KZ parts at a time.
-template <int R, int KZ>
+__device__ __forceinline__ float sigmoid_score(float l) { return 1.0f / (1.0f + expf(-l)); }
+
+// The value an expert is ranked by: its logit (softmax score), or with the sigmoid score (SIG)
+// sigmoid(logit) + its selection bias (sel_bias, or none if NULL).
+template <int R, int KZ, bool SIG>
 __device__ __forceinline__ void load_keys(int E, const float* logits_t, long long ls, int np,
-                                          unsigned long long (&key)[R]) {
+                                          const float* sel_bias, unsigned long long (&key)[R]) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   float l[R];
 #pragma unroll
@@ -134,7 +138,9 @@ __device__ __forceinline__ void load_keys(int E, const float* logits_t, long lon
 #pragma unroll
   for (int q = 0; q < R; ++q) {
     const int e = lane + 32 * (warp + nw * q);
-    key[q] = (e < E) ? topk_key(l[q], e) : 0ull;
+    float v = l[q];
+    if (SIG && e < E) v = sigmoid_score(v) + (sel_bias ? __ldg(&sel_bias[e]) : 0.0f);
+    key[q] = (e < E) ? topk_key(v, e) : 0ull;
   }
 }
 
@@ -147,13 +153,13 @@ __device__ __forceinline__ void load_keys(int E, const float* logits_t, long lon
 // more than k) are gathered in shared memory and each is ranked by counting the candidates above
 // it. If more candidates than threads turn up (ties at the threshold's scale, or tiny E), the
 // two-stage selection runs instead: every warp's k best, then the k best of those.
-template <int R, int KZ>
-__device__ void topk_select(int E, int k, const float* logits_t, long long ls, int np, unsigned long long* cand,
-                            unsigned long long* sel, unsigned long long* s_thr, int* s_n) {
+template <int R, int KZ, bool SIG>
+__device__ void topk_select(int E, int k, const float* logits_t, long long ls, int np, const float* sel_bias,
+                            unsigned long long* cand, unsigned long long* sel, unsigned long long* s_thr, int* s_n) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   const int m = (k + nw - 1) / nw;
   unsigned long long key[R];
-  load_keys<R, KZ>(E, logits_t, ls, np, key);
+  load_keys<R, KZ, SIG>(E, logits_t, ls, np, sel_bias, key);
   const unsigned long long mine = warp_topk<R>(key, m);  // clears the picked keys in `key`
   if (lane < m) s_thr[warp * m + lane] = mine;
   if (threadIdx.x == 0) *s_n = 0;
@@ -182,7 +188,7 @@ __device__ void topk_select(int E, int k, const float* logits_t, long long ls, i
     }
     if ((int)threadIdx.x < k && (int)threadIdx.x >= n) sel[threadIdx.x] = 0ull;  // fewer than k experts
   } else {
-    load_keys<R, KZ>(E, logits_t, ls, np, key);
+    load_keys<R, KZ, SIG>(E, logits_t, ls, np, sel_bias, key);
     const unsigned long long top = warp_topk<R>(key, k);
     cand[warp * 32 + lane] = (lane < k) ? top : 0ull;
     __syncthreads();
@@ -197,27 +203,42 @@ __device__ void topk_select(int E, int k, const float* logits_t, long long ls, i
   __syncthreads();
 }
 
-// Top-k and renormalised softmax gates of one token, by the whole CTA (2 to 8 warps), from `np` partial
-// logits `ls` floats apart. `cand` is shared memory for blockDim.x keys. Ends with __syncthreads.
+// Top-k and gates of one token, by the whole CTA (2 to 8 warps), from `np` partial logits `ls` floats
+// apart. Softmax score (SIG false): ranked by logit, gates = softmax over the selected logits. Sigmoid
+// score (kimi-k3-in-c review, list of public-header invariants: the routing bias skews only the
+// selection, the combine weights come from the unbiased sigmoid): ranked by sigmoid(logit) + sel_bias,
+// gates = the selected sigmoid scores renormalised. `cand` is shared memory for blockDim.x keys. Ends
+// with __syncthreads.
 // `idx_sm` / `w_sm` (shared memory, or NULL) receive a copy of the selection for the permutation.
-template <int KZ>
-__device__ void topk_block(int E, int k, const float* logits_t, long long ls, int np, unsigned long long* cand,
-                           int* idx_out, float* w_out, int* idx_user, float* w_user, int* idx_sm, float* w_sm) {
+template <int KZ, bool SIG>
+__device__ void topk_block(int E, int k, const float* logits_t, long long ls, int np, const float* sel_bias,
+                           unsigned long long* cand, int* idx_out, float* w_out, int* idx_user, float* w_user,
+                           int* idx_sm, float* w_sm) {
   __shared__ unsigned long long s_sel[32], s_thr[64];
   __shared__ int s_n;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   const int per_lane = (E + 32 * nw - 1) / (32 * nw);
-  if (per_lane <= 1) topk_select<1, KZ>(E, k, logits_t, ls, np, cand, s_sel, s_thr, &s_n);
-  else if (per_lane <= 2) topk_select<2, KZ>(E, k, logits_t, ls, np, cand, s_sel, s_thr, &s_n);
-  else if (per_lane <= 4) topk_select<4, KZ>(E, k, logits_t, ls, np, cand, s_sel, s_thr, &s_n);
-  else if (per_lane <= 8) topk_select<8, KZ>(E, k, logits_t, ls, np, cand, s_sel, s_thr, &s_n);
-  else topk_select<16, KZ>(E, k, logits_t, ls, np, cand, s_sel, s_thr, &s_n);  // E <= 4096 with 8 warps
+  if (per_lane <= 1) topk_select<1, KZ, SIG>(E, k, logits_t, ls, np, sel_bias, cand, s_sel, s_thr, &s_n);
+  else if (per_lane <= 2) topk_select<2, KZ, SIG>(E, k, logits_t, ls, np, sel_bias, cand, s_sel, s_thr, &s_n);
+  else if (per_lane <= 4) topk_select<4, KZ, SIG>(E, k, logits_t, ls, np, sel_bias, cand, s_sel, s_thr, &s_n);
+  else if (per_lane <= 8) topk_select<8, KZ, SIG>(E, k, logits_t, ls, np, sel_bias, cand, s_sel, s_thr, &s_n);
+  else topk_select<16, KZ, SIG>(E, k, logits_t, ls, np, sel_bias, cand, s_sel, s_thr, &s_n);  // E <= 4096 with 8 warps
   if (warp == 0) {
     const unsigned long long best = (lane < k) ? s_sel[lane] : 0ull;
     const int my_e = key_expert(best);
-    const float my_l = (lane < k) ? key_logit(best) : 0.0f;  // the key holds the logit's bits
-    const float lmax = __shfl_sync(0xffffffffu, my_l, 0);
-    const float ex = (lane < k) ? expf(my_l - lmax) : 0.0f;
+    float ex;
+    if (SIG) {  // the unbiased score of the selected expert: its logit again, parts added in order
+      float l = 0.0f;
+      if (lane < k) {
+        l = __ldcg(&logits_t[my_e]);
+        for (int z = 1; z < np; ++z) l += __ldcg(&logits_t[z * ls + my_e]);
+      }
+      ex = (lane < k) ? sigmoid_score(l) : 0.0f;
+    } else {
+      const float my_l = (lane < k) ? key_logit(best) : 0.0f;  // the key holds the logit's bits
+      const float lmax = __shfl_sync(0xffffffffu, my_l, 0);
+      ex = (lane < k) ? expf(my_l - lmax) : 0.0f;
+    }
     float sum = ex;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
@@ -487,7 +508,8 @@ __host__ __device__ __forceinline__ size_t route_tile_bytes(const Cfg& c, int tt
 // each), so that every warp issues all router-weight loads of its quarter at once (the weights are
 // read once and stream; the latency of one batch is paid, not four). The token tile of x is staged
 // in shared memory meanwhile. Warps also produce the E4M3 terms of x, one 32-element block each.
-template <int TT>
+// SIG: the sigmoid score (c.sigmoid), selected at launch.
+template <int TT, bool SIG>
 __global__ void __launch_bounds__(256, 3) k_route(RouteArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ int s_last;
@@ -590,7 +612,7 @@ __global__ void __launch_bounds__(256, 3) k_route(RouteArgs a) {
     const int er = blockIdx.x * 2 + rr;
     if (dots && er < c.E && tt < ntt) {
       const float v = ((s_part[4 * rr][tt] + s_part[4 * rr + 1][tt]) + s_part[4 * rr + 2][tt]) + s_part[4 * rr + 3][tt];
-      a.ws.logits[(t0 + tt) * c.E + er] = v + (a.bias ? a.bias[er] : 0.0f);
+      a.ws.logits[(t0 + tt) * c.E + er] = v + (a.bias && !SIG ? a.bias[er] : 0.0f);  // (sigmoid: bias at selection)
     }
   }
   // E4M3 terms of x: warp gw of the grid takes the 32-element blocks gw, gw + 8 * gridDim.x, ...
@@ -625,7 +647,8 @@ __global__ void __launch_bounds__(256, 3) k_route(RouteArgs a) {
   const bool tile_sm = gridDim.y == 1 && (long long)ntt * c.k <= (long long)blockDim.x && ntt * c.k <= 8 * 32;
   for (int tt = 0; tt < ntt; ++tt) {
     const long long t = t0 + tt;
-    topk_block<2>(c.E, c.k, a.ws.logits + t * c.E, a.T * c.E, dots ? 1 : c.rsplit, cand, a.ws.topk_idx + t * c.k,
+    topk_block<2, SIG>(c.E, c.k, a.ws.logits + t * c.E, a.T * c.E, dots ? 1 : c.rsplit, SIG ? a.bias : nullptr,
+                       cand, a.ws.topk_idx + t * c.k,
                a.ws.topk_w + t * c.k,
                (a.mode & RM_USER_OUT) && a.out_idx ? a.out_idx + t * c.k : nullptr,
                (a.mode & RM_USER_OUT) && a.out_w ? a.out_w + t * c.k : nullptr, tile_sm ? s_tk_idx + tt * c.k : nullptr,
@@ -706,7 +729,7 @@ __global__ void k_residual_add(float* x, const float* y, long long n) {
 __host__ __forceinline__ unsigned select_ctas(long long T) { return T < 256 ? 5u : (T < 1024 ? 2u : 1u); }
 // KZ: partial logits loaded per round; MINB: CTAs per SM the registers are sized for (with one part,
 // three CTAs per SM; with several, two, whose registers hold four parts' loads without spilling).
-template <int KZ, int MINB>
+template <int KZ, int MINB, bool SIG>
 __global__ void __launch_bounds__(256, MINB) k_select(RouteArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];  // [x row | permutation scratch][top-k candidates]
   __shared__ int s_last;
@@ -735,7 +758,8 @@ __global__ void __launch_bounds__(256, MINB) k_select(RouteArgs a) {
   }
   if (blockIdx.x > 0) return;
   unsigned long long* cand = reinterpret_cast<unsigned long long*>(smem + route_tile_bytes(c, 1, true));
-  topk_block<KZ>(c.E, c.k, a.ws.logits + t * c.E, a.T * c.E, c.rsplit, cand, a.ws.topk_idx + t * c.k,
+  topk_block<KZ, SIG>(c.E, c.k, a.ws.logits + t * c.E, a.T * c.E, c.rsplit, SIG ? a.bias : nullptr,
+                      cand, a.ws.topk_idx + t * c.k,
                 a.ws.topk_w + t * c.k, (a.mode & RM_USER_OUT) && a.out_idx ? a.out_idx + t * c.k : nullptr,
                 (a.mode & RM_USER_OUT) && a.out_w ? a.out_w + t * c.k : nullptr, nullptr, nullptr);
   // the last selecting CTA builds the permutation
@@ -753,34 +777,39 @@ __global__ void __launch_bounds__(256, MINB) k_select(RouteArgs a) {
 }
 
 bool g_route_attr_set = false;
-template <int KZ, int MINB>
+template <int KZ, int MINB, bool SIG>
 cudaError_t launch_select(const RouteArgs& a, cudaStream_t st) {
   const size_t smem = route_tile_bytes(a.c, 1, true) + sizeof(unsigned long long) * 256;
   if (smem > (size_t)kRouteMaxSmem) return cudaErrorInvalidValue;
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_select<KZ, MINB>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRouteMaxSmem);
+    cudaError_t e = cudaFuncSetAttribute(k_select<KZ, MINB, SIG>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRouteMaxSmem);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  return launch_pdl(k_select<KZ, MINB>, dim3(select_ctas(a.T), (unsigned)a.T), dim3(256), smem, st, a);
+  return launch_pdl(k_select<KZ, MINB, SIG>, dim3(select_ctas(a.T), (unsigned)a.T), dim3(256), smem, st, a);
 }
 
 }  // namespace
 
-template <int TT>
-cudaError_t launch_route_tt(const RouteArgs& a, int warps, cudaStream_t st) {
+template <int TT, bool SIG>
+cudaError_t launch_route_tt2(const RouteArgs& a, int warps, cudaStream_t st) {
   const size_t smem = route_tile_bytes(a.c, TT, !(a.mode & RM_LOGITS_READY)) + sizeof(unsigned long long) * 32 * warps;
   if (smem > (size_t)kRouteMaxSmem) return cudaErrorInvalidValue;
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_route<TT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRouteMaxSmem);
+    cudaError_t e = cudaFuncSetAttribute(k_route<TT, SIG>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRouteMaxSmem);
     if (e != cudaSuccess) return e;
     attr = true;
   }
   // with precomputed logits one CTA per token tile selects, writes the activation terms and permutes
   dim3 grid((a.mode & RM_LOGITS_READY) ? 1u : (unsigned)((a.c.E + 1) / 2), (unsigned)((a.T + TT - 1) / TT));
-  return launch_pdl(k_route<TT>, grid, dim3(warps * 32), smem, st, a);
+  return launch_pdl(k_route<TT, SIG>, grid, dim3(warps * 32), smem, st, a);
+}
+
+template <int TT>
+cudaError_t launch_route_tt(const RouteArgs& a, int warps, cudaStream_t st) {
+  return a.c.sigmoid ? launch_route_tt2<TT, true>(a, warps, st) : launch_route_tt2<TT, false>(a, warps, st);
 }
 
 cudaError_t launch_route(const Cfg& c, const Ws& ws, const void* x, long long T, const float* W, const float* bias,
@@ -792,7 +821,8 @@ cudaError_t launch_route(const Cfg& c, const Ws& ws, const void* x, long long T,
            (size_t)kRouteMaxSmem;
   };
   if (mode & RM_LOGITS_READY)  // selection and activation terms from the tensor cores' partial logits
-    return c.rsplit > 1 ? launch_select<4, 2>(a, st) : launch_select<1, 3>(a, st);
+    return c.sigmoid ? (c.rsplit > 1 ? launch_select<4, 2, true>(a, st) : launch_select<1, 3, true>(a, st))
+                     : (c.rsplit > 1 ? launch_select<4, 2, false>(a, st) : launch_select<1, 3, false>(a, st));
   if (T >= 8 && fits(8, 8)) return launch_route_tt<8>(a, 8, st);
   if (T >= 4 && fits(4, 8)) return launch_route_tt<4>(a, 8, st);
   if (T >= 2 && fits(2, 8)) return launch_route_tt<2>(a, 8, st);

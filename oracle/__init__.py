@@ -21,8 +21,9 @@ _SRC = os.path.join(_HERE, "k3oracle.c")
 
 FAULTS = {
     "none": 0, "nibble_order": 1, "scale_bias": 2, "drop_shared": 3, "no_renorm": 4,
-    "tie_high": 5, "down_transposed": 6, "glu_on_up": 7,
+    "tie_high": 5, "down_transposed": 6, "glu_on_up": 7, "bias_in_gate": 8, "no_bias_select": 9,
 }
+SCORES = {"softmax": 0, "sigmoid_bias": 1}
 
 
 def build(force: bool = False) -> str:
@@ -52,12 +53,13 @@ def lib():
         L.k3o_decode_matrix.restype = ctypes.c_int
         L.k3o_bf16.argtypes = [ctypes.c_uint16]
         L.k3o_bf16.restype = ctypes.c_double
-        L.k3o_route_token.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P, _P, _P]
+        L.k3o_route_token.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P, _P, _P,
+                                      ctypes.c_int32]
         L.k3o_route_token.restype = ctypes.c_int
         L.k3o_expert_token.argtypes = [ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P]
         L.k3o_expert_token.restype = ctypes.c_int
         L.k3o_layer.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
-                                _P, ctypes.c_int32, ctypes.c_int64, _P, _P, _P, _P, _P, _P, _P, _P]
+                                _P, ctypes.c_int32, ctypes.c_int64, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int32]
         L.k3o_layer.restype = ctypes.c_int
         L.k3o_rmsnorm.argtypes = [_P, ctypes.c_int64, ctypes.c_int32, ctypes.c_double, _P]
         L.k3o_rmsnorm.restype = None
@@ -116,8 +118,10 @@ def decode_matrix(codes: np.ndarray, scales: np.ndarray, rows: int, cols: int) -
     return out
 
 
-def route_token(x: np.ndarray, W: np.ndarray, k: int, bias: np.ndarray | None = None):
-    """-> (logits[E], idx[k], w[k]) for one token given as exact float64 values."""
+def route_token(x: np.ndarray, W: np.ndarray, k: int, bias: np.ndarray | None = None, score: str = "softmax"):
+    """-> (logits[E], idx[k], w[k]) for one token given as exact float64 values. score 'softmax' (bias
+    added to the logits) or 'sigmoid_bias' (logits without bias; selection by sigmoid + bias, gates
+    from the unbiased sigmoid)."""
     x = np.ascontiguousarray(x, dtype=np.float64)
     W = np.ascontiguousarray(W, dtype=np.float32)
     E, d = W.shape
@@ -125,7 +129,7 @@ def route_token(x: np.ndarray, W: np.ndarray, k: int, bias: np.ndarray | None = 
     logits = np.empty(E, np.float64)
     idx = np.empty(k, np.int32)
     w = np.empty(k, np.float64)
-    if lib().k3o_route_token(E, d, k, _ptr(x), _ptr(W), _ptr(b), _ptr(logits), _ptr(idx), _ptr(w)):
+    if lib().k3o_route_token(E, d, k, _ptr(x), _ptr(W), _ptr(b), _ptr(logits), _ptr(idx), _ptr(w), SCORES[score]):
         raise ValueError("route_token failed")
     return logits, idx, w
 
@@ -142,7 +146,7 @@ def expert_token(record: np.ndarray, x: np.ndarray, d: int, f: int):
 
 
 def layer(x: np.ndarray, x_dtype: str, W: np.ndarray, bias, routed: dict | list, shared: list,
-          d: int, f: int, k: int):
+          d: int, f: int, k: int, score: str = "softmax"):
     """One MoE layer on T tokens.
 
     x: [T, d] uint16 bf16 bits (x_dtype 'bf16') or float32 ('f32').
@@ -178,7 +182,7 @@ def layer(x: np.ndarray, x_dtype: str, W: np.ndarray, bias, routed: dict | list,
     logits = np.empty((T, E), np.float64)
     rc = lib().k3o_layer(d, f, E, k, len(shared), _ptr(xa), 1 if x_dtype == "bf16" else 0, T, _ptr(W), _ptr(b),
                          ctypes.cast(rp, ctypes.c_void_p), ctypes.cast(sp, ctypes.c_void_p), _ptr(y), _ptr(idx),
-                         _ptr(w), _ptr(logits))
+                         _ptr(w), _ptr(logits), SCORES[score])
     if rc:
         raise ValueError(f"oracle layer failed ({rc})")
     return y, idx, w, logits

@@ -17,10 +17,12 @@
  *    E8M0 scale.
  *  - OCP Microscaling Formats (MX) v1.0: E2M1 element values and E8M0 scale
  *    2^(b-127), b = 0xFF is NaN.
- *  - Router: softmax over the E expert logits, top-k, gates renormalised over
- *    the k selected. (The review's list of header invariants describes another
- *    score: a sigmoid whose routing bias affects only the selection. That
- *    variant is not computed here.)
+ *  - Router, score 0 (softmax): softmax over the E expert logits, top-k, gates
+ *    renormalised over the k selected (the routing bias, if any, is added to the
+ *    logits). Score 1 (sigmoid + bias): the review's list of public-header
+ *    invariants states that the routing bias skews only the selection and that
+ *    the combine weights come from the unbiased sigmoid score: s_e =
+ *    sigmoid(x . W_e), selection by s_e + b_e, gates s_e / sum over the k of s.
  *  - Expert FFN: h = SiLU(W_gate x) * (W_up x), o = W_down h (SiLU-gated GLU,
  *    the stand-in for the pages' unspecified "SiTU-GLU").
  *  - Combine: y = sum_i w_i o_i + sum_s o_s (shared experts weight 1).
@@ -50,6 +52,8 @@ enum {
     FAULT_TIE_HIGH = 5,      /* equal logits -> higher index first               */
     FAULT_DOWN_T = 6,        /* down projection read transposed                  */
     FAULT_GLU_ON_UP = 7,     /* SiLU applied to the up branch instead of the gate */
+    FAULT_BIAS_IN_GATE = 8,  /* sigmoid score: gates from the biased score          */
+    FAULT_NO_BIAS_SELECT = 9,/* sigmoid score: selection ignores the bias           */
 };
 
 /* OCP MX v1.0, FP4 E2M1: magnitudes of the 8 positive codes. */
@@ -119,12 +123,42 @@ static int cmp_desc(const void* a, const void* b) {
 /*
  * Route one token. x[d] (exact input values), W[E][d] fp32, bias[E] or NULL.
  * logits_out[E] (may be NULL), idx_out[k], w_out[k].
- * Steps: logits l_e = sum_j x_j W_ej (+ b_e); full softmax over E; top-k by
- * logit (a full sort, ties to the lower index); gates renormalised over the k.
+ * score 0 (softmax): logits l_e = sum_j x_j W_ej (+ b_e); full softmax over E;
+ * top-k by logit (a full sort, ties to the lower index); gates renormalised
+ * over the k. score 1 (sigmoid + bias): logits l_e = sum_j x_j W_ej (no bias);
+ * s_e = 1 / (1 + exp(-l_e)); top-k by s_e + b_e (a full sort, ties to the lower
+ * index); gates s_e / sum over the k of s.
  */
+static int route_sigmoid(int32_t E, int32_t d, int32_t k, const double* x, const float* W, const float* bias,
+                         double* logits_out, int32_t* idx_out, double* w_out) {
+    scored* s = (scored*)malloc(sizeof(scored) * (size_t)E);
+    double* sg = (double*)malloc(sizeof(double) * (size_t)E);
+    if (!s || !sg) { free(s); free(sg); return -2; }
+    for (int32_t e = 0; e < E; ++e) {
+        double l = 0.0;
+        for (int32_t j = 0; j < d; ++j) l += x[j] * (double)W[(int64_t)e * d + j];
+        if (logits_out) logits_out[e] = l;
+        sg[e] = 1.0 / (1.0 + exp(-l));
+        s[e].l = sg[e] + ((bias && g_fault != FAULT_NO_BIAS_SELECT) ? (double)bias[e] : 0.0);
+        s[e].e = e;
+    }
+    qsort(s, (size_t)E, sizeof(scored), cmp_desc);
+    double zk = 0.0;
+    for (int32_t i = 0; i < k; ++i) zk += (g_fault == FAULT_BIAS_IN_GATE) ? s[i].l : sg[s[i].e];
+    for (int32_t i = 0; i < k; ++i) {
+        idx_out[i] = s[i].e;
+        w_out[i] = ((g_fault == FAULT_BIAS_IN_GATE) ? s[i].l : sg[s[i].e]) / zk;
+    }
+    free(s);
+    free(sg);
+    return 0;
+}
+
 int k3o_route_token(int32_t E, int32_t d, int32_t k, const double* x, const float* W,
-                    const float* bias, double* logits_out, int32_t* idx_out, double* w_out) {
+                    const float* bias, double* logits_out, int32_t* idx_out, double* w_out, int32_t score) {
     if (k < 1 || k > E) return -1;
+    if (score == 1) return route_sigmoid(E, d, k, x, W, bias, logits_out, idx_out, w_out);
+    if (score != 0) return -1;
     scored* s = (scored*)malloc(sizeof(scored) * (size_t)E);
     double* p = (double*)malloc(sizeof(double) * (size_t)E);
     if (!s || !p) { free(s); free(p); return -2; }
@@ -208,11 +242,12 @@ int k3o_expert_token(int32_t d, int32_t f, const uint8_t* record, const double* 
  *   routed: E record pointers (a NULL entry is an error only if that expert is selected)
  *   shared: S record pointers
  *   y: T x d doubles (overwritten); idx/w: T x k (may be NULL); logits: T x E (may be NULL)
+ *   score: 0 softmax, 1 sigmoid + selection-only bias (k3o_route_token)
  * Returns 0, -1 on bad data (NaN scale byte, missing record), -2 on allocation failure.
  */
 int k3o_layer(int32_t d, int32_t f, int32_t E, int32_t k, int32_t S, const void* x, int32_t x_is_bf16,
               int64_t T, const float* W, const float* bias, const uint8_t* const* routed,
-              const uint8_t* const* shared, double* y, int32_t* idx, double* w, double* logits) {
+              const uint8_t* const* shared, double* y, int32_t* idx, double* w, double* logits, int32_t score) {
     int status = 0;
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t t = 0; t < T; ++t) {
@@ -226,7 +261,7 @@ int k3o_layer(int32_t d, int32_t f, int32_t E, int32_t k, int32_t S, const void*
             for (int32_t j = 0; j < d; ++j)
                 xt[j] = x_is_bf16 ? k3o_bf16(((const uint16_t*)x)[t * d + j])
                                   : (double)((const float*)x)[t * d + j];
-            st = k3o_route_token(E, d, k, xt, W, bias, logits ? logits + t * E : NULL, it, wt);
+            st = k3o_route_token(E, d, k, xt, W, bias, logits ? logits + t * E : NULL, it, wt, score);
         }
         double* yt = y + t * d;
         if (!st) for (int32_t j = 0; j < d; ++j) yt[j] = 0.0;

@@ -51,10 +51,10 @@ class DeviceLayer:
     order unless pack=False) plus the host copies (stored order) the oracle needs."""
 
     def __init__(self, shape: synth.LayerShape, seed: int, layer: int = 0, zipf_s: float | None = None,
-                 x_dtype: str = "bf16", stride: int | None = None, pack: bool = True):
+                 x_dtype: str = "bf16", stride: int | None = None, pack: bool = True, score: str = "softmax"):
         import torch
         import mxfp4_routed_expert_k3moe_gb300 as k3
-        self.shape, self.seed, self.layer, self.x_dtype = shape, seed, layer, x_dtype
+        self.shape, self.seed, self.layer, self.x_dtype, self.score = shape, seed, layer, x_dtype, score
         self.stride = stride or shape.record_stride
         E, S = shape.n_routed, shape.n_shared
         self.W_host = synth.router_weights(shape, seed, layer)
@@ -69,7 +69,8 @@ class DeviceLayer:
         if S:
             synth.records_device(shape, seed, layer, E, S, self.shared.data_ptr(), self.stride, st)
         self.cfg = k3.Config.make(shape.d_model, shape.d_ff, E, shape.top_k, S,
-                                  x_dtype=k3.X_BF16 if x_dtype == "bf16" else k3.X_F32, record_stride=self.stride)
+                                  x_dtype=k3.X_BF16 if x_dtype == "bf16" else k3.X_F32, record_stride=self.stride,
+                                  score_func=k3.SCORE_SOFTMAX if score == "softmax" else k3.SCORE_SIGMOID_BIAS)
         if pack:
             k3.pack_records(self.cfg, self.routed, E)
             if S:
@@ -100,12 +101,20 @@ class DeviceLayer:
         # route first (cheap) to know which records the oracle needs
         experts = set()
         for t in range(x.shape[0]):
-            _, idx, _ = oracle.route_token(xf[t], self.W_host, sh.top_k, self.bias_host)
+            _, idx, _ = oracle.route_token(xf[t], self.W_host, sh.top_k, self.bias_host, score=self.score)
             experts.update(int(e) for e in idx)
         routed = self.host_records(sorted(experts))
         shared = list(self.host_records([sh.n_routed + s for s in range(sh.n_shared)]).values())
         return oracle.layer(x, self.x_dtype, self.W_host, self.bias_host, routed, shared, sh.d_model, sh.d_ff,
-                            sh.top_k)
+                            sh.top_k, score=self.score)
+
+    def sel_keys(self, logits_ref: np.ndarray) -> np.ndarray:
+        """The values the oracle ranked (for the near-tie rule): the logits (bias included) for the
+        softmax score; sigmoid(logit) + bias for the sigmoid score."""
+        if self.score == "softmax":
+            return logits_ref
+        from scipy.special import expit
+        return expit(logits_ref) + (0.0 if self.bias_host is None else self.bias_host.astype(np.float64))
 
     def oracle_ffn(self, xh: np.ndarray, idx: np.ndarray, w: np.ndarray):
         """Oracle of the FFN + combine for GIVEN routing (per token: sum_i w_i o_i + sum_s o_s)."""

@@ -62,7 +62,7 @@ def test_workspace_never_shrinks_as_tokens_grow(x_dtype):
     ("record_stride", 17547264 - 256, k3.ERR_INVALID_ARGUMENT),
     ("record_stride", 17547264 + 8, k3.ERR_INVALID_ARGUMENT),
     ("x_dtype", 7, k3.ERR_INVALID_ARGUMENT),
-    ("score_func", k3.SCORE_SIGMOID_BIAS, k3.ERR_UNSUPPORTED),
+    ("score_func", 7, k3.ERR_INVALID_ARGUMENT),
     ("act_mode", k3.ACT_MXFP4, k3.ERR_UNSUPPORTED),
 ])
 def test_invalid_config_rejected_on_host(field, value, code):

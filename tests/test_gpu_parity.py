@@ -38,7 +38,7 @@ def check_layer(L: DeviceLayer, T: int, sample=None, batch=0):
     y, idx, w = run_layer(L, xd, T)
     rows = np.arange(T) if sample is None else np.asarray(sample)
     y_ref, idx_ref, w_ref, logits_ref = L.oracle(xh, rows)
-    ok, near = index_parity(idx[rows], idx_ref, logits_ref, L.shape.top_k)
+    ok, near = index_parity(idx[rows], idx_ref, L.sel_keys(logits_ref), L.shape.top_k)
     assert ok, "top-k indices differ from the oracle beyond the near-tie rule"
     keep = [i for i in range(len(rows)) if i not in near]
     assert gate_err(idx[rows], w[rows], idx_ref, w_ref) < 1e-5
@@ -162,6 +162,34 @@ def test_route_only(T, tol):
     wn = w.cpu().numpy()
     assert np.allclose(wn.sum(axis=1), 1.0, atol=1e-6)
     assert gate_err(idx.cpu().numpy(), wn, idx_ref, w_ref) < tol
+
+
+@pytest.mark.parametrize("T,tol", [(5, 1e-6), (29, 1e-5)])
+def test_route_sigmoid_bias(T, tol):
+    """Sigmoid score with a selection-only bias (of the size of the sigmoid's spread, so that it
+    reorders the selection): same selection as the oracle (near-tie rule on sigmoid + bias) and gates
+    from the unbiased sigmoid; CUDA-core logits at 5 tokens, tensor-core partial logits at 29."""
+    L = DeviceLayer(MID, seed=16, zipf_s=0.05, score="sigmoid_bias")
+    xh, xd = L.tokens(T)
+    idx = torch.empty((T, MID.top_k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, MID.top_k), dtype=torch.float32, device="cuda")
+    ws = torch.zeros(k3.workspace_bytes(L.cfg, T), dtype=torch.uint8, device="cuda")
+    k3.route(L.cfg, xd, T, L.W, L.bias, idx, w, ws)
+    torch.cuda.synchronize()
+    assert k3.check_device_status(ws) == k3.OK
+    _, idx_ref, w_ref, logits_ref = L.oracle(xh)
+    ok, near = index_parity(idx.cpu().numpy(), idx_ref, L.sel_keys(logits_ref), MID.top_k)
+    assert ok
+    wn = w.cpu().numpy()
+    assert np.allclose(wn.sum(axis=1), 1.0, atol=1e-6)
+    keep = [t for t in range(T) if t not in near]
+    assert gate_err(idx.cpu().numpy()[keep], wn[keep], idx_ref[keep], w_ref[keep]) < tol
+
+
+@pytest.mark.parametrize("T", [3, 20])
+def test_layer_sigmoid_bias(T):
+    L = DeviceLayer(MID, seed=17, zipf_s=0.05, score="sigmoid_bias")
+    check_layer(L, T)
 
 
 @pytest.mark.parametrize("T,x_dtype", [(16, "bf16"), (40, "f32"), (512, "bf16"), (700, "bf16"), (600, "f32"), (1100, "bf16")])

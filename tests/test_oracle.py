@@ -4,7 +4,8 @@ Each pin is a function that raises AssertionError when the oracle is wrong.
 `test_planted_mistakes_are_caught` switches the oracle to deliberately wrong
 variants (wrong nibble order, scale bias, dropped shared experts, missing
 renormalisation, wrong tie order, transposed down projection, SiLU on the
-wrong branch) and checks that at least one pin fails for each.
+wrong branch, and for the sigmoid score: the bias in the gates, the bias left
+out of the selection) and checks that at least one pin fails for each.
 """
 import math
 
@@ -164,6 +165,60 @@ def pin_router_counts_k3_shape():
     assert abs(w.sum() - 1.0) < 1e-12
     order = np.argsort(-logits, kind="stable")[: sh.top_k]
     assert list(order) == list(idx)
+
+
+def _diag_router(logit_rows):
+    """Router weights whose logits are the given values exactly: W = diag(l), x = ones (all values are
+    exact in fp32)."""
+    l = np.asarray(logit_rows, dtype=np.float32)
+    return np.diag(l).astype(np.float32), np.ones(len(l))
+
+
+def pin_router_sigmoid_bias_selection_only():
+    """Sigmoid score (review, list of public-header invariants): the routing bias changes only which
+    experts are selected; the gates are the unbiased sigmoid scores renormalised over the selection.
+    Six rows; in five of them a bias swaps the order of the top two (checked against scipy's expit
+    and brute-force ranking), in the sixth it pulls a low expert into the selection."""
+    from scipy.special import expit
+    k = 2
+    rows = [
+        ([2.0, 1.75, 0.5, -0.25, -1.0, 0.0], [0.0, 0.25, 0.0, 0.0, 0.0, 0.0]),
+        ([0.5, 1.0, -2.0, 3.0, 2.5, 0.0], [0.0, 0.0, 0.0, 0.0, 0.125, 0.0]),
+        ([-1.0, -0.5, -0.75, -2.0, -3.0, -0.25], [0.0, 0.5, 0.0, 0.0, 0.0, 0.0]),
+        ([4.0, 3.5, 0.0, 0.0, 0.0, 0.0], [0.0, 0.0625, 0.0, 0.0, 0.0, 0.0]),
+        ([0.0, 0.0, 0.0, 1.0, 0.875, 0.0], [0.0, 0.0, 0.0, 0.0, 0.5, 0.0]),
+        ([2.0, 1.75, 0.5, -0.25, -1.0, 0.0], [0.0, 0.0, 0.0, 0.0, 1.0, 0.0]),
+    ]
+    swapped = 0
+    for l, b in rows:
+        W, x = _diag_router(l)
+        b = np.asarray(b, dtype=np.float32)
+        s = expit(np.asarray(l, dtype=np.float64))
+        keys = s + b.astype(np.float64)
+        logits, idx, w = oracle.route_token(x, W, k, b, score="sigmoid_bias")
+        assert np.array_equal(logits, np.asarray(l, dtype=np.float64))  # no bias in the logits
+        assert list(idx) == _brute_topk(list(keys), k)
+        assert np.allclose(w, s[idx] / s[idx].sum(), rtol=1e-14, atol=0)
+        _, idx0, w0 = oracle.route_token(x, W, k, None, score="sigmoid_bias")
+        assert list(idx0) == _brute_topk(list(s), k)
+        swapped += int(list(idx) == list(idx0[::-1]))
+        # a constant added to every bias changes nothing
+        _, idx1, w1 = oracle.route_token(x, W, k, b + np.float32(0.5), score="sigmoid_bias")
+        assert list(idx1) == list(idx) and np.allclose(w1, w, rtol=1e-15, atol=0)
+    assert swapped == 5
+
+
+def pin_router_sigmoid_unbiased_matches_softmax_selection():
+    """Without a bias the sigmoid is monotone in the logit: the same experts, in the same order, as the
+    softmax score selects (ties to the lower index in both)."""
+    rng = np.random.default_rng(12)
+    for E, d, k in [(8, 16, 3), (40, 32, 7)]:
+        x = rng.standard_normal(d)
+        W = (rng.standard_normal((E, d)) / math.sqrt(d)).astype(np.float32)
+        _, idx_s, _ = oracle.route_token(x, W, k, None, score="softmax")
+        _, idx_g, w_g = oracle.route_token(x, W, k, None, score="sigmoid_bias")
+        assert list(idx_s) == list(idx_g)
+        assert abs(w_g.sum() - 1.0) < 1e-12 and np.all(np.diff(w_g) <= 0)
 
 
 # ----------------------------------------------------------------------------- pins: expert FFN
@@ -342,7 +397,8 @@ def pin_tolerance_budget():
 
 
 PINS = [pin_e2m1_table, pin_e8m0, pin_record_bytes, pin_decode_single_nonzero, pin_decode_block_scale_axis,
-        pin_router_bruteforce, pin_router_ties_lower_index, pin_router_counts_k3_shape, pin_expert_vs_dense,
+        pin_router_bruteforce, pin_router_ties_lower_index, pin_router_counts_k3_shape,
+        pin_router_sigmoid_bias_selection_only, pin_router_sigmoid_unbiased_matches_softmax_selection, pin_expert_vs_dense,
         pin_expert_closed_form, pin_layer_combine_definition, pin_layer_identical_experts, pin_layer_relabel,
         pin_layer_token_independence, pin_layer_zero_gate_branch, pin_layer_down_scale_linear,
         pin_bf16_input_exact, pin_rmsnorm, pin_tolerance_budget]
