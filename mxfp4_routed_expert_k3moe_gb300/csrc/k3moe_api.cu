@@ -180,7 +180,6 @@ Cfg make_cfg(const k3moe_config* c, long long T) {
     k.hterms = 3;
   }
   k.rsplit = (int)router_splits(c, T);
-  k.sigmoid = c->score_func == K3MOE_SCORE_SIGMOID_BIAS ? 1 : 0;
   k.stride = c->record_stride;
   return k;
 }
@@ -227,10 +226,11 @@ k3moe_status k3moe_route(const k3moe_config* cfg, const void* x, int64_t T, cons
   const Cfg c = make_cfg(cfg, T);
   const Ws w = bind(L, ws);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  int mode = k3::RM_USER_OUT;
+  int mode = k3::RM_USER_OUT | (cfg->score_func == K3MOE_SCORE_SIGMOID_BIAS ? k3::RM_SIGMOID : 0);
   if (router_tc(cfg, T)) {
-    cudaError_t e = k3::launch_router_tc(c, w, x, T, w_router, bias, static_cast<char*>(ws) + L.w3,
-                                         static_cast<char*>(ws) + L.x3, st);
+    // (the sigmoid score adds its bias at the selection, not to the logits)
+    cudaError_t e = k3::launch_router_tc(c, w, x, T, w_router, (mode & k3::RM_SIGMOID) ? nullptr : bias,
+                                         static_cast<char*>(ws) + L.w3, static_cast<char*>(ws) + L.x3, st);
     if (e != cudaSuccess) return cuda_status(e);
     mode |= k3::RM_LOGITS_READY;
   }
@@ -288,10 +288,11 @@ k3moe_status layer_impl(const k3moe_config* cfg, const void* x, int64_t T, const
   const long long wgb = wg_bound(cfg, T);
   cudaError_t e = cudaSuccess;
   if (events) e = cudaEventRecord(static_cast<cudaEvent_t>(events[0]), st);
-  int mode = k3::RM_USER_OUT | k3::RM_XPREP | k3::RM_PERMUTE;
+  int mode = k3::RM_USER_OUT | k3::RM_XPREP | k3::RM_PERMUTE |
+             (cfg->score_func == K3MOE_SCORE_SIGMOID_BIAS ? k3::RM_SIGMOID : 0);
   if (e == cudaSuccess && router_tc(cfg, T)) {
-    e = k3::launch_router_tc(c, w, x, T, w_router, bias, static_cast<char*>(ws) + L.w3, static_cast<char*>(ws) + L.x3,
-                             st);
+    e = k3::launch_router_tc(c, w, x, T, w_router, (mode & k3::RM_SIGMOID) ? nullptr : bias,
+                             static_cast<char*>(ws) + L.w3, static_cast<char*>(ws) + L.x3, st);
     mode |= k3::RM_LOGITS_READY;
   }
   if (e == cudaSuccess) e = k3::launch_route(c, w, x, T, w_router, bias, topk_idx_out, topk_w_out, mode, st);

@@ -17,7 +17,6 @@ struct Cfg {
   int xterms;         // terms per activation block of x (E4M3: 2 for bf16 x, 3 for fp32 x; E2M1: 8 or 16)
   int hterms;         // terms per block of h
   int rsplit;         // partial logits the router kernel adds up (parts of the tensor-core reduction; 1: final)
-  int sigmoid;        // router score: 0 softmax (bias added to the logits), 1 sigmoid + selection-only bias
   long long stride;   // bytes between expert records
 };
 

@@ -26,7 +26,8 @@ inline cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, 
 }
 
 // k3moe_route.cu
-enum RouteMode { RM_USER_OUT = 1, RM_XPREP = 2, RM_PERMUTE = 4, RM_LOGITS_READY = 8 };
+// RM_SIGMOID: the sigmoid score with a selection-only bias (else softmax, the bias added to the logits)
+enum RouteMode { RM_USER_OUT = 1, RM_XPREP = 2, RM_PERMUTE = 4, RM_LOGITS_READY = 8, RM_SIGMOID = 16 };
 cudaError_t launch_route(const Cfg& c, const Ws& ws, const void* x, long long T, const float* W, const float* bias,
                          int* out_idx, float* out_w, int mode, cudaStream_t st);
 cudaError_t launch_prep(const Cfg& c, const Ws& ws, const void* x, long long T, const int* idx, const float* w,

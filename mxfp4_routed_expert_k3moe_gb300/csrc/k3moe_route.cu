@@ -508,7 +508,7 @@ __host__ __device__ __forceinline__ size_t route_tile_bytes(const Cfg& c, int tt
 // each), so that every warp issues all router-weight loads of its quarter at once (the weights are
 // read once and stream; the latency of one batch is paid, not four). The token tile of x is staged
 // in shared memory meanwhile. Warps also produce the E4M3 terms of x, one 32-element block each.
-// SIG: the sigmoid score (c.sigmoid), selected at launch.
+// SIG: the sigmoid score (RM_SIGMOID), selected at launch.
 template <int TT, bool SIG>
 __global__ void __launch_bounds__(256, 3) k_route(RouteArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
@@ -809,7 +809,7 @@ cudaError_t launch_route_tt2(const RouteArgs& a, int warps, cudaStream_t st) {
 
 template <int TT>
 cudaError_t launch_route_tt(const RouteArgs& a, int warps, cudaStream_t st) {
-  return a.c.sigmoid ? launch_route_tt2<TT, true>(a, warps, st) : launch_route_tt2<TT, false>(a, warps, st);
+  return (a.mode & RM_SIGMOID) ? launch_route_tt2<TT, true>(a, warps, st) : launch_route_tt2<TT, false>(a, warps, st);
 }
 
 cudaError_t launch_route(const Cfg& c, const Ws& ws, const void* x, long long T, const float* W, const float* bias,
@@ -821,7 +821,7 @@ cudaError_t launch_route(const Cfg& c, const Ws& ws, const void* x, long long T,
            (size_t)kRouteMaxSmem;
   };
   if (mode & RM_LOGITS_READY)  // selection and activation terms from the tensor cores' partial logits
-    return c.sigmoid ? (c.rsplit > 1 ? launch_select<4, 2, true>(a, st) : launch_select<1, 3, true>(a, st))
+    return (mode & RM_SIGMOID) ? (c.rsplit > 1 ? launch_select<4, 2, true>(a, st) : launch_select<1, 3, true>(a, st))
                      : (c.rsplit > 1 ? launch_select<4, 2, false>(a, st) : launch_select<1, 3, false>(a, st));
   if (T >= 8 && fits(8, 8)) return launch_route_tt<8>(a, 8, st);
   if (T >= 4 && fits(4, 8)) return launch_route_tt<4>(a, 8, st);

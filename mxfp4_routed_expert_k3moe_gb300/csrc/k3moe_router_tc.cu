@@ -246,8 +246,7 @@ cudaError_t launch_router_tc(const Cfg& c, const Ws& ws, const void* x, long lon
     attr = true;
   }
   dim3 grid((unsigned)((T + kRM - 1) / kRM), (unsigned)((c.E + kRN - 1) / kRN), (unsigned)c.rsplit);
-  // (the sigmoid score adds its bias at the selection, not to the logits)
-  return launch_pdl(k_router_mma, grid, dim3(kRThreads), smem, st, mx, mw, c.sigmoid ? nullptr : bias, ws.logits, T, c.E, c.d,
+  return launch_pdl(k_router_mma, grid, dim3(kRThreads), smem, st, mx, mw, bias, ws.logits, T, c.E, c.d,
                     c.x_f32 ? 6 : 3, c.rsplit, ws.ctrl);
 }
 
