@@ -38,6 +38,8 @@ WORKLOADS = {
     "prefill_4096": (4096, 3, None),
 }
 FALLBACK_HBM_GBS = 6800.0
+# the metric of both arms (this library, and the oracle as the reference arm)
+METRIC = "MoE-layer tokens/s (K3 shape, one layer) and fraction of HBM roofline"
 
 # DRAM traffic per launch from an ncu capture, keyed by kernel; valid only while the kernel sources
 # hash to the recorded value (see profiles/).
@@ -196,7 +198,7 @@ def run_reference(args, rank, world):
     total = sum(times)
     value = len(times) * n / total
     line = {
-        "impl": "reference", "metric": "MoE-layer tokens/s (K3 shape, one layer)", "value": value, "unit": "tokens/s",
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": 0, "steps": len(times), "warmup": warm, "ms_per_step": 1e3 * total / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": args.workload, "tokens_per_layer_call": T},
@@ -328,7 +330,7 @@ def run_ours(args, rank, world, local_rank):
     value = world * T * args.steps / (elapsed_ms * 1e-3)
 
     line = {
-        "metric": "MoE-layer tokens/s (K3 shape, one layer) and fraction of HBM roofline",
+        "metric": METRIC,
         "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "mxfp4 weights x bf16 activations, fp32 accumulate", "data": "synthetic",
