@@ -178,6 +178,12 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
+def workload_config(workload, T, shape):
+    """The keys that name the workload (the same in both arms' lines)."""
+    return {"workload": workload, "tokens_per_layer_call": T, "d_model": shape.d_model, "d_ff": shape.d_ff,
+            "n_routed": shape.n_routed, "top_k": shape.top_k, "n_shared": shape.n_shared}
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
@@ -201,7 +207,7 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": 0, "steps": len(times), "warmup": warm, "ms_per_step": 1e3 * total / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": args.workload, "tokens_per_layer_call": T},
+        "config": workload_config(args.workload, T, shape),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": min(n, cores), "kind": "oracle",
                          "sample": f"{len(times)} oracle layer calls x {n} tokens of the {args.workload} shape "
                                    f"(each step a bounded sample; stops after {args.ref_budget_s:.0f} s)"},
@@ -334,8 +340,7 @@ def run_ours(args, rank, world, local_rank):
         "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "mxfp4 weights x bf16 activations, fp32 accumulate", "data": "synthetic",
-        "config": {"workload": args.workload, "tokens_per_layer_call": T, "d_model": d, "d_ff": f,
-                   "n_routed": E, "top_k": k, "n_shared": S, "weight_sets_rotated": args.layers,
+        "config": {**workload_config(args.workload, T, shape), "weight_sets_rotated": args.layers,
                    "l2": f"inputs larger than L2: each step reads {bytes_layer / 1e6:.1f} MB of weights from a "
                          f"different layer than the previous step ({args.layers} layers rotated)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
