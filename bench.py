@@ -1,12 +1,19 @@
 #!/usr/bin/env python
 """MoE-layer throughput on GB300: the Kimi-K3-shape MXFP4 MoE layer through libk3moe.so.
 
-Default workload: single-token decode (d_model 7168, d_ff 1536, 896 routed experts top-16 + 2 shared,
-bf16 token N(0,1), fp32 N(0,1/d) router, MXFP4 experts with uniform E2M1 codes and E8M0 exponents
-uniform in -6..-2). One step = one layer call (router, top-k, permutation, gate/up + GLU, down +
-combine) on one batch of tokens. Steps rotate over `--layers` independent weight sets (4 x 15.8 GB),
-so each step's inputs (341 MB at decode b=1) are larger than L2 and were not touched by the
-previous step. Synthetic inputs (no checkpoint exists here): see synth/.
+Shapes (all workloads): d_model 7168, d_ff 1536, 896 routed experts top-16 + 2 shared, fp32 N(0,1/d)
+router, MXFP4 experts with uniform E2M1 codes and E8M0 exponents uniform in -6..-2. Synthetic inputs
+(no checkpoint exists here): see synth/.
+
+Headline (`value`): single-token decode, bf16 token N(0,1). One step = one layer call (router, top-k,
+permutation, gate/up + GLU, down + combine) on one token. Steps rotate over `--layers` independent
+weight sets, so each step's inputs (341.6 MB) are larger than L2 and were not touched by the
+previous step. Exactly --steps steps are timed, with nothing else inside the timed region; the
+per-kernel times come from a separate pass of event-bracketed steps afterwards.
+
+The same JSON line carries, under "workloads", the other configurations the metric names, each timed
+the same way: batched decode (64 tokens, Zipf(1.1)-skewed routing bias), prefill (4096 tokens) and a
+4-layer stack with pre-norm residual at 1 and 64 tokens.
 
 Prints ONE JSON line (rank 0). Under torchrun (--gpus N > 1) every rank runs an independent replica
 (the layer has no exchange step on one GPU; weak scaling) and the time is the max over ranks.
@@ -17,7 +24,6 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
-import math
 import os
 import subprocess
 import sys
@@ -32,40 +38,41 @@ import numpy as np  # noqa: E402
 import synth  # noqa: E402
 
 WORKLOADS = {
-    # name: (tokens per step, seed, zipf s)
-    "decode_b1": (1, 1, None),
-    "decode_b64_zipf": (64, 2, 1.1),
-    "prefill_4096": (4096, 3, None),
+    # name: (tokens per step, seed, zipf s, weight sets rotated)
+    "decode_b1": (1, 1, None, 8),
+    "decode_b64_zipf": (64, 2, 1.1, 2),
+    "prefill_4096": (4096, 3, None, 1),
 }
+STACK_TOKENS = (1, 64)
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_FP4_TFLOPS = 13500.0   # dense FP4 tensor peak of a GB300 (nominal)
+NOMINAL_FP8_TFLOPS = 4500.0    # dense FP8/FP6/FP4-as-f8f6f4 tensor peak (nominal)
 # the metric of both arms (this library, and the oracle as the reference arm)
 METRIC = "MoE-layer tokens/s (K3 shape, one layer) and fraction of HBM roofline"
 
-# DRAM traffic per launch from an ncu capture, keyed by kernel; valid only while the kernel sources
-# hash to the recorded value (see profiles/).
-NCU_TRAFFIC = {
-    # dram__bytes_read.sum + dram__bytes_write.sum of one launch (decode b=1: 16 routed + 2 shared
-    # records, the same per launch at any expert count), profiles/k_tc_ffn_decode_b1.md
-    "k_tc<gate/up>": (213776128, "220f8b4c3ca7401f"),
-    "k_tc<down>": (107876352, "220f8b4c3ca7401f"),
+# Counters from ncu captures of the projection kernels, per launch, keyed by (kernel, workload); valid
+# only while the kernel sources hash to the recorded value (the summaries under profiles/ give the
+# commands): dram__bytes_read.sum + dram__bytes_write.sum, and sm__pipe_tensor_cycles_active as a
+# fraction of elapsed cycles.
+NCU_COUNTERS = {
+    ("k_tc<gate/up>", "decode_b1"): {"traffic": 213776128, "hash": "220f8b4c3ca7401f"},
+    ("k_tc<down>", "decode_b1"): {"traffic": 107876352, "hash": "220f8b4c3ca7401f"},
 }
 
 
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20000)
-    p.add_argument("--warmup", type=int, default=50)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=list(WORKLOADS) + ["stack4_zipf"], default="decode_b1")
-    p.add_argument("--sweep", default="1,8,64,512,4096,16384",
-                   help="stack4_zipf: token counts per layer call (one JSON line each)")
-    p.add_argument("--layers", type=int, default=8,
-                   help="independent weight sets rotated across steps (8: the router weights alone, 206 MB, exceed L2)")
+    p.add_argument("--workload", choices=list(WORKLOADS), default="decode_b1", help="the headline workload")
+    p.add_argument("--extra", default="decode_b64_zipf,prefill_4096,stack4_zipf",
+                   help="other workloads reported in the same line ('' for none)")
+    p.add_argument("--layers", type=int, default=None, help="weight sets rotated (default per workload)")
     p.add_argument("--experts", type=int, default=None, help="override routed experts (small profiling case)")
     p.add_argument("--tokens", type=int, default=None, help="override tokens per layer call (small profiling case)")
-    p.add_argument("--batches", type=int, default=64, help="distinct token batches rotated across steps")
-    p.add_argument("--sample-every", type=int, default=8, help="phase-timed step every N steps")
+    p.add_argument("--phase-steps", type=int, default=24, help="event-bracketed steps of the per-kernel pass")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--ref-budget-s", type=float, default=150.0)
@@ -143,15 +150,6 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- oracle (CPU baseline)
-def kernels_per_layer(T, x_dtype):
-    """Kernels one layer call launches: router, gate/up (with the GLU), down, combine, plus the
-    tensor-core router GEMM and the bf16 splits of its operands from 16 tokens on."""
-    n = 4
-    if T >= 16:
-        n += 2 + (1 if x_dtype == "f32" else 0)
-    return n
-
-
 def oracle_sample(shape, seed, zipf_s, x_dtype, n_tokens):
     """Time the oracle on n_tokens tokens of layer 0 (records generated outside the timed part)."""
     import oracle
@@ -178,6 +176,13 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
+def cpu_baseline(workload, seed, zipf_s):
+    n = max(1, min(cpu_cores(), 16))
+    secs = oracle_sample(synth.K3, seed, zipf_s, "bf16", n)
+    return {"value": n / secs, "unit": "tokens/s", "cores": n, "kind": "oracle",
+            "sample": f"{n} tokens of layer 0 ({workload} shape), one oracle call, OpenMP over tokens, {secs:.1f} s"}
+
+
 def workload_config(workload, T, shape):
     """The keys that name the workload (the same in both arms' lines)."""
     return {"workload": workload, "tokens_per_layer_call": T, "d_model": shape.d_model, "d_ff": shape.d_ff,
@@ -187,7 +192,7 @@ def workload_config(workload, T, shape):
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    T, seed, zipf_s = WORKLOADS[args.workload]
+    T, seed, zipf_s, _ = WORKLOADS[args.workload]
     shape = synth.K3
     cores = cpu_cores()
     n = max(1, min(cores, 16))
@@ -218,7 +223,11 @@ def run_reference(args, rank, world):
 
 # ----------------------------------------------------------------------------- GPU arm
 class LayerWeights:
-    def __init__(self, shape, seed, layer, zipf_s, stride, dev):
+    """One layer's weights on the device, loaded the way a user loads them: records generated on the
+    device, put into the device order (k3moe_pack_records) and the router's bf16 parts prepared
+    (k3moe_prepare_router), once, outside any timed region."""
+
+    def __init__(self, k3, cfg, shape, seed, layer, zipf_s, stride, dev):
         import torch
         self.W = torch.from_numpy(synth.router_weights(shape, seed, layer)).to(dev)
         self.bias = None if zipf_s is None else torch.from_numpy(synth.zipf_bias(shape, seed, zipf_s, layer)).to(dev)
@@ -227,93 +236,90 @@ class LayerWeights:
         st = torch.cuda.current_stream().cuda_stream
         synth.records_device(shape, seed, layer, 0, shape.n_routed, self.routed.data_ptr(), stride, st)
         synth.records_device(shape, seed, layer, shape.n_routed, shape.n_shared, self.shared.data_ptr(), stride, st)
-        # weight loading: records into the device order the kernels read (once, not timed)
-        import mxfp4_routed_expert_k3moe_gb300 as k3
-        cfg = k3.Config.make(shape.d_model, shape.d_ff, shape.n_routed, shape.top_k, shape.n_shared,
-                             record_stride=stride)
         k3.pack_records(cfg, self.routed, shape.n_routed)
         k3.pack_records(cfg, self.shared, shape.n_shared)
+        self.parts = torch.empty(k3.router_parts_bytes(cfg) // 2, dtype=torch.int16, device=dev)
+        k3.prepare_router(cfg, self.W, self.parts)
 
 
-def run_ours(args, rank, world, local_rank):
+def timed(step, steps, world, local_rank):
+    """Device time of exactly `steps` calls of step(i), bracketed by a barrier and synchronize on both
+    sides (CUDA events on the launching stream), with nvidia-smi clocks sampled meanwhile."""
     import torch
-    import mxfp4_routed_expert_k3moe_gb300 as k3
-
-    dev = torch.device("cuda", local_rank)
-    torch.cuda.set_device(dev)
-    T, seed, zipf_s = WORKLOADS[args.workload]
-    T = args.tokens or T
-    base = synth.K3
-    E = args.experts or base.n_routed
-    shape = synth.LayerShape(base.d_model, base.d_ff, E, base.top_k, base.n_shared)
-    stride = shape.record_stride
-    d, f, k, S = shape.d_model, shape.d_ff, shape.top_k, shape.n_shared
-    cfg = k3.Config.make(d, f, E, k, S, x_dtype=k3.X_BF16, record_stride=stride)
-    layers = [LayerWeights(shape, seed, l, zipf_s, stride, dev) for l in range(args.layers)]
-    nb = max(1, args.batches if T <= 64 else min(args.batches, 4))
-    xs_host = np.stack([synth.tokens(shape, seed, T, "bf16", batch=b) for b in range(nb)])  # [nb, T, d] uint16
-    xs = torch.from_numpy(xs_host.view(np.int16)).to(dev)
-    y = torch.empty((T, d), dtype=torch.float32, device=dev)
-    ws = torch.zeros(k3.workspace_bytes(cfg, T), dtype=torch.uint8, device=dev)
-    idx_out = torch.empty((T, k), dtype=torch.int32, device=dev)
-    torch.cuda.synchronize()
-
-    def step(i, events=None, idx=None):
-        L = layers[i % len(layers)]
-        x = xs[i % nb]
-        if events is None:
-            k3.layer(cfg, x, T, L.W, L.bias, L.routed, L.shared, y, ws)
-        else:
-            k3.layer_timed(cfg, x, T, L.W, L.bias, L.routed, L.shared, y, ws, events, topk_idx=idx)
-
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize()
-    if k3.check_device_status(ws) != k3.OK:
-        raise RuntimeError("device status check failed after warm-up")
-
-    # phase events for sampled steps (all recorded inside the timed region, on the launching stream)
-    n_samp = (args.steps + args.sample_every - 1) // args.sample_every
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(n_samp)]
     st = torch.cuda.current_stream()
-    for e4 in ev:  # materialise the handles
-        for e in e4:
-            e.record(st)
-    idx_samples = torch.empty((n_samp, T, k), dtype=torch.int32, device=dev)
-    torch.cuda.synchronize()
-
     clocks = ClockSampler(local_rank)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    start.record(st)
-    for i in range(args.steps):
-        if i % args.sample_every == 0:
-            s = i // args.sample_every
-            step(i, [e.cuda_event for e in ev[s]], idx_samples[s])
-        else:
-            step(i)
-    end.record(st)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(st)
+    for i in range(steps):
+        step(i)
+    b.record(st)
     torch.cuda.synchronize()
     clk = clocks.stop()
-    elapsed_ms = start.elapsed_time(end)
+    ms = a.elapsed_time(b)
     if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
+        t = torch.tensor([ms], device="cuda")
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+        ms = float(t.item())
         torch.distributed.barrier()
-    if k3.check_device_status(ws) != k3.OK:
-        raise RuntimeError("device status check failed in the timed region")
+    return ms, clk
 
-    # per-kernel device times of the sampled steps (events between the kernels; the gate/up kernel
-    # finishes h itself, so its two closing events are adjacent)
+
+def run_layer_workload(args, k3, name, T, seed, zipf_s, n_sets, steps, warmup, world, local_rank, with_cpu):
+    """One layer workload: timed steps, the per-kernel pass, e2e and the CPU baseline."""
+    import torch
+    dev = torch.device("cuda", local_rank)
+    base = synth.K3
+    E = args.experts or base.n_routed
+    shape = synth.LayerShape(base.d_model, base.d_ff, E, base.top_k, base.n_shared)
+    stride = shape.record_stride
+    d, f, k, S = shape.d_model, shape.d_ff, shape.top_k, shape.n_shared
+    cfg = k3.Config.make(d, f, E, k, S, x_dtype=k3.X_BF16, record_stride=stride)
+    layers = [LayerWeights(k3, cfg, shape, seed, l, zipf_s, stride, dev) for l in range(n_sets)]
+    nb = 64 if T <= 64 else 2
+    xs_host = np.stack([synth.tokens(shape, seed, T, "bf16", batch=b) for b in range(nb)])  # [nb, T, d] uint16
+    xs = torch.from_numpy(xs_host.view(np.int16)).to(dev)
+    y = torch.empty((T, d), dtype=torch.float32, device=dev)
+    ws = torch.zeros(k3.workspace_bytes(cfg, T), dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+
+    def step(i):
+        L = layers[i % len(layers)]
+        k3.layer(cfg, xs[i % nb], T, L.W, L.bias, L.routed, L.shared, y, ws, w_parts=L.parts)
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if k3.check_device_status(ws) != k3.OK:
+        raise RuntimeError(f"{name}: device status check failed after warm-up")
+    elapsed_ms, clk = timed(step, steps, world, local_rank)
+    if k3.check_device_status(ws) != k3.OK:
+        raise RuntimeError(f"{name}: device status check failed in the timed region")
+
+    # per-kernel pass (after the headline timing): events recorded between the kernels of each step on
+    # the launching stream; the gate/up kernel finishes h itself, so its two closing events are adjacent
+    st = torch.cuda.current_stream()
+    n_samp = max(3, args.phase_steps if T <= 64 else min(args.phase_steps, 6))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(n_samp)]
+    for e6 in ev:  # materialise the handles
+        for e in e6:
+            e.record(st)
+    idx_samples = torch.empty((n_samp, T, k), dtype=torch.int32, device=dev)
+    torch.cuda.synchronize()
+    for s in range(n_samp):
+        L = layers[s % len(layers)]
+        k3.layer_timed(cfg, xs[s % nb], T, L.W, L.bias, L.routed, L.shared, y, ws, [e.cuda_event for e in ev[s]],
+                       topk_idx=idx_samples[s], w_parts=L.parts)
+    torch.cuda.synchronize()
     ph = np.array([[ev[s][j].elapsed_time(ev[s][j + 1]) for j in range(5)] for s in range(n_samp)])
     route_ms, gateup_ms, _, down_ms, combine_ms = ph.mean(axis=0)
     idxs = idx_samples.cpu().numpy()
     U = float(np.mean([len(np.unique(idxs[s])) for s in range(n_samp)]))
+
     rec = shape.record_bytes
     mat = f * d // 2 + f * d // 32
     # algorithmic bytes: the expert records the step must read, the router weights, x read once and
@@ -322,55 +328,63 @@ def run_ours(args, rank, world, local_rank):
     bytes_down = (U + S) * mat
     bytes_route = E * d * 4 + T * d * 2
     bytes_layer = (U + S) * rec + E * d * 4 + T * d * 2 + T * d * 4
+    # implementation traffic the layer adds on top (written and read back once each): the
+    # per-position down outputs [P, d] fp32 and h as three E4M3 terms with E8M0 scales [P, 3, f (+ f/32)]
+    P = T * (k + S)
+    bytes_partials = 2 * P * d * 4
+    # algorithmic flops: 2 per multiply-add of the three projections of every selected (token, expert)
+    flops_ffn = 2.0 * 3 * d * f * P
     peak, peak_kind = hbm_peak()
-    kernels = {"k_tc<gate/up>": (gateup_ms, bytes_gateup), "k_tc<down>": (down_ms, bytes_down),
-               "k_route": (route_ms, bytes_route)}
+    kernels = {"k_tc<gate/up>": (gateup_ms, bytes_gateup, flops_ffn * 2 / 3),
+               "k_tc<down>": (down_ms, bytes_down, flops_ffn / 3), "k_route": (route_ms, bytes_route, 0.0)}
     dom = max(kernels, key=lambda n: kernels[n][0])
-    dom_ms, dom_bytes = kernels[dom]
+    dom_ms, dom_bytes, dom_flops = kernels[dom]
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
-    traffic = None
-    # (the recorded counters are those of the decode b=1 launch; other workloads report none)
-    if args.workload == "decode_b1" and T == 1 and dom in NCU_TRAFFIC and NCU_TRAFFIC[dom][1] == kernel_hash():
-        traffic = NCU_TRAFFIC[dom][0]
-    ms_per_step = elapsed_ms / args.steps
-    value = world * T * args.steps / (elapsed_ms * 1e-3)
-
-    line = {
-        "metric": METRIC,
-        "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "mxfp4 weights x bf16 activations, fp32 accumulate", "data": "synthetic",
-        "config": {**workload_config(args.workload, T, shape), "weight_sets_rotated": args.layers,
-                   "l2": f"inputs larger than L2: each step reads {bytes_layer / 1e6:.1f} MB of weights from a "
-                         f"different layer than the previous step ({args.layers} layers rotated)",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+    cnt = NCU_COUNTERS.get((dom, name))
+    valid = cnt is not None and cnt["hash"] == kernel_hash() and T == WORKLOADS[name][0] and E == 896
+    ms_per_step = elapsed_ms / steps
+    out = {
+        "value": world * T * steps / (elapsed_ms * 1e-3), "unit": "tokens/s", "steps": steps, "warmup": warmup,
+        "ms_per_step": ms_per_step,
+        "config": {**workload_config(name, T, shape), "weight_sets_rotated": n_sets,
+                   "l2": f"inputs larger than L2: each step reads {bytes_layer / 1e6:.1f} MB of weights "
+                         f"({n_sets} weight set(s) rotated, {nb} token batch(es))"},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic, "peak_kind": f"{peak_kind} (MEASURED_PEAKS hbm_gbs)"
-                     if peak_kind == "measured" else "fallback",
+                     "frac": achieved / peak, "traffic": cnt["traffic"] if valid else None,
+                     "peak_kind": "measured (MEASURED_PEAKS hbm_gbs)" if peak_kind == "measured" else "fallback",
                      "algorithmic_bytes_per_launch": dom_bytes, "avg_launch_ms": dom_ms},
-        "kernels_ms": {"k_route": route_ms, "k_tc<gate/up> (with the GLU)": gateup_ms, "k_tc<down>": down_ms,
-                       "k_combine": combine_ms, "sampled_steps": n_samp,
-                       "note": "events between the kernels remove their launch overlap in the sampled steps"},
+        "kernels_ms": {"router": route_ms, "k_tc<gate/up> (with the GLU)": gateup_ms, "k_tc<down>": down_ms,
+                       "k_combine": combine_ms, "steps": n_samp,
+                       "note": "separate pass after the timed steps; events between the kernels remove their "
+                               "launch overlap"},
         "layer_roofline": {"bytes_per_step": bytes_layer, "achieved_gbs": bytes_layer / (ms_per_step * 1e-3) / 1e9,
-                           "frac": bytes_layer / (ms_per_step * 1e-3) / 1e9 / peak},
+                           "frac": bytes_layer / (ms_per_step * 1e-3) / 1e9 / peak,
+                           "implementation_bytes_per_step": bytes_partials,
+                           "frac_with_implementation_bytes":
+                               (bytes_layer + bytes_partials) / (ms_per_step * 1e-3) / 1e9 / peak},
         "distinct_experts_per_step": U,
-        "gpu_launches": kernels_per_layer(T, "bf16") * args.steps,
+        "gpu_launches": (4 if T < 16 else 5) * steps,
         "clocks": clk,
     }
-
+    if T >= 16:
+        tc = {"algorithmic_tflop_per_step": flops_ffn / 1e12,
+              "fp4_frac_nominal": flops_ffn / (ms_per_step * 1e-3) / 1e12 / NOMINAL_FP4_TFLOPS,
+              "dominant_kernel_fp4_frac_nominal": dom_flops / (dom_ms * 1e-3) / 1e12 / NOMINAL_FP4_TFLOPS,
+              "peak_kind": f"nominal dense FP4 {NOMINAL_FP4_TFLOPS:.0f} TFLOP/s"}
+        if valid and "tensor_active" in cnt:
+            tc["tensor_pipe_active_ncu"] = cnt["tensor_active"]
+        out["tensor"] = tc
     if not args.no_e2e:
-        line["e2e"] = e2e(args, k3, cfg, layers, xs_host, T, d, dev)
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        n = max(1, min(cpu_cores(), 16))
-        secs = oracle_sample(synth.K3, seed, zipf_s, "bf16", n)
-        line["cpu_baseline"] = {"value": n / secs, "unit": "tokens/s", "cores": n, "kind": "oracle",
-                                "sample": f"{n} tokens of layer 0 ({args.workload} shape), one oracle call, "
-                                          f"OpenMP over tokens, {secs:.1f} s"}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
+        out["e2e"] = e2e(k3, cfg, layers, xs_host, T, d, dev, steps, warmup)
+    if with_cpu and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(name, seed, zipf_s)
+    del layers, xs, ws, y
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
 
 
-def e2e(args, k3, cfg, layers, xs_host, T, d, dev):
+def e2e(k3, cfg, layers, xs_host, T, d, dev, steps, warmup):
     """Same metric through the public call with host buffers: pinned x -> device, layer, y -> pinned host."""
     import torch
     nb = xs_host.shape[0]
@@ -379,16 +393,15 @@ def e2e(args, k3, cfg, layers, xs_host, T, d, dev):
     xd = torch.empty((T, d), dtype=torch.int16, device=dev)
     yd = torch.empty((T, d), dtype=torch.float32, device=dev)
     ws = torch.zeros(k3.workspace_bytes(cfg, T), dtype=torch.uint8, device=dev)
-    steps = max(10, args.steps // 4)
     st = torch.cuda.current_stream()
 
     def one(i):
         L = layers[i % len(layers)]
         xd.copy_(xh[i % nb], non_blocking=True)
-        k3.layer(cfg, xd, T, L.W, L.bias, L.routed, L.shared, yd, ws)
+        k3.layer(cfg, xd, T, L.W, L.bias, L.routed, L.shared, yd, ws, w_parts=L.parts)
         yh.copy_(yd, non_blocking=True)
 
-    for i in range(min(args.warmup, 20)):
+    for i in range(max(3, min(warmup, 20))):
         one(i)
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -402,67 +415,111 @@ def e2e(args, k3, cfg, layers, xs_host, T, d, dev):
             "d2h_bytes_per_step": T * d * 4, "steps": steps}
 
 
-def run_stack(args, rank, world, local_rank):
+def run_stack(args, k3, world, local_rank):
     """stack4_zipf: 4 independent layers (seeds 40-43, Zipf 1.1 routing bias), pre-norm residual
-    x <- x + Layer_l(RMSNorm(x)) with fp32 activations, for each token count of --sweep. One step =
-    the 4 layers on one batch; one JSON line per token count (a curve, not the headline)."""
+    x <- x + Layer_l(RMSNorm(x)) with fp32 activations. One step = the 4 layers on one batch. Timed
+    two ways: with the residual add and the next layer's norm fused in k3moe_residual_rmsnorm (whose
+    early launch lets the next layer's router stream its weights during it), and with the separate
+    k3moe_residual_add + k3moe_rmsnorm calls."""
     import torch
-    import mxfp4_routed_expert_k3moe_gb300 as k3
-
     dev = torch.device("cuda", local_rank)
-    torch.cuda.set_device(dev)
     shape = synth.K3
     stride = shape.record_stride
     d, E, k, S = shape.d_model, shape.n_routed, shape.top_k, shape.n_shared
-    layers = [LayerWeights(shape, 40 + l, l, 1.1, stride, dev) for l in range(4)]
     cfg = k3.Config.make(d, shape.d_ff, E, k, S, x_dtype=k3.X_F32, record_stride=stride)
+    layers = [LayerWeights(k3, cfg, shape, 40 + l, l, 1.1, stride, dev) for l in range(4)]
     peak, peak_kind = hbm_peak()
-    for T in [int(t) for t in args.sweep.split(",")]:
-        x = torch.from_numpy(synth.tokens(shape, 40, T, "f32")).to(dev)
+    res = {}
+    for T in STACK_TOKENS:
+        x0 = torch.from_numpy(synth.tokens(shape, 40, T, "f32")).to(dev)
+        x = x0.clone()
         xn = torch.empty_like(x)
         y = torch.empty_like(x)
         ws = torch.zeros(k3.workspace_bytes(cfg, T), dtype=torch.uint8, device=dev)
         idx = [torch.empty((T, k), dtype=torch.int32, device=dev) for _ in range(4)]
 
-        def step(keep_idx=False):
+        def fused(keep_idx=False):
+            k3.rmsnorm(x, T, d, 1e-6, xn)
             for l, L in enumerate(layers):
+                k3.layer(cfg, xn, T, L.W, L.bias, L.routed, L.shared, y, ws, topk_idx=idx[l] if keep_idx else None,
+                         w_parts=L.parts)
+                k3.residual_rmsnorm(x, y, T, d, 1e-6, xn)
+
+        def separate():
+            for L in layers:
                 k3.rmsnorm(x, T, d, 1e-6, xn)
-                k3.layer(cfg, xn, T, L.W, L.bias, L.routed, L.shared, y, ws, topk_idx=idx[l] if keep_idx else None)
+                k3.layer(cfg, xn, T, L.W, L.bias, L.routed, L.shared, y, ws, w_parts=L.parts)
                 k3.residual_add(x, y, T * d)
 
-        steps = max(3, min(args.steps, int(2e5 // max(T, 1))))
-        for _ in range(max(3, min(args.warmup, 5))):
-            step()
-        step(keep_idx=True)
+        steps = max(3, min(args.steps, 200 if T <= 64 else 20))
+        out = {}
+        for label, fn in (("fused", fused), ("separate", separate)):
+            x.copy_(x0)
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            x.copy_(x0)
+            ms, clk = timed(lambda i: fn(), steps, world, local_rank)
+            out[label] = {"layer_tokens_per_s": 4 * T * steps / (ms * 1e-3) * world, "ms_per_step": ms / steps,
+                          "steps": steps, "clocks": clk}
+        x.copy_(x0)
+        fused(keep_idx=True)
         torch.cuda.synchronize()
         if k3.check_device_status(ws) != k3.OK:
             raise RuntimeError("device status check failed in the stack")
         U = [int(torch.unique(i).numel()) for i in idx]
-        clocks = ClockSampler(local_rank)
-        clocks.start()
-        time.sleep(0.2)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        for _ in range(steps):
-            step()
-        b.record()
-        torch.cuda.synchronize()
-        clk = clocks.stop()
-        ms = a.elapsed_time(b) / steps
         rec = shape.record_bytes
         bytes_step = sum((u + S) * rec + E * d * 4 + T * d * 4 * 2 for u in U)
-        line = {"metric": "MoE-layer tokens/s (K3 shape, 4-layer stack with pre-norm residual)",
-                "value": 4 * T / (ms * 1e-3), "unit": "layer-tokens/s", "stack_tokens_per_s": T / (ms * 1e-3),
-                "ms_per_step": ms, "steps": steps, "higher_is_better": True, "dtype": "mxfp4 weights x fp32 activations, fp32 accumulate",
-                "data": "synthetic", "config": {"workload": "stack4_zipf", "tokens_per_layer_call": T, "layers": 4},
-                "distinct_experts_per_layer": U,
-                "layer_roofline": {"bytes_per_step": bytes_step, "achieved_gbs": bytes_step / (ms * 1e-3) / 1e9,
-                                   "frac": bytes_step / (ms * 1e-3) / 1e9 / peak, "peak": peak, "peak_kind": peak_kind},
-                "clocks": clk}
-        if rank == 0:
-            print(json.dumps(line), flush=True)
-        del ws, x, xn, y
-        torch.cuda.empty_cache()
+        ms = out["fused"]["ms_per_step"]
+        res[f"T{T}"] = {**out, "distinct_experts_per_layer": U,
+                        "layer_roofline": {"bytes_per_step": bytes_step, "frac": bytes_step / (ms * 1e-3) / 1e9 / peak,
+                                           "peak": peak, "peak_kind": peak_kind}}
+        del ws, x, x0, xn, y
+    del layers
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return {"metric": "layer-tokens/s of a 4-layer stack with pre-norm residual (x <- x + Layer(RMSNorm(x)))",
+            "config": {"workload": "stack4_zipf", "layers": 4, "x_dtype": "f32", "zipf_s": 1.1}, **res}
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import mxfp4_routed_expert_k3moe_gb300 as k3
+
+    torch.cuda.set_device(local_rank)
+    T, seed, zipf_s, n_sets = WORKLOADS[args.workload]
+    T = args.tokens or T
+    n_sets = args.layers or n_sets
+    head = run_layer_workload(args, k3, args.workload, T, seed, zipf_s, n_sets, args.steps, args.warmup, world,
+                              local_rank, with_cpu=rank == 0 and world == 1)
+    extra = {}
+    for name in [w for w in args.extra.split(",") if w]:
+        if name == args.workload:
+            continue
+        if name == "stack4_zipf":
+            extra[name] = run_stack(args, k3, world, local_rank)
+            continue
+        Tw, sw, zw, nw = WORKLOADS[name]
+        # the same step count as the headline, capped so that a workload takes seconds
+        steps = max(3, min(args.steps, 400 if Tw <= 64 else 40))
+        extra[name] = run_layer_workload(args, k3, name, Tw, sw, zw, nw, steps, max(3, min(args.warmup, 5)), world,
+                                         local_rank, with_cpu=rank == 0 and world == 1)
+    launches = head["gpu_launches"] + sum(v.get("gpu_launches", 0) for v in extra.values())
+    line = {
+        "metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "mxfp4 weights x bf16 activations, fp32 accumulate", "data": "synthetic",
+        "config": {**head["config"], "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": head["roofline"], "layer_roofline": head["layer_roofline"], "kernels_ms": head["kernels_ms"],
+        "distinct_experts_per_step": head["distinct_experts_per_step"],
+        "gpu_launches": head["gpu_launches"], "gpu_launches_all_workloads": launches, "clocks": head["clocks"],
+    }
+    for key in ("e2e", "cpu_baseline"):
+        if key in head:
+            line[key] = head[key]
+    line["workloads"] = extra
+    if rank == 0:
+        print(json.dumps(line), flush=True)
 
 
 def main():
@@ -478,10 +535,7 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
-    if args.workload == "stack4_zipf":
-        run_stack(args, rank, world, local_rank)
-    else:
-        run_ours(args, rank, world, local_rank)
+    run_ours(args, rank, world, local_rank)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

@@ -23,14 +23,19 @@
  *
  * Conventions shared by every call below:
  *  - Pointers are DEVICE pointers unless marked "host". The caller owns all memory; nothing is
- *    allocated by a compute call and nothing is kept after it returns.
+ *    allocated by a compute call and nothing is kept after it returns (one exception:
+ *    k3moe_layer_static keeps its scratch array, and that array's address, between calls).
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream).
  *  - Invalid arguments return K3MOE_ERR_INVALID_ARGUMENT synchronously and launch nothing:
- *    a NULL required pointer, T < 0, T > the workspace's token capacity, top_k < 1 or
- *    top_k > min(n_routed, 32), n_routed > 4096, n_shared < 0 or > 8, d_model or d_ff not a
- *    positive multiple of 128, record_stride < the record size or not a multiple of 256,
- *    a pointer not 16-byte aligned, or an unknown enum value.
- *    Legal configurations this library does not implement return K3MOE_ERR_UNSUPPORTED.
+ *    a NULL required pointer, T < 0, top_k < 1 or top_k > min(n_routed, 32), n_routed > 4096,
+ *    n_shared < 0 or > 8, d_model or d_ff not a positive multiple of 32, record_stride < the
+ *    record size or not a multiple of 4096 (records are 4 KiB aligned), a pointer not 16-byte
+ *    aligned, or an unknown enum value.
+ *    Legal configurations this library does not implement return K3MOE_ERR_UNSUPPORTED
+ *    without launching anything: d_model or d_ff a multiple of 32 but not of 128 (the
+ *    tensor-core tiles are 128 rows), d_model > 25600, act_mode K3MOE_ACT_MXFP4, and records
+ *    in the stored order (record_order K3MOE_ORDER_STORED) given to a call that reads them.
+ *    A workspace smaller than k3moe_workspace_bytes(cfg, T) returns K3MOE_ERR_WORKSPACE.
  *  - T = 0 is a no-op that returns K3MOE_OK.
  *  - Bad data found on the device (an expert index outside [0, n_routed) given to
  *    k3moe_expert_ffn, or an E8M0 scale byte 0xFF) sets a status word in the workspace; the
@@ -39,8 +44,9 @@
  *  - CUDA launch errors return K3MOE_ERR_CUDA.
  *  - The workspace (`ws`, `ws_bytes`) is scratch owned by the caller: size it with
  *    k3moe_workspace_bytes, zero-fill it once after allocation, and do not run two calls
- *    that share a workspace concurrently. Calls on different workspaces are independent;
- *    the library has no other mutable global state.
+ *    that share a workspace concurrently. Calls on different workspaces are independent.
+ *    Other mutable global state: caches of tensor-map descriptors and device properties
+ *    (guarded by a mutex), and k3moe_layer_static's scratch array, which all its calls share.
  */
 #ifndef K3MOE_H
 #define K3MOE_H
@@ -77,6 +83,16 @@ enum { K3MOE_SCORE_SOFTMAX = 0, K3MOE_SCORE_SIGMOID_BIAS = 1 };
 enum { K3MOE_ACT_EXACT = 0, K3MOE_ACT_MXFP4 = 1 };
 /* Element type of the token activations x. */
 enum { K3MOE_X_BF16 = 0, K3MOE_X_F32 = 1 };
+/* Order of the bytes inside the expert records the caller passes: the stored order (the layout
+   below, as the records are kept on disk) or the device order that k3moe_pack_records produces.
+   The compute calls read the device order only; they refuse records marked as stored
+   (K3MOE_ERR_UNSUPPORTED), so that records never packed cannot be used by mistake. A
+   zero-initialised config says "stored". */
+enum { K3MOE_ORDER_STORED = 0, K3MOE_ORDER_DEVICE = 1 };
+/* Format of the shared experts' records: MXFP4 like the routed experts (the default), or bf16
+   (the README's parameter budget counts every non-routed parameter in bfloat16). bf16 shared
+   records are legal but not implemented yet (K3MOE_ERR_UNSUPPORTED). */
+enum { K3MOE_SHARED_MXFP4 = 0, K3MOE_SHARED_BF16 = 1 };
 
 typedef struct {
   int32_t d_model;       /* hidden size d (7168 for the K3 shape) */
@@ -87,7 +103,11 @@ typedef struct {
   int32_t score_func;    /* K3MOE_SCORE_* */
   int32_t act_mode;      /* K3MOE_ACT_* */
   int32_t x_dtype;       /* K3MOE_X_* */
-  int64_t record_stride; /* bytes between expert records (>= record size, multiple of 256) */
+  int32_t record_order;  /* K3MOE_ORDER_* of the records passed to the call */
+  int32_t shared_format; /* K3MOE_SHARED_* */
+  int64_t record_stride; /* bytes between expert records (>= record size, multiple of 4096) */
+  int64_t shared_stride; /* bytes between shared records; 0: record_stride (MXFP4 shared records)
+                            or the bf16 record size rounded up to 4096 (bf16 shared records) */
 } k3moe_config;
 
 /*
@@ -120,6 +140,23 @@ K3MOE_API size_t k3moe_record_bytes(const k3moe_config* cfg /* host */);
 K3MOE_API size_t k3moe_workspace_bytes(const k3moe_config* cfg /* host */, int64_t max_tokens);
 
 /*
+ * Bytes of the router weights' three bf16 parts, 3 * n_routed * d_model * 2 (host only; 0 if the
+ * config is invalid).
+ */
+K3MOE_API size_t k3moe_router_parts_bytes(const k3moe_config* cfg /* host */);
+
+/*
+ * Weight-loading step of the router (once per set of router weights, like k3moe_pack_records):
+ * writes w_parts[3][n_routed][d_model] bf16 with W = W0 + W1 + W2, each part the bf16 rounding of
+ * what the earlier parts leave (24 significant bits of every fp32 weight are kept). From 16 tokens
+ * the router computes its logits on the tensor cores from these parts; k3moe_route and k3moe_layer
+ * take them as `w_router_parts`. w_router [n_routed, d_model] fp32; w_parts 16-byte aligned,
+ * k3moe_router_parts_bytes(cfg) bytes. Asynchronous on `stream`.
+ */
+K3MOE_API k3moe_status k3moe_prepare_router(const k3moe_config* cfg /* host */, const float* w_router,
+                                            uint16_t* w_parts, void* stream);
+
+/*
  * Router: softmax over the n_routed logits of each token, top-k, renormalised gates.
  * With score_func K3MOE_SCORE_SIGMOID_BIAS (the review's list of public-header invariants: the
  * routing bias skews only the selection, the combine weights come from the unbiased sigmoid score):
@@ -127,14 +164,16 @@ K3MOE_API size_t k3moe_workspace_bytes(const k3moe_config* cfg /* host */, int64
  * and the gates are s_e / sum over the selected of s.
  *   x        [T, d_model] bf16 or fp32 (cfg->x_dtype), row-major
  *   w_router [n_routed, d_model] fp32, row-major
+ *   w_router_parts  [3, n_routed, d_model] bf16 from k3moe_prepare_router, or NULL: then calls of
+ *            16 tokens or more split the weights into the workspace on every call
  *   bias     [n_routed] fp32, or NULL: softmax score: added to every logit before selection and
  *            softmax; sigmoid score: added to the sigmoid scores for the selection only
  *   topk_idx [T, top_k] int32 out: expert ids, descending ranked value, ties to the lower id
  *   topk_w   [T, top_k] fp32 out: gates, summing to 1 per token
  */
 K3MOE_API k3moe_status k3moe_route(const k3moe_config* cfg /* host */, const void* x, int64_t T,
-                         const float* w_router, const float* bias, int32_t* topk_idx, float* topk_w,
-                         void* ws, size_t ws_bytes, void* stream);
+                         const float* w_router, const uint16_t* w_router_parts, const float* bias,
+                         int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes, void* stream);
 
 /*
  * Expert FFN and combine for given routing (review, table "KDA·MLA·MoE": the experts multiply
@@ -158,9 +197,23 @@ K3MOE_API k3moe_status k3moe_expert_ffn(const k3moe_config* cfg /* host */, cons
  *   topk_idx_out / topk_w_out: optional [T, top_k] outputs of the routing (NULL to skip).
  */
 K3MOE_API k3moe_status k3moe_layer(const k3moe_config* cfg /* host */, const void* x, int64_t T,
-                         const float* w_router, const float* bias, const uint8_t* routed_records,
-                         const uint8_t* shared_records, float* y, int32_t* topk_idx_out,
-                         float* topk_w_out, void* ws, size_t ws_bytes, void* stream);
+                         const float* w_router, const uint16_t* w_router_parts, const float* bias,
+                         const uint8_t* routed_records, const uint8_t* shared_records, float* y,
+                         int32_t* topk_idx_out, float* topk_w_out, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * k3moe_layer with an explicit bound on the waits of its tensor-core kernels: `wait_limit` polls of
+ * a pipeline barrier before the waiting CTA gives up, sets K3MOE_ERR_TIMEOUT in the workspace's
+ * status word (read by k3moe_check_device_status), stops its work, lets the copies and MMAs it
+ * started complete, frees its tensor memory and exits. k3moe_layer uses 2^24 polls (seconds). A
+ * limit of 1 makes the first wait that is not already satisfied give up: this is how the timeout
+ * path is tested (the output of such a call is not trusted; the context stays usable). 0 is invalid.
+ */
+K3MOE_API k3moe_status k3moe_layer_bounded(const k3moe_config* cfg /* host */, const void* x, int64_t T,
+                                           const float* w_router, const uint16_t* w_router_parts,
+                                           const float* bias, const uint8_t* routed_records,
+                                           const uint8_t* shared_records, float* y, void* ws, size_t ws_bytes,
+                                           uint32_t wait_limit, void* stream);
 
 /*
  * k3moe_layer with phase timing, for profiling: `events` points to 6 cudaEvent_t handles created by
@@ -170,10 +223,11 @@ K3MOE_API k3moe_status k3moe_layer(const k3moe_config* cfg /* host */, const voi
  * Same kernels and results as k3moe_layer (an event between two kernels only removes their overlap).
  */
 K3MOE_API k3moe_status k3moe_layer_timed(const k3moe_config* cfg /* host */, const void* x, int64_t T,
-                                         const float* w_router, const float* bias,
-                                         const uint8_t* routed_records, const uint8_t* shared_records,
-                                         float* y, int32_t* topk_idx_out, float* topk_w_out, void* ws,
-                                         size_t ws_bytes, void* stream, void* const* events /* host */);
+                                         const float* w_router, const uint16_t* w_router_parts,
+                                         const float* bias, const uint8_t* routed_records,
+                                         const uint8_t* shared_records, float* y, int32_t* topk_idx_out,
+                                         float* topk_w_out, void* ws, size_t ws_bytes, void* stream,
+                                         void* const* events /* host */);
 
 /*
  * The whole layer for callers that cannot allocate device memory (no counterpart in the pages:
@@ -181,12 +235,14 @@ K3MOE_API k3moe_status k3moe_layer_timed(const k3moe_config* cfg /* host */, con
  * their own pool and forbid other cudaMalloc calls, and latency-critical callers cannot afford
  * cudaMalloc's device synchronisation; this call needs no workspace from them. Its scratch is a
  * fixed K3MOE_STATIC_SCRATCH_BYTES array in device memory declared by the library (resident on
- * every GPU that loads it until exit); calls needing more (k3moe_workspace_bytes(cfg, T) larger,
- * i.e. T > 4 at the 7168/1536/896 shape) return K3MOE_ERR_WORKSPACE. It allocates nothing,
- * clears the scratch it uses at the start of each call, and otherwise behaves like k3moe_layer
- * without the optional top-k outputs. All calls on a device share the array: calls that overlap
- * on the GPU race and give wrong results. The first call on a device looks up the array's
- * address; make it before any stream capture. Device-side data checks are not reported.
+ * every GPU that loads it until exit); calls needing more (k3moe_workspace_bytes(cfg, T) larger)
+ * return K3MOE_ERR_WORKSPACE: at the 7168/1536/896 top-16 shape with 2 shared experts, T <= 6 is
+ * served and T >= 7 is refused. It allocates nothing, clears the scratch it uses at the start of
+ * each call, and otherwise behaves like k3moe_layer without the optional outputs (same argument
+ * checks and status codes; the router weights are used as fp32, which is all that calls of this
+ * size read). All calls on a device share the array: calls that overlap on the GPU race and give
+ * wrong results. The first call on a device looks up the array's address; make it before any
+ * stream capture, and do not reset the device after it. Device-side data checks are not reported.
  */
 #define K3MOE_STATIC_SCRATCH_BYTES (4u << 20)
 K3MOE_API k3moe_status k3moe_layer_static(const k3moe_config* cfg /* host */, const void* x, int64_t T,
@@ -205,9 +261,20 @@ K3MOE_API k3moe_status k3moe_rmsnorm(const float* x, int64_t T, int32_t d, float
 K3MOE_API k3moe_status k3moe_residual_add(float* x, const float* y, int64_t n, void* stream);
 
 /*
+ * The step between two layers of a stack in one kernel: x += y (skipped if y is NULL), then
+ * xn = RMSNorm(x) with unit weight. x, y, xn: [T, d] fp32, 16-byte aligned, d a multiple of 4.
+ * Like every kernel of this library it is launched with programmatic stream serialization: it is
+ * scheduled while the previous layer's last kernel drains, and the next layer's router kernel is
+ * scheduled while it runs and streams its router weights (which nothing on the stream writes)
+ * before it waits for xn. So layer l+1's router overlaps layer l's tail instead of starting cold.
+ */
+K3MOE_API k3moe_status k3moe_residual_rmsnorm(float* x, const float* y, int64_t T, int32_t d, float eps, float* xn,
+                                              void* stream);
+
+/*
  * Synchronise `stream`, read the workspace's device status word, clear it, and return
- * K3MOE_ERR_DEVICE_CHECK if bad data was seen since the last check, else K3MOE_OK
- * (K3MOE_ERR_CUDA if the stream reports an error).
+ * K3MOE_ERR_TIMEOUT if a bounded wait gave up since the last check, else K3MOE_ERR_DEVICE_CHECK if
+ * bad data was seen, else K3MOE_OK (K3MOE_ERR_CUDA if the stream reports an error).
  */
 K3MOE_API k3moe_status k3moe_check_device_status(void* ws, void* stream);
 

@@ -18,6 +18,7 @@ constexpr int kMaxDModel = 25600;
 constexpr long long kMaxTerms = 3;     // E4M3 terms per activation block (x: 2 bf16 / 3 fp32; h: 3)
 constexpr long long kMaxTermsFp4 = 8;  // E2M1 terms per activation block
 constexpr long long kFp4MaxT = 2;      // the E2M1 / mxf4 path serves up to this many tokens
+constexpr uint32_t kDefaultWaitLimit = 1u << 24;  // polls of a pipeline barrier before a CTA gives up
 
 // E2M1 activation terms and kind::mxf4 MMAs for few tokens (d_model and d_ff multiples of 256).
 bool use_fp4(const k3moe_config* c, long long T) {
@@ -54,9 +55,14 @@ long long record_bytes_of(const k3moe_config* c) {
   return 3LL * ((long long)c->d_model * c->d_ff / 2 + (long long)c->d_model * c->d_ff / 32);
 }
 
-k3moe_status validate(const k3moe_config* c) {
+long long shared_stride_of(const k3moe_config* c) { return c->shared_stride ? c->shared_stride : c->record_stride; }
+
+// Every check of the config that returns K3MOE_ERR_INVALID_ARGUMENT, then those that return
+// K3MOE_ERR_UNSUPPORTED, except the tile geometry (d_model and d_ff multiples of 128), which
+// validate() adds.
+k3moe_status validate_fields(const k3moe_config* c) {
   if (!c) return K3MOE_ERR_INVALID_ARGUMENT;
-  if (c->d_model <= 0 || c->d_model % 128 || c->d_ff <= 0 || c->d_ff % 128) return K3MOE_ERR_INVALID_ARGUMENT;
+  if (c->d_model <= 0 || c->d_model % 32 || c->d_ff <= 0 || c->d_ff % 32) return K3MOE_ERR_INVALID_ARGUMENT;
   if (c->n_routed < 1 || c->n_routed > kMaxE) return K3MOE_ERR_INVALID_ARGUMENT;
   if (c->top_k < 1 || c->top_k > kMaxK || c->top_k > c->n_routed) return K3MOE_ERR_INVALID_ARGUMENT;
   if (c->n_shared < 0 || c->n_shared > kMaxS) return K3MOE_ERR_INVALID_ARGUMENT;
@@ -64,11 +70,29 @@ k3moe_status validate(const k3moe_config* c) {
     return K3MOE_ERR_INVALID_ARGUMENT;
   if (c->act_mode != K3MOE_ACT_EXACT && c->act_mode != K3MOE_ACT_MXFP4) return K3MOE_ERR_INVALID_ARGUMENT;
   if (c->x_dtype != K3MOE_X_BF16 && c->x_dtype != K3MOE_X_F32) return K3MOE_ERR_INVALID_ARGUMENT;
-  if (c->record_stride < record_bytes_of(c) || c->record_stride % 256) return K3MOE_ERR_INVALID_ARGUMENT;
+  if (c->record_order != K3MOE_ORDER_STORED && c->record_order != K3MOE_ORDER_DEVICE) return K3MOE_ERR_INVALID_ARGUMENT;
+  if (c->shared_format != K3MOE_SHARED_MXFP4 && c->shared_format != K3MOE_SHARED_BF16) return K3MOE_ERR_INVALID_ARGUMENT;
   if ((long long)c->d_model * c->d_ff > (1LL << 40)) return K3MOE_ERR_INVALID_ARGUMENT;
+  if (c->record_stride < record_bytes_of(c) || c->record_stride % 4096) return K3MOE_ERR_INVALID_ARGUMENT;
+  if (c->shared_stride < 0 || c->shared_stride % 4096) return K3MOE_ERR_INVALID_ARGUMENT;
+  const long long shared_need = c->shared_format == K3MOE_SHARED_BF16 ? 6LL * c->d_model * c->d_ff : record_bytes_of(c);
+  if (c->shared_stride && c->shared_stride < shared_need) return K3MOE_ERR_INVALID_ARGUMENT;
   if (c->act_mode != K3MOE_ACT_EXACT) return K3MOE_ERR_UNSUPPORTED;
   if (c->d_model > kMaxDModel) return K3MOE_ERR_UNSUPPORTED;  // router rows are staged in shared memory
+  if (c->shared_format != K3MOE_SHARED_MXFP4) return K3MOE_ERR_UNSUPPORTED;
   return K3MOE_OK;
+}
+
+k3moe_status validate(const k3moe_config* c) {
+  const k3moe_status s = validate_fields(c);
+  if (s != K3MOE_OK) return s;
+  if (c->d_model % 128 || c->d_ff % 128) return K3MOE_ERR_UNSUPPORTED;  // 128-row tensor-core tiles
+  return K3MOE_OK;
+}
+
+// The calls that read expert records read them in the device order only.
+k3moe_status records_readable(const k3moe_config* c) {
+  return c->record_order == K3MOE_ORDER_DEVICE ? K3MOE_OK : K3MOE_ERR_UNSUPPORTED;
 }
 
 bool tokens_ok(const k3moe_config* c, int64_t T) {
@@ -180,7 +204,9 @@ Cfg make_cfg(const k3moe_config* c, long long T) {
     k.hterms = 3;
   }
   k.rsplit = (int)router_splits(c, T);
+  k.wait_limit = kDefaultWaitLimit;
   k.stride = c->record_stride;
+  k.sstride = shared_stride_of(c);
   return k;
 }
 
@@ -202,6 +228,20 @@ size_t k3moe_record_bytes(const k3moe_config* cfg) {
   return (size_t)record_bytes_of(cfg);
 }
 
+size_t k3moe_router_parts_bytes(const k3moe_config* cfg) {
+  const k3moe_status s = validate(cfg);
+  if (s != K3MOE_OK && s != K3MOE_ERR_UNSUPPORTED) return 0;
+  return (size_t)3 * cfg->n_routed * cfg->d_model * 2;
+}
+
+k3moe_status k3moe_prepare_router(const k3moe_config* cfg, const float* w_router, uint16_t* w_parts, void* stream) {
+  const k3moe_status s = validate(cfg);
+  if (s != K3MOE_OK) return s;
+  if (!w_router || !w_parts || !aligned16(w_router) || !aligned16(w_parts)) return K3MOE_ERR_INVALID_ARGUMENT;
+  return cuda_status(k3::launch_split_router(w_router, (long long)cfg->n_routed * cfg->d_model, w_parts,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
 size_t k3moe_workspace_bytes(const k3moe_config* cfg, int64_t max_tokens) {
   if (validate(cfg) != K3MOE_OK || !tokens_ok(cfg, max_tokens)) return 0;
   // the layout grows with T except, possibly, where the E2M1 activation form gives way to the E4M3
@@ -211,14 +251,15 @@ size_t k3moe_workspace_bytes(const k3moe_config* cfg, int64_t max_tokens) {
   return a > b ? a : b;
 }
 
-k3moe_status k3moe_route(const k3moe_config* cfg, const void* x, int64_t T, const float* w_router, const float* bias,
-                         int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes, void* stream) {
+k3moe_status k3moe_route(const k3moe_config* cfg, const void* x, int64_t T, const float* w_router,
+                         const uint16_t* w_router_parts, const float* bias, int32_t* topk_idx, float* topk_w, void* ws,
+                         size_t ws_bytes, void* stream) {
   k3moe_status s = validate(cfg);
   if (s != K3MOE_OK) return s;
   if (!tokens_ok(cfg, T)) return K3MOE_ERR_INVALID_ARGUMENT;
   if (!x || !w_router || !topk_idx || !topk_w) return K3MOE_ERR_INVALID_ARGUMENT;
   if (!aligned16(x) || !aligned16(w_router) || (bias && !aligned16(bias)) || !aligned16(topk_idx) ||
-      !aligned16(topk_w))
+      !aligned16(topk_w) || (w_router_parts && !aligned16(w_router_parts)))
     return K3MOE_ERR_INVALID_ARGUMENT;
   if (T == 0) return K3MOE_OK;
   Layout L;
@@ -229,7 +270,7 @@ k3moe_status k3moe_route(const k3moe_config* cfg, const void* x, int64_t T, cons
   int mode = k3::RM_USER_OUT | (cfg->score_func == K3MOE_SCORE_SIGMOID_BIAS ? k3::RM_SIGMOID : 0);
   if (router_tc(cfg, T)) {
     // (the sigmoid score adds its bias at the selection, not to the logits)
-    cudaError_t e = k3::launch_router_tc(c, w, x, T, w_router, (mode & k3::RM_SIGMOID) ? nullptr : bias,
+    cudaError_t e = k3::launch_router_tc(c, w, x, T, w_router, w_router_parts, (mode & k3::RM_SIGMOID) ? nullptr : bias,
                                          static_cast<char*>(ws) + L.w3, static_cast<char*>(ws) + L.x3, st);
     if (e != cudaSuccess) return cuda_status(e);
     mode |= k3::RM_LOGITS_READY;
@@ -248,6 +289,7 @@ k3moe_status k3moe_expert_ffn(const k3moe_config* cfg, const void* x, int64_t T,
   if (!aligned16(x) || !aligned16(topk_idx) || !aligned16(topk_w) || !aligned16(routed_records) || !aligned16(y) ||
       (shared_records && !aligned16(shared_records)))
     return K3MOE_ERR_INVALID_ARGUMENT;
+  if ((s = records_readable(cfg)) != K3MOE_OK) return s;
   if (T == 0) return K3MOE_OK;
   Layout L;
   if ((s = check_ws(cfg, T, ws, ws_bytes, &L)) != K3MOE_OK) return s;
@@ -264,9 +306,10 @@ k3moe_status k3moe_expert_ffn(const k3moe_config* cfg, const void* x, int64_t T,
 
 namespace {
 
-k3moe_status layer_impl(const k3moe_config* cfg, const void* x, int64_t T, const float* w_router, const float* bias,
-                        const uint8_t* routed_records, const uint8_t* shared_records, float* y, int32_t* topk_idx_out,
-                        float* topk_w_out, void* ws, size_t ws_bytes, void* stream, void* const* events) {
+k3moe_status layer_impl(const k3moe_config* cfg, const void* x, int64_t T, const float* w_router,
+                        const uint16_t* w_router_parts, const float* bias, const uint8_t* routed_records,
+                        const uint8_t* shared_records, float* y, int32_t* topk_idx_out, float* topk_w_out, void* ws,
+                        size_t ws_bytes, void* stream, void* const* events, uint32_t wait_limit) {
   k3moe_status s = validate(cfg);
   if (s != K3MOE_OK) return s;
   if (!tokens_ok(cfg, T)) return K3MOE_ERR_INVALID_ARGUMENT;
@@ -274,15 +317,18 @@ k3moe_status layer_impl(const k3moe_config* cfg, const void* x, int64_t T, const
     return K3MOE_ERR_INVALID_ARGUMENT;
   if (!aligned16(x) || !aligned16(w_router) || (bias && !aligned16(bias)) || !aligned16(routed_records) ||
       !aligned16(y) || (shared_records && !aligned16(shared_records)) || (topk_idx_out && !aligned16(topk_idx_out)) ||
-      (topk_w_out && !aligned16(topk_w_out)))
+      (topk_w_out && !aligned16(topk_w_out)) || (w_router_parts && !aligned16(w_router_parts)))
     return K3MOE_ERR_INVALID_ARGUMENT;
   if (events)
     for (int i = 0; i < 6; ++i)
       if (!events[i]) return K3MOE_ERR_INVALID_ARGUMENT;
+  if (wait_limit == 0) return K3MOE_ERR_INVALID_ARGUMENT;
+  if ((s = records_readable(cfg)) != K3MOE_OK) return s;
   if (T == 0) return K3MOE_OK;
   Layout L;
   if ((s = check_ws(cfg, T, ws, ws_bytes, &L)) != K3MOE_OK) return s;
-  const Cfg c = make_cfg(cfg, T);
+  Cfg c = make_cfg(cfg, T);
+  c.wait_limit = wait_limit;
   const Ws w = bind(L, ws);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const long long wgb = wg_bound(cfg, T);
@@ -291,7 +337,7 @@ k3moe_status layer_impl(const k3moe_config* cfg, const void* x, int64_t T, const
   int mode = k3::RM_USER_OUT | k3::RM_XPREP | k3::RM_PERMUTE |
              (cfg->score_func == K3MOE_SCORE_SIGMOID_BIAS ? k3::RM_SIGMOID : 0);
   if (e == cudaSuccess && router_tc(cfg, T)) {
-    e = k3::launch_router_tc(c, w, x, T, w_router, (mode & k3::RM_SIGMOID) ? nullptr : bias,
+    e = k3::launch_router_tc(c, w, x, T, w_router, w_router_parts, (mode & k3::RM_SIGMOID) ? nullptr : bias,
                              static_cast<char*>(ws) + L.w3, static_cast<char*>(ws) + L.x3, st);
     mode |= k3::RM_LOGITS_READY;
   }
@@ -309,28 +355,39 @@ k3moe_status layer_impl(const k3moe_config* cfg, const void* x, int64_t T, const
 
 extern "C" {
 
-k3moe_status k3moe_layer(const k3moe_config* cfg, const void* x, int64_t T, const float* w_router, const float* bias,
-                         const uint8_t* routed_records, const uint8_t* shared_records, float* y, int32_t* topk_idx_out,
-                         float* topk_w_out, void* ws, size_t ws_bytes, void* stream) {
-  return layer_impl(cfg, x, T, w_router, bias, routed_records, shared_records, y, topk_idx_out, topk_w_out, ws,
-                    ws_bytes, stream, nullptr);
+k3moe_status k3moe_layer(const k3moe_config* cfg, const void* x, int64_t T, const float* w_router,
+                         const uint16_t* w_router_parts, const float* bias, const uint8_t* routed_records,
+                         const uint8_t* shared_records, float* y, int32_t* topk_idx_out, float* topk_w_out, void* ws,
+                         size_t ws_bytes, void* stream) {
+  return layer_impl(cfg, x, T, w_router, w_router_parts, bias, routed_records, shared_records, y, topk_idx_out,
+                    topk_w_out, ws, ws_bytes, stream, nullptr, kDefaultWaitLimit);
+}
+
+k3moe_status k3moe_layer_bounded(const k3moe_config* cfg, const void* x, int64_t T, const float* w_router,
+                                 const uint16_t* w_router_parts, const float* bias, const uint8_t* routed_records,
+                                 const uint8_t* shared_records, float* y, void* ws, size_t ws_bytes, uint32_t wait_limit,
+                                 void* stream) {
+  return layer_impl(cfg, x, T, w_router, w_router_parts, bias, routed_records, shared_records, y, nullptr, nullptr, ws,
+                    ws_bytes, stream, nullptr, wait_limit);
 }
 
 k3moe_status k3moe_layer_timed(const k3moe_config* cfg, const void* x, int64_t T, const float* w_router,
-                               const float* bias, const uint8_t* routed_records, const uint8_t* shared_records,
-                               float* y, int32_t* topk_idx_out, float* topk_w_out, void* ws, size_t ws_bytes,
-                               void* stream, void* const* events) {
+                               const uint16_t* w_router_parts, const float* bias, const uint8_t* routed_records,
+                               const uint8_t* shared_records, float* y, int32_t* topk_idx_out, float* topk_w_out,
+                               void* ws, size_t ws_bytes, void* stream, void* const* events) {
   if (!events) return K3MOE_ERR_INVALID_ARGUMENT;
-  return layer_impl(cfg, x, T, w_router, bias, routed_records, shared_records, y, topk_idx_out, topk_w_out, ws,
-                    ws_bytes, stream, events);
+  return layer_impl(cfg, x, T, w_router, w_router_parts, bias, routed_records, shared_records, y, topk_idx_out,
+                    topk_w_out, ws, ws_bytes, stream, events, kDefaultWaitLimit);
 }
 
 k3moe_status k3moe_pack_records(const k3moe_config* cfg, uint8_t* records, int64_t n_records, int32_t to_device,
                                 void* stream) {
-  k3moe_status s = validate(cfg);
-  if (s != K3MOE_OK && s != K3MOE_ERR_UNSUPPORTED) return s;  // only the record geometry matters here
+  // only the record geometry matters here (d_model, d_ff, record_stride)
+  k3moe_status s = validate_fields(cfg);
+  if (s != K3MOE_OK && s != K3MOE_ERR_UNSUPPORTED) return s;
   if (!records || !aligned16(records) || n_records < 0 || (to_device != 0 && to_device != 1))
     return K3MOE_ERR_INVALID_ARGUMENT;
+  if (cfg->d_model % 128 || cfg->d_ff % 128) return K3MOE_ERR_UNSUPPORTED;
   if (n_records == 0) return K3MOE_OK;
   return cuda_status(k3::launch_pack_records(records, n_records, cfg->record_stride, cfg->d_model, cfg->d_ff, to_device,
                                             static_cast<cudaStream_t>(stream)));
@@ -346,6 +403,15 @@ k3moe_status k3moe_residual_add(float* x, const float* y, int64_t n, void* strea
   if (!x || !y || n < 0) return K3MOE_ERR_INVALID_ARGUMENT;
   if (n == 0) return K3MOE_OK;
   return cuda_status(k3::launch_residual_add(x, y, n, static_cast<cudaStream_t>(stream)));
+}
+
+k3moe_status k3moe_residual_rmsnorm(float* x, const float* y, int64_t T, int32_t d, float eps, float* xn,
+                                    void* stream) {
+  if (!x || !xn || T < 0 || d <= 0 || d % 4 || !(eps >= 0.0f) || !aligned16(x) || !aligned16(xn) ||
+      (y && !aligned16(y)))
+    return K3MOE_ERR_INVALID_ARGUMENT;
+  if (T == 0) return K3MOE_OK;
+  return cuda_status(k3::launch_residual_rmsnorm(x, y, T, d, eps, xn, static_cast<cudaStream_t>(stream)));
 }
 
 k3moe_status k3moe_check_device_status(void* ws, void* stream) {

@@ -17,7 +17,9 @@ struct Cfg {
   int xterms;         // terms per activation block of x (E4M3: 2 for bf16 x, 3 for fp32 x; E2M1: 8 or 16)
   int hterms;         // terms per block of h
   int rsplit;         // partial logits the router kernel adds up (parts of the tensor-core reduction; 1: final)
-  long long stride;   // bytes between expert records
+  uint32_t wait_limit;  // polls of a pipeline barrier before a CTA gives up (K3MOE_ERR_TIMEOUT)
+  long long stride;   // bytes between routed expert records
+  long long sstride;  // bytes between shared expert records
 };
 
 // Control block at the start of the workspace (int32 slots).

@@ -33,13 +33,18 @@ cudaError_t launch_route(const Cfg& c, const Ws& ws, const void* x, long long T,
 cudaError_t launch_prep(const Cfg& c, const Ws& ws, const void* x, long long T, const int* idx, const float* w,
                         cudaStream_t st);
 cudaError_t launch_rmsnorm(const float* x, long long T, int d, float eps, float* out, cudaStream_t st);
+cudaError_t launch_residual_rmsnorm(float* x, const float* y, long long T, int d, float eps, float* out,
+                                    cudaStream_t st);
 
 // k3moe_router_tc.cu: router logits on the tensor cores (the token counts where this runs are chosen
 // in k3moe_api.cu). `w3` is workspace for the three bf16 parts of the router weights ([3, E, d]), `x3`
 // for those of fp32 tokens ([3, T, d]); the logits are written as c.rsplit partial sums ([rsplit, T, E],
 // see Cfg).
-cudaError_t launch_router_tc(const Cfg& c, const Ws& ws, const void* x, long long T, const float* W, const float* bias,
-                             void* w3, void* x3, cudaStream_t st);
+// `w_parts` ([3, E, d] bf16, prepared at weight-loading time) replaces the per-call split into w3 if given.
+cudaError_t launch_router_tc(const Cfg& c, const Ws& ws, const void* x, long long T, const float* W,
+                             const void* w_parts, const float* bias, void* w3, void* x3, cudaStream_t st);
+// The three bf16 parts of n fp32 values (n a multiple of 4, both pointers 16-byte aligned).
+cudaError_t launch_split_router(const float* W, long long n, void* parts, cudaStream_t st);
 cudaError_t launch_residual_add(float* x, const float* y, long long n, cudaStream_t st);
 
 // k3moe_tc.cu (tcgen05 expert FFN)

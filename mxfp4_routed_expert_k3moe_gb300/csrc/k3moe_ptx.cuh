@@ -28,6 +28,17 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Non-blocking test of a phase (used when a caller asks for a very small wait bound: unlike
+// try_wait, it never suspends the thread, so one poll is one poll).
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.b32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 // L2 policy for data read once (the weight stream): evicted first, so that the small arrays that
 // every CTA reads repeatedly (work groups, activation terms) stay in L2 instead of queueing behind
 // the stream at the DRAM.

@@ -50,9 +50,11 @@ __device__ void xterms_rows(const Cfg& c, const Ws& ws, const void* x, long long
     }
 }
 
-// Orderable 64-bit key: larger logit first, then lower expert id. Key 0 marks an empty entry.
+// Orderable 64-bit key: larger logit first, then lower expert id. Key 0 marks an empty entry. -0 is
+// keyed as +0, so that the two zeros compare equal (and the lower id wins) as they do in the oracle.
 __device__ __forceinline__ unsigned long long topk_key(float l, int e) {
   uint32_t u = __float_as_uint(l);
+  if (u == 0x80000000u) u = 0u;
   uint32_t o = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
   return ((unsigned long long)o << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)e);
 }
@@ -698,6 +700,8 @@ __global__ void __launch_bounds__(256) k_prep(PrepArgs a) {
 
 __global__ void __launch_bounds__(256) k_rmsnorm(const float* x, long long T, int d, float eps, float* out) {
   __shared__ float s_red[8];
+  pdl_wait();
+  pdl_launch_dependents();
   for (long long t = blockIdx.x; t < T; t += gridDim.x) {
     const float* xr = x + t * d;
     float ss = 0.0f;
@@ -715,8 +719,51 @@ __global__ void __launch_bounds__(256) k_rmsnorm(const float* x, long long T, in
 }
 
 __global__ void k_residual_add(float* x, const float* y, long long n) {
+  pdl_wait();
+  pdl_launch_dependents();
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
     x[i] += y[i];
+}
+
+// x += y (if y), then out = RMSNorm(x), one CTA per token row, 16-byte accesses (d a multiple of 4).
+// The dependents are released at once: the next layer's router kernel is scheduled while this one
+// runs and starts streaming its weights (which no kernel writes) before it waits for this one.
+__global__ void __launch_bounds__(256) k_residual_rmsnorm(float* x, const float* y, long long T, int d, float eps,
+                                                          float* out) {
+  __shared__ float s_red[8];
+  pdl_wait();
+  pdl_launch_dependents();
+  for (long long t = blockIdx.x; t < T; t += gridDim.x) {
+    float* xr = x + t * d;
+    float ss = 0.0f;
+    for (int j = 4 * threadIdx.x; j < d; j += 4 * blockDim.x) {
+      float4 v = *reinterpret_cast<const float4*>(xr + j);
+      if (y) {
+        const float4 u = *reinterpret_cast<const float4*>(y + t * d + j);
+        v.x += u.x;
+        v.y += u.y;
+        v.z += u.z;
+        v.w += u.w;
+        *reinterpret_cast<float4*>(xr + j) = v;
+      }
+      ss = fmaf(v.x, v.x, ss);
+      ss = fmaf(v.y, v.y, ss);
+      ss = fmaf(v.z, v.z, ss);
+      ss = fmaf(v.w, v.w, ss);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    float tot = 0.0f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += s_red[w];
+    const float r = 1.0f / sqrtf(tot / (float)d + eps);
+    for (int j = 4 * threadIdx.x; j < d; j += 4 * blockDim.x) {  // (the same thread's x values as above)
+      const float4 v = *reinterpret_cast<const float4*>(xr + j);
+      *reinterpret_cast<float4*>(out + t * d + j) = make_float4(v.x * r, v.y * r, v.z * r, v.w * r);
+    }
+    __syncthreads();
+  }
 }
 
 // Selection with logits computed by the tensor cores (k_router_mma): grid (G, T). CTA (0, t) selects
@@ -844,16 +891,20 @@ cudaError_t launch_prep(const Cfg& c, const Ws& ws, const void* x, long long T, 
 }
 
 cudaError_t launch_rmsnorm(const float* x, long long T, int d, float eps, float* out, cudaStream_t st) {
-  long long blocks = T < 152 * 16 ? T : 152 * 16;
-  k_rmsnorm<<<(unsigned)blocks, 256, 0, st>>>(x, T, d, eps, out);
-  return cudaGetLastError();
+  const long long blocks = T < 152 * 16 ? T : 152 * 16;
+  return launch_pdl(k_rmsnorm, dim3((unsigned)blocks), dim3(256), 0, st, x, T, d, eps, out);
 }
 
 cudaError_t launch_residual_add(float* x, const float* y, long long n, cudaStream_t st) {
   long long blocks = (n + 255) / 256;
   if (blocks > 152 * 32) blocks = 152 * 32;
-  k_residual_add<<<(unsigned)blocks, 256, 0, st>>>(x, y, n);
-  return cudaGetLastError();
+  return launch_pdl(k_residual_add, dim3((unsigned)blocks), dim3(256), 0, st, x, y, n);
+}
+
+cudaError_t launch_residual_rmsnorm(float* x, const float* y, long long T, int d, float eps, float* out,
+                                    cudaStream_t st) {
+  const long long blocks = T < 152 * 16 ? T : 152 * 16;
+  return launch_pdl(k_residual_rmsnorm, dim3((unsigned)blocks), dim3(256), 0, st, x, y, T, d, eps, out);
 }
 
 }  // namespace k3

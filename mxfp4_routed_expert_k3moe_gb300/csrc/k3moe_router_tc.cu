@@ -39,7 +39,8 @@ constexpr int kRStages = 4;
 constexpr int kRThreads = 128;
 constexpr int kRA = kRM * kRK * 2;        // 16 KB
 constexpr int kRB = kRN * kRK * 2;        // 32 KB
-constexpr uint32_t kRWaitLimit = 1u << 24;
+constexpr uint32_t kRWaitLimit = 1u << 24;  // bound of the drain waits (the pipeline's come with the call)
+constexpr uint32_t kRPollTestBelow = 64;    // pipeline bounds below this poll with test_wait
 
 struct RCtl {
   uint64_t full[kRStages];
@@ -49,14 +50,25 @@ struct RCtl {
   volatile int abort;
 };
 
-__device__ __forceinline__ bool rwait(uint32_t bar, uint32_t parity, RCtl* ctl, int* status) {
-  for (uint32_t it = 0; it < kRWaitLimit; ++it) {
-    if (mbar_try(bar, parity)) return true;
+// Pipeline wait: at most `limit` polls, then ST_TIMEOUT and the CTA's abort flag.
+__device__ __forceinline__ bool rwait(uint32_t bar, uint32_t parity, RCtl* ctl, int* status, uint32_t limit) {
+  const bool test = limit < kRPollTestBelow;
+  for (uint32_t it = 0; it < limit; ++it) {
+    if (test ? mbar_test(bar, parity) : mbar_try(bar, parity)) return true;
     if (ctl->abort) return false;
     if (it > 256) __nanosleep(64);
   }
   ctl->abort = 1;
   atomicOr(&status[CTRL_STATUS], ST_TIMEOUT);
+  return false;
+}
+
+// Wait for copies or MMAs this CTA started (bounded, not cut short by the abort flag).
+__device__ __forceinline__ bool rdrain(uint32_t bar, uint32_t parity) {
+  for (uint32_t it = 0; it < kRWaitLimit; ++it) {
+    if (mbar_try(bar, parity)) return true;
+    if (it > 256) __nanosleep(64);
+  }
   return false;
 }
 
@@ -88,7 +100,8 @@ __global__ void __launch_bounds__(256) k_split_w(const float* W, long long n, __
 
 __global__ void __launch_bounds__(kRThreads, 1)
     k_router_mma(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
-                 const float* bias, float* logits, long long T, int E, int d, int npairs, int nsplit, int* status) {
+                 const float* bias, float* logits, long long T, int E, int d, int npairs, int nsplit, int* status,
+                 uint32_t wait_limit) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   RCtl* ctl = reinterpret_cast<RCtl*>(smem + kRStages * (kRA + kRB));
@@ -118,10 +131,15 @@ __global__ void __launch_bounds__(kRThreads, 1)
   bool ok = true;
   if (warp == 0) {
     if (lane == 0) {  // tensor copies
+      int filled = 0;  // stages filled (the last fill of stage s was round (filled - 1 - s) / kRStages)
       for (int ks = kb, s = 0; ks < ke && ok; ++ks) {
         const int i = ks - kb;
         const uint32_t round = (uint32_t)(i / kRStages);
-        if (i >= kRStages && !rwait(su32(&ctl->empty[s]), (round - 1) & 1u, ctl, status)) { ok = false; break; }
+        if (i >= kRStages && !rwait(su32(&ctl->empty[s]), (round - 1) & 1u, ctl, status, wait_limit)) {
+          ok = false;
+          break;
+        }
+        filled = i + 1;
         const int pair = ks / kpp, k0 = (ks - pair * kpp) * kRK;
         uint8_t* st = smem + (size_t)s * (kRA + kRB);
         mbar_expect_tx(su32(&ctl->full[s]), kRA + kRB);
@@ -129,15 +147,20 @@ __global__ void __launch_bounds__(kRThreads, 1)
         tma_load_3d(su32(st + kRA), &map_w, k0, nt * kRN, kPairB[pair], su32(&ctl->full[s]));
         if (++s == kRStages) s = 0;
       }
-      // after a timeout, give copies still in flight time to land before the CTA exits
+      // after a timeout, the last fill of every stage lands before the CTA frees its memory (earlier
+      // fills were consumed by MMAs that completed before the stage was refilled)
       if (!ok)
-        for (int w = 0; w < 1000; ++w) __nanosleep(1000);
+        for (int s2 = 0; s2 < kRStages && s2 < filled; ++s2)
+          rdrain(su32(&ctl->full[s2]), (uint32_t)((filled - 1 - s2) / kRStages) & 1u);
     }
   } else if (warp == 1) {
     if (lane == 0) {  // MMAs
       const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kRN >> 3) << 17) | ((uint32_t)(kRM >> 4) << 24);
       for (int ks = kb, s = 0; ks < ke; ++ks) {
-        if (!rwait(su32(&ctl->full[s]), (uint32_t)((ks - kb) / kRStages) & 1u, ctl, status)) { ok = false; break; }
+        if (!rwait(su32(&ctl->full[s]), (uint32_t)((ks - kb) / kRStages) & 1u, ctl, status, wait_limit)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         const uint8_t* st = smem + (size_t)s * (kRA + kRB);
         const uint64_t da = sw128_desc(su32(st)), db = sw128_desc(su32(st + kRA));
@@ -154,7 +177,8 @@ __global__ void __launch_bounds__(kRThreads, 1)
   // are free once every MMA completed (rows of kRN + 1 floats: conflict-free both ways), and each warp
   // then stores whole rows of logits (a thread per accumulator row stored 32 scattered rows per
   // instruction)
-  const bool have = __syncthreads_and(__all_sync(0xffffffffu, rwait(su32(&ctl->done), 0, ctl, status)));
+  // (every MMA issued has completed once `done` arrives, aborted or not: the wait is not cut short)
+  const bool have = __syncthreads_and(__all_sync(0xffffffffu, rdrain(su32(&ctl->done), 0)) && !ctl->abort);
   tc_fence_after();
   float* tile = reinterpret_cast<float*>(smem);
   if (have) {
@@ -204,16 +228,25 @@ cudaError_t encode_fn() {
 
 }  // namespace
 
-cudaError_t launch_router_tc(const Cfg& c, const Ws& ws, const void* x, long long T, const float* W, const float* bias,
-                             void* w3, void* x3, cudaStream_t st) {
+cudaError_t launch_split_router(const float* W, long long n, void* parts, cudaStream_t st) {
+  if (n % 4) return cudaErrorInvalidValue;
+  return launch_pdl(k_split_w, dim3(4 * 152), dim3(256), 0, st, W, n, static_cast<__nv_bfloat16*>(parts));
+}
+
+cudaError_t launch_router_tc(const Cfg& c, const Ws& ws, const void* x, long long T, const float* W,
+                             const void* w_parts, const float* bias, void* w3, void* x3, cudaStream_t st) {
   if (c.d % kRK != 0 || T > (1LL << 31) - kRM || (c.x_f32 && !x3) || c.rsplit < 1 ||
       c.rsplit > (c.x_f32 ? 6 : 3) * (c.d / kRK))
     return cudaErrorInvalidValue;
   cudaError_t e = encode_fn();
   if (e != cudaSuccess) return e;
   const long long n = (long long)c.E * c.d;
-  e = launch_pdl(k_split_w, dim3(4 * 152), dim3(256), 0, st, W, n, static_cast<__nv_bfloat16*>(w3));
-  if (e != cudaSuccess) return e;
+  if (w_parts) {  // prepared when the weights were loaded
+    w3 = const_cast<void*>(w_parts);
+  } else {
+    e = launch_pdl(k_split_w, dim3(4 * 152), dim3(256), 0, st, W, n, static_cast<__nv_bfloat16*>(w3));
+    if (e != cudaSuccess) return e;
+  }
   if (c.x_f32) {  // fp32 tokens: three bf16 parts as well
     e = launch_pdl(k_split_w, dim3(4 * 152), dim3(256), 0, st, static_cast<const float*>(x), T * c.d,
                    static_cast<__nv_bfloat16*>(x3));
@@ -247,7 +280,7 @@ cudaError_t launch_router_tc(const Cfg& c, const Ws& ws, const void* x, long lon
   }
   dim3 grid((unsigned)((T + kRM - 1) / kRM), (unsigned)((c.E + kRN - 1) / kRN), (unsigned)c.rsplit);
   return launch_pdl(k_router_mma, grid, dim3(kRThreads), smem, st, mx, mw, bias, ws.logits, T, c.E, c.d,
-                    c.x_f32 ? 6 : 3, c.rsplit, ws.ctrl);
+                    c.x_f32 ? 6 : 3, c.rsplit, ws.ctrl, c.wait_limit);
 }
 
 }  // namespace k3

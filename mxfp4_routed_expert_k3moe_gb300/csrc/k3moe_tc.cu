@@ -66,7 +66,8 @@ constexpr int kMaxStages = 16;
 constexpr int kMaxBuf = 4;               // accumulator buffers per issuer
 constexpr int kEpRing = 4;               // work groups the epilogue fetches ahead (cp.async)
 constexpr int kATile = 128 * 128;        // A tile of a chunk in shared memory (both forms)
-constexpr uint32_t kWaitLimit = 1u << 24;
+constexpr uint32_t kWaitLimit = 1u << 24;  // bound of the drain waits (the pipeline's come with the call)
+constexpr uint32_t kPollTestBelow = 64;    // wait bounds below this poll with test_wait (one poll = one test)
 
 using namespace ptx;
 
@@ -103,15 +104,27 @@ struct Ring {
   }
 };
 
-// Bounded wait; on timeout raises ST_TIMEOUT and the CTA-wide abort flag.
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Ctl* ctl, int* status) {
-  for (uint32_t it = 0; it < kWaitLimit; ++it) {
-    if (mbar_try(bar, parity)) return true;
+// Bounded wait of the pipeline: at most `limit` polls; on timeout it raises ST_TIMEOUT and the
+// CTA-wide abort flag, and every later wait of the CTA returns false at once.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Ctl* ctl, int* status, uint32_t limit) {
+  const bool test = limit < kPollTestBelow;
+  for (uint32_t it = 0; it < limit; ++it) {
+    if (test ? mbar_test(bar, parity) : mbar_try(bar, parity)) return true;
     if (ctl->abort) return false;
     if (it > 256) __nanosleep(64);
   }
   ctl->abort = 1;
   atomicOr(&status[CTRL_STATUS], ST_TIMEOUT);
+  return false;
+}
+
+// Wait for copies or MMAs that this CTA started, before it frees the memory they write: bounded by
+// kWaitLimit whatever bound the call gave the pipeline, and not cut short by the abort flag.
+__device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity) {
+  for (uint32_t it = 0; it < kWaitLimit; ++it) {
+    if (mbar_try(bar, parity)) return true;
+    if (it > 256) __nanosleep(64);
+  }
   return false;
 }
 
@@ -205,7 +218,7 @@ __device__ __forceinline__ const uint8_t* scale_tile(const TcArgs& a, const Item
   const Cfg& c = a.c;
   const long long nc = (long long)c.d * c.f / 2, ns = (long long)c.d * c.f / 32;
   const uint8_t* rec = it.wg.expert < c.E ? a.routed + (long long)it.wg.expert * c.stride
-                                          : a.shared + (long long)(it.wg.expert - c.E) * c.stride;
+                                          : a.shared + (long long)(it.wg.expert - c.E) * c.sstride;
   const int K = MODE == GATEUP ? c.d : c.f;
   const long long off = MODE == GATEUP ? (it.mat == 0 ? nc : 2 * nc + ns) : 2 * (nc + ns) + nc;
   return rec + off + (long long)it.mt * 128 * (K / 32);
@@ -315,6 +328,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     Item it;
     long long kk = 0;
+    uint32_t issued = 0;  // bit s: this loader filled slot s at least once; its last round's parity is bit s of `par`
+    uint32_t par = 0;
     for (long long ii = blockIdx.x; ok && item_geom<MODE>(a, ii, n_items, it); ii += gridDim.x, ++kk) {
       const int slot = (int)(kk % kEpRing);
       // the group committed two items ago holds this item's tokens and the work group two ahead
@@ -363,8 +378,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = it.j0; j < it.j1; j += CH, rg.next(S)) {
         const int s = rg.s;
         if (s % kLoaders != lv) continue;
-        if (rg.wrapped) ok = __all_sync(0xffffffffu, wait_bar(su32(&ctl->empty[s]), rg.ph ^ 1u, ctl, status));
+        if (rg.wrapped)
+          ok = __all_sync(0xffffffffu, wait_bar(su32(&ctl->empty[s]), rg.ph ^ 1u, ctl, status, c.wait_limit));
         if (!ok) break;
+        issued |= 1u << s;
+        par = (par & ~(1u << s)) | (rg.ph << s);
         uint8_t* st = smem + (size_t)s * a.stage_bytes;
         if (lane == 0) {
           // weight codes (tensor copy) and the chunks' A scale groups (one bulk copy each: the
@@ -404,9 +422,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
-    // after a timeout, give a weight tile still in flight time to land before the CTA exits
+    // after a timeout: the last fill of each of this loader's slots (tensor and bulk copies, and the
+    // lanes' cp.async, all counted by the slot's full barrier) lands before the CTA frees its memory.
+    // Earlier fills of a slot have landed: the slot was refilled only after their MMAs completed.
     if (!ok && lane == 0)
-      for (int w = 0; w < 1000; ++w) __nanosleep(1000);
+      for (int s = 0; s < S; ++s)
+        if ((issued >> s) & 1u) drain_wait(su32(&ctl->full[s]), (par >> s) & 1u);
+    __syncwarp();
   } else if (warp >= kWarpIss) {
     // ------------------------------------------------------------ MMA issuers
     const int w = warp - kWarpIss;
@@ -427,14 +449,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (long long ii = blockIdx.x; ok && item_geom<MODE>(a, ii, n_items, it); ii += gridDim.x, ++i) {
         const long long rb = i / a.n_buf;  // the buffer's round
         const int b = (int)(i - rb * a.n_buf);
-        if (rb > 0 && !wait_bar(su32(&ctl->acc_empty[b]), (uint32_t)((rb - 1) & 1), ctl, status)) break;
+        if (rb > 0 && !wait_bar(su32(&ctl->acc_empty[b]), (uint32_t)((rb - 1) & 1), ctl, status, c.wait_limit)) break;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)((b * a.n_iss + w) * a.n_acc * a.acc_cols);
         uint32_t started = 0;  // bit h: accumulator h already holds a partial sum of this item
         for (int j = it.j0; j < it.j1; j += CH, rg.next(S)) {
           const int s = rg.s;
           if (s % a.n_iss != w) continue;
-          if (!wait_bar(su32(&ctl->full[s]), rg.ph, ctl, status)) { ok = false; break; }
+          if (!wait_bar(su32(&ctl->full[s]), rg.ph, ctl, status, c.wait_limit)) { ok = false; break; }
           tc_fence_after();
           fence_async_smem();  // B rows and scale words arrived through cp.async (generic proxy)
           const uint64_t so = (uint64_t)(s * st16);
@@ -471,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_commit(su32(&ctl->acc_full[b]));
       }
       tc_commit(su32(&ctl->drain));  // every MMA issued above has completed when this arrives
-      wait_bar(su32(&ctl->drain), 0, ctl, status);
+      drain_wait(su32(&ctl->drain), 0);
     }
   } else {
     // ------------------------------------------------------------ epilogue (warps 0-3)
@@ -507,7 +529,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nst = (it.j1 - it.j0) / CH;  // stages of the item
       const long long rb = i / a.n_buf;
       const int b = (int)(i - rb * a.n_buf);
-      bool okw = __all_sync(0xffffffffu, wait_bar(su32(&ctl->acc_full[b]), (uint32_t)(rb & 1), ctl, status));
+      bool okw =
+          __all_sync(0xffffffffu, wait_bar(su32(&ctl->acc_full[b]), (uint32_t)(rb & 1), ctl, status, c.wait_limit));
       // gate/up: the four warps agree (they meet at a barrier below); this also keeps the exchange
       // area of the previous item until every warp has read it
       if (MODE == GATEUP) okw = bar_and(1, 128, okw);
@@ -887,16 +910,17 @@ cudaError_t setup(const Cfg& c, const uint8_t* routed, const uint8_t* shared, in
   const long long nc = (long long)c.d * c.f / 2, ns = (long long)c.d * c.f / 32;
   sh = (c.S > 0 && shared) ? shared : routed;
   const long long sh_n = c.S > 0 ? c.S : 1;
+  const long long sh_stride = (c.S > 0 && shared) ? c.sstride : c.stride;
   cudaError_t e;
   if (ch_gu > 0) {
     if ((e = weight_map(routed, c.d, c.f, c.E, c.stride, ch_gu, f4, &m.gr)) != cudaSuccess) return e;
     if ((e = weight_map(routed + nc + ns, c.d, c.f, c.E, c.stride, ch_gu, f4, &m.ur)) != cudaSuccess) return e;
-    if ((e = weight_map(sh, c.d, c.f, sh_n, c.stride, ch_gu, f4, &m.gs)) != cudaSuccess) return e;
-    if ((e = weight_map(sh + nc + ns, c.d, c.f, sh_n, c.stride, ch_gu, f4, &m.us)) != cudaSuccess) return e;
+    if ((e = weight_map(sh, c.d, c.f, sh_n, sh_stride, ch_gu, f4, &m.gs)) != cudaSuccess) return e;
+    if ((e = weight_map(sh + nc + ns, c.d, c.f, sh_n, sh_stride, ch_gu, f4, &m.us)) != cudaSuccess) return e;
   }
   if (ch_dn > 0) {
     if ((e = weight_map(routed + 2 * (nc + ns), c.f, c.d, c.E, c.stride, ch_dn, f4, &m.dr)) != cudaSuccess) return e;
-    if ((e = weight_map(sh + 2 * (nc + ns), c.f, c.d, sh_n, c.stride, ch_dn, f4, &m.ds)) != cudaSuccess) return e;
+    if ((e = weight_map(sh + 2 * (nc + ns), c.f, c.d, sh_n, sh_stride, ch_dn, f4, &m.ds)) != cudaSuccess) return e;
   }
   return cudaSuccess;
 }

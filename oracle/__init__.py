@@ -56,6 +56,9 @@ def lib():
         L.k3o_route_token.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P, _P, _P,
                                       ctypes.c_int32]
         L.k3o_route_token.restype = ctypes.c_int
+        L.k3o_route_tokens.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P, ctypes.c_int32,
+                                       ctypes.c_int64, _P, _P, _P, _P, _P, ctypes.c_int32]
+        L.k3o_route_tokens.restype = ctypes.c_int
         L.k3o_expert_token.argtypes = [ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P]
         L.k3o_expert_token.restype = ctypes.c_int
         L.k3o_layer.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
@@ -131,6 +134,26 @@ def route_token(x: np.ndarray, W: np.ndarray, k: int, bias: np.ndarray | None = 
     w = np.empty(k, np.float64)
     if lib().k3o_route_token(E, d, k, _ptr(x), _ptr(W), _ptr(b), _ptr(logits), _ptr(idx), _ptr(w), SCORES[score]):
         raise ValueError("route_token failed")
+    return logits, idx, w
+
+
+def route_tokens(x: np.ndarray, x_dtype: str, W: np.ndarray, k: int, bias: np.ndarray | None = None,
+                 score: str = "softmax"):
+    """Routing of T tokens (route_token per token, tokens in parallel): x [T, d] uint16 bf16 bits
+    ('bf16') or float32 ('f32'). -> (logits[T, E], idx[T, k], w[T, k])."""
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    E, d = W.shape
+    xa = np.ascontiguousarray(x, dtype=np.uint16 if x_dtype == "bf16" else np.float32)
+    if xa.ndim != 2 or xa.shape[1] != d:
+        raise ValueError("route_tokens: x must be [T, d]")
+    T = xa.shape[0]
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    logits = np.empty((T, E), np.float64)
+    idx = np.empty((T, k), np.int32)
+    w = np.empty((T, k), np.float64)
+    if lib().k3o_route_tokens(E, d, k, _ptr(xa), 1 if x_dtype == "bf16" else 0, T, _ptr(W), _ptr(b), _ptr(logits),
+                              _ptr(idx), _ptr(w), SCORES[score]):
+        raise ValueError("route_tokens failed")
     return logits, idx, w
 
 

@@ -187,6 +187,36 @@ int k3o_route_token(int32_t E, int32_t d, int32_t k, const double* x, const floa
     return 0;
 }
 
+/*
+ * Route T tokens (the per-token routine above, tokens in parallel): x is T x d,
+ * bf16 bit patterns (x_is_bf16 = 1) or fp32 (0); logits_out[T][E] (may be NULL),
+ * idx_out[T][k], w_out[T][k]. Used by the tests to check every token's selection
+ * at prefill sizes, where the expert FFN of every token would take too long.
+ */
+int k3o_route_tokens(int32_t E, int32_t d, int32_t k, const void* x, int32_t x_is_bf16, int64_t T,
+                     const float* W, const float* bias, double* logits_out, int32_t* idx_out,
+                     double* w_out, int32_t score) {
+    int status = 0;
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t t = 0; t < T; ++t) {
+        double* xt = (double*)malloc(sizeof(double) * (size_t)d);
+        int st = xt ? 0 : -2;
+        if (!st) {
+            for (int32_t j = 0; j < d; ++j)
+                xt[j] = x_is_bf16 ? k3o_bf16(((const uint16_t*)x)[t * d + j])
+                                  : (double)((const float*)x)[t * d + j];
+            st = k3o_route_token(E, d, k, xt, W, bias, logits_out ? logits_out + t * E : NULL,
+                                 idx_out + t * k, w_out + t * k, score);
+        }
+        if (st) {
+#pragma omp critical
+            if (!status) status = st;
+        }
+        free(xt);
+    }
+    return status;
+}
+
 /* ------------------------------------------------------------------ expert FFN */
 static double silu(double z) { return z / (1.0 + exp(-z)); }
 

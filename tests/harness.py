@@ -70,7 +70,8 @@ class DeviceLayer:
             synth.records_device(shape, seed, layer, E, S, self.shared.data_ptr(), self.stride, st)
         self.cfg = k3.Config.make(shape.d_model, shape.d_ff, E, shape.top_k, S,
                                   x_dtype=k3.X_BF16 if x_dtype == "bf16" else k3.X_F32, record_stride=self.stride,
-                                  score_func=k3.SCORE_SOFTMAX if score == "softmax" else k3.SCORE_SIGMOID_BIAS)
+                                  score_func=k3.SCORE_SOFTMAX if score == "softmax" else k3.SCORE_SIGMOID_BIAS,
+                                  record_order=k3.ORDER_DEVICE if pack else k3.ORDER_STORED)
         if pack:
             k3.pack_records(self.cfg, self.routed, E)
             if S:
@@ -108,6 +109,11 @@ class DeviceLayer:
         return oracle.layer(x, self.x_dtype, self.W_host, self.bias_host, routed, shared, sh.d_model, sh.d_ff,
                             sh.top_k, score=self.score)
 
+    def oracle_route(self, xh: np.ndarray):
+        """Oracle routing of every token (logits[T, E], idx[T, k], w[T, k]), tokens in parallel."""
+        import oracle
+        return oracle.route_tokens(xh, self.x_dtype, self.W_host, self.shape.top_k, self.bias_host, score=self.score)
+
     def sel_keys(self, logits_ref: np.ndarray) -> np.ndarray:
         """The values the oracle ranked (for the near-tie rule): the logits (bias included) for the
         softmax score; sigmoid(logit) + bias for the sigmoid score."""
@@ -132,28 +138,47 @@ class DeviceLayer:
         return y
 
 
-def index_parity(idx_gpu: np.ndarray, idx_ref: np.ndarray, logits_ref: np.ndarray, k: int):
-    """Per token: True if the top-k matches the oracle (positions where adjacent oracle logits differ by
-    >= INDEX_GAP must agree; a set difference is allowed only when the oracle's k-th and (k+1)-th logits
-    are within INDEX_GAP). Returns (ok_all, list of near-tie token ids)."""
+def oracle_order(keys: np.ndarray) -> np.ndarray:
+    """The oracle's ranking of one token's experts: larger value first, equal values lower index first."""
+    return np.lexsort((np.arange(len(keys)), -keys))
+
+
+def index_parity(idx_gpu: np.ndarray, idx_ref: np.ndarray, keys_ref: np.ndarray, k: int):
+    """The contract on the top-k indices, per token (keys_ref: the values the oracle ranked, fp64):
+    * the GPU's k ids are distinct and in range;
+    * the set equals the oracle's, except that where the oracle's k-th and (k+1)-th values differ by
+      less than INDEX_GAP (and are not equal) the GPU may hold the (k+1)-th expert in place of the k-th:
+      that exchange and no other;
+    * the order: any two GPU positions i < j rank as the oracle ranks them (larger value first, equal
+      values lower id first), except two experts whose values differ by less than INDEX_GAP without
+      being equal. Exactly equal values get no excuse: the lower id comes first.
+    Returns (ok_all, list of tokens that took the exchange, first failure message or None)."""
     near = []
+    E = keys_ref.shape[1]
     for t in range(idx_ref.shape[0]):
-        srt = np.sort(logits_ref[t])[::-1]
-        gap = srt[k - 1] - srt[k] if len(srt) > k else np.inf
-        if set(idx_gpu[t].tolist()) != set(idx_ref[t].tolist()):
-            if gap >= INDEX_GAP:
-                return False, near
+        keys = keys_ref[t]
+        g = [int(e) for e in idx_gpu[t]]
+        order = oracle_order(keys)
+        if [int(e) for e in order[:k]] != [int(e) for e in idx_ref[t]]:
+            return False, near, f"token {t}: oracle selection is not its own ranking"
+        if len(set(g)) != k or min(g) < 0 or max(g) >= E:
+            return False, near, f"token {t}: GPU ids {g} not {k} distinct ids in [0, {E})"
+        sg, sr = set(g), set(int(e) for e in idx_ref[t])
+        if sg != sr:
+            kth, k1th = int(order[k - 1]), int(order[k]) if E > k else -1
+            gap = keys[kth] - keys[k1th] if k1th >= 0 else np.inf
+            if not (sg - sr == {k1th} and sr - sg == {kth} and 0.0 < gap < INDEX_GAP):
+                return False, near, f"token {t}: sets differ by {sorted(sg - sr)} / {sorted(sr - sg)} (gap {gap:.3g})"
             near.append(t)
-            continue
-        lg = logits_ref[t][idx_ref[t]]
         for i in range(k):
-            if idx_gpu[t][i] != idx_ref[t][i]:
-                # allowed only inside a run of near-equal logits
-                j = list(idx_ref[t]).index(idx_gpu[t][i])
-                lo, hi = min(i, j), max(i, j)
-                if lg[lo] - lg[hi] >= INDEX_GAP:
-                    return False, near
-    return True, near
+            for j in range(i + 1, k):
+                a, b = g[i], g[j]
+                if keys[a] > keys[b] or (keys[a] == keys[b] and a < b):
+                    continue
+                if keys[a] != keys[b] and abs(keys[a] - keys[b]) < INDEX_GAP:
+                    continue
+                return False, near, f"token {t}: positions {i}, {j} hold {a}, {b} out of the oracle's order"
+    return True, near, None
 
 
 def rel_err(y_gpu: np.ndarray, y_ref: np.ndarray) -> float:

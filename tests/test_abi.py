@@ -53,25 +53,48 @@ def test_workspace_never_shrinks_as_tokens_grow(x_dtype):
 
 
 @pytest.mark.parametrize("field,value,code", [
-    ("d_model", 100, k3.ERR_INVALID_ARGUMENT),
+    ("d_model", 100, k3.ERR_INVALID_ARGUMENT),   # not a multiple of 32
+    ("d_model", 160, k3.ERR_UNSUPPORTED),        # a multiple of 32, not of 128: legal, not implemented
     ("d_ff", 0, k3.ERR_INVALID_ARGUMENT),
+    ("d_ff", 1504, k3.ERR_UNSUPPORTED),
     ("top_k", 0, k3.ERR_INVALID_ARGUMENT),
     ("top_k", 33, k3.ERR_INVALID_ARGUMENT),
     ("n_routed", 5000, k3.ERR_INVALID_ARGUMENT),
     ("n_shared", -1, k3.ERR_INVALID_ARGUMENT),
-    ("record_stride", 17547264 - 256, k3.ERR_INVALID_ARGUMENT),
+    ("record_stride", 17547264 - 4096, k3.ERR_INVALID_ARGUMENT),  # below the record size
+    ("record_stride", 17547264 + 256, k3.ERR_INVALID_ARGUMENT),   # not 4 KiB aligned
     ("record_stride", 17547264 + 8, k3.ERR_INVALID_ARGUMENT),
+    ("shared_stride", 4096, k3.ERR_INVALID_ARGUMENT),             # below the shared record size
+    ("shared_stride", 17547264 + 100, k3.ERR_INVALID_ARGUMENT),
     ("x_dtype", 7, k3.ERR_INVALID_ARGUMENT),
     ("score_func", 7, k3.ERR_INVALID_ARGUMENT),
+    ("record_order", 7, k3.ERR_INVALID_ARGUMENT),
+    ("shared_format", 7, k3.ERR_INVALID_ARGUMENT),
     ("act_mode", k3.ACT_MXFP4, k3.ERR_UNSUPPORTED),
+    ("shared_format", k3.SHARED_BF16, k3.ERR_UNSUPPORTED),
+    ("record_order", k3.ORDER_STORED, k3.ERR_UNSUPPORTED),        # records never packed are refused
 ])
 def test_invalid_config_rejected_on_host(field, value, code):
     cfg = k3.Config.make(**K3CFG)
     setattr(cfg, field, value)
     lib = k3.load()
     fake = ctypes.c_void_p(1 << 20)  # never dereferenced: validation fails first
-    rc = lib.k3moe_layer(ctypes.byref(cfg), fake, 1, fake, None, fake, fake, fake, None, None, fake, 1 << 30, None)
+    rc = lib.k3moe_layer(ctypes.byref(cfg), fake, 1, fake, None, None, fake, fake, fake, None, None, fake, 1 << 30, None)
     assert rc == code
+    rc = lib.k3moe_expert_ffn(ctypes.byref(cfg), fake, 1, fake, fake, fake, fake, fake, fake, 1 << 30, None)
+    assert rc == code
+    rc = lib.k3moe_layer_static(ctypes.byref(cfg), fake, 1, fake, None, fake, fake, fake, None)
+    assert rc == code
+
+
+def test_stored_order_is_refused_only_by_calls_that_read_records():
+    cfg = k3.Config.make(**K3CFG, record_order=k3.ORDER_STORED)
+    lib = k3.load()
+    a = ctypes.c_void_p(1 << 20)
+    assert lib.k3moe_route(ctypes.byref(cfg), a, 0, a, None, None, a, a, a, 1 << 30, None) == k3.OK
+    assert lib.k3moe_layer(ctypes.byref(cfg), a, 0, a, None, None, a, a, a, None, None, a, 0, None) == k3.ERR_UNSUPPORTED
+    # a zero-initialised config (no order given) is the stored order
+    assert k3.Config().record_order == k3.ORDER_STORED
 
 
 def test_invalid_pointers_rejected_on_host():
@@ -80,14 +103,26 @@ def test_invalid_pointers_rejected_on_host():
     a = ctypes.c_void_p(1 << 20)
     mis = ctypes.c_void_p((1 << 20) + 8)
     big = 1 << 34
-    assert lib.k3moe_layer(ctypes.byref(cfg), None, 1, a, None, a, a, a, None, None, a, big, None) == 1
-    assert lib.k3moe_layer(ctypes.byref(cfg), mis, 1, a, None, a, a, a, None, None, a, big, None) == 1
-    assert lib.k3moe_layer(ctypes.byref(cfg), a, -1, a, None, a, a, a, None, None, a, big, None) == 1
-    assert lib.k3moe_route(ctypes.byref(cfg), a, 1, a, None, None, a, a, big, None) == 1
+    assert lib.k3moe_layer(ctypes.byref(cfg), None, 1, a, None, None, a, a, a, None, None, a, big, None) == 1
+    assert lib.k3moe_layer(ctypes.byref(cfg), mis, 1, a, None, None, a, a, a, None, None, a, big, None) == 1
+    assert lib.k3moe_layer(ctypes.byref(cfg), a, -1, a, None, None, a, a, a, None, None, a, big, None) == 1
+    assert lib.k3moe_layer(ctypes.byref(cfg), a, 1, a, mis, None, a, a, a, None, None, a, big, None) == 1  # parts
+    assert lib.k3moe_route(ctypes.byref(cfg), a, 1, a, None, None, None, a, a, big, None) == 1
     assert lib.k3moe_expert_ffn(ctypes.byref(cfg), a, 1, a, a, a, None, a, a, big, None) == 1  # shared missing
     ws_mis = ctypes.c_void_p((1 << 20) + 16)
-    assert lib.k3moe_layer(ctypes.byref(cfg), a, 1, a, None, a, a, a, None, None, ws_mis, big, None) == 1
-    assert lib.k3moe_layer(ctypes.byref(cfg), a, 4, a, None, a, a, a, None, None, a, 1024, None) == k3.ERR_WORKSPACE
+    assert lib.k3moe_layer(ctypes.byref(cfg), a, 1, a, None, None, a, a, a, None, None, ws_mis, big, None) == 1
+    assert lib.k3moe_layer(ctypes.byref(cfg), a, 4, a, None, None, a, a, a, None, None, a, 1024, None) == k3.ERR_WORKSPACE
+    assert lib.k3moe_layer_bounded(ctypes.byref(cfg), a, 1, a, None, None, a, a, a, a, big, 0, None) == 1  # bound 0
+    assert lib.k3moe_prepare_router(ctypes.byref(cfg), None, a, None) == 1
+    assert lib.k3moe_prepare_router(ctypes.byref(cfg), a, mis, None) == 1
+    assert lib.k3moe_residual_rmsnorm(a, None, 1, 7166, 1e-6, a, None) == 1   # d not a multiple of 4
+    assert lib.k3moe_residual_rmsnorm(a, mis, 1, 7168, 1e-6, a, None) == 1
+    assert lib.k3moe_residual_rmsnorm(a, None, 0, 7168, 1e-6, a, None) == k3.OK
+
+
+def test_router_parts_bytes():
+    cfg = k3.Config.make(**K3CFG)
+    assert k3.router_parts_bytes(cfg) == 3 * 896 * 7168 * 2
 
 
 def test_pack_records_rejects_bad_arguments_on_host():
@@ -102,13 +137,15 @@ def test_pack_records_rejects_bad_arguments_on_host():
     bad = k3.Config.make(**K3CFG)
     bad.d_ff = 100
     assert lib.k3moe_pack_records(ctypes.byref(bad), a, 1, 1, None) == k3.ERR_INVALID_ARGUMENT
+    bad.d_ff = 1504  # a multiple of 32, not of 128: the device order is defined on 128-row tiles
+    assert lib.k3moe_pack_records(ctypes.byref(bad), a, 1, 1, None) == k3.ERR_UNSUPPORTED
 
 
 def test_zero_tokens_launches_nothing():
     cfg = k3.Config.make(**K3CFG)
     lib = k3.load()
     a = ctypes.c_void_p(1 << 20)
-    assert lib.k3moe_layer(ctypes.byref(cfg), a, 0, a, None, a, a, a, None, None, a, 0, None) == k3.OK
+    assert lib.k3moe_layer(ctypes.byref(cfg), a, 0, a, None, None, a, a, a, None, None, a, 0, None) == k3.OK
 
 
 def test_status_strings():

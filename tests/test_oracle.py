@@ -419,3 +419,19 @@ def test_planted_mistakes_are_caught(name):
             except (AssertionError, ValueError):
                 failed.append(pin.__name__)
     assert failed, f"no pin catches the planted mistake {name!r}"
+
+
+def test_route_tokens_is_route_token_per_token():
+    """The batched routing the GPU tests use for every token of a prefill is the per-token routine,
+    token by token (bf16 and fp32 tokens, with a bias, both scores)."""
+    sh = synth.LayerShape(d_model=256, d_ff=128, n_routed=32, top_k=4, n_shared=1)
+    W = synth.router_weights(sh, 3)
+    bias = synth.zipf_bias(sh, 3, 1.1)
+    for x_dtype in ("bf16", "f32"):
+        x = synth.tokens(sh, 3, 9, x_dtype)
+        xf = synth.tokens_as_f64(x, x_dtype)
+        for score in ("softmax", "sigmoid_bias"):
+            lg, idx, w = oracle.route_tokens(x, x_dtype, W, sh.top_k, bias, score=score)
+            for t in range(x.shape[0]):
+                lg1, idx1, w1 = oracle.route_token(xf[t], W, sh.top_k, bias, score=score)
+                assert np.array_equal(lg[t], lg1) and np.array_equal(idx[t], idx1) and np.array_equal(w[t], w1)

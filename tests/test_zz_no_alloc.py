@@ -60,9 +60,10 @@ def test_static_scratch_matches_workspace_entry_point(shape, T, x_dtype, zipf):
 
 
 def test_static_scratch_rejects_calls_beyond_its_size():
+    """The documented limit at the K3 shape: up to 6 tokens are served, 7 are refused."""
     L = DeviceLayer(synth.K3, seed=22)
-    T = next(t for t in range(1, 64) if k3.workspace_bytes(L.cfg, t) > (4 << 20))  # 5 at this shape
-    assert T > 2
+    T = next(t for t in range(1, 64) if k3.workspace_bytes(L.cfg, t) > (4 << 20))
+    assert T == 7
     _, xd = L.tokens(T)
     y = torch.empty((T, synth.K3.d_model), dtype=torch.float32, device="cuda")
     assert _static_call(L, xd, T, y) == k3.ERR_WORKSPACE
