@@ -19,6 +19,7 @@ constexpr long long kMaxTerms = 3;     // E4M3 terms per activation block (x: 2 
 constexpr long long kMaxTermsFp4 = 8;  // E2M1 terms per activation block
 constexpr long long kFp4MaxT = 2;      // the E2M1 / mxf4 path serves up to this many tokens
 constexpr uint32_t kDefaultWaitLimit = 1u << 24;  // polls of a pipeline barrier before a CTA gives up
+constexpr long long kWholeExpertTokens = 48;       // mean tokens per expert from which work groups are whole
 
 // E2M1 activation terms and kind::mxf4 MMAs for few tokens (d_model and d_ff multiples of 256).
 bool use_fp4(const k3moe_config* c, long long T) {
@@ -189,13 +190,6 @@ Cfg make_cfg(const k3moe_config* c, long long T) {
   k.S = c->n_shared;
   k.x_f32 = c->x_dtype == K3MOE_X_F32 ? 1 : 0;
   k.fp4 = use_fp4(c, T) ? 1 : 0;
-  // tokens per work group. Gate/up: 32 (16 with the E2M1 terms; 42, which reads an expert's record
-  // fewer times, measured slower at prefill sizes, 16 slower from 256 tokens on). Down: 16, which
-  // keeps its MMA N at 48 with two issuers and two accumulator buffers (32, N = 96 with one of
-  // either, measured 35 % slower at 64 tokens, 45 % at 512, 9 % at 4096; 8 slower than 16)
-  const long long wmax = k.fp4 ? 16 : 32, wmax_dn = 16;
-  k.wgt = (int)(T < wmax ? T : wmax);
-  k.wgt_dn = (int)(T < wmax_dn ? T : wmax_dn);
   if (k.fp4) {
     k.xterms = 8;  // at most 2^-23 of the block maximum per element
     k.hterms = 8;
@@ -203,6 +197,16 @@ Cfg make_cfg(const k3moe_config* c, long long T) {
     k.xterms = k.x_f32 ? 3 : 2;
     k.hterms = 3;
   }
+  // tokens per work group. Gate/up: 32 (16 with the E2M1 terms; 42 measured slower at prefill sizes,
+  // 16 slower from 256 tokens on). Down: 16, which keeps its MMA N at 48 with two issuers and two
+  // accumulator buffers (32, N = 96 with one of either, measured 35 % slower at 64 tokens, 45 % at
+  // 512). From kWholeExpertTokens tokens per expert on average (prefill sizes), a work group holds up
+  // to 256 MMA columns of tokens x terms (128 bf16 tokens, 85 fp32 tokens or 85 positions of h): an
+  // expert's whole token list in one group, so that each 128-row weight tile is read once per expert.
+  const bool whole = !k.fp4 && T * c->top_k >= kWholeExpertTokens * c->n_routed;
+  const long long wmax = k.fp4 ? 16 : (whole ? 256 / k.xterms : 32), wmax_dn = whole ? 256 / k.hterms : 16;
+  k.wgt = (int)(T < wmax ? T : wmax);
+  k.wgt_dn = (int)(T < wmax_dn ? T : wmax_dn);
   k.rsplit = (int)router_splits(c, T);
   k.wait_limit = kDefaultWaitLimit;
   k.stride = c->record_stride;

@@ -212,19 +212,27 @@ __device__ void topk_select(int E, int k, const float* logits_t, long long ls, i
 // gates = the selected sigmoid scores renormalised. `cand` is shared memory for blockDim.x keys. Ends
 // with __syncthreads.
 // `idx_sm` / `w_sm` (shared memory, or NULL) receive a copy of the selection for the permutation.
+// topk_select with the keys per thread that E needs (E <= 4096 with 8 warps).
+template <int KZ, bool SIG>
+__device__ void topk_select_any(int E, int k, const float* logits_t, long long ls, int np, const float* sel_bias,
+                                unsigned long long* cand, unsigned long long* sel, unsigned long long* s_thr, int* s_n) {
+  const int nw = blockDim.x >> 5;
+  const int per_lane = (E + 32 * nw - 1) / (32 * nw);
+  if (per_lane <= 1) topk_select<1, KZ, SIG>(E, k, logits_t, ls, np, sel_bias, cand, sel, s_thr, s_n);
+  else if (per_lane <= 2) topk_select<2, KZ, SIG>(E, k, logits_t, ls, np, sel_bias, cand, sel, s_thr, s_n);
+  else if (per_lane <= 4) topk_select<4, KZ, SIG>(E, k, logits_t, ls, np, sel_bias, cand, sel, s_thr, s_n);
+  else if (per_lane <= 8) topk_select<8, KZ, SIG>(E, k, logits_t, ls, np, sel_bias, cand, sel, s_thr, s_n);
+  else topk_select<16, KZ, SIG>(E, k, logits_t, ls, np, sel_bias, cand, sel, s_thr, s_n);
+}
+
 template <int KZ, bool SIG>
 __device__ void topk_block(int E, int k, const float* logits_t, long long ls, int np, const float* sel_bias,
                            unsigned long long* cand, int* idx_out, float* w_out, int* idx_user, float* w_user,
                            int* idx_sm, float* w_sm) {
   __shared__ unsigned long long s_sel[32], s_thr[64];
   __shared__ int s_n;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  const int per_lane = (E + 32 * nw - 1) / (32 * nw);
-  if (per_lane <= 1) topk_select<1, KZ, SIG>(E, k, logits_t, ls, np, sel_bias, cand, s_sel, s_thr, &s_n);
-  else if (per_lane <= 2) topk_select<2, KZ, SIG>(E, k, logits_t, ls, np, sel_bias, cand, s_sel, s_thr, &s_n);
-  else if (per_lane <= 4) topk_select<4, KZ, SIG>(E, k, logits_t, ls, np, sel_bias, cand, s_sel, s_thr, &s_n);
-  else if (per_lane <= 8) topk_select<8, KZ, SIG>(E, k, logits_t, ls, np, sel_bias, cand, s_sel, s_thr, &s_n);
-  else topk_select<16, KZ, SIG>(E, k, logits_t, ls, np, sel_bias, cand, s_sel, s_thr, &s_n);  // E <= 4096 with 8 warps
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  topk_select_any<KZ, SIG>(E, k, logits_t, ls, np, sel_bias, cand, s_sel, s_thr, &s_n);
   if (warp == 0) {
     const unsigned long long best = (lane < k) ? s_sel[lane] : 0ull;
     const int my_e = key_expert(best);
@@ -255,6 +263,107 @@ __device__ void topk_block(int E, int k, const float* logits_t, long long ls, in
     }
   }
   __syncthreads();
+}
+
+// Logits from the tensor cores carry the rounding of the MMA's fp32 accumulation (measured ~1e-5 at
+// d_model 7168, against ~1e-6 for fp32 dot products), enough to swap two experts whose logits differ
+// by a little more than 1e-5. Before the final selection of a token, every expert whose ranked value
+// (logit, or sigmoid + selection bias) lies within kRefineMargin of the k-th value is recomputed on
+// the CUDA cores and written over the partial logits (part 0 takes the value, the other parts zero,
+// so the parts still add up to it exactly). No expert below the margin can enter the selection. The
+// whole CTA computes the candidates together, kRefineBatch at a time: thread i sums the fp32 products
+// of its d / blockDim.x consecutive elements of x and of each candidate's fp32 router row, then the
+// warps' sums and the per-warp partials are added in order (+ the bias for the softmax score). If
+// more than blockDim.x experts lie within the margin (a token whose logits are all equal, x = 0), the
+// tensor-core values stand: exact ties are then exact zeros.
+constexpr float kRefineMargin = 2e-4f;
+constexpr int kRefineBatch = 16;
+
+template <int R, int KZ, bool SIG>
+__device__ void refine_candidates_r(const Cfg& c, float* logits_t, long long ls, int np, const float* sel_bias,
+                                    const float* W, const float* logit_bias, const uint8_t* xrow, float tau,
+                                    int* s_cid, int* s_nc, float (*s_red)[kRefineBatch]) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  unsigned long long key[R];
+  load_keys<R, KZ, SIG>(c.E, logits_t, ls, np, sel_bias, key);
+  if (threadIdx.x == 0) *s_nc = 0;
+  __syncthreads();
+#pragma unroll
+  for (int q = 0; q < R; ++q)
+    if (key[q] != 0ull && key_logit(key[q]) >= tau) {
+      const int at = atomicAdd(s_nc, 1);
+      if (at < (int)blockDim.x) s_cid[at] = key_expert(key[q]);
+    }
+  __syncthreads();
+  const int n = *s_nc;
+  if (n > (int)blockDim.x) return;
+  // this thread's slice of the reduction axis: [j0, j1), a multiple of 4 elements (d is a multiple of 128)
+  const int per = ((c.d / 4 + blockDim.x - 1) / blockDim.x) * 4;
+  const int j0 = min(c.d, (int)threadIdx.x * per), j1 = min(c.d, j0 + per);
+  for (int b0 = 0; b0 < n; b0 += kRefineBatch) {
+    const int nb = min(kRefineBatch, n - b0);
+    float acc[kRefineBatch];
+#pragma unroll
+    for (int u = 0; u < kRefineBatch; ++u) acc[u] = 0.0f;
+    for (int j = j0; j < j1; j += 4) {
+      float xv[4];
+      if (c.x_f32) {
+        const float4 q4 = *reinterpret_cast<const float4*>(xrow + 4 * j);
+        xv[0] = q4.x; xv[1] = q4.y; xv[2] = q4.z; xv[3] = q4.w;
+      } else {
+        const uint2 q2 = *reinterpret_cast<const uint2*>(xrow + 2 * j);
+        xv[0] = __uint_as_float(q2.x << 16); xv[1] = __uint_as_float(q2.x & 0xFFFF0000u);
+        xv[2] = __uint_as_float(q2.y << 16); xv[3] = __uint_as_float(q2.y & 0xFFFF0000u);
+      }
+#pragma unroll
+      for (int u = 0; u < kRefineBatch; ++u)
+        if (u < nb) {
+          const float4 w4 = __ldg(reinterpret_cast<const float4*>(W + (long long)s_cid[b0 + u] * c.d + j));
+          acc[u] = fmaf(w4.x, xv[0], acc[u]);
+          acc[u] = fmaf(w4.y, xv[1], acc[u]);
+          acc[u] = fmaf(w4.z, xv[2], acc[u]);
+          acc[u] = fmaf(w4.w, xv[3], acc[u]);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < kRefineBatch; ++u) {
+      float v = acc[u];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0) s_red[warp][u] = v;
+    }
+    __syncthreads();
+    if ((int)threadIdx.x < nb) {
+      const int e = s_cid[b0 + threadIdx.x];
+      float v = 0.0f;
+      for (int w = 0; w < nw; ++w) v += s_red[w][threadIdx.x];
+      logits_t[e] = v + (logit_bias ? __ldg(&logit_bias[e]) : 0.0f);
+      for (int z = 1; z < np; ++z) logits_t[z * ls + e] = 0.0f;
+    }
+    __syncthreads();
+  }
+  __threadfence_block();
+  __syncthreads();
+}
+
+// One token: the selection on the tensor cores' partial logits, then the recomputation of the experts
+// near its k-th value (above); the final selection runs on the corrected logits.
+template <int KZ, bool SIG>
+__device__ void refine_candidates(const Cfg& c, float* logits_t, long long ls, int np, const float* sel_bias,
+                                  const float* W, const float* logit_bias, const uint8_t* xrow,
+                                  unsigned long long* cand) {
+  __shared__ unsigned long long s_sel[32], s_thr[64];
+  __shared__ int s_n, s_nc, s_cid[256];
+  __shared__ float s_red[8][kRefineBatch];
+  topk_select_any<KZ, SIG>(c.E, c.k, logits_t, ls, np, sel_bias, cand, s_sel, s_thr, &s_n);
+  const float tau = key_logit(s_sel[c.k - 1]) - kRefineMargin;
+  const int nw = blockDim.x >> 5;
+  const int per_lane = (c.E + 32 * nw - 1) / (32 * nw);
+  if (per_lane <= 1) refine_candidates_r<1, KZ, SIG>(c, logits_t, ls, np, sel_bias, W, logit_bias, xrow, tau, s_cid, &s_nc, s_red);
+  else if (per_lane <= 2) refine_candidates_r<2, KZ, SIG>(c, logits_t, ls, np, sel_bias, W, logit_bias, xrow, tau, s_cid, &s_nc, s_red);
+  else if (per_lane <= 4) refine_candidates_r<4, KZ, SIG>(c, logits_t, ls, np, sel_bias, W, logit_bias, xrow, tau, s_cid, &s_nc, s_red);
+  else if (per_lane <= 8) refine_candidates_r<8, KZ, SIG>(c, logits_t, ls, np, sel_bias, W, logit_bias, xrow, tau, s_cid, &s_nc, s_red);
+  else refine_candidates_r<16, KZ, SIG>(c, logits_t, ls, np, sel_bias, W, logit_bias, xrow, tau, s_cid, &s_nc, s_red);
 }
 
 // Exclusive block-wide scan of two int arrays of length n (in place into out0/out1, total at [n]).
@@ -805,6 +914,17 @@ __global__ void __launch_bounds__(256, MINB) k_select(RouteArgs a) {
   }
   if (blockIdx.x > 0) return;
   unsigned long long* cand = reinterpret_cast<unsigned long long*>(smem + route_tile_bytes(c, 1, true));
+  if (!(tc0 == 0 && (a.mode & RM_XPREP))) {  // the token's row of x, for the recomputed logits
+    const int esz = c.x_f32 ? 4 : 2;
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(a.x) + t * c.d * esz;
+    const uint32_t dst = (uint32_t)__cvta_generic_to_shared(smem);
+    for (int off = threadIdx.x * 16; off < c.d * esz; off += blockDim.x * 16)
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + off), "l"(src + off) : "memory");
+    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
+  }
+  refine_candidates<KZ, SIG>(c, a.ws.logits + t * c.E, a.T * c.E, c.rsplit, SIG ? a.bias : nullptr, a.W,
+                             SIG ? nullptr : a.bias, smem, cand);
   topk_block<KZ, SIG>(c.E, c.k, a.ws.logits + t * c.E, a.T * c.E, c.rsplit, SIG ? a.bias : nullptr,
                       cand, a.ws.topk_idx + t * c.k,
                 a.ws.topk_w + t * c.k, (a.mode & RM_USER_OUT) && a.out_idx ? a.out_idx + t * c.k : nullptr,
