@@ -163,6 +163,7 @@ struct TcArgs {
   int n_tile;   // largest MMA N (multiple of 16, <= kMaxN); an item's MMAs use N = its own B rows, rounded to 16
   int acc_cols; // tensor-memory columns per accumulator (>= n_tile, multiple of 16)
   int n_iss;    // MMA-issuing threads
+  int nsplit;   // 1: the issuers split N (issuer w: columns 128 w .. of every stage), 0: they split the stages
   int n_acc;    // accumulators per issuer (the MMAs of a chunk alternate between them)
   int n_buf;    // accumulator buffers (items in flight between the issuers and the epilogue)
   int sf_base;  // first column of the scale slots, one per chunk of every stage (after 2 buffers x
@@ -284,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(su32(&ctl->full[s]), 1 + 32);
-      mbar_init(su32(&ctl->empty[s]), 1);
+      mbar_init(su32(&ctl->empty[s]), a.nsplit ? a.n_iss : 1);
     }
     for (int b = 0; b < a.n_buf; ++b) {
       mbar_init(su32(&ctl->acc_full[b]), a.n_iss);
@@ -465,26 +466,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t started = 0;  // bit h: accumulator h already holds a partial sum of this item
         for (int j = it.j0; j < it.j1; j += CH, rg.next(S)) {
           const int s = rg.s;
-          if (s % a.n_iss != w) continue;
+          if (!a.nsplit && s % a.n_iss != w) continue;
           if (!wait_bar(su32(&ctl->full[s]), rg.ph, ctl, status, c.wait_limit)) { ok = false; break; }
           tc_fence_after();
           fence_async_smem();  // B rows and scale words arrived through cp.async (generic proxy)
           const uint64_t so = (uint64_t)(s * st16);
-          const uint32_t nn = *reinterpret_cast<volatile const uint32_t*>(&ctl->stage_n[s]);
+          uint32_t nn = *reinterpret_cast<volatile const uint32_t*>(&ctl->stage_n[s]);
+          if (a.nsplit) nn = nn > 128u * w ? min(nn - 128u * w, 128u) : 0u;  // this issuer's columns
           const uint32_t idesc = idesc0 | ((nn >> 3) << 17);
-          for (int cc = 0; cc < CH; ++cc) {
-            // scale words of the chunk: A word w to column col + 16 w, B word w to col + 16 (wpc + w); above
-            // N = 128 the second 128-row image of B (rows 128 ..) follows its first in the next four
-            // columns, col + 16 (wpc + w) + 4 (one column per 32 rows, as in the first image).
+          for (int cc = 0; cc < CH && nn > 0; ++cc) {
+            // scale words of the chunk: A word w to column col + 16 w, B word w to col + 16 (wpc + w).
+            // With the issuers splitting N, issuer w takes B's 128-row image w (B rows 128 w ..) and
+            // has its own 32 columns of the slot for both images.
             // The scale slot belongs to the stage: it is rewritten only after the stage's previous MMAs
             // completed (the loader refilled the stage after its empty barrier).
-            const uint32_t col = tmem + (uint32_t)(a.sf_base + (s * CH + cc) * a.sf_slot);
+            const uint32_t col = tmem + (uint32_t)(a.sf_base + (s * CH + cc) * a.sf_slot + (a.nsplit ? 32 * w : 0));
             const uint64_t dsc = dsa0 + so + (uint64_t)(cc * (a.sf_bytes >> 4));
-            for (int w2 = 0; w2 < 2 * wpc; ++w2) tc_cp_32x128b_x4(col + 16 * w2, dsc + (uint64_t)(w2 * (512 >> 4)));
-            if (nn > 128)
-              for (int h = 0; h < wpc; ++h)
-                tc_cp_32x128b_x4(col + 16 * (wpc + h) + 4, dsc + (uint64_t)((2 * wpc + h) * (512 >> 4)));
-            const uint64_t da = da0 + so + (uint64_t)(cc * (kATile >> 4)), db = db0 + so + (uint64_t)(cc * bb16);
+            for (int w2 = 0; w2 < wpc; ++w2) tc_cp_32x128b_x4(col + 16 * w2, dsc + (uint64_t)(w2 * (512 >> 4)));
+            for (int w2 = 0; w2 < wpc; ++w2)
+              tc_cp_32x128b_x4(col + 16 * (wpc + w2),
+                               dsc + (uint64_t)((wpc + (a.nsplit ? w * wpc : 0) + w2) * (512 >> 4)));
+            const uint64_t da = da0 + so + (uint64_t)(cc * (kATile >> 4));
+            // (the issuer's B rows start 128 w rows = 16 KB w into the tile)
+            const uint64_t db = db0 + so + (uint64_t)(cc * bb16) + (uint64_t)(a.nsplit ? w * (16384 >> 4) : 0);
             if (a.fp4) {
               // K = 64 per MMA; MMA k uses scale word k / 2, byte pair 2 (k % 2)
 #pragma unroll
@@ -557,8 +561,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ncols = it.wg.ntok * a.terms;
       // issuers that received stages: owners (slot mod n_iss) of slots g0, g0 + 1, ...; their partial
       // sums are added in issuer order
+      // (issuers splitting N write adjacent column ranges of one accumulator: read as one)
       unsigned mask = 0;
       for (int t = 0, sl = g0; t < nst && t < S; ++t, sl = (sl + 1 == S) ? 0 : sl + 1) mask |= 1u << (sl % a.n_iss);
+      if (a.nsplit) mask = 1u;
       const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * a.n_iss * a.acc_cols);
       float run = 0.0f;
       bool nan_row = false;
@@ -891,23 +897,25 @@ int chunks_per_stage(long long nch, long long parts) {
 
 // With fewer than 4 stages of ch chunks the stage shrinks to one chunk.
 void size_tiles(TcArgs& a, int ch, int mtiles, int mode) {
-  a.sf_slot = a.fp4 ? 64 : 32;
-  // scale words of a chunk: A's image, then B's (two 128-row images above N = 128; E4M3 form only),
-  // in a multiple of 1 KB so that every stage's tiles stay 1 KB aligned (128-byte swizzle)
-  a.sf_bytes = a.fp4 ? 2048 : (a.n_tile > 128 ? 2048 : 1024);
+  // above N = 128 (E4M3 form only) two issuers split N, each with 128 columns and 32 scale columns
+  a.nsplit = a.n_tile > 128 ? 1 : 0;
+  a.sf_slot = (a.fp4 || a.nsplit) ? 64 : 32;
+  // scale words of a chunk: A's image, then B's (two 128-row images above N = 128), in a multiple of
+  // 1 KB so that every stage's tiles stay 1 KB aligned (128-byte swizzle)
+  a.sf_bytes = (a.fp4 || a.nsplit) ? 2048 : 1024;
   a.div_parts.init((uint32_t)a.parts);
   a.div_mtiles.init((uint32_t)mtiles);
-  a.acc_cols = 16;  // a power of two >= n_tile: every accumulator starts at a multiple of its width
-  while (a.acc_cols < a.n_tile) a.acc_cols *= 2;
+  a.acc_cols = 16;  // a power of two >= an issuer's N: every accumulator starts at a multiple of its width
+  while (a.acc_cols < (a.nsplit ? 128 : a.n_tile)) a.acc_cols *= 2;
   // issuers and accumulator buffers: small N needs several issuers (issue rate); three (each owning
   // two of the six stages at N = 16) measured faster than four (two owning two, two owning one) or
   // two. Above 64 columns: with few tokens per work group (T < 256) two issuers with one buffer each
   // (measured faster), at prefill sizes one issuer with two buffers (deeper ring, overlapped epilogue).
-  // Above 128 columns (whole experts' token lists at prefill sizes) one issuer and one buffer: the
-  // scale slots need the other half of the tensor memory.
-  a.n_iss = a.n_tile <= 32 ? 3 : (a.n_tile <= 64 || (a.T < 256 && a.n_tile <= 128) ? 2 : 1);
+  // Above 128 columns (whole experts' token lists at prefill sizes) two issuers split N and one
+  // buffer: the scale slots need the other half of the tensor memory.
+  a.n_iss = a.nsplit ? 2 : (a.n_tile <= 32 ? 3 : (a.n_tile <= 64 || a.T < 256 ? 2 : 1));
   a.n_acc = 1;  // two alternating accumulators measured no faster at any N
-  a.n_buf = a.acc_cols > 128 ? 1 : ((a.n_tile <= 64 || a.T >= 256) ? 2 : 1);  // (three measured no faster)
+  a.n_buf = a.nsplit ? 1 : ((a.n_tile <= 64 || a.T >= 256) ? 2 : 1);  // (three measured no faster)
   a.sf_base = (a.n_buf * a.n_iss * a.n_acc * a.acc_cols + 31) / 32 * 32;
   a.b_bytes = (a.n_tile * 128 + 1023) / 1024 * 1024;
   for (;; ch = 1) {
