@@ -19,7 +19,6 @@ constexpr long long kMaxTerms = 3;     // E4M3 terms per activation block (x: 2 
 constexpr long long kMaxTermsFp4 = 8;  // E2M1 terms per activation block
 constexpr long long kFp4MaxT = 2;      // the E2M1 / mxf4 path serves up to this many tokens
 constexpr uint32_t kDefaultWaitLimit = 1u << 24;  // polls of a pipeline barrier before a CTA gives up
-constexpr long long kWholeExpertTokens = 48;       // mean tokens per expert from which work groups are whole
 
 // E2M1 activation terms and kind::mxf4 MMAs for few tokens (d_model and d_ff multiples of 256).
 bool use_fp4(const k3moe_config* c, long long T) {
@@ -197,14 +196,13 @@ Cfg make_cfg(const k3moe_config* c, long long T) {
     k.xterms = k.x_f32 ? 3 : 2;
     k.hterms = 3;
   }
-  // tokens per work group. Gate/up: 32 (16 with the E2M1 terms; 42 measured slower at prefill sizes,
-  // 16 slower from 256 tokens on). Down: 16, which keeps its MMA N at 48 with two issuers and two
-  // accumulator buffers (32, N = 96 with one of either, measured 35 % slower at 64 tokens, 45 % at
-  // 512). From kWholeExpertTokens tokens per expert on average (prefill sizes), a work group holds up
-  // to 256 MMA columns of tokens x terms (128 bf16 tokens, 85 fp32 tokens or 85 positions of h): an
-  // expert's whole token list in one group, so that each 128-row weight tile is read once per expert.
-  const bool whole = !k.fp4 && T * c->top_k >= kWholeExpertTokens * c->n_routed;
-  const long long wmax = k.fp4 ? 16 : (whole ? 256 / k.xterms : 32), wmax_dn = whole ? 256 / k.hterms : 16;
+  // tokens per work group. Gate/up: 32 (16 with the E2M1 terms; 42, which reads an expert's record
+  // fewer times, measured slower at prefill sizes, 16 slower from 256 tokens on; whole experts' token
+  // lists of up to 128 tokens, MMA N 256 over two issuers, measured slower at 4096 tokens: 13.0 against
+  // 10.3 ms in the same build, whose down projection gained 17 % from lists of 85 positions). Down:
+  // 16, which keeps its MMA N at 48 with two issuers and two accumulator buffers (32, N = 96 with one
+  // of either, measured 35 % slower at 64 tokens, 45 % at 512, 9 % at 4096; 8 slower than 16)
+  const long long wmax = k.fp4 ? 16 : 32, wmax_dn = 16;
   k.wgt = (int)(T < wmax ? T : wmax);
   k.wgt_dn = (int)(T < wmax_dn ? T : wmax_dn);
   k.rsplit = (int)router_splits(c, T);

@@ -267,10 +267,13 @@ __device__ void topk_block(int E, int k, const float* logits_t, long long ls, in
 
 // Logits from the tensor cores carry the rounding of the MMA's fp32 accumulation (measured ~1e-5 at
 // d_model 7168, against ~1e-6 for fp32 dot products), enough to swap two experts whose logits differ
-// by a little more than 1e-5. Before the final selection of a token, every expert whose ranked value
-// (logit, or sigmoid + selection bias) lies within kRefineMargin of the k-th value is recomputed on
-// the CUDA cores and written over the partial logits (part 0 takes the value, the other parts zero,
-// so the parts still add up to it exactly). No expert below the margin can enter the selection. The
+// by a little more than 1e-5. Before the final selection of a token, the experts whose place is in
+// doubt are recomputed on the CUDA cores and written over the partial logits (part 0 takes the value,
+// the other parts zero, so the parts still add up to it exactly): every expert whose ranked value
+// (logit, or sigmoid + selection bias) lies within kRefineMargin of the k-th value, and every selected
+// expert within kRefineMargin of its neighbour in the selection. Any other pair of experts differs by
+// more than the margin in the tensor cores' values, far more than their error, so their order (and
+// whether they are selected) stands. The
 // whole CTA computes the candidates together, kRefineBatch at a time: thread i sums the fp32 products
 // of its d / blockDim.x consecutive elements of x and of each candidate's fp32 router row, then the
 // warps' sums and the per-warp partials are added in order (+ the bias for the softmax score). If
@@ -281,16 +284,27 @@ constexpr int kRefineBatch = 16;
 
 template <int R, int KZ, bool SIG>
 __device__ void refine_candidates_r(const Cfg& c, float* logits_t, long long ls, int np, const float* sel_bias,
-                                    const float* W, const float* logit_bias, const uint8_t* xrow, float tau,
-                                    int* s_cid, int* s_nc, float (*s_red)[kRefineBatch]) {
+                                    const float* W, const float* logit_bias, const uint8_t* xrow,
+                                    const unsigned long long* sel, int* s_cid, int* s_nc,
+                                    float (*s_red)[kRefineBatch]) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const float vk = key_logit(sel[c.k - 1]);
   unsigned long long key[R];
   load_keys<R, KZ, SIG>(c.E, logits_t, ls, np, sel_bias, key);
   if (threadIdx.x == 0) *s_nc = 0;
   __syncthreads();
+  if (warp == 0) {  // selected experts close to a neighbour in the selection (sorted, descending)
+    const float v = lane < c.k ? key_logit(sel[lane]) : 0.0f;
+    const float vp = __shfl_up_sync(0xffffffffu, v, 1), vn = __shfl_down_sync(0xffffffffu, v, 1);
+    const bool amb = lane < c.k && ((lane > 0 && vp - v < kRefineMargin) || (lane + 1 < c.k && v - vn < kRefineMargin));
+    if (amb && fabsf(v - vk) > kRefineMargin) {  // (those near the k-th value are taken below)
+      const int at = atomicAdd(s_nc, 1);
+      if (at < (int)blockDim.x) s_cid[at] = key_expert(sel[lane]);
+    }
+  }
 #pragma unroll
   for (int q = 0; q < R; ++q)
-    if (key[q] != 0ull && key_logit(key[q]) >= tau) {
+    if (key[q] != 0ull && fabsf(key_logit(key[q]) - vk) <= kRefineMargin) {
       const int at = atomicAdd(s_nc, 1);
       if (at < (int)blockDim.x) s_cid[at] = key_expert(key[q]);
     }
@@ -356,14 +370,13 @@ __device__ void refine_candidates(const Cfg& c, float* logits_t, long long ls, i
   __shared__ int s_n, s_nc, s_cid[256];
   __shared__ float s_red[8][kRefineBatch];
   topk_select_any<KZ, SIG>(c.E, c.k, logits_t, ls, np, sel_bias, cand, s_sel, s_thr, &s_n);
-  const float tau = key_logit(s_sel[c.k - 1]) - kRefineMargin;
   const int nw = blockDim.x >> 5;
   const int per_lane = (c.E + 32 * nw - 1) / (32 * nw);
-  if (per_lane <= 1) refine_candidates_r<1, KZ, SIG>(c, logits_t, ls, np, sel_bias, W, logit_bias, xrow, tau, s_cid, &s_nc, s_red);
-  else if (per_lane <= 2) refine_candidates_r<2, KZ, SIG>(c, logits_t, ls, np, sel_bias, W, logit_bias, xrow, tau, s_cid, &s_nc, s_red);
-  else if (per_lane <= 4) refine_candidates_r<4, KZ, SIG>(c, logits_t, ls, np, sel_bias, W, logit_bias, xrow, tau, s_cid, &s_nc, s_red);
-  else if (per_lane <= 8) refine_candidates_r<8, KZ, SIG>(c, logits_t, ls, np, sel_bias, W, logit_bias, xrow, tau, s_cid, &s_nc, s_red);
-  else refine_candidates_r<16, KZ, SIG>(c, logits_t, ls, np, sel_bias, W, logit_bias, xrow, tau, s_cid, &s_nc, s_red);
+  if (per_lane <= 1) refine_candidates_r<1, KZ, SIG>(c, logits_t, ls, np, sel_bias, W, logit_bias, xrow, s_sel, s_cid, &s_nc, s_red);
+  else if (per_lane <= 2) refine_candidates_r<2, KZ, SIG>(c, logits_t, ls, np, sel_bias, W, logit_bias, xrow, s_sel, s_cid, &s_nc, s_red);
+  else if (per_lane <= 4) refine_candidates_r<4, KZ, SIG>(c, logits_t, ls, np, sel_bias, W, logit_bias, xrow, s_sel, s_cid, &s_nc, s_red);
+  else if (per_lane <= 8) refine_candidates_r<8, KZ, SIG>(c, logits_t, ls, np, sel_bias, W, logit_bias, xrow, s_sel, s_cid, &s_nc, s_red);
+  else refine_candidates_r<16, KZ, SIG>(c, logits_t, ls, np, sel_bias, W, logit_bias, xrow, s_sel, s_cid, &s_nc, s_red);
 }
 
 // Exclusive block-wide scan of two int arrays of length n (in place into out0/out1, total at [n]).

@@ -59,8 +59,7 @@ constexpr int kWarpLoad = 4, kWarpIss = kWarpLoad + kLoaders, kWarpEnd = kWarpIs
 constexpr int kThreads = 32 * kWarpEnd;
 constexpr int kMaxCh = 2;                 // chunks per stage
 constexpr int kTmemCols = 512;
-constexpr int kMaxN = 256;               // largest MMA N (B rows per tile)
-constexpr int kXbRound = 16;             // tokens per round of the gate/up epilogue's g/u exchange
+constexpr int kMaxN = 128;               // largest MMA N (B rows per tile)
 // TMEM columns per chunk: E4M3 form: A scales at +0..3, B at +16..19 (32 columns); E2M1 form:
 // two scale words per row (8 blocks of 32): A at +0..3 and +16..19, B at +32.. and +48.. (64 columns)
 constexpr int kMaxStages = 16;
@@ -82,14 +81,12 @@ struct Ctl {
   uint32_t tmem;
   volatile int abort;
   int last;
-  uint32_t stage_n[kMaxStages];  // MMA N of the stage's item (written by its loader before the stage's arrival)
   alignas(16) WorkGroup ep_wg[4][kEpRing];
   alignas(16) WorkGroup ld_wg[kLoaders][kEpRing];  // loader v's copies of its next items' work groups
+  int ld_tok[kLoaders][kEpRing][32];               // ... and the tokens of their positions (gate/up)
+  uint32_t ld_row[kLoaders][kMaxN];                // B row n of loader v's current item: activation row, or ~0
 };
-// After the control block (offsets in TcArgs): the tokens of the positions of each loader's next items
-// (gate/up) int [kLoaders][kEpRing][wgt]; each loader's table of its current item's B rows uint32
-// [kLoaders][n_tile] (activation row, or ~0); the gate/up exchange area float [4 epilogue warps]
-// [kXbRound tokens][32 lanes].
+// Gate/up exchange area after the control block: float [4 epilogue warps][xb_tok tokens][32 lanes].
 __host__ __device__ constexpr size_t ctl_bytes() { return (sizeof(Ctl) + 15) / 16 * 16; }
 
 // Position in the ring of pipeline stages: slot s, phase parity of its current round, and whether
@@ -160,10 +157,9 @@ struct TcArgs {
   const uint8_t* shared;
   float* y;
   long long T;
-  int n_tile;   // largest MMA N (multiple of 16, <= kMaxN); an item's MMAs use N = its own B rows, rounded to 16
+  int n_tile;   // MMA N (multiple of 16, <= kMaxN)
   int acc_cols; // tensor-memory columns per accumulator (>= n_tile, multiple of 16)
   int n_iss;    // MMA-issuing threads
-  int nsplit;   // 1: the issuers split N (issuer w: columns 128 w .. of every stage), 0: they split the stages
   int n_acc;    // accumulators per issuer (the MMAs of a chunk alternate between them)
   int n_buf;    // accumulator buffers (items in flight between the issuers and the epilogue)
   int sf_base;  // first column of the scale slots, one per chunk of every stage (after 2 buffers x
@@ -173,14 +169,14 @@ struct TcArgs {
   int fp4;      // E2M1 form (kind::mxf4, 256-code chunks) or E4M3 form (kind::mxf8f6f4, 128-code chunks)
   int nch;      // chunks along the reduction axis
   int sf_slot;  // TMEM columns of the scales of a chunk
-  int sf_bytes; // shared-memory bytes of the scale words of a chunk (A, then B: two 128-row images above N = 128)
+  int sf_bytes; // shared-memory bytes of the scale words of a chunk
   int terms;    // B rows per token in this kernel (x terms for gate/up, h terms for down)
   int hterms;   // h terms written by the gate/up epilogue
-  int wgt_max;  // positions per work group (this kernel's list)
-  int off_tok, off_row, off_xb;  // byte offsets of the loaders' token and row tables and of the exchange area
+  int xb_tok;   // tokens per item in the gate/up exchange area (0 for the down projection)
   int parts;    // reduction parts per row tile (1: whole items)
   FastDiv div_parts, div_mtiles;
   int stages;   // pipeline depth (<= kMaxStages)
+  int pf_dist;  // chunks ahead of its tensor copy that a loader prefetches a weight tile into L2 (0: none)
   int stage_bytes;  // ch x (A tile + B tile + scale words)
 };
 
@@ -285,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(su32(&ctl->full[s]), 1 + 32);
-      mbar_init(su32(&ctl->empty[s]), a.nsplit ? a.n_iss : 1);
+      mbar_init(su32(&ctl->empty[s]), 1);
     }
     for (int b = 0; b < a.n_buf; ++b) {
       mbar_init(su32(&ctl->acc_full[b]), a.n_iss);
@@ -310,8 +306,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     Ring rg;
     bool ok = true;
     WorkGroup* rwg = ctl->ld_wg[lv];
-    int* ltok = reinterpret_cast<int*>(smem + a.off_tok) + lv * kEpRing * a.wgt_max;  // [kEpRing][wgt_max]
-    uint32_t* rtab = reinterpret_cast<uint32_t*>(smem + a.off_row) + lv * a.n_tile;  // [n_tile]
     auto fetch_wg = [&](long long idx, int slot) {  // the work group of item idx, if any
       if (lane == 0 && idx < n_items) {
         Item g;
@@ -322,8 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto fetch_tok = [&](long long idx, int slot) {  // tokens of item idx's positions (its work group is in `slot`)
       if (MODE == GATEUP && idx < n_items) {
         const WorkGroup g = rwg[slot];
-        for (int i = lane; i < g.ntok && i < a.wgt_max; i += 32)
-          cp4(su32(&ltok[slot * a.wgt_max + i]), &a.ws.perm_tok[g.pos0 + i], 4);
+        if (lane < g.ntok && lane < 32) cp4(su32(&ctl->ld_tok[lv][slot][lane]), &a.ws.perm_tok[g.pos0 + lane], 4);
       }
     };
     // prologue: work groups of the first kEpRing items and tokens of the first two, waited for here
@@ -351,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int i = n / a.terms;
         bsrc[q] = -1;
         if (n < a.n_tile && i < it.wg.ntok)
-          bsrc[q] = MODE == GATEUP ? ltok[slot * a.wgt_max + i] : it.wg.pos0 + i;
+          bsrc[q] = MODE == GATEUP ? ctl->ld_tok[lv][slot][i] : it.wg.pos0 + i;
       }
       __syncwarp();
       // refill: the work group kEpRing ahead into this slot, the tokens of the item two ahead
@@ -362,14 +355,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       const CUtensorMap* map = routed ? (it.mat == 0 ? &map_r0 : &map_r1) : (it.mat == 0 ? &map_s0 : &map_s1);
       const int ecoord = routed ? it.wg.expert : it.wg.expert - c.E;
       const uint8_t* atile = scale_tile<MODE>(a, it);
+      // the CTA's next item (its work group arrived with the group committed three items ago), whose
+      // first chunks this item's last stages prefetch into L2
+      Item nx;
+      const CUtensorMap* nx_map = nullptr;
+      int nx_e = 0;
+      const uint8_t* nx_sc = nullptr;
+      if (a.pf_dist > 0 && item_geom<MODE>(a, ii + gridDim.x, n_items, nx)) {
+        nx.wg = rwg[(kk + 1) % kEpRing];
+        const bool r2 = nx.wg.expert < c.E;
+        nx_map = r2 ? (nx.mat == 0 ? &map_r0 : &map_r1) : (nx.mat == 0 ? &map_s0 : &map_s1);
+        nx_e = r2 ? nx.wg.expert : nx.wg.expert - c.E;
+        nx_sc = scale_tile<MODE>(a, nx);
+      }
       // B row n of the tile = activation row (token or position) * terms + term; the rows' indices go
       // to this loader's table, which the code copies below read, and the scale pointers of rows
       // lane + 32 q stay in registers
       const int kk = MODE == GATEUP ? c.d : c.f;
       const long long row_bytes = a.fp4 ? kk / 2 : kk;
       const uint8_t* bbase = MODE == GATEUP ? a.ws.xq : a.ws.hq;
+      uint32_t* rtab = ctl->ld_row[lv];
       const int nrows = min(a.n_tile, it.wg.ntok * a.terms);  // rows past these are not read
-      const uint32_t n_item = (uint32_t)((nrows + 15) / 16 * 16);  // the item's MMA N
       const uint8_t* bscales[kMaxN / 32];
 #pragma unroll
       for (int q = 0; q < kMaxN / 32; ++q) {
@@ -394,9 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* st = smem + (size_t)s * a.stage_bytes;
         if (lane == 0) {
           // weight codes (tensor copy) and the chunks' A scale groups (one bulk copy each: the
-          // groups of a chunk are contiguous in the device order) complete on the same barrier; the
-          // item's N is published with the stage (the arrival below releases it)
-          ctl->stage_n[s] = n_item;
+          // groups of a chunk are contiguous in the device order) complete on the same barrier
           mbar_expect_tx(su32(&ctl->full[s]), (tx_chunk + 512 * wpc) * CH);
           tma_load_4d(su32(st), map, 0, it.mt * 128, j, ecoord, su32(&ctl->full[s]), pol);
           for (int cc = 0; cc < CH; ++cc)
@@ -406,8 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int cc = 0; cc < CH; ++cc) {
           const int jj = j + cc;
           const uint32_t sb = su32(st + b_off + cc * a.b_bytes), sc = su32(st + sf_off + cc * a.sf_bytes);
-          // scale words: A word h at sc + 512 h (bulk copy above); word h of B's 128-row image g (rows
-          // 128 g ..) at sc + 512 (wpc + g wpc + h)
+          // scale words: A word h at sc + 512 h (bulk copy above), B word h at sc + 512 (wpc + h)
           // codes: lane = 16-byte segment k16 of row 4 it + lane / 8, so that one copy instruction
           // reads four 128-byte rows (one row per lane read 32 rows: a quarter of the L1 rate)
           // (four rows per lane at a time: their table reads are issued before the copies)
@@ -427,9 +430,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int q = 0; q < kMaxN / 32; ++q)
             if (bscales[q])
               for (int h = 0; h < wpc; ++h)
-                cp4(sc + 512 * (wpc + (q >> 2) * wpc + h) + 16 * lane + 4 * (q & 3), bscales[q] + 4 * (wpc * jj + h), 4);
+                cp4(sc + 512 * (wpc + h) + 16 * lane + 4 * q, bscales[q] + 4 * (wpc * jj + h), 4);
         }
         cp_arrive_noinc(su32(&ctl->full[s]));
+        // L2 prefetch of the weight tile and scale groups pf_dist chunks ahead (this item, or the next
+        // one): more DRAM reads in flight than the ring's stages hold
+        if (lane == 0 && a.pf_dist > 0) {
+          const int jp = j + a.pf_dist;
+          if (jp < it.j1) {
+            tma_prefetch_4d(map, 0, it.mt * 128, jp, ecoord);
+            bulk_prefetch(atile + (size_t)512 * wpc * jp, 512 * wpc * CH);
+          } else if (nx_map && jp - it.j1 + nx.j0 < nx.j1) {
+            const int jn = jp - it.j1 + nx.j0;
+            tma_prefetch_4d(nx_map, 0, nx.mt * 128, jn, nx_e);
+            bulk_prefetch(nx_sc + (size_t)512 * wpc * jn, 512 * wpc * CH);
+          }
+        }
       }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
@@ -444,9 +460,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuers
     const int w = warp - kWarpIss;
     if (lane == 0 && w < a.n_iss) {
-      // instruction descriptor: A/B formats (mxf4: E2M1 = 1; mxf8f6f4: A E2M1 = 5, B E4M3 = 0), UE8M0, M;
-      // N (bits 17-22, N / 8) is the stage's: its item's B rows rounded up to 16
-      const uint32_t idesc0 = (a.fp4 ? ((1u << 7) | (1u << 10)) : (5u << 7)) | (1u << 23) | ((uint32_t)(128 >> 4) << 24);
+      // instruction descriptor: A/B formats (mxf4: E2M1 = 1; mxf8f6f4: A E2M1 = 5, B E4M3 = 0), N, UE8M0, M
+      const uint32_t idesc = (a.fp4 ? ((1u << 7) | (1u << 10)) : (5u << 7)) | ((uint32_t)(a.n_tile >> 3) << 17) |
+                             (1u << 23) | ((uint32_t)(128 >> 4) << 24);
       // descriptors of stage 0, chunk 0; stage s / chunk cc add their byte offsets / 16 to the
       // start-address field
       const uint64_t da0 = sw128_desc(su32(smem)), db0 = sw128_desc(su32(smem) + b_off);
@@ -466,29 +482,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t started = 0;  // bit h: accumulator h already holds a partial sum of this item
         for (int j = it.j0; j < it.j1; j += CH, rg.next(S)) {
           const int s = rg.s;
-          if (!a.nsplit && s % a.n_iss != w) continue;
+          if (s % a.n_iss != w) continue;
           if (!wait_bar(su32(&ctl->full[s]), rg.ph, ctl, status, c.wait_limit)) { ok = false; break; }
           tc_fence_after();
           fence_async_smem();  // B rows and scale words arrived through cp.async (generic proxy)
           const uint64_t so = (uint64_t)(s * st16);
-          uint32_t nn = *reinterpret_cast<volatile const uint32_t*>(&ctl->stage_n[s]);
-          if (a.nsplit) nn = nn > 128u * w ? min(nn - 128u * w, 128u) : 0u;  // this issuer's columns
-          const uint32_t idesc = idesc0 | ((nn >> 3) << 17);
-          for (int cc = 0; cc < CH && nn > 0; ++cc) {
-            // scale words of the chunk: A word w to column col + 16 w, B word w to col + 16 (wpc + w).
-            // With the issuers splitting N, issuer w takes B's 128-row image w (B rows 128 w ..) and
-            // has its own 32 columns of the slot for both images.
+          for (int cc = 0; cc < CH; ++cc) {
+            // scale words of the chunk: A word w to column col + 16 w, B word w to col + 16 (wpc + w)
             // The scale slot belongs to the stage: it is rewritten only after the stage's previous MMAs
             // completed (the loader refilled the stage after its empty barrier).
-            const uint32_t col = tmem + (uint32_t)(a.sf_base + (s * CH + cc) * a.sf_slot + (a.nsplit ? 32 * w : 0));
+            const uint32_t col = tmem + (uint32_t)(a.sf_base + (s * CH + cc) * a.sf_slot);
             const uint64_t dsc = dsa0 + so + (uint64_t)(cc * (a.sf_bytes >> 4));
-            for (int w2 = 0; w2 < wpc; ++w2) tc_cp_32x128b_x4(col + 16 * w2, dsc + (uint64_t)(w2 * (512 >> 4)));
-            for (int w2 = 0; w2 < wpc; ++w2)
-              tc_cp_32x128b_x4(col + 16 * (wpc + w2),
-                               dsc + (uint64_t)((wpc + (a.nsplit ? w * wpc : 0) + w2) * (512 >> 4)));
-            const uint64_t da = da0 + so + (uint64_t)(cc * (kATile >> 4));
-            // (the issuer's B rows start 128 w rows = 16 KB w into the tile)
-            const uint64_t db = db0 + so + (uint64_t)(cc * bb16) + (uint64_t)(a.nsplit ? w * (16384 >> 4) : 0);
+            for (int w2 = 0; w2 < 2 * wpc; ++w2) tc_cp_32x128b_x4(col + 16 * w2, dsc + (uint64_t)(w2 * (512 >> 4)));
+            const uint64_t da = da0 + so + (uint64_t)(cc * (kATile >> 4)), db = db0 + so + (uint64_t)(cc * bb16);
             if (a.fp4) {
               // K = 64 per MMA; MMA k uses scale word k / 2, byte pair 2 (k % 2)
 #pragma unroll
@@ -524,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // current one is waited for: while the weight stream saturates the DRAM, a read that misses L2
     // waits microseconds.
     const int q = warp;
-    float* xb = reinterpret_cast<float*>(smem + a.off_xb);  // gate/up exchange [4][kXbRound][32]
+    float* xb = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ctl) + ctl_bytes());  // gate/up exchange
     long long i = 0;
     int bad = 0;
     int g0 = 0;  // ring slot of the item's first stage
@@ -561,10 +567,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ncols = it.wg.ntok * a.terms;
       // issuers that received stages: owners (slot mod n_iss) of slots g0, g0 + 1, ...; their partial
       // sums are added in issuer order
-      // (issuers splitting N write adjacent column ranges of one accumulator: read as one)
       unsigned mask = 0;
       for (int t = 0, sl = g0; t < nst && t < S; ++t, sl = (sl + 1 == S) ? 0 : sl + 1) mask |= 1u << (sl % a.n_iss);
-      if (a.nsplit) mask = 1u;
       const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * a.n_iss * a.acc_cols);
       float run = 0.0f;
       bool nan_row = false;
@@ -572,72 +576,46 @@ __global__ void __launch_bounds__(kThreads, 1)
       // at the smallest N (four issuers of 16 columns, one token's terms) one load takes all partials:
       // every tensor-memory load waits in the tensor pipe with the MMAs, so fewer loads cost less
       const bool one_load = a.n_iss * a.acc_cols == 64 && ncols <= 16;
-      // gate/up: rounds of kXbRound tokens (a whole number of 16-column blocks), each summed into the
-      // exchange area and finished (GLU, terms of h) before the next; down: one round
-      const int round_tok = MODE == GATEUP ? kXbRound : it.wg.ntok;
-      const int nb = c.f / 32, p = q & 1, blk = 4 * it.mt + 2 * it.mat + p;  // (gate/up) 32-block of h
-      for (int tr = 0; tr < it.wg.ntok; tr += round_tok) {
-        const int tend = min(it.wg.ntok, tr + round_tok), cend = tend * a.terms;
-        for (int cb = tr * a.terms; cb < cend; cb += 16) {
-          uint32_t u[kMaxIss][16];
-          if (one_load) {
-            tc_ld64(lane_base, &u[0][0]);
-          } else {
-#pragma unroll
-            for (int w = 0; w < kMaxIss; ++w)
-              if ((mask >> w) & 1u) tc_ld16(lane_base + (uint32_t)(w * a.acc_cols + cb), u[w]);
-          }
-          tc_wait_ld();
-          if (cb + 16 >= ncols) {  // buffer read completely: hand it back
-            tc_fence_before();
-            mbar_arrive(su32(&ctl->acc_empty[b]));
-          }
-          float v[16];
-#pragma unroll
-          for (int cc = 0; cc < 16; ++cc) v[cc] = 0.0f;
+      for (int cb = 0; cb < ncols; cb += 16) {
+        uint32_t u[kMaxIss][16];
+        if (one_load) {
+          tc_ld64(lane_base, &u[0][0]);
+        } else {
 #pragma unroll
           for (int w = 0; w < kMaxIss; ++w)
-            if ((mask >> w) & 1u) {
-#pragma unroll
-              for (int cc = 0; cc < 16; ++cc) v[cc] += __uint_as_float(u[w][cc]);
-            }
-#pragma unroll
-          for (int cc = 0; cc < 16; ++cc) {
-            const int col = cb + cc;
-            if (col < cend) {
-              run += v[cc];
-              if (++jt == a.terms) {
-                jt = 0;
-                const long long pos = it.wg.pos0 + tk;
-                nan_row |= (run != run);
-                if (MODE == GATEUP)
-                  xb[(q * kXbRound + (tk - tr)) * 32 + lane] = run;
-                else
-                  a.ws.part[pos * c.d + row] = run;  // the gate weight is applied by the combine
-                run = 0.0f;
-                ++tk;
-              }
-            }
-          }
+            if ((mask >> w) & 1u) tc_ld16(lane_base + (uint32_t)(w * a.acc_cols + cb), u[w]);
         }
-        if (MODE == GATEUP) {
-          // The stacked tile's rows 0-63 are gate rows and 64-127 the up rows of the same 64 rows of h
-          // (k3moe_pack_records): warp q and warp q ^ 2 hold g and u of h rows 32 (q & 1) + lane of
-          // them. After the exchange, warps 0-1 finish the round's even tokens, warps 2-3 the odd;
-          // the second barrier keeps the area until both have read it.
-          bar_sync(1, 128);
-          for (int i = tr + (q >> 1); i < tend; i += 2) {
-            const float g = xb[(p * kXbRound + i - tr) * 32 + lane], uu = xb[((p + 2) * kXbRound + i - tr) * 32 + lane];
-            const float h = silu(g) * uu;
-            const long long pos = it.wg.pos0 + i;
-            if (c.fp4)
-              split_terms_fp4(h, c.hterms, a.ws.hq + (pos * c.hterms) * (c.f / 2) + blk * 16, c.f / 2,
-                              a.ws.hs + (pos * c.hterms) * nb + blk, nb, lane);
-            else
-              split_terms(h, c.hterms, a.ws.hq + (pos * c.hterms) * c.f + blk * 32 + lane, c.f,
-                          a.ws.hs + (pos * c.hterms) * nb + blk, nb, lane);
+        tc_wait_ld();
+        if (cb + 16 >= ncols) {  // buffer read completely: hand it back
+          tc_fence_before();
+          mbar_arrive(su32(&ctl->acc_empty[b]));
+        }
+        float v[16];
+#pragma unroll
+        for (int cc = 0; cc < 16; ++cc) v[cc] = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kMaxIss; ++w)
+          if ((mask >> w) & 1u) {
+#pragma unroll
+            for (int cc = 0; cc < 16; ++cc) v[cc] += __uint_as_float(u[w][cc]);
           }
-          bar_sync(1, 128);
+#pragma unroll
+        for (int cc = 0; cc < 16; ++cc) {
+          const int col = cb + cc;
+          if (col < ncols) {
+            run += v[cc];
+            if (++jt == a.terms) {
+              jt = 0;
+              const long long pos = it.wg.pos0 + tk;
+              nan_row |= (run != run);
+              if (MODE == GATEUP)
+                xb[(q * a.xb_tok + tk) * 32 + lane] = run;
+              else
+                a.ws.part[pos * c.d + row] = run;  // the gate weight is applied by the combine
+              run = 0.0f;
+              ++tk;
+            }
+          }
         }
       }
       // activations are finite by construction, so a NaN sum means a NaN weight scale: find it
@@ -645,6 +623,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint8_t* sg = scale_tile<MODE>(a, it) + 16 * lane + 4 * q;  // row 32 q + lane of the tile
         for (int g = it.j0 * wpc; g < it.j1 * wpc; ++g)
           bad |= (__vcmpeq4(__ldg(reinterpret_cast<const unsigned*>(sg + (size_t)512 * g)), 0xFFFFFFFFu) != 0u);
+      }
+      if (MODE == GATEUP) {
+        // The stacked tile's rows 0-63 are gate rows and 64-127 the up rows of the same 64 rows of h
+        // (k3moe_pack_records): warp q and warp q ^ 2 hold g and u of h rows 32 (q & 1) + lane of
+        // them. After the exchange, warps 0-1 finish the even tokens of the item, warps 2-3 the odd.
+        bar_sync(1, 128);
+        const int p = q & 1;
+        const int nb = c.f / 32, blk = 4 * it.mt + 2 * it.mat + p;  // 32-block of h
+        for (int i = q >> 1; i < it.wg.ntok; i += 2) {
+          const float g = xb[(p * a.xb_tok + i) * 32 + lane], u = xb[((p + 2) * a.xb_tok + i) * 32 + lane];
+          const float h = silu(g) * u;
+          const long long pos = it.wg.pos0 + i;
+          if (c.fp4)
+            split_terms_fp4(h, c.hterms, a.ws.hq + (pos * c.hterms) * (c.f / 2) + blk * 16, c.f / 2,
+                            a.ws.hs + (pos * c.hterms) * nb + blk, nb, lane);
+          else
+            split_terms(h, c.hterms, a.ws.hq + (pos * c.hterms) * c.f + blk * 32 + lane, c.f,
+                        a.ws.hs + (pos * c.hterms) * nb + blk, nb, lane);
+        }
       }
       g0 = (g0 + nst) % S;
     }
@@ -861,20 +858,14 @@ cudaError_t weight_map(const uint8_t* base, long long K, long long rows, long lo
   return cudaSuccess;
 }
 
-// Bytes after the control block: the loaders' token tables (gate/up) and row tables, and the gate/up
-// exchange area (float per epilogue warp, token of a round and lane).
-size_t tok_bytes(const TcArgs& a, int mode) {
-  return mode == GATEUP ? ((size_t)kLoaders * kEpRing * a.wgt_max * 4 + 15) / 16 * 16 : 0;
-}
-size_t row_bytes(const TcArgs& a) { return ((size_t)kLoaders * a.n_tile * 4 + 15) / 16 * 16; }
-size_t xb_bytes(int mode) { return mode == GATEUP ? (size_t)4 * kXbRound * 32 * sizeof(float) : 0; }
-size_t aux_bytes(const TcArgs& a, int mode) { return ctl_bytes() + tok_bytes(a, mode) + row_bytes(a) + xb_bytes(mode); }
+// Bytes of the gate/up exchange area (float per epilogue warp, token and lane).
+size_t xb_bytes(const TcArgs& a) { return (size_t)4 * a.xb_tok * 32 * sizeof(float); }
 
 template <int MODE>
 cudaError_t launch_tc(const TcArgs& a, const CUtensorMap& r0, const CUtensorMap& r1, const CUtensorMap& s0,
                       const CUtensorMap& s1, long long items_max, cudaStream_t st) {
   if (items_max >= (1LL << 31)) return cudaErrorInvalidValue;  // item indices are decomposed in 32 bits
-  const size_t smem = (size_t)a.stages * a.stage_bytes + aux_bytes(a, MODE) + 1024;
+  const size_t smem = (size_t)a.stages * a.stage_bytes + ctl_bytes() + xb_bytes(a) + 1024;
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(k_tc<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
@@ -896,41 +887,33 @@ int chunks_per_stage(long long nch, long long parts) {
 }
 
 // With fewer than 4 stages of ch chunks the stage shrinks to one chunk.
-void size_tiles(TcArgs& a, int ch, int mtiles, int mode) {
-  // above N = 128 (E4M3 form only) two issuers split N, each with 128 columns and 32 scale columns
-  a.nsplit = a.n_tile > 128 ? 1 : 0;
-  a.sf_slot = (a.fp4 || a.nsplit) ? 64 : 32;
-  // scale words of a chunk: A's image, then B's (two 128-row images above N = 128), in a multiple of
-  // 1 KB so that every stage's tiles stay 1 KB aligned (128-byte swizzle)
-  a.sf_bytes = (a.fp4 || a.nsplit) ? 2048 : 1024;
+void size_tiles(TcArgs& a, int ch, int mtiles) {
+  a.sf_slot = a.fp4 ? 64 : 32;
+  a.sf_bytes = a.fp4 ? 2048 : 1024;
   a.div_parts.init((uint32_t)a.parts);
   a.div_mtiles.init((uint32_t)mtiles);
-  a.acc_cols = 16;  // a power of two >= an issuer's N: every accumulator starts at a multiple of its width
-  while (a.acc_cols < (a.nsplit ? 128 : a.n_tile)) a.acc_cols *= 2;
+  a.acc_cols = 16;  // a power of two >= n_tile: every accumulator starts at a multiple of its width
+  while (a.acc_cols < a.n_tile) a.acc_cols *= 2;
   // issuers and accumulator buffers: small N needs several issuers (issue rate); three (each owning
   // two of the six stages at N = 16) measured faster than four (two owning two, two owning one) or
   // two. Above 64 columns: with few tokens per work group (T < 256) two issuers with one buffer each
-  // (measured faster), at prefill sizes one issuer with two buffers (deeper ring, overlapped epilogue).
-  // Above 128 columns (whole experts' token lists at prefill sizes) two issuers split N and one
-  // buffer: the scale slots need the other half of the tensor memory.
-  a.n_iss = a.nsplit ? 2 : (a.n_tile <= 32 ? 3 : (a.n_tile <= 64 || a.T < 256 ? 2 : 1));
+  // (measured faster), at prefill sizes one issuer with two buffers (deeper ring, overlapped epilogue)
+  a.n_iss = a.n_tile <= 32 ? 3 : (a.n_tile <= 64 || a.T < 256 ? 2 : 1);
   a.n_acc = 1;  // two alternating accumulators measured no faster at any N
-  a.n_buf = a.nsplit ? 1 : ((a.n_tile <= 64 || a.T >= 256) ? 2 : 1);  // (three measured no faster)
+  a.n_buf = (a.n_tile <= 64 || a.T >= 256) ? 2 : 1;  // (three, with a stage fewer, measured no faster)
   a.sf_base = (a.n_buf * a.n_iss * a.n_acc * a.acc_cols + 31) / 32 * 32;
   a.b_bytes = (a.n_tile * 128 + 1023) / 1024 * 1024;
   for (;; ch = 1) {
     a.ch = ch;
     a.stage_bytes = ch * (kATile + a.b_bytes + a.sf_bytes);
-    int st = (227 * 1024 - 1024 - (int)aux_bytes(a, mode)) / a.stage_bytes;
+    int st = (227 * 1024 - 1024 - (int)ctl_bytes() - (int)xb_bytes(a)) / a.stage_bytes;
     const int tm = (kTmemCols - a.sf_base) / (a.sf_slot * ch);
     if (st > tm) st = tm;
     if (st > kMaxStages) st = kMaxStages;
     a.stages = st;
     if (st >= 4 || ch == 1) break;
   }
-  a.off_tok = a.stages * a.stage_bytes + (int)ctl_bytes();
-  a.off_row = a.off_tok + (int)tok_bytes(a, mode);
-  a.off_xb = a.off_row + (int)row_bytes(a);
+  a.pf_dist = a.stages * a.ch;  // one ring's worth of chunks beyond the copies in flight
 }
 
 int round16(int v) { return (v + 15) / 16 * 16; }
@@ -989,12 +972,11 @@ cudaError_t launch_gateup(const Cfg& c, const Ws& ws, const uint8_t* routed, con
   TcArgs a = base_args(c, ws, routed, shared, y, T);
   a.terms = c.xterms;
   a.n_tile = round16(c.wgt * c.xterms);
-  a.wgt_max = c.wgt;
+  a.xb_tok = c.wgt;
   a.parts = 1;  // the epilogue needs whole sums (splitting items along d measured slower at decode too)
   a.fp4 = c.fp4;
   a.nch = c.d / (c.fp4 ? 256 : 128);
-  if (a.n_tile > kMaxN || (a.fp4 && a.n_tile > 128)) return cudaErrorInvalidConfiguration;
-  size_tiles(a, chunks_per_stage(a.nch, 1), c.f / 128, GATEUP);
+  size_tiles(a, chunks_per_stage(a.nch, 1), c.f / 128);
   if (a.stages < 2) return cudaErrorInvalidConfiguration;
   TcMaps m;
   cudaError_t e = setup(c, routed, shared, a.ch, 0, m, a.shared);
@@ -1009,12 +991,10 @@ cudaError_t launch_down(const Cfg& c, const Ws& ws, const uint8_t* routed, const
   TcArgs a = base_args(c, ws, routed, shared, y, T);
   a.terms = c.hterms;
   a.n_tile = round16(c.wgt_dn * c.hterms);
-  a.wgt_max = c.wgt_dn;
   a.parts = 1;
   a.fp4 = c.fp4;
   a.nch = c.f / (c.fp4 ? 256 : 128);
-  if (a.n_tile > kMaxN || (a.fp4 && a.n_tile > 128)) return cudaErrorInvalidConfiguration;
-  size_tiles(a, chunks_per_stage(a.nch, 1), c.d / 128, DOWN);
+  size_tiles(a, chunks_per_stage(a.nch, 1), c.d / 128);
   if (a.stages < 2) return cudaErrorInvalidConfiguration;
   TcMaps m;
   cudaError_t e = setup(c, routed, shared, 0, a.ch, m, a.shared);

@@ -120,8 +120,8 @@ def test_layer_tiny_f32():
 @pytest.mark.parametrize("x_dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("T", [1, 2, 5, 37, 600])
 def test_layer_mid_ragged(x_dtype, T):
-    """Ragged token counts; at 600 tokens (~56 per expert) every expert's token list is one work
-    group of up to 128 tokens (85 for fp32 tokens and for h: MMA N up to 256, one item per tile)."""
+    """Ragged token counts; at 600 tokens (~56 per expert) experts' token lists span several work
+    groups, with the tensor-core router (partial logits) and E4M3 activation terms."""
     L = DeviceLayer(MID, seed=7, x_dtype=x_dtype)
     check_layer(L, T)
 
