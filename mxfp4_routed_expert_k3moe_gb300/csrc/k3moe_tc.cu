@@ -176,7 +176,6 @@ struct TcArgs {
   int parts;    // reduction parts per row tile (1: whole items)
   FastDiv div_parts, div_mtiles;
   int stages;   // pipeline depth (<= kMaxStages)
-  int pf_dist;  // chunks ahead of its tensor copy that a loader prefetches a weight tile into L2 (0: none)
   int stage_bytes;  // ch x (A tile + B tile + scale words)
 };
 
@@ -355,19 +354,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const CUtensorMap* map = routed ? (it.mat == 0 ? &map_r0 : &map_r1) : (it.mat == 0 ? &map_s0 : &map_s1);
       const int ecoord = routed ? it.wg.expert : it.wg.expert - c.E;
       const uint8_t* atile = scale_tile<MODE>(a, it);
-      // the CTA's next item (its work group arrived with the group committed three items ago), whose
-      // first chunks this item's last stages prefetch into L2
-      Item nx;
-      const CUtensorMap* nx_map = nullptr;
-      int nx_e = 0;
-      const uint8_t* nx_sc = nullptr;
-      if (a.pf_dist > 0 && item_geom<MODE>(a, ii + gridDim.x, n_items, nx)) {
-        nx.wg = rwg[(kk + 1) % kEpRing];
-        const bool r2 = nx.wg.expert < c.E;
-        nx_map = r2 ? (nx.mat == 0 ? &map_r0 : &map_r1) : (nx.mat == 0 ? &map_s0 : &map_s1);
-        nx_e = r2 ? nx.wg.expert : nx.wg.expert - c.E;
-        nx_sc = scale_tile<MODE>(a, nx);
-      }
       // B row n of the tile = activation row (token or position) * terms + term; the rows' indices go
       // to this loader's table, which the code copies below read, and the scale pointers of rows
       // lane + 32 q stay in registers
@@ -433,19 +419,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 cp4(sc + 512 * (wpc + h) + 16 * lane + 4 * q, bscales[q] + 4 * (wpc * jj + h), 4);
         }
         cp_arrive_noinc(su32(&ctl->full[s]));
-        // L2 prefetch of the weight tile and scale groups pf_dist chunks ahead (this item, or the next
-        // one): more DRAM reads in flight than the ring's stages hold
-        if (lane == 0 && a.pf_dist > 0) {
-          const int jp = j + a.pf_dist;
-          if (jp < it.j1) {
-            tma_prefetch_4d(map, 0, it.mt * 128, jp, ecoord);
-            bulk_prefetch(atile + (size_t)512 * wpc * jp, 512 * wpc * CH);
-          } else if (nx_map && jp - it.j1 + nx.j0 < nx.j1) {
-            const int jn = jp - it.j1 + nx.j0;
-            tma_prefetch_4d(nx_map, 0, nx.mt * 128, jn, nx_e);
-            bulk_prefetch(nx_sc + (size_t)512 * wpc * jn, 512 * wpc * CH);
-          }
-        }
       }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
@@ -913,7 +886,6 @@ void size_tiles(TcArgs& a, int ch, int mtiles) {
     a.stages = st;
     if (st >= 4 || ch == 1) break;
   }
-  a.pf_dist = a.stages * a.ch;  // one ring's worth of chunks beyond the copies in flight
 }
 
 int round16(int v) { return (v + 15) / 16 * 16; }
