@@ -61,8 +61,11 @@ def lib():
         L.k3o_route_tokens.restype = ctypes.c_int
         L.k3o_expert_token.argtypes = [ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P]
         L.k3o_expert_token.restype = ctypes.c_int
+        L.k3o_expert_token_bf16.argtypes = [ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P]
+        L.k3o_expert_token_bf16.restype = ctypes.c_int
         L.k3o_layer.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
-                                _P, ctypes.c_int32, ctypes.c_int64, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int32]
+                                _P, ctypes.c_int32, ctypes.c_int64, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int32,
+                                ctypes.c_int32]
         L.k3o_layer.restype = ctypes.c_int
         L.k3o_rmsnorm.argtypes = [_P, ctypes.c_int64, ctypes.c_int32, ctypes.c_double, _P]
         L.k3o_rmsnorm.restype = None
@@ -168,12 +171,27 @@ def expert_token(record: np.ndarray, x: np.ndarray, d: int, f: int):
     return o, h
 
 
+def expert_token_bf16(record: np.ndarray, x: np.ndarray, d: int, f: int):
+    """-> (o[d], h[f]) of one expert with bf16 weights (record: [gate f x d][up f x d][down d x f] uint16
+    bf16 bit patterns) on one token (exact float64 values)."""
+    record = np.ascontiguousarray(record, dtype=np.uint16)
+    if record.size < 3 * d * f:
+        raise ValueError("expert_token_bf16: record too small")
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    o = np.empty(d, np.float64)
+    h = np.empty(f, np.float64)
+    if lib().k3o_expert_token_bf16(d, f, _ptr(record), _ptr(x), _ptr(o), _ptr(h)):
+        raise ValueError("expert_token_bf16 failed")
+    return o, h
+
+
 def layer(x: np.ndarray, x_dtype: str, W: np.ndarray, bias, routed: dict | list, shared: list,
-          d: int, f: int, k: int, score: str = "softmax"):
+          d: int, f: int, k: int, score: str = "softmax", shared_format: str = "mxfp4"):
     """One MoE layer on T tokens.
 
     x: [T, d] uint16 bf16 bits (x_dtype 'bf16') or float32 ('f32').
     routed: list of E records, or dict {expert id: record} holding at least the selected experts.
+    shared: S records, MXFP4 (shared_format 'mxfp4', uint8) or bf16 ('bf16', uint16 bit patterns).
     Returns (y[T, d] float64, idx[T, k] int32, w[T, k] float64, logits[T, E] float64).
     """
     W = np.ascontiguousarray(W, dtype=np.float32)
@@ -194,9 +212,11 @@ def layer(x: np.ndarray, x_dtype: str, W: np.ndarray, bias, routed: dict | list,
             r = np.ascontiguousarray(r, dtype=np.uint8)
             keep.append(r)
             rp[e] = r.ctypes.data
+    if shared_format not in ("mxfp4", "bf16"):
+        raise ValueError(shared_format)
     sp = (ctypes.c_void_p * max(1, len(shared)))()
     for s, r in enumerate(shared):
-        r = np.ascontiguousarray(r, dtype=np.uint8)
+        r = np.ascontiguousarray(r, dtype=np.uint8 if shared_format == "mxfp4" else np.uint16)
         keep.append(r)
         sp[s] = r.ctypes.data
     y = np.empty((T, d), np.float64)
@@ -205,7 +225,7 @@ def layer(x: np.ndarray, x_dtype: str, W: np.ndarray, bias, routed: dict | list,
     logits = np.empty((T, E), np.float64)
     rc = lib().k3o_layer(d, f, E, k, len(shared), _ptr(xa), 1 if x_dtype == "bf16" else 0, T, _ptr(W), _ptr(b),
                          ctypes.cast(rp, ctypes.c_void_p), ctypes.cast(sp, ctypes.c_void_p), _ptr(y), _ptr(idx),
-                         _ptr(w), _ptr(logits), SCORES[score])
+                         _ptr(w), _ptr(logits), SCORES[score], 1 if shared_format == "bf16" else 0)
     if rc:
         raise ValueError(f"oracle layer failed ({rc})")
     return y, idx, w, logits

@@ -26,6 +26,11 @@
  *  - Expert FFN: h = SiLU(W_gate x) * (W_up x), o = W_down h (SiLU-gated GLU,
  *    the stand-in for the pages' unspecified "SiTU-GLU").
  *  - Combine: y = sum_i w_i o_i + sum_s o_s (shared experts weight 1).
+ *  - Shared experts in bf16 (a variant): the kimi-k3-in-c README's parameter
+ *    budget (after the shard census) counts every non-routed parameter in
+ *    bfloat16. A bf16 shared record is [gate f x d][up f x d][down d x f] bf16,
+ *    row-major; its weights are the exact values of the bf16 bit patterns and
+ *    the FFN is the same.
  *
  * Readings where the pages are silent (layout of a record, block axis, nibble
  * order, tie order): blocks of 32 run along the reduction axis; the even
@@ -264,6 +269,36 @@ int k3o_expert_token(int32_t d, int32_t f, const uint8_t* record, const double* 
     return 0;
 }
 
+/*
+ * One expert with bf16 weights on one token: record = [gate f x d][up f x d][down d x f] bf16 bit
+ * patterns, row-major. out[d] = W_down (SiLU(W_gate x) * (W_up x)), the same loops as above with
+ * each weight the exact value of its bf16 pattern.
+ */
+int k3o_expert_token_bf16(int32_t d, int32_t f, const uint16_t* record, const double* x, double* out,
+                          double* h_out) {
+    const uint16_t* gw = record;
+    const uint16_t* uw = gw + (int64_t)f * d;
+    const uint16_t* dw = uw + (int64_t)f * d;
+    double* h = (double*)malloc(sizeof(double) * (size_t)f);
+    if (!h) return -2;
+    for (int32_t r = 0; r < f; ++r) {
+        double g = 0.0, u = 0.0;
+        for (int32_t c = 0; c < d; ++c) {
+            g += k3o_bf16(gw[(int64_t)r * d + c]) * x[c];
+            u += k3o_bf16(uw[(int64_t)r * d + c]) * x[c];
+        }
+        h[r] = (g_fault == FAULT_GLU_ON_UP) ? silu(u) * g : silu(g) * u;
+        if (h_out) h_out[r] = h[r];
+    }
+    for (int32_t i = 0; i < d; ++i) {
+        double o = 0.0;
+        for (int32_t r = 0; r < f; ++r) o += k3o_bf16(dw[(int64_t)i * f + r]) * h[r];
+        out[i] = o;
+    }
+    free(h);
+    return 0;
+}
+
 /* ------------------------------------------------------------------ layer */
 /*
  * One MoE layer over T tokens.
@@ -273,11 +308,13 @@ int k3o_expert_token(int32_t d, int32_t f, const uint8_t* record, const double* 
  *   shared: S record pointers
  *   y: T x d doubles (overwritten); idx/w: T x k (may be NULL); logits: T x E (may be NULL)
  *   score: 0 softmax, 1 sigmoid + selection-only bias (k3o_route_token)
+ *   shared_bf16: 0 shared records are MXFP4 like the routed ones, 1 they are bf16 records
  * Returns 0, -1 on bad data (NaN scale byte, missing record), -2 on allocation failure.
  */
 int k3o_layer(int32_t d, int32_t f, int32_t E, int32_t k, int32_t S, const void* x, int32_t x_is_bf16,
               int64_t T, const float* W, const float* bias, const uint8_t* const* routed,
-              const uint8_t* const* shared, double* y, int32_t* idx, double* w, double* logits, int32_t score) {
+              const uint8_t* const* shared, double* y, int32_t* idx, double* w, double* logits, int32_t score,
+              int32_t shared_bf16) {
     int status = 0;
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t t = 0; t < T; ++t) {
@@ -301,7 +338,8 @@ int k3o_layer(int32_t d, int32_t f, int32_t E, int32_t k, int32_t S, const void*
             if (!st) for (int32_t j = 0; j < d; ++j) yt[j] += wt[i] * o[j];
         }
         for (int32_t s = 0; s < S && !st && g_fault != FAULT_DROP_SHARED; ++s) {
-            st = k3o_expert_token(d, f, shared[s], xt, o, NULL);
+            st = shared_bf16 ? k3o_expert_token_bf16(d, f, (const uint16_t*)shared[s], xt, o, NULL)
+                             : k3o_expert_token(d, f, shared[s], xt, o, NULL);
             if (!st) for (int32_t j = 0; j < d; ++j) yt[j] += o[j];
         }
         if (!st) {

@@ -8,7 +8,9 @@ with the shapes and value distributions of the workloads:
   (host: ``synth_host.c``; device: ``synth_dev.cu``, bit-identical);
 * router weights: fp32 N(0, 1/d);
 * token activations: N(0, 1), stored as bf16 (round-to-nearest-even) or fp32;
-* an optional Zipf(s) routing bias b_e = -s * ln(r_e), r a seeded permutation of 1..E.
+* an optional Zipf(s) routing bias b_e = -s * ln(r_e), r a seeded permutation of 1..E;
+* bf16 shared-expert records (the bf16 variant): N(0, 1/8^2) weights rounded to bf16, [gate f x d]
+  [up f x d][down d x f] row-major, zero padding to the stride.
 
 All randomness comes from SplitMix64 (Steele, Lea, Flood, OOPSLA 2014) used
 counter-based; normals use the Box-Muller cosine branch.
@@ -27,7 +29,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 GAMMA = 0x9E3779B97F4A7C15
 _M64 = (1 << 64) - 1
 
-KIND_CODES, KIND_SCALES, KIND_ROUTER, KIND_TOKENS, KIND_BIAS = 1, 2, 3, 4, 5
+KIND_CODES, KIND_SCALES, KIND_ROUTER, KIND_TOKENS, KIND_BIAS, KIND_SHARED_BF16 = 1, 2, 3, 4, 5, 6
 
 
 # --------------------------------------------------------------------------- configs
@@ -148,6 +150,26 @@ def tokens(shape: LayerShape, seed: int, T: int, x_dtype: str, batch: int = 0) -
 
 def tokens_as_f64(x: np.ndarray, x_dtype: str) -> np.ndarray:
     return bf16_bits_to_f32(x).astype(np.float64) if x_dtype == "bf16" else np.asarray(x, np.float64)
+
+
+def shared_bf16_record_bytes(shape: LayerShape) -> int:
+    return 3 * shape.d_model * shape.d_ff * 2
+
+
+def shared_bf16_stride(shape: LayerShape) -> int:
+    return (shared_bf16_record_bytes(shape) + 4095) // 4096 * 4096
+
+
+def shared_records_bf16(shape: LayerShape, seed: int, layer: int, n: int, stride: int | None = None) -> np.ndarray:
+    """n bf16 shared-expert records as uint16 [n, stride/2]: N(0, 1/64) values rounded to bf16
+    (nearest-even), gate, up and down matrices row-major, then zero padding."""
+    stride = stride or shared_bf16_stride(shape)
+    m = 3 * shape.d_model * shape.d_ff
+    out = np.zeros((n, stride // 2), dtype=np.uint16)
+    for s_ in range(n):
+        z = normals(stream_key(seed, KIND_SHARED_BF16, layer, s_), m) * 0.125
+        out[s_, :m] = f32_to_bf16_bits(z.astype(np.float32))
+    return out
 
 
 def zipf_bias(shape: LayerShape, seed: int, s: float, layer: int = 0) -> np.ndarray:

@@ -396,12 +396,51 @@ def pin_tolerance_budget():
     assert float(g["printed_rel_err"]) < tol < 2e-3
 
 
+# ----------------------------------------------------------------------------- pins: bf16 shared experts
+
+
+def pin_shared_bf16_vs_dense():
+    """bf16 shared expert (README parameter budget: non-routed parameters in bfloat16): the oracle's
+    loop over bf16 bit patterns equals numpy's float conversion of the patterns and numpy matmuls."""
+    sh = synth.LayerShape(d_model=64, d_ff=32, n_routed=4, top_k=2, n_shared=1)
+    rec = synth.shared_records_bf16(sh, 5, 0, 1)[0]
+    d, f = sh.d_model, sh.d_ff
+    w = synth.bf16_bits_to_f32(rec[:3 * d * f]).astype(np.float64)
+    Wg, Wu, Wd = w[:f * d].reshape(f, d), w[f * d:2 * f * d].reshape(f, d), w[2 * f * d:].reshape(d, f)
+    x = np.random.default_rng(3).standard_normal(d)
+    g, u = Wg @ x, Wu @ x
+    h = _silu(g) * u
+    o, h_or = oracle.expert_token_bf16(rec, x, d, f)
+    assert np.allclose(h_or, h, rtol=1e-12, atol=1e-14)
+    assert np.allclose(o, Wd @ h, rtol=1e-12, atol=1e-14)
+
+
+def pin_shared_bf16_image_of_mxfp4_is_identical():
+    """A bf16 shared record holding exactly the values of an MXFP4 record (E2M1 values times powers of
+    two fit bf16's 8-bit significand) gives the same layer output, bit for bit, as the MXFP4 record."""
+    sh = synth.LayerShape(d_model=64, d_ff=32, n_routed=8, top_k=2, n_shared=1)
+    d, f = sh.d_model, sh.d_ff
+    routed = list(synth.records_host(sh, 6, 0, range(sh.n_routed)))
+    shared_mx = synth.records_host(sh, 6, 0, [sh.n_routed])[0]
+    dense = [oracle.decode_matrix(c, sc, *dims) for (c, sc), dims in
+             zip(oracle.split_record(shared_mx, d, f), [(f, d), (f, d), (d, f)])]
+    flat = np.concatenate([m.ravel() for m in dense]).astype(np.float32)
+    bits = synth.f32_to_bf16_bits(flat)
+    assert np.array_equal(synth.bf16_bits_to_f32(bits).astype(np.float64), np.concatenate([m.ravel() for m in dense]))
+    W = synth.router_weights(sh, 6)
+    x = synth.tokens(sh, 6, 3, "f32")
+    y_mx = oracle.layer(x, "f32", W, None, routed, [shared_mx], d, f, sh.top_k)[0]
+    y_bf = oracle.layer(x, "f32", W, None, routed, [bits], d, f, sh.top_k, shared_format="bf16")[0]
+    assert np.array_equal(y_mx, y_bf)
+
+
 PINS = [pin_e2m1_table, pin_e8m0, pin_record_bytes, pin_decode_single_nonzero, pin_decode_block_scale_axis,
         pin_router_bruteforce, pin_router_ties_lower_index, pin_router_counts_k3_shape,
         pin_router_sigmoid_bias_selection_only, pin_router_sigmoid_unbiased_matches_softmax_selection, pin_expert_vs_dense,
         pin_expert_closed_form, pin_layer_combine_definition, pin_layer_identical_experts, pin_layer_relabel,
         pin_layer_token_independence, pin_layer_zero_gate_branch, pin_layer_down_scale_linear,
-        pin_bf16_input_exact, pin_rmsnorm, pin_tolerance_budget]
+        pin_bf16_input_exact, pin_rmsnorm, pin_tolerance_budget, pin_shared_bf16_vs_dense,
+        pin_shared_bf16_image_of_mxfp4_is_identical]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
