@@ -34,7 +34,8 @@
  *    Legal configurations this library does not implement return K3MOE_ERR_UNSUPPORTED
  *    without launching anything: d_model or d_ff a multiple of 32 but not of 128 (the
  *    tensor-core tiles are 128 rows), d_model > 25600, act_mode K3MOE_ACT_MXFP4, and records
- *    in the stored order (record_order K3MOE_ORDER_STORED) given to a call that reads them.
+ *    in the stored order (record_order K3MOE_ORDER_STORED) given to a call that reads them
+ *    (record_order describes the MXFP4 records; bf16 shared records have a single order).
  *    A workspace smaller than k3moe_workspace_bytes(cfg, T) returns K3MOE_ERR_WORKSPACE.
  *  - T = 0 is a no-op that returns K3MOE_OK.
  *  - Bad data found on the device (an expert index outside [0, n_routed) given to
@@ -90,8 +91,11 @@ enum { K3MOE_X_BF16 = 0, K3MOE_X_F32 = 1 };
    zero-initialised config says "stored". */
 enum { K3MOE_ORDER_STORED = 0, K3MOE_ORDER_DEVICE = 1 };
 /* Format of the shared experts' records: MXFP4 like the routed experts (the default), or bf16
-   (the README's parameter budget counts every non-routed parameter in bfloat16). bf16 shared
-   records are legal but not implemented yet (K3MOE_ERR_UNSUPPORTED). */
+   (the kimi-k3-in-c README's parameter budget counts every non-routed parameter in bfloat16). A bf16
+   shared record is [gate f x d][up f x d][down d x f] bf16, row-major, 6 d f bytes, shared_stride
+   bytes apart; it is used as stored (k3moe_pack_records is for MXFP4 records only). Its FFN runs as
+   bf16 GEMMs on the tensor cores (fp32 accumulation; fp32 tokens and h enter as three bf16 parts,
+   24 significant bits), after the routed experts, and the combine adds its output. */
 enum { K3MOE_SHARED_MXFP4 = 0, K3MOE_SHARED_BF16 = 1 };
 
 typedef struct {
@@ -183,7 +187,8 @@ K3MOE_API k3moe_status k3moe_route(const k3moe_config* cfg /* host */, const voi
  *   topk_w         [T, top_k] fp32 gate weights
  *   routed_records n_routed records, record_stride bytes apart (16-byte aligned base), in the
  *                  device order (k3moe_pack_records)
- *   shared_records n_shared records, record_stride bytes apart, device order (may be NULL
+ *   shared_records n_shared records: MXFP4, record_stride bytes apart, device order; or bf16
+ *                  (shared_format K3MOE_SHARED_BF16), shared_stride bytes apart (may be NULL
  *                  if n_shared == 0)
  *   y              [T, d_model] fp32 out, overwritten
  */

@@ -55,7 +55,14 @@ long long record_bytes_of(const k3moe_config* c) {
   return 3LL * ((long long)c->d_model * c->d_ff / 2 + (long long)c->d_model * c->d_ff / 32);
 }
 
-long long shared_stride_of(const k3moe_config* c) { return c->shared_stride ? c->shared_stride : c->record_stride; }
+bool shared_bf16(const k3moe_config* c) { return c->shared_format == K3MOE_SHARED_BF16 && c->n_shared > 0; }
+
+long long shared_bf16_bytes(const k3moe_config* c) { return 6LL * c->d_model * c->d_ff; }
+
+long long shared_stride_of(const k3moe_config* c) {
+  if (c->shared_stride) return c->shared_stride;
+  return c->shared_format == K3MOE_SHARED_BF16 ? (shared_bf16_bytes(c) + 4095) / 4096 * 4096 : c->record_stride;
+}
 
 // Every check of the config that returns K3MOE_ERR_INVALID_ARGUMENT, then those that return
 // K3MOE_ERR_UNSUPPORTED, except the tile geometry (d_model and d_ff multiples of 128), which
@@ -75,11 +82,10 @@ k3moe_status validate_fields(const k3moe_config* c) {
   if ((long long)c->d_model * c->d_ff > (1LL << 40)) return K3MOE_ERR_INVALID_ARGUMENT;
   if (c->record_stride < record_bytes_of(c) || c->record_stride % 4096) return K3MOE_ERR_INVALID_ARGUMENT;
   if (c->shared_stride < 0 || c->shared_stride % 4096) return K3MOE_ERR_INVALID_ARGUMENT;
-  const long long shared_need = c->shared_format == K3MOE_SHARED_BF16 ? 6LL * c->d_model * c->d_ff : record_bytes_of(c);
+  const long long shared_need = c->shared_format == K3MOE_SHARED_BF16 ? shared_bf16_bytes(c) : record_bytes_of(c);
   if (c->shared_stride && c->shared_stride < shared_need) return K3MOE_ERR_INVALID_ARGUMENT;
   if (c->act_mode != K3MOE_ACT_EXACT) return K3MOE_ERR_UNSUPPORTED;
   if (c->d_model > kMaxDModel) return K3MOE_ERR_UNSUPPORTED;  // router rows are staged in shared memory
-  if (c->shared_format != K3MOE_SHARED_MXFP4) return K3MOE_ERR_UNSUPPORTED;
   return K3MOE_OK;
 }
 
@@ -108,12 +114,24 @@ long long wg_bound(const k3moe_config* c, long long T) {
 
 struct Layout {
   size_t ctrl, logits, topk_idx, topk_w, counts, cursor, offsets, wgoff, perm_tok, perm_w, inv, wgs, wgs_dn, xq, xs, hq, hs,
-      part, rtcnt, w3, x3, total;
+      part, rtcnt, w3, x3, sgu, sh3, sho, total;
 };
+
+// Largest T' * parts(T') over T' <= T when parts(T') is constant on runs of 128 tokens (the tile rows)
+// and 1 from kRouterSplitSms runs on: sized so, a region never shrinks as T grows.
+template <typename F>
+long long max_rows(long long T, F parts) {
+  long long m = T * parts(T);
+  for (long long j = 1; j <= kRouterSplitSms && 128 * j < T; ++j) {
+    const long long r = 128 * j * parts(128 * j);
+    m = r > m ? r : m;
+  }
+  return m;
+}
 
 Layout make_layout(const k3moe_config* c, long long T) {
   const long long E = c->n_routed, k = c->top_k, S = c->n_shared, d = c->d_model, f = c->d_ff;
-  const long long P = T * (k + S);
+  const long long P = T * (k + (shared_bf16(c) ? 0 : S));  // (bf16 shared experts take no positions)
   Layout L{};
   size_t o = 0;
   auto take = [&](size_t& field, size_t bytes) {
@@ -121,15 +139,8 @@ Layout make_layout(const k3moe_config* c, long long T) {
     o = align_up(o + (bytes ? bytes : 1));
   };
   take(L.ctrl, sizeof(int) * k3::CTRL_WORDS);
-  // partial logits: T x parts rows. Within a run of equal tile counts the parts are constant, so the
-  // largest row count over T' <= T is at T or at a run's end (a multiple of 128; parts are 1 beyond
-  // kRouterSplitSms runs): sized for that, the layout never shrinks as T grows
-  long long lrows = T * router_splits(c, T);
-  for (long long j = 1; j <= kRouterSplitSms && 128 * j < T; ++j) {
-    const long long r = 128 * j * router_splits(c, 128 * j);
-    lrows = r > lrows ? r : lrows;
-  }
-  take(L.logits, sizeof(float) * lrows * E);
+  // partial logits: T x parts rows, sized for the largest row count over T' <= T
+  take(L.logits, sizeof(float) * max_rows(T, [&](long long t) { return router_splits(c, t); }) * E);
   take(L.topk_idx, sizeof(int) * T * k);
   take(L.topk_w, sizeof(float) * T * k);
   take(L.counts, sizeof(int) * E);
@@ -150,7 +161,18 @@ Layout make_layout(const k3moe_config* c, long long T) {
   take(L.part, sizeof(float) * P * d);
   take(L.rtcnt, sizeof(int) * T);  // one counter per router token tile (tiles of 1 to 8 tokens)
   take(L.w3, router_tc(c, T) ? (size_t)3 * E * d * 2 : 0);  // bf16 parts of the router weights
-  take(L.x3, router_tc(c, T) && c->x_dtype == K3MOE_X_F32 ? (size_t)3 * T * d * 2 : 0);  // ... of fp32 tokens
+  // three bf16 parts of fp32 tokens (tensor-core router, bf16 shared experts)
+  take(L.x3, (router_tc(c, T) || shared_bf16(c)) && c->x_dtype == K3MOE_X_F32 ? (size_t)3 * T * d * 2 : 0);
+  // bf16 shared experts: partial sums of gate | up, h in three bf16 parts, partial sums of the outputs
+  const bool sb = shared_bf16(c);
+  const int xp = c->x_dtype == K3MOE_X_F32 ? 3 : 1;
+  take(L.sgu, sb ? sizeof(float) * S * 2 * f *
+                       max_rows(T, [&](long long t) { return (long long)k3::shared_gemm_splits(t, 2 * (int)f, (int)d, xp); })
+                 : 0);
+  take(L.sh3, sb ? (size_t)2 * S * 3 * T * f : 0);
+  take(L.sho, sb ? sizeof(float) * S * d *
+                       max_rows(T, [&](long long t) { return (long long)k3::shared_gemm_splits(t, (int)d, (int)f, 3); })
+                 : 0);
   L.total = o;
   return L;
 }
@@ -177,6 +199,9 @@ Ws bind(const Layout& L, void* base) {
   w.hs = reinterpret_cast<uint8_t*>(b + L.hs);
   w.part = reinterpret_cast<float*>(b + L.part);
   w.rtcnt = reinterpret_cast<int*>(b + L.rtcnt);
+  w.sgu = reinterpret_cast<float*>(b + L.sgu);
+  w.sh3 = reinterpret_cast<uint8_t*>(b + L.sh3);
+  w.sho = reinterpret_cast<float*>(b + L.sho);
   return w;
 }
 
@@ -186,7 +211,10 @@ Cfg make_cfg(const k3moe_config* c, long long T) {
   k.f = c->d_ff;
   k.E = c->n_routed;
   k.k = c->top_k;
-  k.S = c->n_shared;
+  k.S = shared_bf16(c) ? 0 : c->n_shared;  // MXFP4 shared experts run as work groups
+  k.Sb = shared_bf16(c) ? c->n_shared : 0;
+  k.nsp1 = k.Sb ? k3::shared_gemm_splits(T, 2 * c->d_ff, c->d_model, c->x_dtype == K3MOE_X_F32 ? 3 : 1) : 0;
+  k.nsp2 = k.Sb ? k3::shared_gemm_splits(T, c->d_model, c->d_ff, 3) : 0;
   k.x_f32 = c->x_dtype == K3MOE_X_F32 ? 1 : 0;
   k.fp4 = use_fp4(c, T) ? 1 : 0;
   if (k.fp4) {
@@ -280,6 +308,27 @@ k3moe_status k3moe_route(const k3moe_config* cfg, const void* x, int64_t T, cons
   return cuda_status(k3::launch_route(c, w, x, T, w_router, bias, topk_idx, topk_w, mode, st));
 }
 
+}  // extern "C"
+
+namespace {
+
+// The bf16 shared experts (their GEMMs on the tensor cores, after the routed projections), then the
+// combine. fp32 tokens are split into three bf16 parts unless the tensor-core router already did.
+cudaError_t shared_bf16_then_combine(const k3moe_config* cfg, const Cfg& c, const Ws& w, const Layout& L, const void* x,
+                                     long long T, const uint8_t* shared, float* y, void* ws, bool x3_ready,
+                                     cudaStream_t st) {
+  char* x3 = static_cast<char*>(ws) + L.x3;
+  cudaError_t e = cudaSuccess;
+  if (c.x_f32 && !x3_ready) e = k3::launch_split_tokens(static_cast<const float*>(x), T * cfg->d_model, x3, st);
+  if (e == cudaSuccess) e = k3::launch_shared_bf16(c, w, x, T, x3, shared, st);
+  if (e == cudaSuccess) e = k3::launch_combine(c, w, y, T, st);
+  return e;
+}
+
+}  // namespace
+
+extern "C" {
+
 k3moe_status k3moe_expert_ffn(const k3moe_config* cfg, const void* x, int64_t T, const int32_t* topk_idx,
                               const float* topk_w, const uint8_t* routed_records, const uint8_t* shared_records,
                               float* y, void* ws, size_t ws_bytes, void* stream) {
@@ -300,7 +349,9 @@ k3moe_status k3moe_expert_ffn(const k3moe_config* cfg, const void* x, int64_t T,
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = k3::launch_prep(c, w, x, T, topk_idx, topk_w, st);
   if (e == cudaSuccess) e = k3::launch_gateup(c, w, routed_records, shared_records, y, T, wg_bound(cfg, T), st);
-  if (e == cudaSuccess) e = k3::launch_down(c, w, routed_records, shared_records, y, T, wg_bound(cfg, T), st);
+  if (e == cudaSuccess)
+    e = k3::launch_down(c, w, routed_records, shared_records, y, T, wg_bound(cfg, T), st, nullptr, c.Sb == 0);
+  if (e == cudaSuccess && c.Sb > 0) e = shared_bf16_then_combine(cfg, c, w, L, x, T, shared_records, y, ws, false, st);
   return cuda_status(e);
 }
 
@@ -348,7 +399,9 @@ k3moe_status layer_impl(const k3moe_config* cfg, const void* x, int64_t T, const
   auto evt = [&](int i) { return events ? static_cast<cudaEvent_t>(events[i]) : nullptr; };
   if (e == cudaSuccess) e = k3::launch_gateup(c, w, routed_records, shared_records, y, T, wgb, st, evt(2));
   if (e == cudaSuccess && events) e = cudaEventRecord(evt(3), st);
-  if (e == cudaSuccess) e = k3::launch_down(c, w, routed_records, shared_records, y, T, wgb, st, evt(4));
+  if (e == cudaSuccess) e = k3::launch_down(c, w, routed_records, shared_records, y, T, wgb, st, evt(4), c.Sb == 0);
+  if (e == cudaSuccess && c.Sb > 0)
+    e = shared_bf16_then_combine(cfg, c, w, L, x, T, shared_records, y, ws, router_tc(cfg, T), st);
   if (e == cudaSuccess && events) e = cudaEventRecord(evt(5), st);
   return cuda_status(e);
 }

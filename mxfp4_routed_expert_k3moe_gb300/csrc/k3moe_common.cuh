@@ -9,7 +9,9 @@ namespace k3 {
 
 // ----------------------------------------------------------------------------- configuration
 struct Cfg {
-  int d, f, E, k, S;  // d_model, d_ff, routed experts, top-k, shared experts
+  int d, f, E, k, S;  // d_model, d_ff, routed experts, top-k, MXFP4 shared experts (in the work groups)
+  int Sb;             // bf16 shared experts (computed apart, added by the combine); S = 0 then
+  int nsp1, nsp2;     // reduction parts of the bf16 shared experts' gate|up and down GEMMs
   int x_f32;          // 1 if x is fp32, 0 if bf16
   int wgt;            // max tokens per work group of the gate/up projection
   int wgt_dn;         // ... of the down projection (the permutation writes both lists)
@@ -59,6 +61,9 @@ struct Ws {
   uint8_t* hs;        // [P * hterms, f/32] their E8M0 block scales
   float* part;        // [P, d] down-projection outputs per position (the combine weights them)
   int* rtcnt;         // [T] router CTAs finished per token tile (tiles of 1 to 8 tokens)
+  float* sgu;         // [Sb][nsp1][T][2 f] bf16 shared experts: partial sums of gate | up
+  uint8_t* sh3;       // [Sb][3][T][f] bf16: their h in three bf16 parts
+  float* sho;         // [Sb][nsp2][T][d] partial sums of their outputs (added by the combine)
 };
 
 // ----------------------------------------------------------------------------- small helpers

@@ -46,13 +46,23 @@ cudaError_t launch_router_tc(const Cfg& c, const Ws& ws, const void* x, long lon
 // The three bf16 parts of n fp32 values (n a multiple of 4, both pointers 16-byte aligned).
 cudaError_t launch_split_router(const float* W, long long n, void* parts, cudaStream_t st);
 cudaError_t launch_residual_add(float* x, const float* y, long long n, cudaStream_t st);
+// bf16 shared experts (c.Sb of them, records c.sstride bytes apart): gate|up GEMM on the tokens (x, or
+// its three bf16 parts x3 for fp32 tokens), GLU into three bf16 parts of h, down GEMM; outputs in ws.sho.
+int shared_gemm_splits(long long T, int N, int K, int npairs);
+cudaError_t launch_shared_bf16(const Cfg& c, const Ws& ws, const void* x, long long T, const void* x3,
+                               const uint8_t* shared, cudaStream_t st);
+// The three bf16 parts of n fp32 values into `parts` ([3][n]), as the router does for fp32 tokens.
+cudaError_t launch_split_tokens(const float* x, long long n, void* parts, cudaStream_t st);
 
 // k3moe_tc.cu (tcgen05 expert FFN)
 // `mid` (optional) is recorded between the projection kernel and the GLU / combine kernel.
 cudaError_t launch_gateup(const Cfg& c, const Ws& ws, const uint8_t* routed, const uint8_t* shared, float* y,
                           long long T, long long wg_max, cudaStream_t st, cudaEvent_t mid = nullptr);
 cudaError_t launch_down(const Cfg& c, const Ws& ws, const uint8_t* routed, const uint8_t* shared, float* y,
-                        long long T, long long wg_max, cudaStream_t st, cudaEvent_t mid = nullptr);
+                        long long T, long long wg_max, cudaStream_t st, cudaEvent_t mid = nullptr,
+                        bool combine = true);
+// y = the gate-weighted routed outputs (slot order) + the shared experts' outputs.
+cudaError_t launch_combine(const Cfg& c, const Ws& ws, float* y, long long T, cudaStream_t st);
 
 // In-place conversion of the records' scale bytes between the stored and the device order.
 cudaError_t launch_pack_records(uint8_t* records, long long n_rec, long long stride, int d, int f, int to_device,

@@ -16,6 +16,11 @@
 // then read the accumulator (lane = token) and store the partial logits (the bias added to part 0).
 // With few tokens the reduction axis is cut into parts so that the grid fills the SMs; the router
 // kernel adds the parts, in part order, when it reads the logits. Every wait is bounded.
+//
+// The same kernel computes the bf16 shared experts' projections (the variant whose non-routed weights
+// are bf16): C[t, n] = sum over parts a of A_a[t, :] . B[n, :], with A the tokens (one bf16 part, or
+// three for fp32 tokens) or h in three bf16 parts, and B a bf16 weight matrix as stored (gate and up
+// stacked as [2 f, d], or down [d, f]); k_shared_glu forms h = SiLU(g) * u between the two.
 #include <cstdint>
 #include <mutex>
 
@@ -72,7 +77,8 @@ __device__ __forceinline__ bool rdrain(uint32_t bar, uint32_t parity) {
   return false;
 }
 
-// Pairs (token part, weight part) of the reduction, in order: bf16 tokens use the first three.
+// Pairs (token part, weight part) of the reduction, in order: bf16 tokens use the first three. With
+// pair_b0 set (the shared experts' GEMMs) pair a is (A part a, B part 0).
 __constant__ int kPairA[6] = {0, 0, 0, 1, 1, 2};
 __constant__ int kPairB[6] = {0, 1, 2, 0, 1, 0};
 
@@ -101,7 +107,7 @@ __global__ void __launch_bounds__(256) k_split_w(const float* W, long long n, __
 __global__ void __launch_bounds__(kRThreads, 1)
     k_router_mma(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
                  const float* bias, float* logits, long long T, int E, int d, int npairs, int nsplit, int* status,
-                 uint32_t wait_limit) {
+                 uint32_t wait_limit, int pair_b0) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   RCtl* ctl = reinterpret_cast<RCtl*>(smem + kRStages * (kRA + kRB));
@@ -143,8 +149,8 @@ __global__ void __launch_bounds__(kRThreads, 1)
         const int pair = ks / kpp, k0 = (ks - pair * kpp) * kRK;
         uint8_t* st = smem + (size_t)s * (kRA + kRB);
         mbar_expect_tx(su32(&ctl->full[s]), kRA + kRB);
-        tma_load_3d(su32(st), &map_x, k0, mt * kRM, kPairA[pair], su32(&ctl->full[s]));
-        tma_load_3d(su32(st + kRA), &map_w, k0, nt * kRN, kPairB[pair], su32(&ctl->full[s]));
+        tma_load_3d(su32(st), &map_x, k0, mt * kRM, pair_b0 ? pair : kPairA[pair], su32(&ctl->full[s]));
+        tma_load_3d(su32(st + kRA), &map_w, k0, nt * kRN, pair_b0 ? 0 : kPairB[pair], su32(&ctl->full[s]));
         if (++s == kRStages) s = 0;
       }
       // after a timeout, the last fill of every stage lands before the CTA frees its memory (earlier
@@ -228,6 +234,11 @@ cudaError_t encode_fn() {
 
 }  // namespace
 
+cudaError_t launch_split_tokens(const float* x, long long n, void* parts, cudaStream_t st) {
+  if (n % 4) return cudaErrorInvalidValue;
+  return launch_pdl(k_split_w, dim3(4 * 152), dim3(256), 0, st, x, n, static_cast<__nv_bfloat16*>(parts));
+}
+
 cudaError_t launch_split_router(const float* W, long long n, void* parts, cudaStream_t st) {
   if (n % 4) return cudaErrorInvalidValue;
   return launch_pdl(k_split_w, dim3(4 * 152), dim3(256), 0, st, W, n, static_cast<__nv_bfloat16*>(parts));
@@ -280,7 +291,114 @@ cudaError_t launch_router_tc(const Cfg& c, const Ws& ws, const void* x, long lon
   }
   dim3 grid((unsigned)((T + kRM - 1) / kRM), (unsigned)((c.E + kRN - 1) / kRN), (unsigned)c.rsplit);
   return launch_pdl(k_router_mma, grid, dim3(kRThreads), smem, st, mx, mw, bias, ws.logits, T, c.E, c.d,
-                    c.x_f32 ? 6 : 3, c.rsplit, ws.ctrl, c.wait_limit);
+                    c.x_f32 ? 6 : 3, c.rsplit, ws.ctrl, c.wait_limit, 0);
+}
+
+namespace {
+
+// 3D map over parts of a bf16 matrix [parts][rows][K] (row-major, parts part_stride bytes apart),
+// boxes of 64 elements x box_rows rows x 1 part, 128-byte swizzle.
+cudaError_t bf16_map(const void* base, long long K, long long rows, long long parts, long long part_stride,
+                     int box_rows, CUtensorMap* out) {
+  cudaError_t e = encode_fn();
+  if (e != cudaSuccess) return e;
+  cuuint64_t gdim[3] = {(cuuint64_t)K, (cuuint64_t)rows, (cuuint64_t)parts};
+  cuuint64_t gstr[2] = {(cuuint64_t)K * 2, (cuuint64_t)part_stride};
+  cuuint32_t box[3] = {kRK, (cuuint32_t)box_rows, 1}, es[3] = {1, 1, 1};
+  if (g_encode_r(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), gdim, gstr, box, es,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  return cudaSuccess;
+}
+
+// h = SiLU(g) * u from the gate|up partial sums gu[z][t][0 .. 2f) (parts added in order), written as
+// three bf16 parts h3[p][t][r] (each the rounding of what the earlier parts leave: 24 significant bits).
+__global__ void __launch_bounds__(256) k_shared_glu(const float* gu, int nsp, long long T, int f, int S,
+                                                    long long gu_stride, long long h3_stride, __nv_bfloat16* h3) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const long long n = (long long)S * T * f;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const long long s = i / (T * f), rem = i - s * T * f, t = rem / f;
+    const int r = (int)(rem - t * f);
+    const float* g0 = gu + s * gu_stride + t * 2 * f;
+    float g = 0.0f, u = 0.0f;
+    for (int z = 0; z < nsp; ++z) {
+      g += g0[(long long)z * T * 2 * f + r];
+      u += g0[(long long)z * T * 2 * f + f + r];
+    }
+    const float h = silu(g) * u;
+    const __nv_bfloat16 p0 = __float2bfloat16_rn(h);
+    const float r1 = h - __bfloat162float(p0);
+    const __nv_bfloat16 p1 = __float2bfloat16_rn(r1);
+    const __nv_bfloat16 p2 = __float2bfloat16_rn(r1 - __bfloat162float(p1));
+    __nv_bfloat16* hp = h3 + s * h3_stride + t * f + r;
+    hp[0] = p0;
+    hp[T * f] = p1;
+    hp[2 * T * f] = p2;
+  }
+}
+
+cudaError_t launch_bf16_gemm(const CUtensorMap& ma, const CUtensorMap& mb, float* out, long long T, int N, int K,
+                             int npairs, int nsplit, int* status, uint32_t wait_limit, cudaStream_t st) {
+  static bool attr = false;
+  const size_t smem = (size_t)kRStages * (kRA + kRB) + sizeof(RCtl) + 1024;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(k_router_mma, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  dim3 grid((unsigned)((T + kRM - 1) / kRM), (unsigned)((N + kRN - 1) / kRN), (unsigned)nsplit);
+  return launch_pdl(k_router_mma, grid, dim3(kRThreads), smem, st, ma, mb, (const float*)nullptr, out, T, N, K, npairs,
+                    nsplit, status, wait_limit, 1);
+}
+
+}  // namespace
+
+// Reduction parts of a shared-expert GEMM over T tokens: enough (128 x 256) tiles x parts to fill the
+// SMs, each part at least 16 of the 64-wide k-steps.
+int shared_gemm_splits(long long T, int N, int K, int npairs) {
+  const long long tiles = ((T + kRM - 1) / kRM) * ((N + kRN - 1) / kRN);
+  const long long nk = (long long)npairs * (K / kRK);
+  long long p = 152 / tiles;
+  if (p > nk / 16) p = nk / 16;
+  return (int)(p < 1 ? 1 : p);
+}
+
+cudaError_t launch_shared_bf16(const Cfg& c, const Ws& ws, const void* x, long long T, const void* x3,
+                               const uint8_t* shared, cudaStream_t st) {
+  if (c.Sb <= 0) return cudaSuccess;
+  const int d = c.d, f = c.f;
+  const int xparts = c.x_f32 ? 3 : 1;
+  const int nsp1 = shared_gemm_splits(T, 2 * f, d, xparts), nsp2 = shared_gemm_splits(T, d, f, 3);
+  if (nsp1 != c.nsp1 || nsp2 != c.nsp2) return cudaErrorInvalidValue;  // (the workspace was laid out for these)
+  CUtensorMap mx;
+  cudaError_t e = bf16_map(c.x_f32 ? x3 : x, d, T, xparts, T * d * 2, kRM, &mx);
+  if (e != cudaSuccess) return e;
+  const long long gu_stride = (long long)nsp1 * T * 2 * f, h3_stride = 3LL * T * f, o_stride = (long long)nsp2 * T * d;
+  for (int s = 0; s < c.Sb; ++s) {
+    CUtensorMap mw;
+    const uint8_t* rec = shared + (long long)s * c.sstride;
+    if ((e = bf16_map(rec, d, 2 * f, 1, 2LL * f * d * 2, kRN, &mw)) != cudaSuccess) return e;
+    if ((e = launch_bf16_gemm(mx, mw, ws.sgu + s * gu_stride, T, 2 * f, d, xparts, nsp1, ws.ctrl, c.wait_limit, st)) !=
+        cudaSuccess)
+      return e;
+  }
+  long long blocks = ((long long)c.Sb * T * f + 255) / 256;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  e = launch_pdl(k_shared_glu, dim3((unsigned)blocks), dim3(256), 0, st, (const float*)ws.sgu, nsp1, T, f, c.Sb,
+                 gu_stride, h3_stride, reinterpret_cast<__nv_bfloat16*>(ws.sh3));
+  if (e != cudaSuccess) return e;
+  for (int s = 0; s < c.Sb; ++s) {
+    CUtensorMap mh, md;
+    const uint8_t* rec = shared + (long long)s * c.sstride;
+    if ((e = bf16_map(ws.sh3 + s * h3_stride * 2, f, T, 3, T * f * 2, kRM, &mh)) != cudaSuccess) return e;
+    if ((e = bf16_map(rec + 4LL * f * d, f, d, 1, (long long)d * f * 2, kRN, &md)) != cudaSuccess) return e;
+    if ((e = launch_bf16_gemm(mh, md, ws.sho + s * o_stride, T, d, f, 3, nsp2, ws.ctrl, c.wait_limit, st)) != cudaSuccess)
+      return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace k3

@@ -655,6 +655,8 @@ __global__ void __launch_bounds__(256) k_combine(Cfg c, Ws ws, float* y, long lo
         if (p >= 0) s += ws.perm_w[p] * ws.part[(long long)p * c.d + row];
       }
       for (int sh = 0; sh < c.S; ++sh) s += ws.part[(P_R + (long long)sh * T + tok) * c.d + row];
+      for (int sb = 0; sb < c.Sb; ++sb)
+        for (int z = 0; z < c.nsp2; ++z) s += ws.sho[((long long)(sb * c.nsp2 + z) * T + tok) * c.d + row];
       y[idx] = s;
       continue;
     }
@@ -681,6 +683,8 @@ __global__ void __launch_bounds__(256) k_combine(Cfg c, Ws ws, float* y, long lo
 #pragma unroll
     for (int sh = 0; sh < kCombMaxS; ++sh)
       if (sh < c.S) s += so[sh];
+    for (int sb = 0; sb < c.Sb; ++sb)
+      for (int z = 0; z < c.nsp2; ++z) s += __ldcg(&ws.sho[((long long)(sb * c.nsp2 + z) * T + tok) * c.d + row]);
     y[idx] = s;
   }
 }
@@ -959,7 +963,7 @@ cudaError_t launch_gateup(const Cfg& c, const Ws& ws, const uint8_t* routed, con
 }
 
 cudaError_t launch_down(const Cfg& c, const Ws& ws, const uint8_t* routed, const uint8_t* shared, float* y,
-                        long long T, long long wg_max, cudaStream_t st, cudaEvent_t mid) {
+                        long long T, long long wg_max, cudaStream_t st, cudaEvent_t mid, bool combine) {
   TcArgs a = base_args(c, ws, routed, shared, y, T);
   a.terms = c.hterms;
   a.n_tile = round16(c.wgt_dn * c.hterms);
@@ -973,7 +977,17 @@ cudaError_t launch_down(const Cfg& c, const Ws& ws, const uint8_t* routed, const
   if (e != cudaSuccess) return e;
   e = launch_tc<DOWN>(a, m.dr, m.dr, m.ds, m.ds, wg_max * (c.d / 128), st);
   if (e == cudaSuccess && mid) e = cudaEventRecord(mid, st);
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess || !combine) return e;
+  return launch_combine(c, ws, y, T, st);
+}
+
+cudaError_t launch_combine(const Cfg& c, const Ws& ws, float* y, long long T, cudaStream_t st) {
+  if (g_sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (g_sms <= 0) g_sms = 1;
+  }
   long long blocks = (T * c.d + 255) / 256;
   if (blocks > 8LL * g_sms) blocks = 8LL * g_sms;
   if (T <= kCombBatchMaxT) return launch_pdl(k_combine<true>, dim3((unsigned)blocks), dim3(256), 0, st, c, ws, y, T);

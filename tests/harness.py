@@ -51,10 +51,12 @@ class DeviceLayer:
     order unless pack=False) plus the host copies (stored order) the oracle needs."""
 
     def __init__(self, shape: synth.LayerShape, seed: int, layer: int = 0, zipf_s: float | None = None,
-                 x_dtype: str = "bf16", stride: int | None = None, pack: bool = True, score: str = "softmax"):
+                 x_dtype: str = "bf16", stride: int | None = None, pack: bool = True, score: str = "softmax",
+                 shared_format: str = "mxfp4"):
         import torch
         import mxfp4_routed_expert_k3moe_gb300 as k3
         self.shape, self.seed, self.layer, self.x_dtype, self.score = shape, seed, layer, x_dtype, score
+        self.shared_format = shared_format
         self.stride = stride or shape.record_stride
         E, S = shape.n_routed, shape.n_shared
         self.W_host = synth.router_weights(shape, seed, layer)
@@ -66,17 +68,36 @@ class DeviceLayer:
         self.shared = torch.empty(max(1, S) * self.stride, dtype=torch.uint8, device=dev)
         st = torch.cuda.current_stream().cuda_stream
         synth.records_device(shape, seed, layer, 0, E, self.routed.data_ptr(), self.stride, st)
-        if S:
+        self.sstride = 0
+        if S and shared_format == "bf16":  # bf16 shared records, drawn on the host, used as stored
+            self.sstride = synth.shared_bf16_stride(shape)
+            self.set_shared_bf16(synth.shared_records_bf16(shape, seed, layer, S, self.sstride))
+        elif S:
             synth.records_device(shape, seed, layer, E, S, self.shared.data_ptr(), self.stride, st)
         self.cfg = k3.Config.make(shape.d_model, shape.d_ff, E, shape.top_k, S,
                                   x_dtype=k3.X_BF16 if x_dtype == "bf16" else k3.X_F32, record_stride=self.stride,
                                   score_func=k3.SCORE_SOFTMAX if score == "softmax" else k3.SCORE_SIGMOID_BIAS,
-                                  record_order=k3.ORDER_DEVICE if pack else k3.ORDER_STORED)
+                                  record_order=k3.ORDER_DEVICE if pack else k3.ORDER_STORED,
+                                  shared_format=k3.SHARED_BF16 if shared_format == "bf16" else k3.SHARED_MXFP4,
+                                  shared_stride=self.sstride)
         if pack:
             k3.pack_records(self.cfg, self.routed, E)
-            if S:
+            if S and shared_format == "mxfp4":
                 k3.pack_records(self.cfg, self.shared, S)
         self._host_records = {}
+
+    def set_shared_bf16(self, recs: np.ndarray):
+        """bf16 shared records (uint16 [S, sstride / 2]) on the device and for the oracle."""
+        import torch
+        self.shared_bf16_host = np.ascontiguousarray(recs, dtype=np.uint16)
+        self.shared = torch.from_numpy(self.shared_bf16_host.view(np.uint8).reshape(-1).copy()).cuda()
+
+    def shared_host(self):
+        """The shared records the oracle takes (MXFP4 records, or bf16 ones)."""
+        sh = self.shape
+        if self.shared_format == "bf16":
+            return [r for r in self.shared_bf16_host]
+        return list(self.host_records([sh.n_routed + s for s in range(sh.n_shared)]).values())
 
     def host_records(self, experts):
         need = [e for e in experts if e not in self._host_records]
@@ -105,9 +126,8 @@ class DeviceLayer:
             _, idx, _ = oracle.route_token(xf[t], self.W_host, sh.top_k, self.bias_host, score=self.score)
             experts.update(int(e) for e in idx)
         routed = self.host_records(sorted(experts))
-        shared = list(self.host_records([sh.n_routed + s for s in range(sh.n_shared)]).values())
-        return oracle.layer(x, self.x_dtype, self.W_host, self.bias_host, routed, shared, sh.d_model, sh.d_ff,
-                            sh.top_k, score=self.score)
+        return oracle.layer(x, self.x_dtype, self.W_host, self.bias_host, routed, self.shared_host(), sh.d_model,
+                            sh.d_ff, sh.top_k, score=self.score, shared_format=self.shared_format)
 
     def oracle_route(self, xh: np.ndarray):
         """Oracle routing of every token (logits[T, E], idx[T, k], w[T, k]), tokens in parallel."""
@@ -128,13 +148,14 @@ class DeviceLayer:
         sh = self.shape
         xf = synth.tokens_as_f64(xh, self.x_dtype)
         recs = self.host_records(sorted(set(int(e) for e in np.unique(idx))))
-        shared = list(self.host_records([sh.n_routed + s for s in range(sh.n_shared)]).values())
+        shared = self.shared_host()
+        run_shared = oracle.expert_token_bf16 if self.shared_format == "bf16" else oracle.expert_token
         y = np.zeros((xh.shape[0], sh.d_model))
         for t in range(xh.shape[0]):
             for e, g in zip(idx[t], w[t]):
                 y[t] += float(g) * oracle.expert_token(recs[int(e)], xf[t], sh.d_model, sh.d_ff)[0]
             for r in shared:
-                y[t] += oracle.expert_token(r, xf[t], sh.d_model, sh.d_ff)[0]
+                y[t] += run_shared(r, xf[t], sh.d_model, sh.d_ff)[0]
         return y
 
 

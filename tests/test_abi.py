@@ -71,7 +71,6 @@ def test_workspace_never_shrinks_as_tokens_grow(x_dtype):
     ("record_order", 7, k3.ERR_INVALID_ARGUMENT),
     ("shared_format", 7, k3.ERR_INVALID_ARGUMENT),
     ("act_mode", k3.ACT_MXFP4, k3.ERR_UNSUPPORTED),
-    ("shared_format", k3.SHARED_BF16, k3.ERR_UNSUPPORTED),
     ("record_order", k3.ORDER_STORED, k3.ERR_UNSUPPORTED),        # records never packed are refused
 ])
 def test_invalid_config_rejected_on_host(field, value, code):
@@ -118,6 +117,22 @@ def test_invalid_pointers_rejected_on_host():
     assert lib.k3moe_residual_rmsnorm(a, None, 1, 7166, 1e-6, a, None) == 1   # d not a multiple of 4
     assert lib.k3moe_residual_rmsnorm(a, mis, 1, 7168, 1e-6, a, None) == 1
     assert lib.k3moe_residual_rmsnorm(a, None, 0, 7168, 1e-6, a, None) == k3.OK
+
+
+def test_bf16_shared_config():
+    """bf16 shared records: the default stride is the bf16 record rounded to 4 KiB; a smaller one is
+    rejected; the workspace holds the shared GEMMs' partial sums and h (and grows with T)."""
+    lib = k3.load()
+    a = ctypes.c_void_p(1 << 20)
+    cfg = k3.Config.make(**K3CFG, shared_format=k3.SHARED_BF16)
+    assert lib.k3moe_layer(ctypes.byref(cfg), a, 0, a, None, None, a, a, a, None, None, a, 0, None) == k3.OK
+    assert k3.workspace_bytes(cfg, 1) > k3.workspace_bytes(k3.Config.make(**K3CFG), 1)
+    sizes = [k3.workspace_bytes(cfg, T) for T in (1, 2, 15, 16, 127, 128, 129, 1000, 4096)]
+    assert all(b >= a_ for a_, b in zip(sizes, sizes[1:]))
+    cfg.shared_stride = 6 * 7168 * 1536 - 4096
+    assert lib.k3moe_layer(ctypes.byref(cfg), a, 0, a, None, None, a, a, a, None, None, a, 0, None) == 1
+    cfg.shared_stride = (6 * 7168 * 1536 + 4095) // 4096 * 4096
+    assert lib.k3moe_layer(ctypes.byref(cfg), a, 0, a, None, None, a, a, a, None, None, a, 0, None) == k3.OK
 
 
 def test_router_parts_bytes():
