@@ -638,8 +638,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 // faster per layer at one token, but its registers halve the occupancy, which made it slower from
 // 64 tokens on (4096 tokens: 0.33 ms).
 constexpr int kCombMaxK = 32, kCombMaxS = 8;  // top_k <= 32, n_shared <= 8 (checked by the API)
+// SB: the shared experts are bf16 ones, whose outputs come as partial sums in ws.sho (its own instance,
+// so that the MXFP4 path keeps its registers and occupancy).
 constexpr long long kCombBatchMaxT = 2;
-template <bool BATCH>
+template <bool BATCH, bool SB>
 __global__ void __launch_bounds__(256) k_combine(Cfg c, Ws ws, float* y, long long T) {
   pdl_wait();
   pdl_launch_dependents();
@@ -655,8 +657,9 @@ __global__ void __launch_bounds__(256) k_combine(Cfg c, Ws ws, float* y, long lo
         if (p >= 0) s += ws.perm_w[p] * ws.part[(long long)p * c.d + row];
       }
       for (int sh = 0; sh < c.S; ++sh) s += ws.part[(P_R + (long long)sh * T + tok) * c.d + row];
-      for (int sb = 0; sb < c.Sb; ++sb)
-        for (int z = 0; z < c.nsp2; ++z) s += ws.sho[((long long)(sb * c.nsp2 + z) * T + tok) * c.d + row];
+      if (SB)
+        for (int sb = 0; sb < c.Sb; ++sb)
+          for (int z = 0; z < c.nsp2; ++z) s += ws.sho[((long long)(sb * c.nsp2 + z) * T + tok) * c.d + row];
       y[idx] = s;
       continue;
     }
@@ -683,8 +686,9 @@ __global__ void __launch_bounds__(256) k_combine(Cfg c, Ws ws, float* y, long lo
 #pragma unroll
     for (int sh = 0; sh < kCombMaxS; ++sh)
       if (sh < c.S) s += so[sh];
-    for (int sb = 0; sb < c.Sb; ++sb)
-      for (int z = 0; z < c.nsp2; ++z) s += __ldcg(&ws.sho[((long long)(sb * c.nsp2 + z) * T + tok) * c.d + row]);
+    if (SB)
+      for (int sb = 0; sb < c.Sb; ++sb)
+        for (int z = 0; z < c.nsp2; ++z) s += __ldcg(&ws.sho[((long long)(sb * c.nsp2 + z) * T + tok) * c.d + row]);
     y[idx] = s;
   }
 }
@@ -990,8 +994,9 @@ cudaError_t launch_combine(const Cfg& c, const Ws& ws, float* y, long long T, cu
   }
   long long blocks = (T * c.d + 255) / 256;
   if (blocks > 8LL * g_sms) blocks = 8LL * g_sms;
-  if (T <= kCombBatchMaxT) return launch_pdl(k_combine<true>, dim3((unsigned)blocks), dim3(256), 0, st, c, ws, y, T);
-  return launch_pdl(k_combine<false>, dim3((unsigned)blocks), dim3(256), 0, st, c, ws, y, T);
+  if (c.Sb > 0) return launch_pdl(k_combine<false, true>, dim3((unsigned)blocks), dim3(256), 0, st, c, ws, y, T);
+  if (T <= kCombBatchMaxT) return launch_pdl(k_combine<true, false>, dim3((unsigned)blocks), dim3(256), 0, st, c, ws, y, T);
+  return launch_pdl(k_combine<false, false>, dim3((unsigned)blocks), dim3(256), 0, st, c, ws, y, T);
 }
 
 cudaError_t launch_pack_records(uint8_t* records, long long n_rec, long long stride, int d, int f, int to_device,
