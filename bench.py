@@ -52,11 +52,16 @@ METRIC = "MoE-layer tokens/s (K3 shape, one layer) and fraction of HBM roofline"
 
 # Counters from ncu captures of the projection kernels, per launch, keyed by (kernel, workload); valid
 # only while the kernel sources hash to the recorded value (the summaries under profiles/ give the
-# commands): dram__bytes_read.sum + dram__bytes_write.sum, and sm__pipe_tensor_cycles_active as a
-# fraction of elapsed cycles.
+# commands): dram__bytes_read.sum + dram__bytes_write.sum of a decode launch (the capture used 128
+# routed experts: a launch reads the same 16 + 2 records as at 896), and the tensor pipe's active
+# fraction (sm__pipe_tensor_cycles_active, of elapsed) at the prefill proxy of 512 tokens x 128 experts.
 NCU_COUNTERS = {
-    ("k_tc<gate/up>", "decode_b1"): {"traffic": 213776128, "hash": "220f8b4c3ca7401f"},
-    ("k_tc<down>", "decode_b1"): {"traffic": 107876352, "hash": "220f8b4c3ca7401f"},
+    ("k_tc<gate/up>", "decode_b1"): {"traffic": 213567744, "hash": "7852fd56c8a9b982"},
+    ("k_tc<down>", "decode_b1"): {"traffic": 107773696, "hash": "7852fd56c8a9b982"},
+    ("k_tc<gate/up>", "prefill_4096"): {"tensor_active": 0.1707, "hash": "7852fd56c8a9b982",
+                                        "case": "ncu at 512 tokens x 128 experts (64 tokens per expert)"},
+    ("k_tc<down>", "prefill_4096"): {"tensor_active": 0.1303, "hash": "7852fd56c8a9b982",
+                                     "case": "ncu at 512 tokens x 128 experts (64 tokens per expert)"},
 }
 
 
@@ -242,17 +247,24 @@ class LayerWeights:
         k3.prepare_router(cfg, self.W, self.parts)
 
 
-def timed(step, steps, world, local_rank):
+def timed(step, steps, world, local_rank, warmup=0, check=None):
     """Device time of exactly `steps` calls of step(i), bracketed by a barrier and synchronize on both
-    sides (CUDA events on the launching stream), with nvidia-smi clocks sampled meanwhile."""
+    sides (CUDA events on the launching stream), with nvidia-smi clocks sampled meanwhile. The sampler
+    starts first; the `warmup` untimed calls run right before the timed ones (then `check()`), so that
+    the timed region does not start from an idle GPU."""
     import torch
     st = torch.cuda.current_stream()
     clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if check:
+        check()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    clocks.start()
-    time.sleep(0.3)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(st)
     for i in range(steps):
@@ -291,12 +303,11 @@ def run_layer_workload(args, k3, name, T, seed, zipf_s, n_sets, steps, warmup, w
         L = layers[i % len(layers)]
         k3.layer(cfg, xs[i % nb], T, L.W, L.bias, L.routed, L.shared, y, ws, w_parts=L.parts)
 
-    for i in range(warmup):
-        step(i)
-    torch.cuda.synchronize()
-    if k3.check_device_status(ws) != k3.OK:
-        raise RuntimeError(f"{name}: device status check failed after warm-up")
-    elapsed_ms, clk = timed(step, steps, world, local_rank)
+    def check_warm():
+        if k3.check_device_status(ws) != k3.OK:
+            raise RuntimeError(f"{name}: device status check failed after warm-up")
+
+    elapsed_ms, clk = timed(step, steps, world, local_rank, warmup=warmup, check=check_warm)
     if k3.check_device_status(ws) != k3.OK:
         raise RuntimeError(f"{name}: device status check failed in the timed region")
 
@@ -342,6 +353,8 @@ def run_layer_workload(args, k3, name, T, seed, zipf_s, n_sets, steps, warmup, w
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
     cnt = NCU_COUNTERS.get((dom, name))
     valid = cnt is not None and cnt["hash"] == kernel_hash() and T == WORKLOADS[name][0] and E == 896
+    if valid and "traffic" not in cnt:
+        cnt = {**cnt, "traffic": None}
     ms_per_step = elapsed_ms / steps
     out = {
         "value": world * T * steps / (elapsed_ms * 1e-3), "unit": "tokens/s", "steps": steps, "warmup": warmup,
@@ -372,7 +385,7 @@ def run_layer_workload(args, k3, name, T, seed, zipf_s, n_sets, steps, warmup, w
               "dominant_kernel_fp4_frac_nominal": dom_flops / (dom_ms * 1e-3) / 1e12 / NOMINAL_FP4_TFLOPS,
               "peak_kind": f"nominal dense FP4 {NOMINAL_FP4_TFLOPS:.0f} TFLOP/s"}
         if valid and "tensor_active" in cnt:
-            tc["tensor_pipe_active_ncu"] = cnt["tensor_active"]
+            tc["tensor_pipe_active_ncu"] = {"value": cnt["tensor_active"], "kernel": dom, "case": cnt["case"]}
         out["tensor"] = tc
     if not args.no_e2e:
         out["e2e"] = e2e(k3, cfg, layers, xs_host, T, d, dev, steps, warmup)
@@ -455,11 +468,7 @@ def run_stack(args, k3, world, local_rank):
         out = {}
         for label, fn in (("fused", fused), ("separate", separate)):
             x.copy_(x0)
-            for _ in range(3):
-                fn()
-            torch.cuda.synchronize()
-            x.copy_(x0)
-            ms, clk = timed(lambda i: fn(), steps, world, local_rank)
+            ms, clk = timed(lambda i: fn(), steps, world, local_rank, warmup=3)
             out[label] = {"layer_tokens_per_s": 4 * T * steps / (ms * 1e-3) * world, "ms_per_step": ms / steps,
                           "steps": steps, "clocks": clk}
         x.copy_(x0)
