@@ -22,7 +22,8 @@
 // CTA layout (one CTA per SM, persistent over work items, 384 threads):
 //   warps 0-3   epilogue: accumulators (double-buffered in tensor memory) -> per-position sums
 //   warps 4-7   loaders: the tensor copy of the weight tile (one lane) and cp.async of the B rows and
-//               of the scale words, each loader for its own ring slots. On this part one thread
+//               of the scale words, each loader for its own ring slots (the down projection's E4M3
+//               terms of h, contiguous per work group, come by a second tensor copy). On this part one thread
 //               issues about one tensor copy per ~500 SM cycles, so a single issuing thread caps the
 //               weight stream near 3 TB/s; four reach the DRAM rate.
 //   warps 8-11  MMA issuers (one lane each): tcgen05.cp of the scale words into tensor memory, then
@@ -176,6 +177,8 @@ struct TcArgs {
   int parts;    // reduction parts per row tile (1: whole items)
   FastDiv div_parts, div_mtiles;
   int stages;   // pipeline depth (<= kMaxStages)
+  int tma_b;    // (down) the B rows of a work group, contiguous positions x terms, come by one tensor copy
+                // per chunk (map_r1 holds the map of the h terms) instead of cp.async row copies
   int stage_bytes;  // ch x (A tile + B tile + scale words)
 };
 
@@ -387,11 +390,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           // weight codes (tensor copy) and the chunks' A scale groups (one bulk copy each: the
           // groups of a chunk are contiguous in the device order) complete on the same barrier
-          mbar_expect_tx(su32(&ctl->full[s]), (tx_chunk + 512 * wpc) * CH);
+          mbar_expect_tx(su32(&ctl->full[s]), (tx_chunk + 512 * wpc + (uint32_t)(a.tma_b ? a.n_tile * 128 : 0)) * CH);
           tma_load_4d(su32(st), map, 0, it.mt * 128, j, ecoord, su32(&ctl->full[s]), pol);
           for (int cc = 0; cc < CH; ++cc)
             bulk_load(su32(st + sf_off + cc * a.sf_bytes), atile + (size_t)512 * wpc * (j + cc), 512 * wpc,
                       su32(&ctl->full[s]), pol);
+          if (MODE == DOWN && a.tma_b)  // the work group's B rows: n_tile rows from position pos0 on
+            for (int cc = 0; cc < CH; ++cc)
+              tma_load_2d(su32(st + b_off + cc * a.b_bytes), &map_r1, (j + cc) * 128, it.wg.pos0 * a.terms,
+                          su32(&ctl->full[s]));
         }
         for (int cc = 0; cc < CH; ++cc) {
           const int jj = j + cc;
@@ -401,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // reads four 128-byte rows (one row per lane read 32 rows: a quarter of the L1 rate)
           // (four rows per lane at a time: their table reads are issued before the copies)
           const int k16 = lane & 7;
-          for (int n0 = lane >> 3; n0 < nrows; n0 += 16) {
+          for (int n0 = lane >> 3; n0 < nrows && !(MODE == DOWN && a.tma_b); n0 += 16) {
             uint32_t r[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) r[u] = n0 + 4 * u < nrows ? rtab[n0 + 4 * u] : ~0u;
@@ -979,7 +986,23 @@ cudaError_t launch_down(const Cfg& c, const Ws& ws, const uint8_t* routed, const
   TcMaps m;
   cudaError_t e = setup(c, routed, shared, 0, a.ch, m, a.shared);
   if (e != cudaSuccess) return e;
-  e = launch_tc<DOWN>(a, m.dr, m.dr, m.ds, m.ds, wg_max * (c.d / 128), st);
+  // E4M3 form: the h terms of a work group's positions are rows pos0 * 3 .. of h, contiguous: one tensor
+  // copy of n_tile rows x 128 bytes per chunk (rows past the group's are loaded too; their MMA columns
+  // are not read)
+  CUtensorMap mh = m.dr;
+  if (!c.fp4) {
+    if ((e = get_encode()) != cudaSuccess) return e;
+    const long long P = T * (c.k + c.S);
+    cuuint64_t gdim[2] = {(cuuint64_t)c.f, (cuuint64_t)(P * c.hterms)};
+    cuuint64_t gstr[1] = {(cuuint64_t)c.f};
+    cuuint32_t box[2] = {128, (cuuint32_t)a.n_tile}, es[2] = {1, 1};
+    if (g_encode(&mh, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, ws.hq, gdim, gstr, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+        CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+    a.tma_b = 1;
+  }
+  e = launch_tc<DOWN>(a, m.dr, mh, m.ds, m.ds, wg_max * (c.d / 128), st);
   if (e == cudaSuccess && mid) e = cudaEventRecord(mid, st);
   if (e != cudaSuccess || !combine) return e;
   return launch_combine(c, ws, y, T, st);
