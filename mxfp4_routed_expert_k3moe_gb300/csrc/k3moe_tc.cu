@@ -261,9 +261,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + (size_t)S * a.stage_bytes);
   const Cfg& c = a.c;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  pdl_wait();  // the routing (or the gate/up results) come from the previous kernel
+  if (tid == 0) {  // the maps' descriptors, fetched while the previous kernel finishes
+    prefetch_tmap(&map_r0);
+    prefetch_tmap(&map_r1);
+    prefetch_tmap(&map_s0);
+    prefetch_tmap(&map_s1);
+  }
+  // The gate/up kernel reads the routing, which the previous kernel writes. The down kernel's work
+  // groups come from the routing kernel two launches back: it completed before the gate/up kernel
+  // (this kernel's predecessor) passed its own grid-dependency wait, hence before this grid was
+  // launched. So the down kernel reads its work groups, and its loaders request the weight tiles of
+  // the first ring round, before the wait; only the activation rows (h) and everything the epilogue
+  // writes come after it.
+  if (MODE == GATEUP) pdl_wait();
   pdl_launch_dependents();
-  const int n_wg = a.ws.ctrl[MODE == GATEUP ? CTRL_NWG : CTRL_NWG_DN];
+  const int n_wg = __ldcg(&a.ws.ctrl[MODE == GATEUP ? CTRL_NWG : CTRL_NWG_DN]);
   const WorkGroup* wgs = MODE == GATEUP ? a.ws.wgs : a.ws.wgs_dn;
   const int nmat = MODE == GATEUP ? 2 : 1;
   const int mtiles = (MODE == GATEUP ? c.f : c.d) / 128;
@@ -273,7 +285,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tx_chunk = a.fp4 ? 128 * 128 : 128 * 64;  // bytes a chunk's tensor copy delivers
   const int wpc = a.fp4 ? 2 : 1;                            // scale words per row per chunk
 
-  if (n_wg == 0) return;  // nothing routed and no shared experts (k_combine writes y = 0)
+  if (n_wg == 0) {  // nothing routed and no shared experts (k_combine writes y = 0)
+    if (MODE == DOWN) pdl_wait();
+    return;
+  }
 
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&ctl->tmem)),
@@ -297,8 +312,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem;
+  const bool loader = warp >= kWarpLoad && warp < kWarpIss;
+  if (MODE == DOWN && !loader) pdl_wait();
 
-  if (warp >= kWarpLoad && warp < kWarpIss) {
+  if (loader) {
     // ------------------------------------------------------------ loaders (one per slot class)
     // Work groups (kEpRing items ahead) and the tokens of their positions (two items ahead) arrive by
     // cp.async into this loader's ring, so that no load stalls the loader between items (with the
@@ -321,16 +338,53 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane < g.ntok && lane < 32) cp4(su32(&ctl->ld_tok[lv][slot][lane]), &a.ws.perm_tok[g.pos0 + lane], 4);
       }
     };
+    // Weight codes (tensor copy) and the chunks' A scale groups (one bulk copy each: the groups of a
+    // chunk are contiguous in the device order) of chunks j.. of item `it` into stage s, on the
+    // stage's full barrier with one arrival.
+    auto issue_a = [&](const Item& ia, int j, int s) {
+      const bool routed = ia.wg.expert < c.E;
+      const CUtensorMap* map = routed ? (ia.mat == 0 ? &map_r0 : &map_r1) : (ia.mat == 0 ? &map_s0 : &map_s1);
+      const int ecoord = routed ? ia.wg.expert : ia.wg.expert - c.E;
+      const uint8_t* atile = scale_tile<MODE>(a, ia);
+      uint8_t* st = smem + (size_t)s * a.stage_bytes;
+      mbar_expect_tx(su32(&ctl->full[s]), (tx_chunk + 512 * wpc) * CH);
+      tma_load_4d(su32(st), map, 0, ia.mt * 128, j, ecoord, su32(&ctl->full[s]), pol);
+      for (int cc = 0; cc < CH; ++cc)
+        bulk_load(su32(st + sf_off + cc * a.sf_bytes), atile + (size_t)512 * wpc * (j + cc), 512 * wpc,
+                  su32(&ctl->full[s]), pol);
+    };
     // prologue: work groups of the first kEpRing items and tokens of the first two, waited for here
     for (int r = 0; r < kEpRing; ++r) fetch_wg(blockIdx.x + (long long)r * gridDim.x, r);
-    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    // Meanwhile the weight tiles of the first ring round (its stages need no empty wait) are requested
+    // as soon as their items' work groups are read; the loop below adds their activation rows and
+    // scale words. `pre`: global stages of this CTA whose weight tiles are requested here.
+    long long pre = 0;
+    uint32_t pre_mask = 0;  // this loader's stages among them (bit s)
+    if (lane == 0) {
+      for (long long ii = blockIdx.x; pre < S && ii < n_items; ii += gridDim.x) {
+        Item pi;
+        item_geom<MODE>(a, ii, n_items, pi);
+        const int4 wv = __ldcg(reinterpret_cast<const int4*>(&wgs[pi.wgi]));
+        pi.wg = WorkGroup{wv.x, wv.y, wv.z, wv.w};
+        for (int j = pi.j0; j < pi.j1 && pre < S; j += CH, ++pre)
+          if ((int)pre % kLoaders == lv) {
+            issue_a(pi, j, (int)pre);
+            pre_mask |= 1u << pre;
+          }
+      }
+    }
+    pre = __shfl_sync(0xffffffffu, pre, 0);
+    pre_mask = __shfl_sync(0xffffffffu, pre_mask, 0);
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
     __syncwarp();
+    if (MODE == DOWN) pdl_wait();
     fetch_tok(blockIdx.x, 0);
     fetch_tok(blockIdx.x + (long long)gridDim.x, 1);
     asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
     __syncwarp();
     Item it;
-    long long kk = 0;
+    long long kk = 0, gst = 0;  // items, global stages of this CTA
     uint32_t issued = 0;  // bit s: this loader filled slot s at least once; its last round's parity is bit s of `par`
     uint32_t par = 0;
     for (long long ii = blockIdx.x; ok && item_geom<MODE>(a, ii, n_items, it); ii += gridDim.x, ++kk) {
@@ -353,10 +407,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       fetch_wg(ii + (long long)kEpRing * gridDim.x, slot);
       fetch_tok(ii + 2LL * gridDim.x, (int)((kk + 2) % kEpRing));
       asm volatile("cp.async.commit_group;" ::: "memory");
-      const bool routed = it.wg.expert < c.E;
-      const CUtensorMap* map = routed ? (it.mat == 0 ? &map_r0 : &map_r1) : (it.mat == 0 ? &map_s0 : &map_s1);
-      const int ecoord = routed ? it.wg.expert : it.wg.expert - c.E;
-      const uint8_t* atile = scale_tile<MODE>(a, it);
       // B row n of the tile = activation row (token or position) * terms + term; the rows' indices go
       // to this loader's table, which the code copies below read, and the scale pointers of rows
       // lane + 32 q stay in registers
@@ -380,6 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       for (int j = it.j0; j < it.j1; j += CH, rg.next(S)) {
         const int s = rg.s;
+        const long long g = gst++;
         if (s % kLoaders != lv) continue;
         if (rg.wrapped)
           ok = __all_sync(0xffffffffu, wait_bar(su32(&ctl->empty[s]), rg.ph ^ 1u, ctl, status, c.wait_limit));
@@ -388,17 +439,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         par = (par & ~(1u << s)) | (rg.ph << s);
         uint8_t* st = smem + (size_t)s * a.stage_bytes;
         if (lane == 0) {
-          // weight codes (tensor copy) and the chunks' A scale groups (one bulk copy each: the
-          // groups of a chunk are contiguous in the device order) complete on the same barrier
-          mbar_expect_tx(su32(&ctl->full[s]), (tx_chunk + 512 * wpc + (uint32_t)(a.tma_b ? a.n_tile * 128 : 0)) * CH);
-          tma_load_4d(su32(st), map, 0, it.mt * 128, j, ecoord, su32(&ctl->full[s]), pol);
-          for (int cc = 0; cc < CH; ++cc)
-            bulk_load(su32(st + sf_off + cc * a.sf_bytes), atile + (size_t)512 * wpc * (j + cc), 512 * wpc,
-                      su32(&ctl->full[s]), pol);
-          if (MODE == DOWN && a.tma_b)  // the work group's B rows: n_tile rows from position pos0 on
+          if (g >= pre) issue_a(it, j, s);
+          if (MODE == DOWN && a.tma_b) {  // the work group's B rows: n_tile rows from position pos0 on
+            mbar_expect_tx_only(su32(&ctl->full[s]), (uint32_t)(a.n_tile * 128 * CH));
             for (int cc = 0; cc < CH; ++cc)
               tma_load_2d(su32(st + b_off + cc * a.b_bytes), &map_r1, (j + cc) * 128, it.wg.pos0 * a.terms,
                           su32(&ctl->full[s]));
+          }
         }
         for (int cc = 0; cc < CH; ++cc) {
           const int jj = j + cc;
@@ -431,10 +478,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("cp.async.wait_all;" ::: "memory");
     // after a timeout: the last fill of each of this loader's slots (tensor and bulk copies, and the
     // lanes' cp.async, all counted by the slot's full barrier) lands before the CTA frees its memory.
-    // Earlier fills of a slot have landed: the slot was refilled only after their MMAs completed.
-    if (!ok && lane == 0)
+    // Earlier fills of a slot have landed: the slot was refilled only after their MMAs completed. A
+    // slot of the first round whose weight tiles were requested early but which the loop did not
+    // reach gets the lanes' arrivals here, so that its barrier completes when those tiles land.
+    if (!ok) {
+      const uint32_t unreached = pre_mask & ~issued;
       for (int s = 0; s < S; ++s)
-        if ((issued >> s) & 1u) drain_wait(su32(&ctl->full[s]), (par >> s) & 1u);
+        if ((unreached >> s) & 1u) cp_arrive_noinc(su32(&ctl->full[s]));
+      if (lane == 0)
+        for (int s = 0; s < S; ++s)
+          if (((issued | unreached) >> s) & 1u) drain_wait(su32(&ctl->full[s]), ((par & issued) >> s) & 1u);
+    }
     __syncwarp();
   } else if (warp >= kWarpIss) {
     // ------------------------------------------------------------ MMA issuers
