@@ -225,6 +225,42 @@ __device__ void topk_select_any(int E, int k, const float* logits_t, long long l
   else topk_select<16, KZ, SIG>(E, k, logits_t, ls, np, sel_bias, cand, sel, s_thr, s_n);
 }
 
+// Warp 0 after topk_select: lane r < k takes the r-th selected expert and its gate (written to the
+// workspace's and the caller's top-k arrays); lanes >= k return expert -1.
+template <bool SIG>
+__device__ __forceinline__ void gates_warp(int k, const float* logits_t, long long ls, int np,
+                                           const unsigned long long* sel, int* idx_out, float* w_out, int* idx_user,
+                                           float* w_user, int& my_e, float& w) {
+  const int lane = threadIdx.x & 31;
+  const unsigned long long best = (lane < k) ? sel[lane] : 0ull;
+  my_e = key_expert(best);
+  float ex;
+  if (SIG) {  // the unbiased score of the selected expert: its logit again, parts added in order
+    float l = 0.0f;
+    if (lane < k) {
+      l = __ldcg(&logits_t[my_e]);
+      for (int z = 1; z < np; ++z) l += __ldcg(&logits_t[z * ls + my_e]);
+    }
+    ex = (lane < k) ? sigmoid_score(l) : 0.0f;
+  } else {
+    const float my_l = (lane < k) ? key_logit(best) : 0.0f;  // the key holds the logit's bits
+    const float lmax = __shfl_sync(0xffffffffu, my_l, 0);
+    ex = (lane < k) ? expf(my_l - lmax) : 0.0f;
+  }
+  float sum = ex;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  w = ex / sum;
+  if (lane < k) {
+    idx_out[lane] = my_e;
+    w_out[lane] = w;
+    if (idx_user) idx_user[lane] = my_e;
+    if (w_user) w_user[lane] = w;
+  } else {
+    my_e = -1;
+  }
+}
+
 template <int KZ, bool SIG>
 __device__ void topk_block(int E, int k, const float* logits_t, long long ls, int np, const float* sel_bias,
                            unsigned long long* cand, int* idx_out, float* w_out, int* idx_user, float* w_user,
@@ -234,35 +270,54 @@ __device__ void topk_block(int E, int k, const float* logits_t, long long ls, in
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   topk_select_any<KZ, SIG>(E, k, logits_t, ls, np, sel_bias, cand, s_sel, s_thr, &s_n);
   if (warp == 0) {
-    const unsigned long long best = (lane < k) ? s_sel[lane] : 0ull;
-    const int my_e = key_expert(best);
-    float ex;
-    if (SIG) {  // the unbiased score of the selected expert: its logit again, parts added in order
-      float l = 0.0f;
-      if (lane < k) {
-        l = __ldcg(&logits_t[my_e]);
-        for (int z = 1; z < np; ++z) l += __ldcg(&logits_t[z * ls + my_e]);
-      }
-      ex = (lane < k) ? sigmoid_score(l) : 0.0f;
-    } else {
-      const float my_l = (lane < k) ? key_logit(best) : 0.0f;  // the key holds the logit's bits
-      const float lmax = __shfl_sync(0xffffffffu, my_l, 0);
-      ex = (lane < k) ? expf(my_l - lmax) : 0.0f;
-    }
-    float sum = ex;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    int my_e;
+    float w;
+    gates_warp<SIG>(k, logits_t, ls, np, s_sel, idx_out, w_out, idx_user, w_user, my_e, w);
     if (lane < k) {
-      const float w = ex / sum;
-      idx_out[lane] = my_e;
-      w_out[lane] = w;
-      if (idx_user) idx_user[lane] = my_e;
-      if (w_user) w_user[lane] = w;
       if (idx_sm) idx_sm[lane] = my_e;
       if (w_sm) w_sm[lane] = w;
     }
   }
   __syncthreads();
+}
+
+// One token (T = 1, k <= 32 <= ... selected experts all distinct and valid, as top_k <= n_routed):
+// the top-k, the gates and the whole permutation in warp 0, from registers. It writes what the
+// general builder writes for one token: routed slot r goes to position p_r = the number of selected
+// experts with a lower id (positions sorted by expert), each position is a work group of one token
+// in both lists, the shared experts' positions and groups follow at k, k + 1, ...
+template <int KZ, bool SIG>
+__device__ void topk_permute_one_token(const Cfg& c, const Ws& ws, const float* logits_t, long long ls, int np,
+                                       const float* sel_bias, unsigned long long* cand, int* idx_user, float* w_user) {
+  __shared__ unsigned long long s_sel[32], s_thr[64];
+  __shared__ int s_n;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  topk_select_any<KZ, SIG>(c.E, c.k, logits_t, ls, np, sel_bias, cand, s_sel, s_thr, &s_n);
+  if (warp != 0) return;
+  int my_e;
+  float w;
+  gates_warp<SIG>(c.k, logits_t, ls, np, s_sel, ws.topk_idx, ws.topk_w, idx_user, w_user, my_e, w);
+  int pos = 0;
+  for (int j = 0; j < c.k; ++j) pos += (__shfl_sync(0xffffffffu, my_e, j) < my_e) ? 1 : 0;
+  if (lane < c.k) {
+    ws.perm_tok[pos] = 0;
+    ws.perm_w[pos] = w;
+    ws.inv[lane] = pos;
+    ws.wgs[pos] = WorkGroup{my_e, pos, 1, 0};
+    ws.wgs_dn[pos] = WorkGroup{my_e, pos, 1, 0};
+  }
+  if (lane < c.S) {
+    const int p = c.k + lane;
+    ws.perm_tok[p] = 0;
+    ws.perm_w[p] = 1.0f;
+    ws.wgs[p] = WorkGroup{c.E + lane, p, 1, 0};
+    ws.wgs_dn[p] = WorkGroup{c.E + lane, p, 1, 0};
+  }
+  if (lane == 0) {
+    ws.ctrl[CTRL_NWG] = c.k + c.S;
+    ws.ctrl[CTRL_NWG_DN] = c.k + c.S;
+    ws.ctrl[CTRL_NPOS] = c.k;
+  }
 }
 
 // Logits from the tensor cores carry the rounding of the MMA's fp32 accumulation (measured ~1e-5 at
@@ -759,6 +814,13 @@ __global__ void __launch_bounds__(256, 3) k_route(RouteArgs a) {
   __syncthreads();
   if (!s_last) return;
   __threadfence();
+  if (a.T == 1 && (a.mode & RM_PERMUTE)) {  // one token: selection and permutation in one warp
+    topk_permute_one_token<2, SIG>(c, a.ws, a.ws.logits, a.T * c.E, dots ? 1 : c.rsplit, SIG ? a.bias : nullptr, cand,
+                                   (a.mode & RM_USER_OUT) ? a.out_idx : nullptr,
+                                   (a.mode & RM_USER_OUT) ? a.out_w : nullptr);
+    if (threadIdx.x == 0) a.ws.rtcnt[0] = 0;
+    return;
+  }
   // one token tile whose routed slots fit the block: the permutation reads the selection from shared memory
   const bool tile_sm = gridDim.y == 1 && (long long)ntt * c.k <= (long long)blockDim.x && ntt * c.k <= 8 * 32;
   for (int tt = 0; tt < ntt; ++tt) {
