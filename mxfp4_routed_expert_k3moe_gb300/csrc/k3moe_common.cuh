@@ -155,5 +155,13 @@ __device__ __forceinline__ void split_terms(float v, int terms, uint8_t* codes, 
 }
 
 __device__ __forceinline__ void set_status(int* ctrl, int bits) { atomicOr(&ctrl[CTRL_STATUS], bits); }
+// GPU-scope release-acquire add, for the last-CTA handshakes: between two CTA barriers, the release
+// orders the CTA's earlier writes before the count, and the acquire in the CTA that reads the final
+// count orders its later reads after it.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
 
 }  // namespace k3

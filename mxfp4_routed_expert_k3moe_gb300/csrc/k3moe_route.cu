@@ -166,18 +166,36 @@ __device__ void topk_select(int E, int k, const float* logits_t, long long ls, i
   if (lane < m) s_thr[warp * m + lane] = mine;
   if (threadIdx.x == 0) *s_n = 0;
   __syncthreads();
-  unsigned long long tau = ~0ull;
-  for (int i = 0; i < nw * m; ++i) tau = s_thr[i] < tau ? s_thr[i] : tau;
+  // tau: the smallest of the warps' picks (every warp forms the minimum of all nw m picks)
+  unsigned long long tv = ~0ull;
+  for (int i = lane; i < nw * m; i += 32) tv = s_thr[i] < tv ? s_thr[i] : tv;
+  const uint32_t tau_hi = __reduce_min_sync(0xffffffffu, (uint32_t)(tv >> 32));
+  const uint32_t tau_lo = __reduce_min_sync(0xffffffffu, (uint32_t)(tv >> 32) == tau_hi ? (uint32_t)tv : 0xFFFFFFFFu);
+  const unsigned long long tau = ((unsigned long long)tau_hi << 32) | tau_lo;
   const int cap = blockDim.x;
+  // the candidates go to `cand` with one shared-memory atomic per warp: a lane's candidates take the
+  // slots after those of the lanes below it
+  int cnt = (lane < m && mine != 0ull) ? 1 : 0;
+#pragma unroll
+  for (int q = 0; q < R; ++q) cnt += (key[q] != 0ull && key[q] >= tau) ? 1 : 0;
+  int incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  int base = 0;
+  if (lane == 31 && incl > 0) base = atomicAdd(s_n, incl);
+  int at = __shfl_sync(0xffffffffu, base, 31) + incl - cnt;
   if (lane < m && mine != 0ull) {
-    const int at = atomicAdd(s_n, 1);
     if (at < cap) cand[at] = mine;
+    ++at;
   }
 #pragma unroll
   for (int q = 0; q < R; ++q)
     if (key[q] != 0ull && key[q] >= tau) {
-      const int at = atomicAdd(s_n, 1);
       if (at < cap) cand[at] = key[q];
+      ++at;
     }
   __syncthreads();
   const int n = *s_n;
@@ -803,17 +821,14 @@ __global__ void __launch_bounds__(256, 3) k_route(RouteArgs a) {
       }
     }
   }
-  __threadfence();
-
   // the last CTA of each token tile selects the top-k of its tokens ...
   __syncthreads();
   if (threadIdx.x == 0) {
-    const int prev = atomicAdd(&a.ws.rtcnt[blockIdx.y], 1);
+    const int prev = atom_add_acq_rel_gpu(&a.ws.rtcnt[blockIdx.y], 1);
     s_last = (prev == (int)gridDim.x - 1);
   }
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
   if (a.T == 1 && (a.mode & RM_PERMUTE)) {  // one token: selection and permutation in one warp
     topk_permute_one_token<2, SIG>(c, a.ws, a.ws.logits, a.T * c.E, dots ? 1 : c.rsplit, SIG ? a.bias : nullptr, cand,
                                    (a.mode & RM_USER_OUT) ? a.out_idx : nullptr,
