@@ -25,6 +25,12 @@ bool use_fp4(const k3moe_config* c, long long T) {
   return T <= kFp4MaxT && c->d_model % 256 == 0 && c->d_ff % 256 == 0;
 }
 
+// Gate/up B tiles from the x terms in position order (one tensor copy per chunk) from kGatherMinT
+// tokens on, where the loaders' 16-byte copies of rows gathered by token bound the projection. The
+// gather costs P x xterms x d bytes written and read once more.
+constexpr long long kGatherMinT = 256;
+bool gather_x(const k3moe_config* c, long long T) { return !use_fp4(c, T) && T >= kGatherMinT; }
+
 size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // Router logits on the tensor cores from kRouterTcMinT tokens, else on the CUDA cores. Below it the
@@ -113,8 +119,8 @@ long long wg_bound(const k3moe_config* c, long long T) {
 }
 
 struct Layout {
-  size_t ctrl, logits, topk_idx, topk_w, counts, cursor, offsets, wgoff, perm_tok, perm_w, inv, wgs, wgs_dn, xq, xs, hq, hs,
-      part, rtcnt, w3, x3, sgu, sh3, sho, total;
+  size_t ctrl, logits, topk_idx, topk_w, counts, cursor, offsets, wgoff, perm_tok, perm_w, inv, wgs, wgs_dn, xq, xs, xp, hq,
+      hs, part, rtcnt, w3, x3, sgu, sh3, sho, total;
 };
 
 // Largest T' * parts(T') over T' <= T when parts(T') is constant on runs of 128 tokens (the tile rows)
@@ -156,6 +162,7 @@ Layout make_layout(const k3moe_config* c, long long T) {
   const long long terms = fp4 ? kMaxTermsFp4 : kMaxTerms;
   take(L.xq, (size_t)(T * terms * (fp4 ? d / 2 : d)));
   take(L.xs, (size_t)(T * terms * (d / 32)));
+  take(L.xp, gather_x(c, T) ? (size_t)(P * terms * d) : 0);
   take(L.hq, (size_t)(P * terms * (fp4 ? f / 2 : f)));
   take(L.hs, (size_t)(P * terms * (f / 32)));
   take(L.part, sizeof(float) * P * d);
@@ -195,6 +202,7 @@ Ws bind(const Layout& L, void* base) {
   w.wgs_dn = reinterpret_cast<k3::WorkGroup*>(b + L.wgs_dn);
   w.xq = reinterpret_cast<uint8_t*>(b + L.xq);
   w.xs = reinterpret_cast<uint8_t*>(b + L.xs);
+  w.xp = reinterpret_cast<uint8_t*>(b + L.xp);
   w.hq = reinterpret_cast<uint8_t*>(b + L.hq);
   w.hs = reinterpret_cast<uint8_t*>(b + L.hs);
   w.part = reinterpret_cast<float*>(b + L.part);
@@ -234,6 +242,7 @@ Cfg make_cfg(const k3moe_config* c, long long T) {
   k.wgt = (int)(T < wmax ? T : wmax);
   k.wgt_dn = (int)(T < wmax_dn ? T : wmax_dn);
   k.rsplit = (int)router_splits(c, T);
+  k.gx = gather_x(c, T) ? 1 : 0;
   k.wait_limit = kDefaultWaitLimit;
   k.stride = c->record_stride;
   k.sstride = shared_stride_of(c);
@@ -348,6 +357,7 @@ k3moe_status k3moe_expert_ffn(const k3moe_config* cfg, const void* x, int64_t T,
   const Ws w = bind(L, ws);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = k3::launch_prep(c, w, x, T, topk_idx, topk_w, st);
+  if (e == cudaSuccess && c.gx) e = k3::launch_gather_x(c, w, T, st);
   if (e == cudaSuccess) e = k3::launch_gateup(c, w, routed_records, shared_records, y, T, wg_bound(cfg, T), st);
   if (e == cudaSuccess)
     e = k3::launch_down(c, w, routed_records, shared_records, y, T, wg_bound(cfg, T), st, nullptr, c.Sb == 0);
@@ -397,6 +407,7 @@ k3moe_status layer_impl(const k3moe_config* cfg, const void* x, int64_t T, const
   if (e == cudaSuccess) e = k3::launch_route(c, w, x, T, w_router, bias, topk_idx_out, topk_w_out, mode, st);
   if (e == cudaSuccess && events) e = cudaEventRecord(static_cast<cudaEvent_t>(events[1]), st);
   auto evt = [&](int i) { return events ? static_cast<cudaEvent_t>(events[i]) : nullptr; };
+  if (e == cudaSuccess && c.gx) e = k3::launch_gather_x(c, w, T, st);
   if (e == cudaSuccess) e = k3::launch_gateup(c, w, routed_records, shared_records, y, T, wgb, st, evt(2));
   if (e == cudaSuccess && events) e = cudaEventRecord(evt(3), st);
   if (e == cudaSuccess) e = k3::launch_down(c, w, routed_records, shared_records, y, T, wgb, st, evt(4), c.Sb == 0);

@@ -19,6 +19,7 @@ struct Cfg {
   int xterms;         // terms per activation block of x (E4M3: 2 for bf16 x, 3 for fp32 x; E2M1: 8 or 16)
   int hterms;         // terms per block of h
   int rsplit;         // partial logits the router kernel adds up (parts of the tensor-core reduction; 1: final)
+  int gx;             // 1: the gate/up B tiles come from xp (the x terms in position order) by tensor copies
   uint32_t wait_limit;  // polls of a pipeline barrier before a CTA gives up (K3MOE_ERR_TIMEOUT)
   long long stride;   // bytes between routed expert records
   long long sstride;  // bytes between shared expert records
@@ -57,6 +58,7 @@ struct Ws {
   WorkGroup* wgs_dn;  // [WGmax] work groups of the down projection (wgt_dn positions at most)
   uint8_t* xq;        // [T * xterms, d] E4M3 (or [.., d/2] packed E2M1) terms of x (row t*xterms + j)
   uint8_t* xs;        // [T * xterms, d/32] their E8M0 block scales
+  uint8_t* xp;        // [P * xterms, d] E4M3 terms of x in position order (row p*xterms + j), when Cfg::gx
   uint8_t* hq;        // [P * hterms, f] E4M3 (or [.., f/2] packed E2M1) terms of h (row p*hterms + j)
   uint8_t* hs;        // [P * hterms, f/32] their E8M0 block scales
   float* part;        // [P, d] down-projection outputs per position (the combine weights them)

@@ -32,6 +32,8 @@ cudaError_t launch_route(const Cfg& c, const Ws& ws, const void* x, long long T,
                          int* out_idx, float* out_w, int mode, cudaStream_t st);
 cudaError_t launch_prep(const Cfg& c, const Ws& ws, const void* x, long long T, const int* idx, const float* w,
                         cudaStream_t st);
+// x terms in position order (ws.xp, c.gx): after the permutation and the x terms, before gate/up.
+cudaError_t launch_gather_x(const Cfg& c, const Ws& ws, long long T, cudaStream_t st);
 cudaError_t launch_rmsnorm(const float* x, long long T, int d, float eps, float* out, cudaStream_t st);
 cudaError_t launch_residual_rmsnorm(float* x, const float* y, long long T, int d, float eps, float* out,
                                     cudaStream_t st);

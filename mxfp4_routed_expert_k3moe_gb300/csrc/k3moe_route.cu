@@ -1092,6 +1092,34 @@ cudaError_t launch_prep(const Cfg& c, const Ws& ws, const void* x, long long T, 
   return launch_pdl(k_prep, dim3((unsigned)ctas), dim3(256), sizeof(int) * perm_ints(c.E), st, a);
 }
 
+// The E4M3 terms of x in position order: row p * xterms + j of xp is row perm_tok[p] * xterms + j of xq,
+// for the routed positions below the routed count and every shared position (one warp per row, d bytes
+// as 16-byte words). A gate/up work group's B rows are then consecutive rows of xp, one tensor copy
+// per chunk, instead of rows gathered by token with 16-byte copies.
+__global__ void __launch_bounds__(256) k_gather_x(Cfg c, Ws ws, long long T) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const long long PR = T * c.k, P = T * (c.k + c.S);
+  const long long npos = __ldcg(&ws.ctrl[CTRL_NPOS]);
+  const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
+  const int lane = threadIdx.x & 31, words = c.d / 16;
+  for (long long r = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < P * c.xterms; r += nwarps) {
+    const long long p = r / c.xterms;
+    if (p >= npos && p < PR) continue;  // (slots without a valid expert)
+    const long long src = (long long)__ldcg(&ws.perm_tok[p]) * c.xterms + (r - p * c.xterms);
+    const uint4* s = reinterpret_cast<const uint4*>(ws.xq + src * c.d);
+    uint4* o = reinterpret_cast<uint4*>(ws.xp + r * c.d);
+    for (int v = lane; v < words; v += 32) o[v] = __ldcg(s + v);
+  }
+}
+
+cudaError_t launch_gather_x(const Cfg& c, const Ws& ws, long long T, cudaStream_t st) {
+  const long long rows = T * (c.k + c.S) * c.xterms;
+  long long blocks = (rows + 7) / 8;
+  if (blocks > 152 * 8) blocks = 152 * 8;
+  return launch_pdl(k_gather_x, dim3((unsigned)blocks), dim3(256), 0, st, c, ws, T);
+}
+
 cudaError_t launch_rmsnorm(const float* x, long long T, int d, float eps, float* out, cudaStream_t st) {
   const long long blocks = T < 152 * 16 ? T : 152 * 16;
   return launch_pdl(k_rmsnorm, dim3((unsigned)blocks), dim3(256), 0, st, x, T, d, eps, out);

@@ -177,8 +177,8 @@ struct TcArgs {
   int parts;    // reduction parts per row tile (1: whole items)
   FastDiv div_parts, div_mtiles;
   int stages;   // pipeline depth (<= kMaxStages)
-  int tma_b;    // (down) the B rows of a work group, contiguous positions x terms, come by one tensor copy
-                // per chunk (map_r1 holds the map of the h terms) instead of cp.async row copies
+  int tma_b;    // the B rows of a work group, contiguous positions x terms, come by one tensor copy per
+                // chunk (map_b: the h terms, or the x terms in position order) instead of cp.async row copies
   int stage_bytes;  // ch x (A tile + B tile + scale words)
 };
 
@@ -254,7 +254,8 @@ __device__ __forceinline__ bool b_row(const TcArgs& a, const Item& it, int n, co
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     k_tc(const __grid_constant__ CUtensorMap map_r0, const __grid_constant__ CUtensorMap map_r1,
-         const __grid_constant__ CUtensorMap map_s0, const __grid_constant__ CUtensorMap map_s1, TcArgs a) {
+         const __grid_constant__ CUtensorMap map_s0, const __grid_constant__ CUtensorMap map_s1,
+         const __grid_constant__ CUtensorMap map_b, TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const int S = a.stages, CH = a.ch;
@@ -266,6 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&map_r1);
     prefetch_tmap(&map_s0);
     prefetch_tmap(&map_s1);
+    if (a.tma_b) prefetch_tmap(&map_b);
   }
   // The gate/up kernel reads the routing, which the previous kernel writes. The down kernel's work
   // groups come from the routing kernel two launches back: it completed before the gate/up kernel
@@ -440,10 +442,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* st = smem + (size_t)s * a.stage_bytes;
         if (lane == 0) {
           if (g >= pre) issue_a(it, j, s);
-          if (MODE == DOWN && a.tma_b) {  // the work group's B rows: n_tile rows from position pos0 on
+          if (a.tma_b) {  // the work group's B rows: n_tile rows from position pos0 on
             mbar_expect_tx_only(su32(&ctl->full[s]), (uint32_t)(a.n_tile * 128 * CH));
             for (int cc = 0; cc < CH; ++cc)
-              tma_load_2d(su32(st + b_off + cc * a.b_bytes), &map_r1, (j + cc) * 128, it.wg.pos0 * a.terms,
+              tma_load_2d(su32(st + b_off + cc * a.b_bytes), &map_b, (j + cc) * 128, it.wg.pos0 * a.terms,
                           su32(&ctl->full[s]));
           }
         }
@@ -455,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // reads four 128-byte rows (one row per lane read 32 rows: a quarter of the L1 rate)
           // (four rows per lane at a time: their table reads are issued before the copies)
           const int k16 = lane & 7;
-          for (int n0 = lane >> 3; n0 < nrows && !(MODE == DOWN && a.tma_b); n0 += 16) {
+          for (int n0 = lane >> 3; n0 < nrows && !a.tma_b; n0 += 16) {
             uint32_t r[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) r[u] = n0 + 4 * u < nrows ? rtab[n0 + 4 * u] : ~0u;
@@ -905,7 +907,7 @@ size_t xb_bytes(const TcArgs& a) { return (size_t)4 * a.xb_tok * 32 * sizeof(flo
 
 template <int MODE>
 cudaError_t launch_tc(const TcArgs& a, const CUtensorMap& r0, const CUtensorMap& r1, const CUtensorMap& s0,
-                      const CUtensorMap& s1, long long items_max, cudaStream_t st) {
+                      const CUtensorMap& s1, const CUtensorMap& b, long long items_max, cudaStream_t st) {
   if (items_max >= (1LL << 31)) return cudaErrorInvalidValue;  // item indices are decomposed in 32 bits
   const size_t smem = (size_t)a.stages * a.stage_bytes + ctl_bytes() + xb_bytes(a) + 1024;
   static bool attr = false;
@@ -916,7 +918,7 @@ cudaError_t launch_tc(const TcArgs& a, const CUtensorMap& r0, const CUtensorMap&
   }
   long long grid = items_max < g_sms ? items_max : g_sms;
   if (grid < 1) grid = 1;
-  return launch_pdl(k_tc<MODE>, dim3((unsigned)grid), dim3(kThreads), smem, st, r0, r1, s0, s1, a);
+  return launch_pdl(k_tc<MODE>, dim3((unsigned)grid), dim3(kThreads), smem, st, r0, r1, s0, s1, b, a);
 }
 
 // Tile geometry for an MMA N of n_tile: TMEM holds two accumulator buffers per issuer and then one
@@ -1006,6 +1008,21 @@ TcArgs base_args(const Cfg& c, const Ws& ws, const uint8_t* routed, const uint8_
   return a;
 }
 
+// Map over `rows` activation rows of `row_bytes` E4M3 codes (the terms of x in position order, or of
+// h): boxes of 128 bytes x n_tile rows, the B tile of one chunk of a work group.
+cudaError_t rows_map(CUtensorMap* m, const void* base, long long row_bytes, long long rows, int n_tile) {
+  cudaError_t e = get_encode();
+  if (e != cudaSuccess) return e;
+  cuuint64_t gdim[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+  cuuint64_t gstr[1] = {(cuuint64_t)row_bytes};
+  cuuint32_t box[2] = {128, (cuuint32_t)n_tile}, es[2] = {1, 1};
+  if (g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), gdim, gstr, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  return cudaSuccess;
+}
+
 }  // namespace
 
 cudaError_t launch_gateup(const Cfg& c, const Ws& ws, const uint8_t* routed, const uint8_t* shared, float* y,
@@ -1022,7 +1039,13 @@ cudaError_t launch_gateup(const Cfg& c, const Ws& ws, const uint8_t* routed, con
   TcMaps m;
   cudaError_t e = setup(c, routed, shared, a.ch, 0, m, a.shared);
   if (e != cudaSuccess) return e;
-  e = launch_tc<GATEUP>(a, m.gr, m.ur, m.gs, m.us, wg_max * 2 * (c.f / 128), st);
+  // x terms in position order (c.gx): a work group's B rows are rows pos0 * xterms .. of xp
+  CUtensorMap mx = m.gr;
+  if (c.gx) {
+    if ((e = rows_map(&mx, ws.xp, c.d, T * (c.k + c.S) * c.xterms, a.n_tile)) != cudaSuccess) return e;
+    a.tma_b = 1;
+  }
+  e = launch_tc<GATEUP>(a, m.gr, m.ur, m.gs, m.us, mx, wg_max * 2 * (c.f / 128), st);
   if (e == cudaSuccess && mid) e = cudaEventRecord(mid, st);
   return e;
 }
@@ -1045,18 +1068,10 @@ cudaError_t launch_down(const Cfg& c, const Ws& ws, const uint8_t* routed, const
   // are not read)
   CUtensorMap mh = m.dr;
   if (!c.fp4) {
-    if ((e = get_encode()) != cudaSuccess) return e;
-    const long long P = T * (c.k + c.S);
-    cuuint64_t gdim[2] = {(cuuint64_t)c.f, (cuuint64_t)(P * c.hterms)};
-    cuuint64_t gstr[1] = {(cuuint64_t)c.f};
-    cuuint32_t box[2] = {128, (cuuint32_t)a.n_tile}, es[2] = {1, 1};
-    if (g_encode(&mh, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, ws.hq, gdim, gstr, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
-        CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
+    if ((e = rows_map(&mh, ws.hq, c.f, T * (c.k + c.S) * c.hterms, a.n_tile)) != cudaSuccess) return e;
     a.tma_b = 1;
   }
-  e = launch_tc<DOWN>(a, m.dr, mh, m.ds, m.ds, wg_max * (c.d / 128), st);
+  e = launch_tc<DOWN>(a, m.dr, m.dr, m.ds, m.ds, mh, wg_max * (c.d / 128), st);
   if (e == cudaSuccess && mid) e = cudaEventRecord(mid, st);
   if (e != cudaSuccess || !combine) return e;
   return launch_combine(c, ws, y, T, st);

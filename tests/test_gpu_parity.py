@@ -262,6 +262,43 @@ def test_expert_ffn_given_routing():
     assert rel_err(y.cpu().numpy(), y_ref) <= REL_TOL
 
 
+@pytest.mark.parametrize("x_dtype", ["bf16", "f32"])
+def test_expert_ffn_given_routing_position_ordered_x(x_dtype):
+    """From 256 tokens the gate/up projection reads x's terms in position order (gathered once per
+    call, one tensor copy per work group and chunk); routed slots with overlapping expert sets and a
+    ragged tail of tokens."""
+    L = DeviceLayer(MID, seed=16, x_dtype=x_dtype)
+    T = 301
+    xh, xd = L.tokens(T)
+    rng = np.random.default_rng(2)
+    idx = np.stack([rng.choice(MID.n_routed, MID.top_k, replace=False) for _ in range(T)]).astype(np.int32)
+    idx[7, :] = np.arange(MID.top_k)
+    idx[8, :] = np.arange(MID.top_k)
+    w = rng.random((T, MID.top_k)).astype(np.float32)
+    y = torch.empty((T, MID.d_model), dtype=torch.float32, device="cuda")
+    ws = torch.zeros(k3.workspace_bytes(L.cfg, T), dtype=torch.uint8, device="cuda")
+    k3.expert_ffn(L.cfg, xd, T, torch.from_numpy(idx).cuda(), torch.from_numpy(w).cuda(), L.routed, L.shared, y, ws)
+    assert k3.check_device_status(ws) == k3.OK
+    assert rel_err(y.cpu().numpy(), L.oracle_ffn(xh, idx, w)) <= REL_TOL
+
+
+def test_bad_expert_id_with_position_ordered_x():
+    """A rejected slot leaves a hole in the routed positions; the gather skips it and the layer still
+    reports the bad id."""
+    L = DeviceLayer(MID, seed=17)
+    T = 260
+    _, xd = L.tokens(T)
+    rng = np.random.default_rng(3)
+    idx = np.stack([rng.choice(MID.n_routed, MID.top_k, replace=False) for _ in range(T)]).astype(np.int32)
+    idx[100, 2] = 999
+    w = torch.full((T, MID.top_k), 1.0 / MID.top_k, device="cuda")
+    y = torch.empty((T, MID.d_model), device="cuda")
+    ws = torch.zeros(k3.workspace_bytes(L.cfg, T), dtype=torch.uint8, device="cuda")
+    k3.expert_ffn(L.cfg, xd, T, torch.from_numpy(idx).cuda(), w, L.routed, L.shared, y, ws)
+    assert k3.check_device_status(ws) == k3.ERR_DEVICE_CHECK
+    assert k3.check_device_status(ws) == k3.OK
+
+
 def test_zero_tokens_is_noop():
     L = DeviceLayer(MID, seed=12)
     y = torch.full((1, MID.d_model), 7.0, device="cuda")
