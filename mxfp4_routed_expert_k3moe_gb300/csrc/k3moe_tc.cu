@@ -87,7 +87,10 @@ struct Ctl {
   int ld_tok[kLoaders][kEpRing][32];               // ... and the tokens of their positions (gate/up)
   uint32_t ld_row[kLoaders][kMaxN];                // B row n of loader v's current item: activation row, or ~0
 };
-// Gate/up exchange area after the control block: float [4 epilogue warps][xb_tok tokens][32 lanes].
+// Gate/up exchange area after the control block: float [4 epilogue warps][xb_tok tokens][kXb], lane l
+// of a warp at [..][..][l]; a row holds 32 values padded to kXb floats, so that a thread reading one
+// token's row and its neighbours reading the next tokens' rows fall in distinct banks.
+constexpr int kXb = 33;
 __host__ __device__ constexpr size_t ctl_bytes() { return (sizeof(Ctl) + 15) / 16 * 16; }
 
 // Position in the ring of pipeline stages: slot s, phase parity of its current round, and whether
@@ -645,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const long long pos = it.wg.pos0 + tk;
               nan_row |= (run != run);
               if (MODE == GATEUP)
-                xb[(q * a.xb_tok + tk) * 32 + lane] = run;
+                xb[(q * a.xb_tok + tk) * kXb + lane] = run;
               else
                 a.ws.part[pos * c.d + row] = run;  // the gate weight is applied by the combine
               run = 0.0f;
@@ -667,16 +670,59 @@ __global__ void __launch_bounds__(kThreads, 1)
         bar_sync(1, 128);
         const int p = q & 1;
         const int nb = c.f / 32, blk = 4 * it.mt + 2 * it.mat + p;  // 32-block of h
-        for (int i = q >> 1; i < it.wg.ntok; i += 2) {
-          const float g = xb[(p * a.xb_tok + i) * 32 + lane], u = xb[((p + 2) * a.xb_tok + i) * 32 + lane];
-          const float h = silu(g) * u;
-          const long long pos = it.wg.pos0 + i;
-          if (c.fp4)
-            split_terms_fp4(h, c.hterms, a.ws.hq + (pos * c.hterms) * (c.f / 2) + blk * 16, c.f / 2,
+        if (c.fp4) {
+          for (int i = q >> 1; i < it.wg.ntok; i += 2) {
+            const float g = xb[(p * a.xb_tok + i) * kXb + lane], u = xb[((p + 2) * a.xb_tok + i) * kXb + lane];
+            const long long pos = it.wg.pos0 + i;
+            split_terms_fp4(silu(g) * u, c.hterms, a.ws.hq + (pos * c.hterms) * (c.f / 2) + blk * 16, c.f / 2,
                             a.ws.hs + (pos * c.hterms) * nb + blk, nb, lane);
-          else
-            split_terms(h, c.hterms, a.ws.hq + (pos * c.hterms) * c.f + blk * 32 + lane, c.f,
-                        a.ws.hs + (pos * c.hterms) * nb + blk, nb, lane);
+          }
+        } else {
+          // E4M3 terms: one thread per (token, 32-row half of h): its block's 32 values of g and u, h,
+          // and the terms of the block in registers, the steps of split_terms element by element (the
+          // block maximum as a loop, not as a chain of warp shuffles per term and token)
+          const int t = 32 * q + lane;
+          if (t < 2 * it.wg.ntok) {
+            const int i = t >> 1, hp = t & 1;
+            const float* gs = xb + (hp * a.xb_tok + i) * kXb;
+            const float* us = xb + ((hp + 2) * a.xb_tok + i) * kXb;
+            float r[32];
+            float amax = 0.0f;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              r[e] = silu(gs[e]) * us[e];
+              amax = fmaxf(amax, fabsf(r[e]));
+            }
+            const int hblk = 4 * it.mt + 2 * it.mat + hp;
+            const long long pos = it.wg.pos0 + i;
+            uint8_t* cdst = a.ws.hq + (pos * c.hterms) * c.f + hblk * 32;
+            uint8_t* sdst = a.ws.hs + (pos * c.hterms) * nb + hblk;
+            for (int j = 0; j < c.hterms; ++j) {
+              int e = 0;
+              if (amax > 0.0f && amax <= 3.402823466e38f) e = ilogbf(amax) - 7;
+              e = e < -127 ? -127 : (e > 127 ? 127 : e);
+              const float sc = pow2i(-e), back = pow2i(e);
+              uint32_t w[8];
+              float nmax = 0.0f;
+#pragma unroll
+              for (int k = 0; k < 16; ++k) {
+                uint16_t q2;
+                asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(q2) : "f"(r[2 * k + 1] * sc), "f"(r[2 * k] * sc));
+                uint32_t h2;
+                asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(q2));
+                r[2 * k] -= __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu))) * back;
+                r[2 * k + 1] -= __half2float(__ushort_as_half((unsigned short)(h2 >> 16))) * back;
+                nmax = fmaxf(nmax, fmaxf(fabsf(r[2 * k]), fabsf(r[2 * k + 1])));
+                if (k & 1) w[k >> 1] |= (uint32_t)q2 << 16;
+                else w[k >> 1] = q2;
+              }
+              uint4* cv = reinterpret_cast<uint4*>(cdst + (long long)j * c.f);
+              cv[0] = make_uint4(w[0], w[1], w[2], w[3]);
+              cv[1] = make_uint4(w[4], w[5], w[6], w[7]);
+              sdst[(long long)j * nb] = (uint8_t)(e + 127);
+              amax = nmax;
+            }
+          }
         }
       }
       g0 = (g0 + nst) % S;
@@ -903,7 +949,7 @@ cudaError_t weight_map(const uint8_t* base, long long K, long long rows, long lo
 }
 
 // Bytes of the gate/up exchange area (float per epilogue warp, token and lane).
-size_t xb_bytes(const TcArgs& a) { return (size_t)4 * a.xb_tok * 32 * sizeof(float); }
+size_t xb_bytes(const TcArgs& a) { return ((size_t)4 * a.xb_tok * kXb * sizeof(float) + 15) / 16 * 16; }
 
 template <int MODE>
 cudaError_t launch_tc(const TcArgs& a, const CUtensorMap& r0, const CUtensorMap& r1, const CUtensorMap& s0,
