@@ -43,6 +43,10 @@ WORKLOADS = {
     "decode_b64_zipf": (64, 2, 1.1, 2),
     "prefill_4096": (4096, 3, None, 1),
 }
+# Activation mode of the library per workload: from 3 tokens on the layer runs with h as two E4M3 terms
+# (K3MOE_ACT_BF16H, bf16-class h, output within the same 2e-3 bound); each such line also reports the
+# exact mode's time. One token is the same in both modes (eight E2M1 terms).
+BF16H_MIN_T = 3
 STACK_TOKENS = (1, 64)
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_FP4_TFLOPS = 13500.0   # dense FP4 tensor peak of a GB300 (nominal)
@@ -290,7 +294,9 @@ def run_layer_workload(args, k3, name, T, seed, zipf_s, n_sets, steps, warmup, w
     shape = synth.LayerShape(base.d_model, base.d_ff, E, base.top_k, base.n_shared)
     stride = shape.record_stride
     d, f, k, S = shape.d_model, shape.d_ff, shape.top_k, shape.n_shared
-    cfg = k3.Config.make(d, f, E, k, S, x_dtype=k3.X_BF16, record_stride=stride)
+    bf16h = T >= BF16H_MIN_T
+    cfg = k3.Config.make(d, f, E, k, S, x_dtype=k3.X_BF16, record_stride=stride,
+                         act_mode=k3.ACT_BF16H if bf16h else k3.ACT_EXACT)
     layers = [LayerWeights(k3, cfg, shape, seed, l, zipf_s, stride, dev) for l in range(n_sets)]
     nb = 64 if T <= 64 else 2
     xs_host = np.stack([synth.tokens(shape, seed, T, "bf16", batch=b) for b in range(nb)])  # [nb, T, d] uint16
@@ -310,6 +316,19 @@ def run_layer_workload(args, k3, name, T, seed, zipf_s, n_sets, steps, warmup, w
     elapsed_ms, clk = timed(step, steps, world, local_rank, warmup=warmup, check=check_warm)
     if k3.check_device_status(ws) != k3.OK:
         raise RuntimeError(f"{name}: device status check failed in the timed region")
+    exact = None
+    if bf16h:  # the same steps in the exact mode (h as three E4M3 terms), timed the same way
+        cfg_x = k3.Config.make(d, f, E, k, S, x_dtype=k3.X_BF16, record_stride=stride, act_mode=k3.ACT_EXACT)
+
+        def step_x(i):
+            L = layers[i % len(layers)]
+            k3.layer(cfg_x, xs[i % nb], T, L.W, L.bias, L.routed, L.shared, y, ws, w_parts=L.parts)
+
+        ms_x, _ = timed(step_x, steps, world, local_rank, warmup=warmup)
+        if k3.check_device_status(ws) != k3.OK:
+            raise RuntimeError(f"{name}: device status check failed in the exact-mode pass")
+        exact = {"act_mode": "exact (h as three E4M3 terms, ~2^-22)", "value": world * T * steps / (ms_x * 1e-3),
+                 "unit": "tokens/s", "ms_per_step": ms_x / steps}
 
     # per-kernel pass (after the headline timing): events recorded between the kernels of each step on
     # the launching stream; the gate/up kernel finishes h itself, so its two closing events are adjacent
@@ -340,7 +359,7 @@ def run_layer_workload(args, k3, name, T, seed, zipf_s, n_sets, steps, warmup, w
     bytes_route = E * d * 4 + T * d * 2
     bytes_layer = (U + S) * rec + E * d * 4 + T * d * 2 + T * d * 4
     # implementation traffic the layer adds on top (written and read back once each): the
-    # per-position down outputs [P, d] fp32 and h as three E4M3 terms with E8M0 scales [P, 3, f (+ f/32)]
+    # per-position down outputs [P, d] fp32 (h's E4M3 terms and x's in position order are not counted)
     P = T * (k + S)
     bytes_partials = 2 * P * d * 4
     # algorithmic flops: 2 per multiply-add of the three projections of every selected (token, expert)
@@ -360,6 +379,7 @@ def run_layer_workload(args, k3, name, T, seed, zipf_s, n_sets, steps, warmup, w
         "value": world * T * steps / (elapsed_ms * 1e-3), "unit": "tokens/s", "steps": steps, "warmup": warmup,
         "ms_per_step": ms_per_step,
         "config": {**workload_config(name, T, shape), "weight_sets_rotated": n_sets,
+                   "act_mode": "bf16h (h as two E4M3 terms, bf16-class)" if bf16h else "exact",
                    "l2": f"inputs larger than L2: each step reads {bytes_layer / 1e6:.1f} MB of weights "
                          f"({n_sets} weight set(s) rotated, {nb} token batch(es))"},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -376,7 +396,7 @@ def run_layer_workload(args, k3, name, T, seed, zipf_s, n_sets, steps, warmup, w
                            "frac_with_implementation_bytes":
                                (bytes_layer + bytes_partials) / (ms_per_step * 1e-3) / 1e9 / peak},
         "distinct_experts_per_step": U,
-        "gpu_launches": (4 if T < 16 else 5) * steps,
+        "gpu_launches": (4 if T < 16 else (5 if T < 256 else 6)) * steps,
         "clocks": clk,
     }
     if T >= 16:
@@ -387,6 +407,8 @@ def run_layer_workload(args, k3, name, T, seed, zipf_s, n_sets, steps, warmup, w
         if valid and "tensor_active" in cnt:
             tc["tensor_pipe_active_ncu"] = {"value": cnt["tensor_active"], "kernel": dom, "case": cnt["case"]}
         out["tensor"] = tc
+    if exact is not None:
+        out["exact_mode"] = exact
     if not args.no_e2e:
         out["e2e"] = e2e(k3, cfg, layers, xs_host, T, d, dev, steps, warmup)
     if with_cpu and not args.no_cpu_baseline:

@@ -18,7 +18,7 @@ __all__ = ["Config", "K3moeError", "load", "record_bytes", "workspace_bytes", "r
 
 OK, ERR_INVALID_ARGUMENT, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE_CHECK, ERR_TIMEOUT = range(7)
 SCORE_SOFTMAX, SCORE_SIGMOID_BIAS = 0, 1
-ACT_EXACT, ACT_MXFP4 = 0, 1
+ACT_EXACT, ACT_MXFP4, ACT_BF16H = 0, 1, 2
 X_BF16, X_F32 = 0, 1
 ORDER_STORED, ORDER_DEVICE = 0, 1
 SHARED_MXFP4, SHARED_BF16 = 0, 1

@@ -81,7 +81,8 @@ k3moe_status validate_fields(const k3moe_config* c) {
   if (c->n_shared < 0 || c->n_shared > kMaxS) return K3MOE_ERR_INVALID_ARGUMENT;
   if (c->score_func != K3MOE_SCORE_SOFTMAX && c->score_func != K3MOE_SCORE_SIGMOID_BIAS)
     return K3MOE_ERR_INVALID_ARGUMENT;
-  if (c->act_mode != K3MOE_ACT_EXACT && c->act_mode != K3MOE_ACT_MXFP4) return K3MOE_ERR_INVALID_ARGUMENT;
+  if (c->act_mode != K3MOE_ACT_EXACT && c->act_mode != K3MOE_ACT_MXFP4 && c->act_mode != K3MOE_ACT_BF16H)
+    return K3MOE_ERR_INVALID_ARGUMENT;
   if (c->x_dtype != K3MOE_X_BF16 && c->x_dtype != K3MOE_X_F32) return K3MOE_ERR_INVALID_ARGUMENT;
   if (c->record_order != K3MOE_ORDER_STORED && c->record_order != K3MOE_ORDER_DEVICE) return K3MOE_ERR_INVALID_ARGUMENT;
   if (c->shared_format != K3MOE_SHARED_MXFP4 && c->shared_format != K3MOE_SHARED_BF16) return K3MOE_ERR_INVALID_ARGUMENT;
@@ -90,7 +91,7 @@ k3moe_status validate_fields(const k3moe_config* c) {
   if (c->shared_stride < 0 || c->shared_stride % 4096) return K3MOE_ERR_INVALID_ARGUMENT;
   const long long shared_need = c->shared_format == K3MOE_SHARED_BF16 ? shared_bf16_bytes(c) : record_bytes_of(c);
   if (c->shared_stride && c->shared_stride < shared_need) return K3MOE_ERR_INVALID_ARGUMENT;
-  if (c->act_mode != K3MOE_ACT_EXACT) return K3MOE_ERR_UNSUPPORTED;
+  if (c->act_mode == K3MOE_ACT_MXFP4) return K3MOE_ERR_UNSUPPORTED;
   if (c->d_model > kMaxDModel) return K3MOE_ERR_UNSUPPORTED;  // router rows are staged in shared memory
   return K3MOE_OK;
 }
@@ -230,15 +231,17 @@ Cfg make_cfg(const k3moe_config* c, long long T) {
     k.hterms = 8;
   } else {
     k.xterms = k.x_f32 ? 3 : 2;
-    k.hterms = 3;
+    k.hterms = c->act_mode == K3MOE_ACT_BF16H ? 2 : 3;
   }
   // tokens per work group. Gate/up: 32 (16 with the E2M1 terms; 42, which reads an expert's record
   // fewer times, measured slower at prefill sizes, 16 slower from 256 tokens on; whole experts' token
   // lists of up to 128 tokens, MMA N 256 over two issuers, measured slower at 4096 tokens: 13.0 against
   // 10.3 ms in the same build, whose down projection gained 17 % from lists of 85 positions). Down:
   // 16, which keeps its MMA N at 48 with two issuers and two accumulator buffers (32, N = 96 with one
-  // of either, measured 35 % slower at 64 tokens, 45 % at 512, 9 % at 4096; 8 slower than 16)
-  const long long wmax = k.fp4 ? 16 : 32, wmax_dn = 16;
+  // of either, measured 35 % slower at 64 tokens, 45 % at 512, 9 % at 4096; 8 slower than 16). With
+  // two terms of h (K3MOE_ACT_BF16H) 32 positions make the gate/up projection's N = 64 and stream each
+  // down record half as often (4096 tokens: down 7.6 -> 4.4 ms).
+  const long long wmax = k.fp4 ? 16 : 32, wmax_dn = (!k.fp4 && k.hterms == 2) ? 32 : 16;
   k.wgt = (int)(T < wmax ? T : wmax);
   k.wgt_dn = (int)(T < wmax_dn ? T : wmax_dn);
   k.rsplit = (int)router_splits(c, T);

@@ -52,7 +52,7 @@ class DeviceLayer:
 
     def __init__(self, shape: synth.LayerShape, seed: int, layer: int = 0, zipf_s: float | None = None,
                  x_dtype: str = "bf16", stride: int | None = None, pack: bool = True, score: str = "softmax",
-                 shared_format: str = "mxfp4"):
+                 shared_format: str = "mxfp4", act: str = "exact"):
         import torch
         import mxfp4_routed_expert_k3moe_gb300 as k3
         self.shape, self.seed, self.layer, self.x_dtype, self.score = shape, seed, layer, x_dtype, score
@@ -79,7 +79,8 @@ class DeviceLayer:
                                   score_func=k3.SCORE_SOFTMAX if score == "softmax" else k3.SCORE_SIGMOID_BIAS,
                                   record_order=k3.ORDER_DEVICE if pack else k3.ORDER_STORED,
                                   shared_format=k3.SHARED_BF16 if shared_format == "bf16" else k3.SHARED_MXFP4,
-                                  shared_stride=self.sstride)
+                                  shared_stride=self.sstride,
+                                  act_mode=k3.ACT_BF16H if act == "bf16h" else k3.ACT_EXACT)
         if pack:
             k3.pack_records(self.cfg, self.routed, E)
             if S and shared_format == "mxfp4":

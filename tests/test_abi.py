@@ -71,6 +71,7 @@ def test_workspace_never_shrinks_as_tokens_grow(x_dtype):
     ("record_order", 7, k3.ERR_INVALID_ARGUMENT),
     ("shared_format", 7, k3.ERR_INVALID_ARGUMENT),
     ("act_mode", k3.ACT_MXFP4, k3.ERR_UNSUPPORTED),
+    ("act_mode", 3, k3.ERR_INVALID_ARGUMENT),
     ("record_order", k3.ORDER_STORED, k3.ERR_UNSUPPORTED),        # records never packed are refused
 ])
 def test_invalid_config_rejected_on_host(field, value, code):

@@ -161,6 +161,40 @@ def test_layer_prefill_4096_sampled():
     check_layer(L, 4096, sample=[0, 1, 777, 2048, 4095])
 
 
+# ------------------------------------------------------------------ h as two E4M3 terms (K3MOE_ACT_BF16H)
+
+@pytest.mark.parametrize("x_dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("T", [2, 3, 37, 600])
+def test_layer_bf16h_mid(x_dtype, T):
+    """The bf16-class h mode against the exact oracle at the same 2e-3 bound: 2 tokens take the exact
+    E2M1 form, from 3 on h enters as two E4M3 terms with 32-position down work groups (600: from 256
+    on, with x's terms in position order)."""
+    L = DeviceLayer(MID, seed=40 + T, x_dtype=x_dtype, act="bf16h")
+    err = check_layer(L, T)
+    if T < 3:
+        assert err < 1e-4
+
+
+def test_layer_bf16h_k3_prefill_sampled():
+    """Indices and gates of all 1024 tokens at the K3 shape, y of five."""
+    L = DeviceLayer(synth.K3, seed=41, act="bf16h")
+    check_layer(L, 1024, sample=[0, 3, 511, 800, 1023])
+
+
+def test_expert_ffn_bf16h_given_routing():
+    L = DeviceLayer(MID, seed=42, x_dtype="f32", act="bf16h")
+    T = 300
+    xh, xd = L.tokens(T)
+    rng = np.random.default_rng(4)
+    idx = np.stack([rng.choice(MID.n_routed, MID.top_k, replace=False) for _ in range(T)]).astype(np.int32)
+    w = rng.random((T, MID.top_k)).astype(np.float32)
+    y = torch.empty((T, MID.d_model), dtype=torch.float32, device="cuda")
+    ws = torch.zeros(k3.workspace_bytes(L.cfg, T), dtype=torch.uint8, device="cuda")
+    k3.expert_ffn(L.cfg, xd, T, torch.from_numpy(idx).cuda(), torch.from_numpy(w).cuda(), L.routed, L.shared, y, ws)
+    assert k3.check_device_status(ws) == k3.OK
+    assert rel_err(y.cpu().numpy(), L.oracle_ffn(xh, idx, w)) <= REL_TOL
+
+
 # ------------------------------------------------------------------ separate entry points
 
 
