@@ -250,10 +250,12 @@ __device__ __forceinline__ bool b_row(const TcArgs& a, const Item& it, int n, co
 }
 
 // ------------------------------------------------------------------------------- the kernel
-// Shared memory of a stage: [A tiles: ch x 16 KB][B tiles: ch x b_bytes][scale words: ch x 1 KB].
-// Scale words of a chunk: 512 bytes for the 128 weight rows, then 512 for the B rows; the word of
-// row 32c + i (4 E8M0 bytes, one per 32-block of the chunk) sits at byte 16 i + 4 c, the layout
-// that the 32x128b.warpx4 copy spreads to TMEM lane 32q + i, column c of every quarter q.
+// Shared memory of a stage: [A tiles: ch x 16 KB][B tiles: ch x b_bytes][scale words: ch x wpc x 1 KB].
+// Scale words: the weight rows' words of every chunk first (word h of chunk cc at 512 (cc wpc + h),
+// so that one bulk copy brings them all: they are contiguous in the device order too), then the B
+// rows' (word h of chunk cc at 512 (ch wpc + cc wpc + h)). In a 512-byte group the word of row
+// 32c + i (4 E8M0 bytes, one per 32-block) sits at byte 16 i + 4 c, the layout that the
+// 32x128b.warpx4 copy spreads to TMEM lane 32q + i, column c of every quarter q.
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     k_tc(const __grid_constant__ CUtensorMap map_r0, const __grid_constant__ CUtensorMap map_r1,
@@ -354,9 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t* st = smem + (size_t)s * a.stage_bytes;
       mbar_expect_tx(su32(&ctl->full[s]), (tx_chunk + 512 * wpc) * CH);
       tma_load_4d(su32(st), map, 0, ia.mt * 128, j, ecoord, su32(&ctl->full[s]), pol);
-      for (int cc = 0; cc < CH; ++cc)
-        bulk_load(su32(st + sf_off + cc * a.sf_bytes), atile + (size_t)512 * wpc * (j + cc), 512 * wpc,
-                  su32(&ctl->full[s]), pol);
+      bulk_load(su32(st + sf_off), atile + (size_t)512 * wpc * j, 512 * wpc * CH, su32(&ctl->full[s]), pol);
     };
     // prologue: work groups of the first kEpRing items and tokens of the first two, waited for here
     for (int r = 0; r < kEpRing; ++r) fetch_wg(blockIdx.x + (long long)r * gridDim.x, r);
@@ -445,17 +445,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* st = smem + (size_t)s * a.stage_bytes;
         if (lane == 0) {
           if (g >= pre) issue_a(it, j, s);
-          if (a.tma_b) {  // the work group's B rows: n_tile rows from position pos0 on
+          if (a.tma_b) {  // the work group's B rows of the stage's chunks: n_tile rows from position pos0 on
             mbar_expect_tx_only(su32(&ctl->full[s]), (uint32_t)(a.n_tile * 128 * CH));
-            for (int cc = 0; cc < CH; ++cc)
-              tma_load_2d(su32(st + b_off + cc * a.b_bytes), &map_b, (j + cc) * 128, it.wg.pos0 * a.terms,
-                          su32(&ctl->full[s]));
+            tma_load_3d(su32(st + b_off), &map_b, 0, it.wg.pos0 * a.terms, j, su32(&ctl->full[s]));
           }
         }
         for (int cc = 0; cc < CH; ++cc) {
           const int jj = j + cc;
-          const uint32_t sb = su32(st + b_off + cc * a.b_bytes), sc = su32(st + sf_off + cc * a.sf_bytes);
-          // scale words: A word h at sc + 512 h (bulk copy above), B word h at sc + 512 (wpc + h)
+          const uint32_t sb = su32(st + b_off + cc * a.b_bytes);
+          const uint32_t sc = su32(st + sf_off) + 512 * wpc * (CH + cc);  // B rows' scale words of the chunk
           // codes: lane = 16-byte segment k16 of row 4 it + lane / 8, so that one copy instruction
           // reads four 128-byte rows (one row per lane read 32 rows: a quarter of the L1 rate)
           // (four rows per lane at a time: their table reads are issued before the copies)
@@ -475,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int q = 0; q < kMaxN / 32; ++q)
             if (bscales[q])
               for (int h = 0; h < wpc; ++h)
-                cp4(sc + 512 * (wpc + h) + 16 * lane + 4 * q, bscales[q] + 4 * (wpc * jj + h), 4);
+                cp4(sc + 512 * h + 16 * lane + 4 * q, bscales[q] + 4 * (wpc * jj + h), 4);
         }
         cp_arrive_noinc(su32(&ctl->full[s]));
       }
@@ -531,8 +529,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // The scale slot belongs to the stage: it is rewritten only after the stage's previous MMAs
             // completed (the loader refilled the stage after its empty barrier).
             const uint32_t col = tmem + (uint32_t)(a.sf_base + (s * CH + cc) * a.sf_slot);
-            const uint64_t dsc = dsa0 + so + (uint64_t)(cc * (a.sf_bytes >> 4));
-            for (int w2 = 0; w2 < 2 * wpc; ++w2) tc_cp_32x128b_x4(col + 16 * w2, dsc + (uint64_t)(w2 * (512 >> 4)));
+            for (int w2 = 0; w2 < 2 * wpc; ++w2) {
+              const int grp = w2 < wpc ? cc * wpc + w2 : (CH + cc) * wpc + (w2 - wpc);  // 512-byte group
+              tc_cp_32x128b_x4(col + 16 * w2, dsa0 + so + (uint64_t)(grp * (512 >> 4)));
+            }
             const uint64_t da = da0 + so + (uint64_t)(cc * (kATile >> 4)), db = db0 + so + (uint64_t)(cc * bb16);
             if (a.fp4) {
               // K = 64 per MMA; MMA k uses scale word k / 2, byte pair 2 (k % 2)
@@ -1055,14 +1055,15 @@ TcArgs base_args(const Cfg& c, const Ws& ws, const uint8_t* routed, const uint8_
 }
 
 // Map over `rows` activation rows of `row_bytes` E4M3 codes (the terms of x in position order, or of
-// h): boxes of 128 bytes x n_tile rows, the B tile of one chunk of a work group.
-cudaError_t rows_map(CUtensorMap* m, const void* base, long long row_bytes, long long rows, int n_tile) {
+// h) as {128 bytes, rows, 128-byte chunks}: a box of 128 bytes x n_tile rows x ch chunks is the B
+// tiles of one stage of a work group, chunk after chunk (n_tile x 128 bytes each).
+cudaError_t rows_map(CUtensorMap* m, const void* base, long long row_bytes, long long rows, int n_tile, int ch) {
   cudaError_t e = get_encode();
   if (e != cudaSuccess) return e;
-  cuuint64_t gdim[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
-  cuuint64_t gstr[1] = {(cuuint64_t)row_bytes};
-  cuuint32_t box[2] = {128, (cuuint32_t)n_tile}, es[2] = {1, 1};
-  if (g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), gdim, gstr, box, es,
+  cuuint64_t gdim[3] = {128, (cuuint64_t)rows, (cuuint64_t)(row_bytes / 128)};
+  cuuint64_t gstr[2] = {(cuuint64_t)row_bytes, 128};
+  cuuint32_t box[3] = {128, (cuuint32_t)n_tile, (cuuint32_t)ch}, es[3] = {1, 1, 1};
+  if (g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), gdim, gstr, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
@@ -1088,7 +1089,7 @@ cudaError_t launch_gateup(const Cfg& c, const Ws& ws, const uint8_t* routed, con
   // x terms in position order (c.gx): a work group's B rows are rows pos0 * xterms .. of xp
   CUtensorMap mx = m.gr;
   if (c.gx) {
-    if ((e = rows_map(&mx, ws.xp, c.d, T * (c.k + c.S) * c.xterms, a.n_tile)) != cudaSuccess) return e;
+    if ((e = rows_map(&mx, ws.xp, c.d, T * (c.k + c.S) * c.xterms, a.n_tile, a.ch)) != cudaSuccess) return e;
     a.tma_b = 1;
   }
   e = launch_tc<GATEUP>(a, m.gr, m.ur, m.gs, m.us, mx, wg_max * 2 * (c.f / 128), st);
@@ -1114,7 +1115,7 @@ cudaError_t launch_down(const Cfg& c, const Ws& ws, const uint8_t* routed, const
   // are not read)
   CUtensorMap mh = m.dr;
   if (!c.fp4) {
-    if ((e = rows_map(&mh, ws.hq, c.f, T * (c.k + c.S) * c.hterms, a.n_tile)) != cudaSuccess) return e;
+    if ((e = rows_map(&mh, ws.hq, c.f, T * (c.k + c.S) * c.hterms, a.n_tile, a.ch)) != cudaSuccess) return e;
     a.tma_b = 1;
   }
   e = launch_tc<DOWN>(a, m.dr, m.dr, m.ds, m.ds, mh, wg_max * (c.d / 128), st);
