@@ -256,7 +256,8 @@ __device__ __forceinline__ bool b_row(const TcArgs& a, const Item& it, int n, co
 // rows' (word h of chunk cc at 512 (ch wpc + cc wpc + h)). In a 512-byte group the word of row
 // 32c + i (4 E8M0 bytes, one per 32-block) sits at byte 16 i + 4 c, the layout that the
 // 32x128b.warpx4 copy spreads to TMEM lane 32q + i, column c of every quarter q.
-template <int MODE>
+// F4: the E2M1 form (a.fp4) as its own instance, so that each form's kernel holds only its own code.
+template <int MODE, bool F4>
 __global__ void __launch_bounds__(kThreads, 1)
     k_tc(const __grid_constant__ CUtensorMap map_r0, const __grid_constant__ CUtensorMap map_r1,
          const __grid_constant__ CUtensorMap map_s0, const __grid_constant__ CUtensorMap map_s1,
@@ -272,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&map_r1);
     prefetch_tmap(&map_s0);
     prefetch_tmap(&map_s1);
-    if (a.tma_b) prefetch_tmap(&map_b);
+    if (!F4 && a.tma_b) prefetch_tmap(&map_b);
   }
   // The gate/up kernel reads the routing, which the previous kernel writes. The down kernel's work
   // groups come from the routing kernel two launches back: it completed before the gate/up kernel
@@ -289,8 +290,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const long long n_items = (long long)n_wg * nmat * mtiles * a.parts;
   int* status = a.ws.ctrl;
   const int b_off = CH * kATile, sf_off = CH * (kATile + a.b_bytes);
-  const uint32_t tx_chunk = a.fp4 ? 128 * 128 : 128 * 64;  // bytes a chunk's tensor copy delivers
-  const int wpc = a.fp4 ? 2 : 1;                            // scale words per row per chunk
+  const uint32_t tx_chunk = F4 ? 128 * 128 : 128 * 64;  // bytes a chunk's tensor copy delivers
+  const int wpc = F4 ? 2 : 1;                            // scale words per row per chunk
 
   if (n_wg == 0) {  // nothing routed and no shared experts (k_combine writes y = 0)
     if (MODE == DOWN) pdl_wait();
@@ -416,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // to this loader's table, which the code copies below read, and the scale pointers of rows
       // lane + 32 q stay in registers
       const int kk = MODE == GATEUP ? c.d : c.f;
-      const long long row_bytes = a.fp4 ? kk / 2 : kk;
+      const long long row_bytes = F4 ? kk / 2 : kk;
       const uint8_t* bbase = MODE == GATEUP ? a.ws.xq : a.ws.hq;
       uint32_t* rtab = ctl->ld_row[lv];
       const int nrows = min(a.n_tile, it.wg.ntok * a.terms);  // rows past these are not read
@@ -445,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* st = smem + (size_t)s * a.stage_bytes;
         if (lane == 0) {
           if (g >= pre) issue_a(it, j, s);
-          if (a.tma_b) {  // the work group's B rows of the stage's chunks: n_tile rows from position pos0 on
+          if (!F4 && a.tma_b) {  // the work group's B rows of the stage's chunks: n_tile rows from position pos0 on
             mbar_expect_tx_only(su32(&ctl->full[s]), (uint32_t)(a.n_tile * 128 * CH));
             tma_load_3d(su32(st + b_off), &map_b, 0, it.wg.pos0 * a.terms, j, su32(&ctl->full[s]));
           }
@@ -458,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // reads four 128-byte rows (one row per lane read 32 rows: a quarter of the L1 rate)
           // (four rows per lane at a time: their table reads are issued before the copies)
           const int k16 = lane & 7;
-          for (int n0 = lane >> 3; n0 < nrows && !a.tma_b; n0 += 16) {
+          for (int n0 = lane >> 3; n0 < nrows && !(!F4 && a.tma_b); n0 += 16) {
             uint32_t r[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) r[u] = n0 + 4 * u < nrows ? rtab[n0 + 4 * u] : ~0u;
@@ -498,13 +499,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int w = warp - kWarpIss;
     if (lane == 0 && w < a.n_iss) {
       // instruction descriptor: A/B formats (mxf4: E2M1 = 1; mxf8f6f4: A E2M1 = 5, B E4M3 = 0), N, UE8M0, M
-      const uint32_t idesc = (a.fp4 ? ((1u << 7) | (1u << 10)) : (5u << 7)) | ((uint32_t)(a.n_tile >> 3) << 17) |
+      const uint32_t idesc = (F4 ? ((1u << 7) | (1u << 10)) : (5u << 7)) | ((uint32_t)(a.n_tile >> 3) << 17) |
                              (1u << 23) | ((uint32_t)(128 >> 4) << 24);
       // descriptors of stage 0, chunk 0; stage s / chunk cc add their byte offsets / 16 to the
       // start-address field
       const uint64_t da0 = sw128_desc(su32(smem)), db0 = sw128_desc(su32(smem) + b_off);
       const uint64_t dsa0 = sf_desc(su32(smem) + sf_off);
-      const int wpc = a.fp4 ? 2 : 1;
+      const int wpc = F4 ? 2 : 1;
       const uint32_t st16 = (uint32_t)a.stage_bytes >> 4, bb16 = (uint32_t)a.b_bytes >> 4;
       long long i = 0;
       Ring rg;
@@ -534,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc_cp_32x128b_x4(col + 16 * w2, dsa0 + so + (uint64_t)(grp * (512 >> 4)));
             }
             const uint64_t da = da0 + so + (uint64_t)(cc * (kATile >> 4)), db = db0 + so + (uint64_t)(cc * bb16);
-            if (a.fp4) {
+            if (F4) {
               // K = 64 per MMA; MMA k uses scale word k / 2, byte pair 2 (k % 2)
 #pragma unroll
               for (int k = 0; k < 4; ++k) {
@@ -670,7 +671,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bar_sync(1, 128);
         const int p = q & 1;
         const int nb = c.f / 32, blk = 4 * it.mt + 2 * it.mat + p;  // 32-block of h
-        if (c.fp4) {
+        if (F4) {
           for (int i = q >> 1; i < it.wg.ntok; i += 2) {
             const float g = xb[(p * a.xb_tok + i) * kXb + lane], u = xb[((p + 2) * a.xb_tok + i) * kXb + lane];
             const long long pos = it.wg.pos0 + i;
@@ -958,13 +959,16 @@ cudaError_t launch_tc(const TcArgs& a, const CUtensorMap& r0, const CUtensorMap&
   const size_t smem = (size_t)a.stages * a.stage_bytes + ctl_bytes() + xb_bytes(a) + 1024;
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_tc<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    cudaError_t e = cudaFuncSetAttribute(k_tc<MODE, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k_tc<MODE, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (e != cudaSuccess) return e;
     attr = true;
   }
   long long grid = items_max < g_sms ? items_max : g_sms;
   if (grid < 1) grid = 1;
-  return launch_pdl(k_tc<MODE>, dim3((unsigned)grid), dim3(kThreads), smem, st, r0, r1, s0, s1, b, a);
+  return launch_pdl(a.fp4 ? k_tc<MODE, true> : k_tc<MODE, false>, dim3((unsigned)grid), dim3(kThreads), smem, st, r0,
+                    r1, s0, s1, b, a);
 }
 
 // Tile geometry for an MMA N of n_tile: TMEM holds two accumulator buffers per issuer and then one
