@@ -264,7 +264,11 @@ __global__ void __launch_bounds__(kThreads, 1)
          const __grid_constant__ CUtensorMap map_b, TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  const int S = a.stages, CH = a.ch;
+  // the E2M1 form's tile shape is fixed (launch_tc checks it): one chunk per stage, three issuers with
+  // two accumulator buffers of 16 columns, MMA N = 16, 8 terms per activation row
+  const int S = a.stages, CH = F4 ? 1 : a.ch;
+  const int n_iss = F4 ? 3 : a.n_iss, n_buf = F4 ? 2 : a.n_buf, n_acc = F4 ? 1 : a.n_acc;
+  const int acc_cols = F4 ? 16 : a.acc_cols, n_tile = F4 ? 16 : a.n_tile, terms = F4 ? 8 : a.terms;
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + (size_t)S * a.stage_bytes);
   const Cfg& c = a.c;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -308,11 +312,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(su32(&ctl->full[s]), 1 + 32);
       mbar_init(su32(&ctl->empty[s]), 1);
     }
-    for (int b = 0; b < a.n_buf; ++b) {
-      mbar_init(su32(&ctl->acc_full[b]), a.n_iss);
+    for (int b = 0; b < n_buf; ++b) {
+      mbar_init(su32(&ctl->acc_full[b]), n_iss);
       mbar_init(su32(&ctl->acc_empty[b]), 128);
     }
-    mbar_init(su32(&ctl->drain), a.n_iss);
+    mbar_init(su32(&ctl->drain), n_iss);
     ctl->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -403,9 +407,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int q = 0; q < kMaxN / 32; ++q) {
         const int n = lane + 32 * q;
-        const int i = n / a.terms;
+        const int i = n / terms;
         bsrc[q] = -1;
-        if (n < a.n_tile && i < it.wg.ntok)
+        if (n < n_tile && i < it.wg.ntok)
           bsrc[q] = MODE == GATEUP ? ctl->ld_tok[lv][slot][i] : it.wg.pos0 + i;
       }
       __syncwarp();
@@ -420,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const long long row_bytes = F4 ? kk / 2 : kk;
       const uint8_t* bbase = MODE == GATEUP ? a.ws.xq : a.ws.hq;
       uint32_t* rtab = ctl->ld_row[lv];
-      const int nrows = min(a.n_tile, it.wg.ntok * a.terms);  // rows past these are not read
+      const int nrows = min(n_tile, it.wg.ntok * terms);  // rows past these are not read
       const uint8_t* bscales[kMaxN / 32];
 #pragma unroll
       for (int q = 0; q < kMaxN / 32; ++q) {
@@ -428,10 +432,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n = lane + 32 * q;
         uint32_t r = ~0u;  // (rows < 3 * 2^30: positions < 2^30, at most 3 terms above 2 tokens)
         if (bsrc[q] >= 0) {
-          r = (uint32_t)bsrc[q] * (uint32_t)a.terms + (uint32_t)(n - (n / a.terms) * a.terms);
+          r = (uint32_t)bsrc[q] * (uint32_t)terms + (uint32_t)(n - (n / terms) * terms);
           bscales[q] = (MODE == GATEUP ? a.ws.xs : a.ws.hs) + (long long)r * (kk / 32);
         }
-        if (n < a.n_tile) rtab[n] = r;
+        if (n < n_tile) rtab[n] = r;
       }
       __syncwarp();
       for (int j = it.j0; j < it.j1; j += CH, rg.next(S)) {
@@ -447,8 +451,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           if (g >= pre) issue_a(it, j, s);
           if (!F4 && a.tma_b) {  // the work group's B rows of the stage's chunks: n_tile rows from position pos0 on
-            mbar_expect_tx_only(su32(&ctl->full[s]), (uint32_t)(a.n_tile * 128 * CH));
-            tma_load_3d(su32(st + b_off), &map_b, 0, it.wg.pos0 * a.terms, j, su32(&ctl->full[s]));
+            mbar_expect_tx_only(su32(&ctl->full[s]), (uint32_t)(n_tile * 128 * CH));
+            tma_load_3d(su32(st + b_off), &map_b, 0, it.wg.pos0 * terms, j, su32(&ctl->full[s]));
           }
         }
         for (int cc = 0; cc < CH; ++cc) {
@@ -497,9 +501,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= kWarpIss) {
     // ------------------------------------------------------------ MMA issuers
     const int w = warp - kWarpIss;
-    if (lane == 0 && w < a.n_iss) {
+    if (lane == 0 && w < n_iss) {
       // instruction descriptor: A/B formats (mxf4: E2M1 = 1; mxf8f6f4: A E2M1 = 5, B E4M3 = 0), N, UE8M0, M
-      const uint32_t idesc = (F4 ? ((1u << 7) | (1u << 10)) : (5u << 7)) | ((uint32_t)(a.n_tile >> 3) << 17) |
+      const uint32_t idesc = (F4 ? ((1u << 7) | (1u << 10)) : (5u << 7)) | ((uint32_t)(n_tile >> 3) << 17) |
                              (1u << 23) | ((uint32_t)(128 >> 4) << 24);
       // descriptors of stage 0, chunk 0; stage s / chunk cc add their byte offsets / 16 to the
       // start-address field
@@ -512,15 +516,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       Item it;
       bool ok = true;
       for (long long ii = blockIdx.x; ok && item_geom<MODE>(a, ii, n_items, it); ii += gridDim.x, ++i) {
-        const long long rb = i / a.n_buf;  // the buffer's round
-        const int b = (int)(i - rb * a.n_buf);
+        const long long rb = i / n_buf;  // the buffer's round
+        const int b = (int)(i - rb * n_buf);
         if (rb > 0 && !wait_bar(su32(&ctl->acc_empty[b]), (uint32_t)((rb - 1) & 1), ctl, status, c.wait_limit)) break;
         tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)((b * a.n_iss + w) * a.n_acc * a.acc_cols);
+        const uint32_t d = tmem + (uint32_t)((b * n_iss + w) * n_acc * acc_cols);
         uint32_t started = 0;  // bit h: accumulator h already holds a partial sum of this item
         for (int j = it.j0; j < it.j1; j += CH, rg.next(S)) {
           const int s = rg.s;
-          if (s % a.n_iss != w) continue;
+          if (s % n_iss != w) continue;
           if (!wait_bar(su32(&ctl->full[s]), rg.ph, ctl, status, c.wait_limit)) { ok = false; break; }
           tc_fence_after();
           fence_async_smem();  // B rows and scale words arrived through cp.async (generic proxy)
@@ -547,8 +551,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
 #pragma unroll
               for (int k = 0; k < 4; ++k) {
-                const int h = k & (a.n_acc - 1);
-                tc_mma(d + (uint32_t)(h * a.acc_cols), da + 2 * k, db + 2 * k,
+                const int h = k & (n_acc - 1);
+                tc_mma(d + (uint32_t)(h * acc_cols), da + 2 * k, db + 2 * k,
                        idesc | ((uint32_t)k << 4) | ((uint32_t)k << 29), col, col + 16, (started >> h) & 1u);
                 started |= 1u << h;
               }
@@ -594,8 +598,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       fetch_wg(ii + (long long)kEpRing * gridDim.x, slot);  // reuses the slot just read
       const int nst = (it.j1 - it.j0) / CH;  // stages of the item
-      const long long rb = i / a.n_buf;
-      const int b = (int)(i - rb * a.n_buf);
+      const long long rb = i / n_buf;
+      const int b = (int)(i - rb * n_buf);
       bool okw =
           __all_sync(0xffffffffu, wait_bar(su32(&ctl->acc_full[b]), (uint32_t)(rb & 1), ctl, status, c.wait_limit));
       // gate/up: the four warps agree (they meet at a barrier below); this also keeps the exchange
@@ -604,18 +608,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!okw) break;
       tc_fence_after();
       const int row = it.mt * 128 + 32 * q + lane;
-      const int ncols = it.wg.ntok * a.terms;
+      const int ncols = it.wg.ntok * terms;
       // issuers that received stages: owners (slot mod n_iss) of slots g0, g0 + 1, ...; their partial
       // sums are added in issuer order
       unsigned mask = 0;
-      for (int t = 0, sl = g0; t < nst && t < S; ++t, sl = (sl + 1 == S) ? 0 : sl + 1) mask |= 1u << (sl % a.n_iss);
-      const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * a.n_iss * a.acc_cols);
+      for (int t = 0, sl = g0; t < nst && t < S; ++t, sl = (sl + 1 == S) ? 0 : sl + 1) mask |= 1u << (sl % n_iss);
+      const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * n_iss * acc_cols);
       float run = 0.0f;
       bool nan_row = false;
       int tk = 0, jt = 0;  // token and term of the current column
       // at the smallest N (four issuers of 16 columns, one token's terms) one load takes all partials:
       // every tensor-memory load waits in the tensor pipe with the MMAs, so fewer loads cost less
-      const bool one_load = a.n_iss * a.acc_cols == 64 && ncols <= 16;
+      const bool one_load = n_iss * acc_cols == 64 && ncols <= 16;
       for (int cb = 0; cb < ncols; cb += 16) {
         uint32_t u[kMaxIss][16];
         if (one_load) {
@@ -623,7 +627,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
 #pragma unroll
           for (int w = 0; w < kMaxIss; ++w)
-            if ((mask >> w) & 1u) tc_ld16(lane_base + (uint32_t)(w * a.acc_cols + cb), u[w]);
+            if ((mask >> w) & 1u) tc_ld16(lane_base + (uint32_t)(w * acc_cols + cb), u[w]);
         }
         tc_wait_ld();
         if (cb + 16 >= ncols) {  // buffer read completely: hand it back
@@ -644,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int col = cb + cc;
           if (col < ncols) {
             run += v[cc];
-            if (++jt == a.terms) {
+            if (++jt == terms) {
               jt = 0;
               const long long pos = it.wg.pos0 + tk;
               nan_row |= (run != run);
@@ -956,6 +960,10 @@ template <int MODE>
 cudaError_t launch_tc(const TcArgs& a, const CUtensorMap& r0, const CUtensorMap& r1, const CUtensorMap& s0,
                       const CUtensorMap& s1, const CUtensorMap& b, long long items_max, cudaStream_t st) {
   if (items_max >= (1LL << 31)) return cudaErrorInvalidValue;  // item indices are decomposed in 32 bits
+  // the E2M1 instance compiles its tile shape in
+  if (a.fp4 && (a.ch != 1 || a.n_iss != 3 || a.n_buf != 2 || a.n_acc != 1 || a.acc_cols != 16 || a.n_tile != 16 ||
+                a.terms != 8))
+    return cudaErrorInvalidConfiguration;
   const size_t smem = (size_t)a.stages * a.stage_bytes + ctl_bytes() + xb_bytes(a) + 1024;
   static bool attr = false;
   if (!attr) {
