@@ -256,19 +256,25 @@ __device__ __forceinline__ bool b_row(const TcArgs& a, const Item& it, int n, co
 // rows' (word h of chunk cc at 512 (ch wpc + cc wpc + h)). In a 512-byte group the word of row
 // 32c + i (4 E8M0 bytes, one per 32-block) sits at byte 16 i + 4 c, the layout that the
 // 32x128b.warpx4 copy spreads to TMEM lane 32q + i, column c of every quarter q.
-// F4: the E2M1 form (a.fp4) as its own instance, so that each form's kernel holds only its own code.
-template <int MODE, bool F4>
+// FORM: the E2M1 form (a.fp4) and the E4M3 form are separate instances, so that each kernel holds only
+// its own form's code; the E2M1 form's tile shape, and the E4M3 one of two-term rows with N = 64 (32
+// positions or tokens), are compile-time constants in their instances (launch_tc picks and checks).
+enum { kFormE4M3 = 0, kFormE2M1 = 1, kFormE4M3N64 = 2 };
+template <int MODE, int FORM>
 __global__ void __launch_bounds__(kThreads, 1)
     k_tc(const __grid_constant__ CUtensorMap map_r0, const __grid_constant__ CUtensorMap map_r1,
          const __grid_constant__ CUtensorMap map_s0, const __grid_constant__ CUtensorMap map_s1,
          const __grid_constant__ CUtensorMap map_b, TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  // the E2M1 form's tile shape is fixed (launch_tc checks it): one chunk per stage, three issuers with
-  // two accumulator buffers of 16 columns, MMA N = 16, 8 terms per activation row
-  const int S = a.stages, CH = F4 ? 1 : a.ch;
-  const int n_iss = F4 ? 3 : a.n_iss, n_buf = F4 ? 2 : a.n_buf, n_acc = F4 ? 1 : a.n_acc;
-  const int acc_cols = F4 ? 16 : a.acc_cols, n_tile = F4 ? 16 : a.n_tile, terms = F4 ? 8 : a.terms;
+  // fixed tile shapes: E2M1 one chunk per stage, three issuers with two accumulator buffers of 16
+  // columns, N = 16, 8 terms per activation row; E4M3 N64 two chunks per stage, two issuers with two
+  // buffers of 64 columns, N = 64, 2 terms
+  constexpr bool F4 = FORM == kFormE2M1, N64 = FORM == kFormE4M3N64;
+  const int S = a.stages, CH = F4 ? 1 : (N64 ? 2 : a.ch);
+  const int n_iss = F4 ? 3 : (N64 ? 2 : a.n_iss), n_buf = F4 || N64 ? 2 : a.n_buf, n_acc = F4 || N64 ? 1 : a.n_acc;
+  const int acc_cols = F4 ? 16 : (N64 ? 64 : a.acc_cols), n_tile = F4 ? 16 : (N64 ? 64 : a.n_tile);
+  const int terms = F4 ? 8 : (N64 ? 2 : a.terms);
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + (size_t)S * a.stage_bytes);
   const Cfg& c = a.c;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -960,23 +966,27 @@ template <int MODE>
 cudaError_t launch_tc(const TcArgs& a, const CUtensorMap& r0, const CUtensorMap& r1, const CUtensorMap& s0,
                       const CUtensorMap& s1, const CUtensorMap& b, long long items_max, cudaStream_t st) {
   if (items_max >= (1LL << 31)) return cudaErrorInvalidValue;  // item indices are decomposed in 32 bits
-  // the E2M1 instance compiles its tile shape in
+  // the E2M1 instance compiles its tile shape in; so does the E4M3 N64 one, taken when the shape is its
+  const bool n64 = !a.fp4 && a.ch == 2 && a.n_iss == 2 && a.n_buf == 2 && a.n_acc == 1 && a.acc_cols == 64 &&
+                   a.n_tile == 64 && a.terms == 2;
   if (a.fp4 && (a.ch != 1 || a.n_iss != 3 || a.n_buf != 2 || a.n_acc != 1 || a.acc_cols != 16 || a.n_tile != 16 ||
                 a.terms != 8))
     return cudaErrorInvalidConfiguration;
   const size_t smem = (size_t)a.stages * a.stage_bytes + ctl_bytes() + xb_bytes(a) + 1024;
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_tc<MODE, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    cudaError_t e = cudaFuncSetAttribute(k_tc<MODE, kFormE2M1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(k_tc<MODE, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+      e = cudaFuncSetAttribute(k_tc<MODE, kFormE4M3>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k_tc<MODE, kFormE4M3N64>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (e != cudaSuccess) return e;
     attr = true;
   }
   long long grid = items_max < g_sms ? items_max : g_sms;
   if (grid < 1) grid = 1;
-  return launch_pdl(a.fp4 ? k_tc<MODE, true> : k_tc<MODE, false>, dim3((unsigned)grid), dim3(kThreads), smem, st, r0,
-                    r1, s0, s1, b, a);
+  return launch_pdl(a.fp4 ? k_tc<MODE, kFormE2M1> : (n64 ? k_tc<MODE, kFormE4M3N64> : k_tc<MODE, kFormE4M3>),
+                    dim3((unsigned)grid), dim3(kThreads), smem, st, r0, r1, s0, s1, b, a);
 }
 
 // Tile geometry for an MMA N of n_tile: TMEM holds two accumulator buffers per issuer and then one
