@@ -267,11 +267,11 @@ __global__ void __launch_bounds__(kThreads, 1)
          const __grid_constant__ CUtensorMap map_b, TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  // fixed tile shapes: E2M1 one chunk per stage, three issuers with two accumulator buffers of 16
-  // columns, N = 16, 8 terms per activation row; E4M3 N64 two chunks per stage, two issuers with two
-  // buffers of 64 columns, N = 64, 2 terms
+  // fixed tile shapes: E2M1 six stages of one chunk, three issuers with two accumulator buffers of 16
+  // columns, N = 16, 8 terms per activation row; E4M3 N64 four stages of two chunks, two issuers with
+  // two buffers of 64 columns, N = 64, 2 terms (the stages: as many as tensor memory holds scale slots)
   constexpr bool F4 = FORM == kFormE2M1, N64 = FORM == kFormE4M3N64;
-  const int S = a.stages, CH = F4 ? 1 : (N64 ? 2 : a.ch);
+  const int S = F4 ? 6 : (N64 ? 4 : a.stages), CH = F4 ? 1 : (N64 ? 2 : a.ch);
   const int n_iss = F4 ? 3 : (N64 ? 2 : a.n_iss), n_buf = F4 || N64 ? 2 : a.n_buf, n_acc = F4 || N64 ? 1 : a.n_acc;
   const int acc_cols = F4 ? 16 : (N64 ? 64 : a.acc_cols), n_tile = F4 ? 16 : (N64 ? 64 : a.n_tile);
   const int terms = F4 ? 8 : (N64 ? 2 : a.terms);
@@ -967,10 +967,10 @@ cudaError_t launch_tc(const TcArgs& a, const CUtensorMap& r0, const CUtensorMap&
                       const CUtensorMap& s1, const CUtensorMap& b, long long items_max, cudaStream_t st) {
   if (items_max >= (1LL << 31)) return cudaErrorInvalidValue;  // item indices are decomposed in 32 bits
   // the E2M1 instance compiles its tile shape in; so does the E4M3 N64 one, taken when the shape is its
-  const bool n64 = !a.fp4 && a.ch == 2 && a.n_iss == 2 && a.n_buf == 2 && a.n_acc == 1 && a.acc_cols == 64 &&
-                   a.n_tile == 64 && a.terms == 2;
-  if (a.fp4 && (a.ch != 1 || a.n_iss != 3 || a.n_buf != 2 || a.n_acc != 1 || a.acc_cols != 16 || a.n_tile != 16 ||
-                a.terms != 8))
+  const bool n64 = !a.fp4 && a.stages == 4 && a.ch == 2 && a.n_iss == 2 && a.n_buf == 2 && a.n_acc == 1 &&
+                   a.acc_cols == 64 && a.n_tile == 64 && a.terms == 2;
+  if (a.fp4 && (a.stages != 6 || a.ch != 1 || a.n_iss != 3 || a.n_buf != 2 || a.n_acc != 1 || a.acc_cols != 16 ||
+                a.n_tile != 16 || a.terms != 8))
     return cudaErrorInvalidConfiguration;
   const size_t smem = (size_t)a.stages * a.stage_bytes + ctl_bytes() + xb_bytes(a) + 1024;
   static bool attr = false;
