@@ -341,14 +341,15 @@ __device__ void topk_permute_one_token(const Cfg& c, const Ws& ws, const float* 
 // Logits from the tensor cores carry the rounding of the MMA's fp32 accumulation (measured ~1e-5 at
 // d_model 7168, against ~1e-6 for fp32 dot products), enough to swap two experts whose logits differ
 // by a little more than 1e-5, and to move the gates by ~1e-5. Before the final selection of a token,
-// every expert whose ranked value (logit, or sigmoid + selection bias) is at least the k-th value
-// minus kRefineMargin (the selection, and the experts that could take its last places) is recomputed
-// on the CUDA cores and written over the partial logits (part 0 takes the value, the other parts
-// zero, so the parts still add up to it exactly). No expert below the margin can enter the selection,
-// and the gates come from the recomputed logits. (Recomputing only the experts near the k-th value
-// and selected neighbours closer than the margin keeps the selection exact but left gates 1.4e-5 off
-// at 4096 tokens.) The
-// whole CTA computes the candidates together, kRefineBatch at a time: thread i sums the fp32 products
+// the experts whose place could depend on that rounding are recomputed on the CUDA cores and written
+// over the partial logits (part 0 takes the value, the other parts zero, so the parts still add up to
+// it exactly): every expert whose ranked value (logit, or sigmoid + selection bias) lies within
+// kRefineMargin of the k-th value, and every selected expert within kRefineMargin of a selected
+// neighbour. Every other selected expert stays more than the margin above the k-th value and its
+// neighbours, every other expert more than the margin below, so the selection and its order are those
+// of exact logits; the gates of the experts not recomputed carry the tensor cores' rounding (~1e-5).
+// (Recomputing every selected expert as well, for gates to ~1e-6, took 23 us per token at 64 tokens.)
+// The whole CTA computes the candidates together, kRefineBatch at a time: thread i sums the fp32 products
 // of its d / blockDim.x consecutive elements of x and of each candidate's fp32 router row, then the
 // warps' sums and the per-warp partials are added in order (+ the bias for the softmax score). If
 // more than blockDim.x experts lie within the margin (a token whose logits are all equal, x = 0), the
@@ -362,17 +363,29 @@ __device__ void refine_candidates_r(const Cfg& c, float* logits_t, long long ls,
                                     const unsigned long long* sel, int* s_cid, int* s_nc,
                                     float (*s_red)[kRefineBatch]) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  const float tau = key_logit(sel[c.k - 1]) - kRefineMargin;
+  const unsigned long long kth = sel[c.k - 1];
+  const float vk = key_logit(kth);
   unsigned long long key[R];
   load_keys<R, KZ, SIG>(c.E, logits_t, ls, np, sel_bias, key);
   if (threadIdx.x == 0) *s_nc = 0;
   __syncthreads();
+  // experts below the k-th within the margin
 #pragma unroll
   for (int q = 0; q < R; ++q)
-    if (key[q] != 0ull && key_logit(key[q]) >= tau) {
+    if (key[q] != 0ull && key[q] < kth && key_logit(key[q]) >= vk - kRefineMargin) {
       const int at = atomicAdd(s_nc, 1);
       if (at < (int)blockDim.x) s_cid[at] = key_expert(key[q]);
     }
+  // selected experts within the margin of the k-th value or of a selected neighbour (lane = rank)
+  if (warp == 0 && lane < c.k && sel[lane] != 0ull) {
+    const float v = key_logit(sel[lane]);
+    const bool near = v - vk <= kRefineMargin || (lane > 0 && key_logit(sel[lane - 1]) - v < kRefineMargin) ||
+                      (lane + 1 < c.k && v - key_logit(sel[lane + 1]) < kRefineMargin);
+    if (near) {
+      const int at = atomicAdd(s_nc, 1);
+      if (at < (int)blockDim.x) s_cid[at] = key_expert(sel[lane]);
+    }
+  }
   __syncthreads();
   const int n = *s_nc;
   if (n > (int)blockDim.x) return;

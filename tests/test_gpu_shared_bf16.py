@@ -7,7 +7,7 @@ import numpy as np
 import pytest
 
 import synth
-from harness import REL_TOL, DeviceLayer, gate_err, index_parity, rel_err
+from harness import REL_TOL, DeviceLayer, gate_err, index_parity, rel_err, GATE_TOL
 
 pytestmark = pytest.mark.gpu
 
@@ -40,7 +40,7 @@ def check(L: DeviceLayer, T: int, rows=None):
     ok, near, msg = index_parity(idx[rows], idx_ref, L.sel_keys(logits_ref), L.shape.top_k)
     assert ok, msg
     keep = [i for i in range(len(rows)) if i not in near]
-    assert gate_err(idx[rows][keep], w[rows][keep], idx_ref[keep], w_ref[keep]) < 1e-5
+    assert gate_err(idx[rows][keep], w[rows][keep], idx_ref[keep], w_ref[keep]) < GATE_TOL
     err = rel_err(y[rows][keep], y_ref[keep])
     assert err <= REL_TOL, err
     return err
