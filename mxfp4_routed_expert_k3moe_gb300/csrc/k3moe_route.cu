@@ -392,6 +392,55 @@ __device__ void refine_candidates_r(const Cfg& c, float* logits_t, long long ls,
   // this thread's slice of the reduction axis: [j0, j1), a multiple of 4 elements (d is a multiple of 128)
   const int per = ((c.d / 4 + blockDim.x - 1) / blockDim.x) * 4;
   const int j0 = min(c.d, (int)threadIdx.x * per), j1 = min(c.d, j0 + per);
+  // one or two candidates (the usual case) and a slice of at most kRefineSlice 4-element steps: each
+  // candidate's loads of the slice are all issued before its products (a loop over the steps waited
+  // for each in turn)
+  constexpr int kRefineSlice = 8;
+  if (n <= 2 && j1 - j0 <= 4 * kRefineSlice) {
+    for (int u = 0; u < n; ++u) {
+      float4 wv[kRefineSlice];
+#pragma unroll
+      for (int v = 0; v < kRefineSlice; ++v) {
+        const int j = j0 + 4 * v;
+        wv[v] = j < j1 ? __ldg(reinterpret_cast<const float4*>(W + (long long)s_cid[u] * c.d + j))
+                       : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      }
+      float acc = 0.0f;
+#pragma unroll
+      for (int v = 0; v < kRefineSlice; ++v) {
+        const int j = j0 + 4 * v;
+        if (j < j1) {  // the products in the order of the general loop below
+          float xv[4];
+          if (c.x_f32) {
+            const float4 q4 = *reinterpret_cast<const float4*>(xrow + 4 * j);
+            xv[0] = q4.x; xv[1] = q4.y; xv[2] = q4.z; xv[3] = q4.w;
+          } else {
+            const uint2 q2 = *reinterpret_cast<const uint2*>(xrow + 2 * j);
+            xv[0] = __uint_as_float(q2.x << 16); xv[1] = __uint_as_float(q2.x & 0xFFFF0000u);
+            xv[2] = __uint_as_float(q2.y << 16); xv[3] = __uint_as_float(q2.y & 0xFFFF0000u);
+          }
+          acc = fmaf(wv[v].x, xv[0], acc);
+          acc = fmaf(wv[v].y, xv[1], acc);
+          acc = fmaf(wv[v].z, xv[2], acc);
+          acc = fmaf(wv[v].w, xv[3], acc);
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if (lane == 0) s_red[warp][u] = acc;
+    }
+    __syncthreads();
+    if ((int)threadIdx.x < n) {
+      const int e = s_cid[threadIdx.x];
+      float v = 0.0f;
+      for (int w = 0; w < nw; ++w) v += s_red[w][threadIdx.x];
+      logits_t[e] = v + (logit_bias ? __ldg(&logit_bias[e]) : 0.0f);
+      for (int z = 1; z < np; ++z) logits_t[z * ls + e] = 0.0f;
+    }
+    __threadfence_block();
+    __syncthreads();
+    return;
+  }
   for (int b0 = 0; b0 < n; b0 += kRefineBatch) {
     const int nb = min(kRefineBatch, n - b0);
     float acc[kRefineBatch];
