@@ -183,6 +183,11 @@ K3MOE_API k3moe_status k3moe_prepare_router(const k3moe_config* cfg /* host */, 
  *            softmax; sigmoid score: added to the sigmoid scores for the selection only
  *   topk_idx [T, top_k] int32 out: expert ids, descending ranked value, ties to the lower id
  *   topk_w   [T, top_k] fp32 out: gates, summing to 1 per token
+ * Below 16 tokens the logits are fp32 dot products. From 16 tokens they come from the tensor cores
+ * (three bf16 parts of the weights; the accumulation rounds by ~1e-5 at d_model 7168); every expert
+ * whose place in the selection that rounding could decide is recomputed as an fp32 dot product, so
+ * the indices are those of fp32 logits, and the other selected experts' gates carry the rounding
+ * (measured below 2e-5).
  */
 K3MOE_API k3moe_status k3moe_route(const k3moe_config* cfg /* host */, const void* x, int64_t T,
                          const float* w_router, const uint16_t* w_router_parts, const float* bias,

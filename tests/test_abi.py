@@ -40,11 +40,13 @@ def test_record_and_workspace_sizes():
     assert 0 < w1 < w64
 
 
+@pytest.mark.parametrize("act_mode", [k3.ACT_EXACT, k3.ACT_BF16H])
 @pytest.mark.parametrize("x_dtype", [k3.X_BF16, k3.X_F32])
-def test_workspace_never_shrinks_as_tokens_grow(x_dtype):
+def test_workspace_never_shrinks_as_tokens_grow(x_dtype, act_mode):
     """A workspace sized for T tokens serves every call with fewer (the router's partial logits vary
-    in count with the token tiles, the activation form changes at 3 tokens, the router at 16)."""
-    cfg = k3.Config.make(**K3CFG, x_dtype=x_dtype)
+    in count with the token tiles, the activation form changes at 3 tokens, the router at 16, x's
+    terms are also kept in position order from 256)."""
+    cfg = k3.Config.make(**K3CFG, x_dtype=x_dtype, act_mode=act_mode)
     Ts = sorted(set(list(range(1, 300)) + [383, 384, 385, 511, 512, 513, 600, 640, 700, 1023, 1024, 1025,
                                            2047, 2048, 4095, 4096, 4097, 16384, 19456, 19457, 20000]))
     sizes = [k3.workspace_bytes(cfg, T) for T in Ts]
