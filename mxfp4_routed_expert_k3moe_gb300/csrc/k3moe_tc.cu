@@ -17,15 +17,17 @@
 // v = sum_j q_j 2^{e_j} with q_j E4M3 and 2^{e_j} an E8M0 block scale, each term taking the
 // rounding residual of the previous ones. Two terms hold a bf16 block exactly (down to elements
 // 2^-13 below the block maximum); three terms leave at most ~2^-12 of the block maximum of an fp32
-// x or of h. The MMA columns of one token's terms are summed in the epilogue.
+// x or of h (two terms of h in the bf16-class activation mode). The MMA columns of one token's terms
+// are summed in the epilogue.
 //
 // CTA layout (one CTA per SM, persistent over work items, 384 threads):
 //   warps 0-3   epilogue: accumulators (double-buffered in tensor memory) -> per-position sums
-//   warps 4-7   loaders: the tensor copy of the weight tile (one lane) and cp.async of the B rows and
-//               of the scale words, each loader for its own ring slots (the down projection's E4M3
-//               terms of h, contiguous per work group, come by a second tensor copy). On this part one thread
-//               issues about one tensor copy per ~500 SM cycles, so a single issuing thread caps the
-//               weight stream near 3 TB/s; four reach the DRAM rate.
+//   warps 4-7   loaders: the tensor copy of the weight tile and the bulk copy of its scale words (one
+//               lane), the B rows by cp.async, or where a work group's rows are consecutive (the
+//               terms of h; the terms of x in position order from 256 tokens) by one more tensor
+//               copy, and the B rows' scale words by cp.async; each loader for its own ring slots.
+//               On this part one thread issues about one tensor copy per ~500 SM cycles, so a single
+//               issuing thread caps the weight stream near 3 TB/s; four reach the DRAM rate.
 //   warps 8-11  MMA issuers (one lane each): tcgen05.cp of the scale words into tensor memory, then
 //               the MMAs. One issuing thread sustains one tcgen05 instruction per ~120-230 SM cycles
 //               whatever N is, so at small N (few tokens) three issuers share the stages, each with
@@ -34,10 +36,13 @@
 // the slots s = w mod n_iss), so each agent waits on a slot's barriers round after round and a
 // parity wait never meets a barrier two phases away.
 // The E8M0 scales of the weights are read in the device order (k3moe_pack_records): the scales of a
-// chunk of 128 rows are one contiguous block, brought by one bulk copy with the tensor copy of the
-// codes. (Fetched row by row, 4 bytes per request, they took a quarter of the DRAM rate.)
+// stage's chunks of 128 rows are one contiguous block, brought by one bulk copy with the tensor copy
+// of the codes. (Fetched row by row, 4 bytes per request, they took a quarter of the DRAM rate.)
 // A pipeline stage holds `ch` consecutive 128-code chunks of the reduction axis, brought by one
 // tensor copy (the per-copy cost of the TMA unit is amortised over more bytes).
+// Each projection has one kernel instance per form; the E2M1 form and the two-term E4M3 rows at
+// N = 64 have their tile shapes and ring depths as compile-time constants (the kernels are sensitive
+// to every instruction of their per-stage chains), other E4M3 shapes take a general instance.
 // Every mbarrier wait is bounded; on a timeout the CTA raises the status word and stops early.
 #include <cstdint>
 #include <cstring>
