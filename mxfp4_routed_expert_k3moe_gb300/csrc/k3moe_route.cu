@@ -343,11 +343,14 @@ __device__ void topk_permute_one_token(const Cfg& c, const Ws& ws, const float* 
 // by a little more than 1e-5, and to move the gates by ~1e-5. Before the final selection of a token,
 // the experts whose place could depend on that rounding are recomputed on the CUDA cores and written
 // over the partial logits (part 0 takes the value, the other parts zero, so the parts still add up to
-// it exactly): every expert whose ranked value (logit, or sigmoid + selection bias) lies within
-// kRefineMargin of the k-th value, and every selected expert within kRefineMargin of a selected
-// neighbour. Every other selected expert stays more than the margin above the k-th value and its
-// neighbours, every other expert more than the margin below, so the selection and its order are those
-// of exact logits; the gates of the experts not recomputed carry the tensor cores' rounding (~1e-5).
+// it exactly): where an unselected expert's ranked value (logit, or sigmoid + selection bias) lies
+// within kRefineMargin of the k-th value (a tight boundary), those experts and the selected ones
+// within the margin of the k-th value; and every selected expert within kRefineMargin of a selected
+// neighbour. Every other selected expert stays more than the margin above its neighbours and, at a
+// tight boundary, above the k-th value; every other expert more than the margin below the k-th value;
+// so the selection and its order are those of exact logits. When nothing is recomputed (the usual
+// case) the first selection stands and only its gates are formed. The gates of the experts not
+// recomputed carry the tensor cores' rounding (~1e-5).
 // (Recomputing every selected expert as well, for gates to ~1e-6, took 23 us per token at 64 tokens.)
 // The whole CTA computes the candidates together, kRefineBatch at a time: thread i sums the fp32 products
 // of its d / blockDim.x consecutive elements of x and of each candidate's fp32 router row, then the
@@ -358,7 +361,7 @@ constexpr float kRefineMargin = 2e-4f;
 constexpr int kRefineBatch = 16;
 
 template <int R, int KZ, bool SIG>
-__device__ void refine_candidates_r(const Cfg& c, float* logits_t, long long ls, int np, const float* sel_bias,
+__device__ int refine_candidates_r(const Cfg& c, float* logits_t, long long ls, int np, const float* sel_bias,
                                     const float* W, const float* logit_bias, const uint8_t* xrow,
                                     const unsigned long long* sel, int* s_cid, int* s_nc,
                                     float (*s_red)[kRefineBatch]) {
@@ -369,17 +372,21 @@ __device__ void refine_candidates_r(const Cfg& c, float* logits_t, long long ls,
   load_keys<R, KZ, SIG>(c.E, logits_t, ls, np, sel_bias, key);
   if (threadIdx.x == 0) *s_nc = 0;
   __syncthreads();
-  // experts below the k-th within the margin
+  // experts below the k-th within the margin (then the boundary is tight)
+  bool below = false;
 #pragma unroll
   for (int q = 0; q < R; ++q)
     if (key[q] != 0ull && key[q] < kth && key_logit(key[q]) >= vk - kRefineMargin) {
+      below = true;
       const int at = atomicAdd(s_nc, 1);
       if (at < (int)blockDim.x) s_cid[at] = key_expert(key[q]);
     }
-  // selected experts within the margin of the k-th value or of a selected neighbour (lane = rank)
+  const bool tight = __syncthreads_or(below);
+  // selected experts within the margin of a tight boundary or of a selected neighbour (lane = rank)
   if (warp == 0 && lane < c.k && sel[lane] != 0ull) {
     const float v = key_logit(sel[lane]);
-    const bool near = v - vk <= kRefineMargin || (lane > 0 && key_logit(sel[lane - 1]) - v < kRefineMargin) ||
+    const bool near = (tight && v - vk <= kRefineMargin) ||
+                      (lane > 0 && key_logit(sel[lane - 1]) - v < kRefineMargin) ||
                       (lane + 1 < c.k && v - key_logit(sel[lane + 1]) < kRefineMargin);
     if (near) {
       const int at = atomicAdd(s_nc, 1);
@@ -388,7 +395,7 @@ __device__ void refine_candidates_r(const Cfg& c, float* logits_t, long long ls,
   }
   __syncthreads();
   const int n = *s_nc;
-  if (n > (int)blockDim.x) return;
+  if (n > (int)blockDim.x) return 0;  // (the tensor-core values stand)
   // this thread's slice of the reduction axis: [j0, j1), a multiple of 4 elements (d is a multiple of 128)
   const int per = ((c.d / 4 + blockDim.x - 1) / blockDim.x) * 4;
   const int j0 = min(c.d, (int)threadIdx.x * per), j1 = min(c.d, j0 + per);
@@ -439,7 +446,7 @@ __device__ void refine_candidates_r(const Cfg& c, float* logits_t, long long ls,
     }
     __threadfence_block();
     __syncthreads();
-    return;
+    return n;
   }
   for (int b0 = 0; b0 < n; b0 += kRefineBatch) {
     const int nb = min(kRefineBatch, n - b0);
@@ -485,25 +492,27 @@ __device__ void refine_candidates_r(const Cfg& c, float* logits_t, long long ls,
   }
   __threadfence_block();
   __syncthreads();
+  return n;
 }
 
 // One token: the selection on the tensor cores' partial logits, then the recomputation of the experts
 // near its k-th value (above); the final selection runs on the corrected logits.
 template <int KZ, bool SIG>
-__device__ void refine_candidates(const Cfg& c, float* logits_t, long long ls, int np, const float* sel_bias,
-                                  const float* W, const float* logit_bias, const uint8_t* xrow,
-                                  unsigned long long* cand) {
-  __shared__ unsigned long long s_sel[32], s_thr[64];
+// Returns the number of experts recomputed (0: no logit changed, and the selection in s_sel stands).
+__device__ int refine_candidates(const Cfg& c, float* logits_t, long long ls, int np, const float* sel_bias,
+                                 const float* W, const float* logit_bias, const uint8_t* xrow,
+                                 unsigned long long* cand, unsigned long long* s_sel) {
+  __shared__ unsigned long long s_thr[64];
   __shared__ int s_n, s_nc, s_cid[256];
   __shared__ float s_red[8][kRefineBatch];
   topk_select_any<KZ, SIG>(c.E, c.k, logits_t, ls, np, sel_bias, cand, s_sel, s_thr, &s_n);
   const int nw = blockDim.x >> 5;
   const int per_lane = (c.E + 32 * nw - 1) / (32 * nw);
-  if (per_lane <= 1) refine_candidates_r<1, KZ, SIG>(c, logits_t, ls, np, sel_bias, W, logit_bias, xrow, s_sel, s_cid, &s_nc, s_red);
-  else if (per_lane <= 2) refine_candidates_r<2, KZ, SIG>(c, logits_t, ls, np, sel_bias, W, logit_bias, xrow, s_sel, s_cid, &s_nc, s_red);
-  else if (per_lane <= 4) refine_candidates_r<4, KZ, SIG>(c, logits_t, ls, np, sel_bias, W, logit_bias, xrow, s_sel, s_cid, &s_nc, s_red);
-  else if (per_lane <= 8) refine_candidates_r<8, KZ, SIG>(c, logits_t, ls, np, sel_bias, W, logit_bias, xrow, s_sel, s_cid, &s_nc, s_red);
-  else refine_candidates_r<16, KZ, SIG>(c, logits_t, ls, np, sel_bias, W, logit_bias, xrow, s_sel, s_cid, &s_nc, s_red);
+  if (per_lane <= 1) return refine_candidates_r<1, KZ, SIG>(c, logits_t, ls, np, sel_bias, W, logit_bias, xrow, s_sel, s_cid, &s_nc, s_red);
+  if (per_lane <= 2) return refine_candidates_r<2, KZ, SIG>(c, logits_t, ls, np, sel_bias, W, logit_bias, xrow, s_sel, s_cid, &s_nc, s_red);
+  if (per_lane <= 4) return refine_candidates_r<4, KZ, SIG>(c, logits_t, ls, np, sel_bias, W, logit_bias, xrow, s_sel, s_cid, &s_nc, s_red);
+  if (per_lane <= 8) return refine_candidates_r<8, KZ, SIG>(c, logits_t, ls, np, sel_bias, W, logit_bias, xrow, s_sel, s_cid, &s_nc, s_red);
+  return refine_candidates_r<16, KZ, SIG>(c, logits_t, ls, np, sel_bias, W, logit_bias, xrow, s_sel, s_cid, &s_nc, s_red);
 }
 
 // Exclusive block-wide scan of two int arrays of length n (in place into out0/out1, total at [n]).
@@ -1067,12 +1076,23 @@ __global__ void __launch_bounds__(256, MINB) k_select(RouteArgs a) {
     asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
     __syncthreads();
   }
-  refine_candidates<KZ, SIG>(c, a.ws.logits + t * c.E, a.T * c.E, c.rsplit, SIG ? a.bias : nullptr, a.W,
-                             SIG ? nullptr : a.bias, smem, cand);
-  topk_block<KZ, SIG>(c.E, c.k, a.ws.logits + t * c.E, a.T * c.E, c.rsplit, SIG ? a.bias : nullptr,
-                      cand, a.ws.topk_idx + t * c.k,
-                a.ws.topk_w + t * c.k, (a.mode & RM_USER_OUT) && a.out_idx ? a.out_idx + t * c.k : nullptr,
-                (a.mode & RM_USER_OUT) && a.out_w ? a.out_w + t * c.k : nullptr, nullptr, nullptr);
+  __shared__ unsigned long long s_sel1[32];
+  const int nref = refine_candidates<KZ, SIG>(c, a.ws.logits + t * c.E, a.T * c.E, c.rsplit, SIG ? a.bias : nullptr,
+                                              a.W, SIG ? nullptr : a.bias, smem, cand, s_sel1);
+  int* idx_user = (a.mode & RM_USER_OUT) && a.out_idx ? a.out_idx + t * c.k : nullptr;
+  float* w_user = (a.mode & RM_USER_OUT) && a.out_w ? a.out_w + t * c.k : nullptr;
+  if (nref == 0) {  // no logit changed: the first selection stands, and its gates are formed
+    if (warp == 0) {
+      int my_e;
+      float w;
+      gates_warp<SIG>(c.k, a.ws.logits + t * c.E, a.T * c.E, c.rsplit, s_sel1, a.ws.topk_idx + t * c.k,
+                      a.ws.topk_w + t * c.k, idx_user, w_user, my_e, w);
+    }
+    __syncthreads();
+  } else {
+    topk_block<KZ, SIG>(c.E, c.k, a.ws.logits + t * c.E, a.T * c.E, c.rsplit, SIG ? a.bias : nullptr, cand,
+                        a.ws.topk_idx + t * c.k, a.ws.topk_w + t * c.k, idx_user, w_user, nullptr, nullptr);
+  }
   // the last selecting CTA builds the permutation
   if (threadIdx.x < 32) __threadfence();
   __syncthreads();
