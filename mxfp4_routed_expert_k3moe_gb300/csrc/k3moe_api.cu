@@ -240,7 +240,10 @@ Cfg make_cfg(const k3moe_config* c, long long T) {
   // 16, which keeps its MMA N at 48 with two issuers and two accumulator buffers (32, N = 96 with one
   // of either, measured 35 % slower at 64 tokens, 45 % at 512, 9 % at 4096; 8 slower than 16). With
   // two terms of h (K3MOE_ACT_BF16H) 32 positions make the gate/up projection's N = 64 and stream each
-  // down record half as often (4096 tokens: down 7.6 -> 4.4 ms).
+  // down record half as often (4096 tokens: down 7.6 -> 4.4 ms). Wider down groups at prefill sizes,
+  // which read each record twice instead of three times at ~73 positions per expert, measured slower
+  // still: 48 or 64 positions (N 96 / 128 on the general instance, one issuer) took the 4096-token
+  // down projection from 3.3 ms to 4.3 ms with stages of two chunks, 5.2-5.7 ms with one.
   const long long wmax = k.fp4 ? 16 : 32, wmax_dn = (!k.fp4 && k.hterms == 2) ? 32 : 16;
   k.wgt = (int)(T < wmax ? T : wmax);
   k.wgt_dn = (int)(T < wmax_dn ? T : wmax_dn);

@@ -181,6 +181,20 @@ def test_layer_bf16h_k3_prefill_sampled():
     check_layer(L, 1024, sample=[0, 3, 511, 800, 1023])
 
 
+def test_layer_bf16h_k3_decode_b64_zipf():
+    """Decode b=64 with Zipf-skewed routing at the K3 shape in the bf16-class h mode, as the bench
+    times it: indices and gates of all 64 tokens, y of every fourth."""
+    L = DeviceLayer(synth.K3, seed=2, zipf_s=1.1, act="bf16h")
+    check_layer(L, 64, sample=list(range(0, 64, 4)))
+
+
+def test_layer_bf16h_k3_prefill_4096_sampled():
+    """Prefill 4096 at the K3 shape in the bf16-class h mode, as the bench times it: indices and gates
+    of all 4096 tokens, y of five."""
+    L = DeviceLayer(synth.K3, seed=3, act="bf16h")
+    check_layer(L, 4096, sample=[0, 1, 777, 2048, 4095])
+
+
 def test_expert_ffn_bf16h_given_routing():
     L = DeviceLayer(MID, seed=42, x_dtype="f32", act="bf16h")
     T = 300
