@@ -259,6 +259,24 @@ class LayerWeights:
         k3.prepare_router(cfg, self.W, self.parts)
 
 
+def max_over_ranks(ms, world, device="cuda"):
+    """The slowest rank's time: every rank gets the largest of the ranks' `ms` (all-reduce MAX over the
+    default process group; `device` is where the collective's tensor lives: cuda for NCCL, cpu for
+    gloo). One rank returns its own time."""
+    if world <= 1:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world, units_per_step, steps, ms):
+    """Whole-job throughput: the units all `world` ranks processed in `steps` steps (each rank
+    `units_per_step` per step: replicas, weak scaling) over the slowest rank's `ms` milliseconds."""
+    return world * units_per_step * steps / (ms * 1e-3)
+
+
 def timed(step, steps, world, local_rank, warmup=0, check=None):
     """Device time of exactly `steps` calls of step(i), bracketed by a barrier and synchronize on both
     sides (CUDA events on the launching stream), with nvidia-smi clocks sampled meanwhile. The sampler
@@ -289,9 +307,7 @@ def timed(step, steps, world, local_rank, warmup=0, check=None):
     clk = clocks.stop()
     ms = a.elapsed_time(b)
     if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+        ms = max_over_ranks(ms, world, "cuda")
         torch.distributed.barrier()
     return ms, clk
 
@@ -338,7 +354,7 @@ def run_layer_workload(args, k3, name, T, seed, zipf_s, n_sets, steps, warmup, w
         ms_x, _ = timed(step_x, steps, world, local_rank, warmup=warmup)
         if k3.check_device_status(ws) != k3.OK:
             raise RuntimeError(f"{name}: device status check failed in the exact-mode pass")
-        exact = {"act_mode": "exact (h as three E4M3 terms, ~2^-22)", "value": world * T * steps / (ms_x * 1e-3),
+        exact = {"act_mode": "exact (h as three E4M3 terms, ~2^-22)", "value": job_rate(world, T, steps, ms_x),
                  "unit": "tokens/s", "ms_per_step": ms_x / steps}
 
     # per-kernel pass (after the headline timing): events recorded between the kernels of each step on
@@ -387,7 +403,7 @@ def run_layer_workload(args, k3, name, T, seed, zipf_s, n_sets, steps, warmup, w
         cnt = {**cnt, "traffic": None}
     ms_per_step = elapsed_ms / steps
     out = {
-        "value": world * T * steps / (elapsed_ms * 1e-3), "unit": "tokens/s", "steps": steps, "warmup": warmup,
+        "value": job_rate(world, T, steps, elapsed_ms), "unit": "tokens/s", "steps": steps, "warmup": warmup,
         "ms_per_step": ms_per_step,
         "config": {**workload_config(name, T, shape), "weight_sets_rotated": n_sets,
                    "act_mode": "bf16h (h as two E4M3 terms, bf16-class)" if bf16h else "exact",
@@ -502,7 +518,7 @@ def run_stack(args, k3, world, local_rank):
         for label, fn in (("fused", fused), ("separate", separate)):
             x.copy_(x0)
             ms, clk = timed(lambda i: fn(), steps, world, local_rank, warmup=3)
-            out[label] = {"layer_tokens_per_s": 4 * T * steps / (ms * 1e-3) * world, "ms_per_step": ms / steps,
+            out[label] = {"layer_tokens_per_s": job_rate(world, 4 * T, steps, ms), "ms_per_step": ms / steps,
                           "steps": steps, "clocks": clk}
         x.copy_(x0)
         fused(keep_idx=True)
