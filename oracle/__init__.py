@@ -22,6 +22,8 @@ _SRC = os.path.join(_HERE, "k3oracle.c")
 FAULTS = {
     "none": 0, "nibble_order": 1, "scale_bias": 2, "drop_shared": 3, "no_renorm": 4,
     "tie_high": 5, "down_transposed": 6, "glu_on_up": 7, "bias_in_gate": 8, "no_bias_select": 9,
+    "silu_sign": 10, "e2m1_table": 11, "shared_gated": 12, "select_lowest": 13, "renorm_short": 14,
+    "rms_sum": 15, "scale_block": 16,
 }
 SCORES = {"softmax": 0, "sigmoid_bias": 1}
 

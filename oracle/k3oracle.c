@@ -59,6 +59,13 @@ enum {
     FAULT_GLU_ON_UP = 7,     /* SiLU applied to the up branch instead of the gate */
     FAULT_BIAS_IN_GATE = 8,  /* sigmoid score: gates from the biased score          */
     FAULT_NO_BIAS_SELECT = 9,/* sigmoid score: selection ignores the bias           */
+    FAULT_SILU_SIGN = 10,    /* SiLU(z) as z / (1 + e^z)                            */
+    FAULT_E2M1_TABLE = 11,   /* one wrong table entry: code 5 read as 2.5           */
+    FAULT_SHARED_GATED = 12, /* shared experts weighted by the first gate, not 1    */
+    FAULT_SELECT_LOWEST = 13,/* the k lowest logits selected                        */
+    FAULT_RENORM_SHORT = 14, /* renormalising sum over k - 1 of the k gates         */
+    FAULT_RMS_SUM = 15,      /* RMSNorm over the sum of squares, not their mean     */
+    FAULT_SCALE_BLOCK = 16,  /* weight scaled by the next block's scale byte        */
 };
 
 /* OCP MX v1.0, FP4 E2M1: magnitudes of the 8 positive codes. */
@@ -66,6 +73,7 @@ static const double E2M1_MAG[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
 
 double k3o_e2m1(int code) {
     double v = E2M1_MAG[code & 7];
+    if (g_fault == FAULT_E2M1_TABLE && (code & 7) == 5) v = 2.5;
     return (code & 8) ? -v : v; /* code 8 is -0.0 */
 }
 
@@ -87,7 +95,9 @@ static int weight(const uint8_t* codes, const uint8_t* scales, int64_t cols, int
     int even_low = (g_fault == FAULT_NIBBLE_ORDER) ? 0 : 1;
     int nib = ((c % 2 == 0) == even_low) ? (byte & 0xF) : (byte >> 4);
     double s;
-    if (k3o_e8m0(scales[r * (cols / 32) + c / 32], &s)) return -1;
+    int64_t blk = c / 32;
+    if (g_fault == FAULT_SCALE_BLOCK) blk = (blk + 1) % (cols / 32);
+    if (k3o_e8m0(scales[r * (cols / 32) + blk], &s)) return -1;
     *w = k3o_e2m1(nib) * s;
     return 0;
 }
@@ -119,8 +129,9 @@ typedef struct {
 static int cmp_desc(const void* a, const void* b) {
     const scored* x = (const scored*)a;
     const scored* y = (const scored*)b;
-    if (x->l > y->l) return -1;
-    if (x->l < y->l) return 1;
+    const int lowest = g_fault == FAULT_SELECT_LOWEST;
+    if (x->l > y->l) return lowest ? 1 : -1;
+    if (x->l < y->l) return lowest ? -1 : 1;
     if (g_fault == FAULT_TIE_HIGH) return (x->e > y->e) ? -1 : (x->e < y->e);
     return (x->e < y->e) ? -1 : (x->e > y->e); /* equal logits: lower index first */
 }
@@ -182,7 +193,7 @@ int k3o_route_token(int32_t E, int32_t d, int32_t k, const double* x, const floa
     for (int32_t e = 0; e < E; ++e) p[e] /= z;
     qsort(s, (size_t)E, sizeof(scored), cmp_desc);
     double zk = 0.0;
-    for (int32_t i = 0; i < k; ++i) zk += p[s[i].e];
+    for (int32_t i = 0; i < k - (g_fault == FAULT_RENORM_SHORT ? 1 : 0); ++i) zk += p[s[i].e];
     for (int32_t i = 0; i < k; ++i) {
         idx_out[i] = s[i].e;
         w_out[i] = (g_fault == FAULT_NO_RENORM) ? p[s[i].e] : p[s[i].e] / zk;
@@ -223,7 +234,7 @@ int k3o_route_tokens(int32_t E, int32_t d, int32_t k, const void* x, int32_t x_i
 }
 
 /* ------------------------------------------------------------------ expert FFN */
-static double silu(double z) { return z / (1.0 + exp(-z)); }
+static double silu(double z) { return z / (1.0 + exp(g_fault == FAULT_SILU_SIGN ? z : -z)); }
 
 /*
  * One expert on one token: record = [gate codes][gate scales][up codes][up scales]
@@ -340,7 +351,8 @@ int k3o_layer(int32_t d, int32_t f, int32_t E, int32_t k, int32_t S, const void*
         for (int32_t s = 0; s < S && !st && g_fault != FAULT_DROP_SHARED; ++s) {
             st = shared_bf16 ? k3o_expert_token_bf16(d, f, (const uint16_t*)shared[s], xt, o, NULL)
                              : k3o_expert_token(d, f, shared[s], xt, o, NULL);
-            if (!st) for (int32_t j = 0; j < d; ++j) yt[j] += o[j];
+            const double ws = g_fault == FAULT_SHARED_GATED ? wt[0] : 1.0;
+            if (!st) for (int32_t j = 0; j < d; ++j) yt[j] += ws * o[j];
         }
         if (!st) {
             if (idx) memcpy(idx + t * k, it, sizeof(int32_t) * (size_t)k);
@@ -360,7 +372,7 @@ void k3o_rmsnorm(const double* x, int64_t T, int32_t d, double eps, double* out)
     for (int64_t t = 0; t < T; ++t) {
         double ss = 0.0;
         for (int32_t j = 0; j < d; ++j) ss += x[t * d + j] * x[t * d + j];
-        double r = 1.0 / sqrt(ss / d + eps);
+        double r = 1.0 / sqrt((g_fault == FAULT_RMS_SUM ? ss : ss / d) + eps);
         for (int32_t j = 0; j < d; ++j) out[t * d + j] = x[t * d + j] * r;
     }
 }

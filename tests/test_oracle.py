@@ -2,10 +2,13 @@
 
 Each pin is a function that raises AssertionError when the oracle is wrong.
 `test_planted_mistakes_are_caught` switches the oracle to deliberately wrong
-variants (wrong nibble order, scale bias, dropped shared experts, missing
-renormalisation, wrong tie order, transposed down projection, SiLU on the
-wrong branch, and for the sigmoid score: the bias in the gates, the bias left
-out of the selection) and checks that at least one pin fails for each.
+variants and checks that at least one pin fails for each: wrong nibble order, scale
+bias, a wrong E2M1 table entry, the next block's scale byte, dropped shared
+experts, shared experts weighted by a gate, missing renormalisation, a
+renormalising sum short of one gate, wrong tie order, the lowest logits
+selected, transposed down projection, SiLU on the wrong branch, SiLU with the
+wrong sign, RMSNorm over the sum of squares, and for the sigmoid score: the bias
+in the gates, the bias left out of the selection.
 """
 import math
 
