@@ -88,7 +88,7 @@ enum { K3MOE_SCORE_SOFTMAX = 0, K3MOE_SCORE_SIGMOID_BIAS = 1 };
    2^-13 of its 32-element block's maximum keeps less), and the down projection's work groups hold
    32 positions instead of 16. The layer output stays within the 2e-3 bound on max|y - y_exact| /
    max|y_exact| (measured 6e-4 to 1e-3 at the test shapes, against ~2e-5 exact) and the down
-   projection runs ~1.7x faster at 4096 tokens. Below 3 tokens it is the exact mode.
+   projection runs ~2x faster at 4096 tokens. Below 3 tokens it is the exact mode.
    K3MOE_ACT_MXFP4 (activations quantised to MXFP4) is legal but not implemented. */
 enum { K3MOE_ACT_EXACT = 0, K3MOE_ACT_MXFP4 = 1, K3MOE_ACT_BF16H = 2 };
 /* Element type of the token activations x. */
