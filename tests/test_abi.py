@@ -170,3 +170,19 @@ def test_status_strings():
     for code in range(7):
         assert k3.status_string(code)
     assert k3.status_string(99) == "unknown status"
+
+
+def test_static_scratch_limit_on_host():
+    """k3moe_layer_static serves calls whose workspace fits its 4 MiB array: at the K3 shape up to 6
+    tokens; 7 are refused with K3MOE_ERR_WORKSPACE before any CUDA call (the header's statement)."""
+    src = open(os.path.join(ROOT, "include", "k3moe.h")).read()
+    m = re.search(r"#define K3MOE_STATIC_SCRATCH_BYTES \((\d+)u << (\d+)\)", src)
+    size = int(m.group(1)) << int(m.group(2))
+    assert size == 4 << 20
+    cfg = k3.Config.make(**K3CFG)
+    assert k3.workspace_bytes(cfg, 6) <= size < k3.workspace_bytes(cfg, 7)
+    lib = k3.load()
+    a = ctypes.c_void_p(1 << 20)
+    assert lib.k3moe_layer_static(ctypes.byref(cfg), a, 7, a, None, a, a, a, None) == k3.ERR_WORKSPACE
+    assert lib.k3moe_layer_static(ctypes.byref(cfg), a, 0, a, None, a, a, a, None) == k3.OK
+    assert lib.k3moe_layer_static(ctypes.byref(cfg), a, -1, a, None, a, a, a, None) == k3.ERR_INVALID_ARGUMENT
