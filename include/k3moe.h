@@ -79,14 +79,17 @@ typedef enum {
    sigmoid of the unbiased logit with a selection-only bias (see k3moe_route). */
 enum { K3MOE_SCORE_SOFTMAX = 0, K3MOE_SCORE_SIGMOID_BIAS = 1 };
 /* Legal but not implemented: d_model > 25600 (the router stages whole rows in shared memory). */
-/* Activation handling in the expert FFN.
-   K3MOE_ACT_EXACT (the default): activations keep their input precision (bf16 exactly, fp32 to
-   ~2^-22) and h = SiLU(g) * u keeps ~2^-22 relative precision (three E4M3 terms per element from 3
-   tokens on, eight E2M1 terms below).
+/* Activation handling in the expert FFN. The activations x and h = SiLU(g) * u enter the tensor
+   cores as sums of terms with E8M0 block scales (one per 32 elements), each term the rounding
+   residual of the previous ones; the bounds below are of |v - sum of terms| against the maximum of
+   the element's 32-element block.
+   K3MOE_ACT_EXACT (the default): with 1 and 2 tokens, x and h as eight E2M1 terms, within 2^-23.
+   From 3 tokens on, bf16 x as two E4M3 terms, exact for every element of at least 2^-13 of the
+   block maximum (smaller ones within 2^-21); fp32 x and h as three E4M3 terms, within 2^-12
+   (about 2^-14 over random blocks).
    K3MOE_ACT_BF16H: x as in the exact mode; from 3 tokens on, h enters the down projection as two
-   E4M3 terms per element, about 8 significant bits (the precision of a bf16 h; an element below
-   2^-13 of its 32-element block's maximum keeps less), and the down projection's work groups hold
-   32 positions instead of 16. The layer output stays within the 2e-3 bound on max|y - y_exact| /
+   E4M3 terms, within 2^-8, every element of at least 2^-13 of the block maximum to 2^-8 of itself
+   (bf16's precision class), and the down projection's work groups hold 32 positions instead of 16. The layer output stays within the 2e-3 bound on max|y - y_exact| /
    max|y_exact| (measured 6e-4 to 1e-3 at the test shapes, against ~2e-5 exact) and the down
    projection runs ~2x faster at 4096 tokens. Below 3 tokens it is the exact mode.
    K3MOE_ACT_MXFP4 (activations quantised to MXFP4) is legal but not implemented. */
