@@ -34,9 +34,11 @@ bool gather_x(const k3moe_config* c, long long T) { return !use_fp4(c, T) && T >
 size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // Router logits on the tensor cores from kRouterTcMinT tokens, else on the CUDA cores. Below it the
-// CUDA-core kernel reads the router weights once per 8-token tile, while the tensor-core path first
-// writes and reads their three bf16 parts (4x the bytes): measured at the K3 shape, bf16 tokens, 72 vs
-// 85 us at 8 tokens, 163 vs 95 us at 32.
+// CUDA-core kernel reads the fp32 router weights once per 8-token tile. The tensor-core path reads
+// their three bf16 parts instead (6 bytes per weight; prepared once by k3moe_prepare_router, else
+// split per call, which writes and reads them first: 4x the fp32 bytes), then selects in a second
+// kernel. The threshold was measured with the per-call split, at the K3 shape with bf16 tokens:
+// 72 vs 85 us at 8 tokens, 163 vs 95 us at 32.
 constexpr long long kRouterTcMinT = 16;
 bool router_tc(const k3moe_config* c, long long T) {
   return T >= kRouterTcMinT && c->d_model % 64 == 0;
