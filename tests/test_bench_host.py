@@ -80,9 +80,11 @@ def _free_port():
 
 
 def _rank_main(rank, world, port, times, q):
+    import datetime
+
     import torch.distributed as dist
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
-    dist.init_process_group("gloo", rank=rank, world_size=world)
+    dist.init_process_group("gloo", rank=rank, world_size=world, timeout=datetime.timedelta(seconds=60))
     try:
         ms = bench.max_over_ranks(times[rank], world, "cpu")
         q.put((rank, ms, bench.job_rate(world, 16, 5, ms)))
@@ -98,13 +100,18 @@ def test_replicas_take_the_slowest_rank_over_gloo():
     q = ctx.Queue()
     times = [12.5, 17.25]
     port = _free_port()
-    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, times, q)) for r in range(2)]
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, times, q), daemon=True) for r in range(2)]
     for p in procs:
         p.start()
-    res = sorted(q.get(timeout=120) for _ in procs)
-    for p in procs:
-        p.join(timeout=60)
-        assert p.exitcode == 0
+    try:
+        res = sorted(q.get(timeout=120) for _ in procs)
+        for p in procs:
+            p.join(timeout=60)
+            assert p.exitcode == 0
+    finally:
+        for p in procs:
+            if p.is_alive():
+                p.kill()
     assert [r for r, _, _ in res] == [0, 1]
     for _, ms, v in res:
         assert ms == 17.25
