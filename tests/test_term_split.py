@@ -1,5 +1,6 @@
 """Precision of the activation terms (CPU): the bounds that include/k3moe.h states for each activation
-mode, checked on a model of the split built from the formats' definitions (OCP Microscaling Formats
+mode (and the exactness of the router weights' three bf16 parts), checked on a model of the split
+built from the formats' definitions (OCP Microscaling Formats
 v1.0: E4M3 with 3 mantissa bits, bias 7, subnormal quantum 2^-9, largest finite 448; E2M1 values
 0, 0.5, 1, 1.5, 2, 3, 4, 6; E8M0 scales 2^(b - 127)) and round-to-nearest-even.
 
@@ -148,3 +149,23 @@ def test_two_e4m3_terms_keep_about_eight_bits_per_element():
     m = np.max(np.abs(v), axis=1, keepdims=True)
     big = (np.abs(v) >= 2.0 ** -13 * m) & (v != 0)
     assert (np.abs(v - approx)[big] / np.abs(v)[big]).max() <= 2.0 ** -8
+
+
+def test_three_bf16_parts_hold_every_fp32_weight():
+    """The router's weight-loading split (k3moe_prepare_router): W = W0 + W1 + W2 with each part the
+    bf16 rounding of what the earlier parts leave. Each part takes 8 significant bits of the residual,
+    and every residual is exact in fp32, so the three parts hold all 24 bits of a normal fp32 weight."""
+    rng = np.random.default_rng(8)
+    w = (rng.standard_normal(200000) * np.exp2(rng.uniform(-40, 40, 200000))).astype(np.float32)
+    w = np.concatenate([w, np.array([1.0, -1.0, 2.0 ** 30, np.float32(1 + 2 ** -23), 0.0], dtype=np.float32)])
+    r = w.copy()
+    parts = []
+    for _ in range(3):
+        p = to_bf16(r)
+        parts.append(p)
+        r = (r - p).astype(np.float32)  # exact: see the docstring
+    total = parts[0].astype(np.float64) + parts[1].astype(np.float64) + parts[2].astype(np.float64)
+    assert np.array_equal(total, w.astype(np.float64))
+    assert np.all(r == 0)
+    two = parts[0].astype(np.float64) + parts[1].astype(np.float64)
+    assert not np.array_equal(two, w.astype(np.float64))  # two parts would not do
