@@ -186,3 +186,42 @@ def test_static_scratch_limit_on_host():
     assert lib.k3moe_layer_static(ctypes.byref(cfg), a, 7, a, None, a, a, a, None) == k3.ERR_WORKSPACE
     assert lib.k3moe_layer_static(ctypes.byref(cfg), a, 0, a, None, a, a, a, None) == k3.OK
     assert lib.k3moe_layer_static(ctypes.byref(cfg), a, -1, a, None, a, a, a, None) == k3.ERR_INVALID_ARGUMENT
+
+
+C_CLIENT = r"""
+#include <stdio.h>
+#include "k3moe.h"
+int main(void) {
+  k3moe_config c = {7168, 1536, 896, 16, 2, K3MOE_SCORE_SOFTMAX, K3MOE_ACT_EXACT, K3MOE_X_BF16,
+                    K3MOE_ORDER_DEVICE, K3MOE_SHARED_MXFP4, 17547264, 0};
+  printf("%zu %zu %zu %d %s\n", k3moe_record_bytes(&c), k3moe_workspace_bytes(&c, 1),
+         k3moe_router_parts_bytes(&c), (int)k3moe_layer(&c, NULL, 1, NULL, NULL, NULL, NULL, NULL, NULL, NULL,
+                                                    NULL, NULL, 0, NULL),
+         k3moe_status_string(K3MOE_ERR_WORKSPACE));
+  return 0;
+}
+"""
+
+
+def test_plain_c_client(tmp_path):
+    """The header is plain C99 (no CUDA or C++ types) and a C program links the library and calls it:
+    host-only queries, and a compute call refused on the host (NULL x) before any CUDA call."""
+    import shutil
+    import subprocess
+    if not shutil.which("gcc"):
+        pytest.skip("gcc not found")
+    lib = k3.load()
+    libdir = os.path.dirname(lib._name)
+    src = tmp_path / "client.c"
+    src.write_text(C_CLIENT)
+    exe = tmp_path / "client"
+    subprocess.check_call(["gcc", "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I",
+                           os.path.join(ROOT, "include"), str(src), "-L", libdir, "-lk3moe",
+                           "-Wl,-rpath," + libdir, "-o", str(exe)])
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split(None, 4)
+    cfg = k3.Config.make(**K3CFG)
+    assert int(out[0]) == 17547264
+    assert int(out[1]) == k3.workspace_bytes(cfg, 1)
+    assert int(out[2]) == 3 * 896 * 7168 * 2
+    assert int(out[3]) == k3.ERR_INVALID_ARGUMENT
+    assert out[4].strip() == k3.status_string(k3.ERR_WORKSPACE)
